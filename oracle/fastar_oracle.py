@@ -1,0 +1,407 @@
+"""fp64 CPU oracle of the FAST-AR per-chunk attention path.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, `__graft_entry__.smoke()` and the
+CPU-baseline leg of `bench.py` may import this module.  The CUDA library
+never calls it and shares no code with it.
+
+Every function is the plain definition of one step, written with numpy in
+float64 (library matmul/sort/isin serve as steps; nothing is blocked, fused
+or reordered beyond the definition).  Inputs are the exact stored values
+(bf16 or fp32) widened to float64.
+
+Sources (page title, then section):
+  [PL]  FAST-AR summary on paperlayer.ai (arXiv 2602.01801v2)
+  [GS]  FAST-AR "Technische samenvatting" on gist.science
+  [RB]  FAST-AR analysis on paper.rainbus.top, "method steps" (方法步骤详情)
+
+Readings taken where the pages are silent:
+  hash    -- bit b of table t is [R_{t*B+b} . x > 0] (a zero dot gives 0),
+             least significant bit = hyperplane t*B+0; one hyperplane set is
+             shared by queries, cached keys and prompt keys.
+  NN      -- new-frame *keys* are matched (cosine) against the
+             representatives refreshed in frame f-1; ties go to the lowest
+             slot; matched iff cosine >= tau; no merging inside a frame.
+  merge   -- all keys matching one group join it; the representative key
+             becomes the matching key with the lowest token index; the
+             stored value is the count-weighted mean rounded to the storage
+             type after each update.
+  insert  -- unmatched keys fill free slots in ascending order, then the
+             slots with the smallest (last_frame, slot) among those not
+             refreshed in this frame are evicted (least recently refreshed).
+  attend  -- a chunk's frames are merged first, then its queries attend the
+             whole live cache; logit = q.k / sqrt(D) + ln m; a query with no
+             allowed key gets a zero output and lse = -inf.
+
+Parity pins of every function live in tests/test_oracle_pins.py; there is
+no worked numeric example on the pages, so the pins are closed forms
+(Lemma 5.1), brute force on tiny inputs, invariants and hand-derived
+fixtures under tests/golden/.
+"""
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass
+
+import numpy as np
+
+HASH_MARGIN = 1e-4   # relative |R.x| / (|R| |x|) below which a bit is listed
+NN_MARGIN = 1e-4     # cosine gap below which an NN decision is listed
+
+
+# --------------------------------------------------------------------------
+# storage rounding (the cache stores merged values in the input type)
+# --------------------------------------------------------------------------
+def round_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values to bf16 or fp32, round-to-nearest-even ("f64": as is).
+
+    bf16 keeps 8 significant bits: write x = mant * 2**e with mant in
+    [0.5, 1), round mant * 2**8 to the nearest integer (ties to even) and
+    scale back.  Exact for every finite value this path produces.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    if dtype == "f64":          # unrounded storage (closed-form checks only)
+        return x
+    if dtype == "f32":
+        return x.astype(np.float32).astype(np.float64)
+    if dtype != "bf16":
+        raise ValueError(dtype)
+    mant, e = np.frexp(x)
+    return np.ldexp(np.rint(mant * 256.0), e - 8)
+
+
+# --------------------------------------------------------------------------
+# step 1: random-hyperplane LSH  ([PL] section 2 "ANN search", section 5
+# "ANN Attention"; [GS] 2.B mechanism: queries and prompt keys projected
+# into one shared LSH space; [RB] "hash once, serves all three modules")
+# --------------------------------------------------------------------------
+def hash_codes(x: np.ndarray, planes: np.ndarray, T: int, B: int):
+    """codes[h][t][i] = sum_b [planes[t*B+b] . x[h][i] > 0] << b.
+
+    x: [H][N][D], planes: [T*B][D].  Returns (codes uint32 [H][T][N],
+    margin_bits uint32 [H][T][N]) where a margin bit marks a dot product
+    with |s| < HASH_MARGIN * |R| * |x| (either bit value is accepted there).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    R = np.asarray(planes, dtype=np.float64)
+    H, N, D = x.shape
+    assert R.shape == (T * B, D)
+    s = np.einsum("hnd,rd->hrn", x, R)                      # [H][T*B][N]
+    bits = (s > 0).astype(np.uint64)
+    thr = HASH_MARGIN * np.linalg.norm(R, axis=1)[None, :, None] \
+        * np.linalg.norm(x, axis=2)[:, None, :]
+    near = (np.abs(s) < thr).astype(np.uint64)
+    codes = np.zeros((H, T, N), dtype=np.uint64)
+    margin = np.zeros((H, T, N), dtype=np.uint64)
+    for t in range(T):
+        for b in range(B):
+            codes[:, t, :] |= bits[:, t * B + b, :] << np.uint64(b)
+            margin[:, t, :] |= near[:, t * B + b, :] << np.uint64(b)
+    return codes.astype(np.uint32), margin.astype(np.uint32)
+
+
+# --------------------------------------------------------------------------
+# step 2: bucket CSR (ids grouped by code, stable)
+# --------------------------------------------------------------------------
+def bucket_csr(codes: np.ndarray, nbuckets: int, n: int | None = None):
+    """Stable grouping of ids 0..n-1 by code.
+
+    codes: [..., N].  Returns perm [..., N] (entries past n are -1) and
+    offsets [..., nbuckets+1] with offsets[c] = #ids (< n) whose code < c.
+    """
+    codes = np.asarray(codes)
+    lead = codes.shape[:-1]
+    N = codes.shape[-1]
+    n = N if n is None else n
+    flat = codes.reshape(-1, N)
+    perm = np.full(flat.shape, -1, dtype=np.int32)
+    offs = np.zeros((flat.shape[0], nbuckets + 1), dtype=np.int32)
+    for g in range(flat.shape[0]):
+        c = flat[g, :n].astype(np.int64)
+        perm[g, :n] = np.argsort(c, kind="stable")
+        offs[g, 1:] = np.cumsum(np.bincount(c, minlength=nbuckets)[:nbuckets])
+    return perm.reshape(lead + (N,)), offs.reshape(lead + (nbuckets + 1,))
+
+
+# --------------------------------------------------------------------------
+# TempCache state ([PL] section 5 "TempCache" and appendix A, Lemma 5.1;
+# [GS] 2.A; [RB] method steps, TempCache)
+# --------------------------------------------------------------------------
+@dataclass
+class CacheState:
+    """Fixed-capacity merged cache of one layer (all heads).
+
+    K, V: [H][C][D] float64 holding stored (bf16/fp32) values.
+    m: [H][C] group counts; codes: [H][T][C]; last_frame: [H][C] (-1 empty);
+    size: [H] live slots (slots >= size are empty); inserted/evicted: [H].
+    """
+    dtype: str
+    K: np.ndarray
+    V: np.ndarray
+    m: np.ndarray
+    codes: np.ndarray
+    last_frame: np.ndarray
+    size: np.ndarray
+    inserted: np.ndarray
+    evicted: np.ndarray
+
+    @staticmethod
+    def empty(H: int, C: int, D: int, T: int, dtype: str) -> "CacheState":
+        return CacheState(dtype, np.zeros((H, C, D)), np.zeros((H, C, D)),
+                          np.zeros((H, C), np.int64), np.zeros((H, T, C), np.uint32),
+                          np.full((H, C), -1, np.int64), np.zeros(H, np.int64),
+                          np.zeros(H, np.int64), np.zeros(H, np.int64))
+
+    def copy(self) -> "CacheState":
+        return dataclasses.replace(self, **{f.name: np.copy(getattr(self, f.name))
+                                            for f in dataclasses.fields(self)
+                                            if f.name != "dtype"})
+
+    @property
+    def H(self):
+        return self.K.shape[0]
+
+    @property
+    def C(self):
+        return self.K.shape[1]
+
+
+class CapacityError(RuntimeError):
+    pass
+
+
+def tempcache_nn(state: CacheState, k: np.ndarray, f: int, tau: float):
+    """Top-1 cosine match of frame f's keys against frame f-1's representatives.
+
+    k: [H][n][D].  Candidates of head h are the live slots s (s < size)
+    with last_frame[s] == f-1, in ascending s.  Returns (match [H][n] slot
+    or -1, listed [H][n] bool).  A decision is listed when the top-1 cosine
+    is within NN_MARGIN of tau, or when the top-2 gap is below NN_MARGIN and
+    the top-1 cosine is at least tau - NN_MARGIN.
+    """
+    k = np.asarray(k, dtype=np.float64)
+    H, n, D = k.shape
+    match = np.full((H, n), -1, dtype=np.int64)
+    listed = np.zeros((H, n), dtype=bool)
+    for h in range(H):
+        size = int(state.size[h])
+        cand = np.nonzero(state.last_frame[h, :size] == f - 1)[0]
+        if cand.size == 0:
+            continue
+        Kc = state.K[h, cand]
+        kn = np.linalg.norm(k[h], axis=1)
+        cn = np.linalg.norm(Kc, axis=1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            cos = (k[h] @ Kc.T) / (kn[:, None] * cn[None, :])
+        cos[~np.isfinite(cos)] = -np.inf          # zero norm: no similarity
+        best = np.argmax(cos, axis=1)              # first max = lowest slot
+        top1 = cos[np.arange(n), best]
+        ok = top1 >= tau
+        match[h, ok] = cand[best[ok]]
+        near_tau = np.abs(top1 - tau) < NN_MARGIN
+        if cand.size > 1:
+            srt = np.sort(cos, axis=1)
+            near_tie = (srt[:, -1] - srt[:, -2]) < NN_MARGIN
+        else:
+            near_tie = np.zeros(n, dtype=bool)
+        # a near tie only matters when the best cosine can reach tau
+        listed[h] = np.isfinite(top1) & (near_tau | (near_tie & (top1 >= tau - NN_MARGIN)))
+    return match, listed
+
+
+def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match) -> CacheState:
+    """Merge one frame's keys into the cache given its NN matches (in place).
+
+    k, v: [H][n][D]; codes: [H][T][n]; match: [H][n] slot or -1.
+    Matched groups (Lemma 5.1): m' = m + |S|, V' = round((m V + sum v)/m'),
+    the representative key, its codes and last_frame come from the lowest
+    matching index.  Unmatched keys become groups of count 1, placed in free
+    slots first, then in evicted slots (smallest (last_frame, slot) among
+    slots with last_frame < f), both in ascending order.
+    """
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    H, n, D = k.shape
+    C = state.C
+    for h in range(H):
+        mh = np.asarray(match[h])
+        for s in np.unique(mh[mh >= 0]):
+            S = np.nonzero(mh == s)[0]              # ascending token index
+            m_old = int(state.m[h, s])
+            m_new = m_old + S.size
+            total = m_old * state.V[h, s]
+            for j in S:
+                total = total + v[h, j]
+            state.V[h, s] = round_storage(total / m_new, state.dtype)
+            state.K[h, s] = k[h, S[0]]
+            state.codes[h, :, s] = codes[h, :, S[0]]
+            state.last_frame[h, s] = f
+            state.m[h, s] = m_new
+        U = np.nonzero(mh < 0)[0]
+        size = int(state.size[h])
+        free = C - size
+        n_app = min(free, U.size)
+        targets = list(range(size, size + n_app))
+        n_evict = U.size - n_app
+        if n_evict > 0:
+            lf = state.last_frame[h, :size]
+            elig = np.nonzero(lf < f)[0]
+            if elig.size < n_evict:
+                raise CapacityError(f"head {h}: {n_evict} evictions needed, "
+                                    f"{elig.size} slots evictable")
+            order = np.lexsort((elig, lf[elig]))    # by last_frame, then slot
+            targets += sorted(elig[order[:n_evict]].tolist())
+        for r, j in enumerate(U):
+            s = targets[r]
+            if s < size:
+                state.evicted[h] += state.m[h, s]
+            state.K[h, s] = k[h, j]
+            state.V[h, s] = v[h, j]
+            state.m[h, s] = 1
+            state.codes[h, :, s] = codes[h, :, j]
+            state.last_frame[h, s] = f
+        state.size[h] = size + n_app
+        state.inserted[h] += n
+    return state
+
+
+def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int,
+                    first_frame: int, tau: float, match_override=None):
+    """Merge a chunk of F frames, frame by frame, into a copy of `state`.
+
+    k_new, v_new: [H][F*n_f][D]; codes_new: [H][T][F*n_f].
+    match_override: optional [H][F*n_f] matches to use instead of the
+    oracle's own (to continue from another implementation's decisions).
+    Returns (new_state, match [H][F*n_f], listed [H][F*n_f]).
+    """
+    st = state.copy()
+    H = st.H
+    match = np.full((H, F * n_f), -1, dtype=np.int64)
+    listed = np.zeros((H, F * n_f), dtype=bool)
+    for fi in range(F):
+        sl = slice(fi * n_f, (fi + 1) * n_f)
+        f = first_frame + fi
+        mt, ls = tempcache_nn(st, np.asarray(k_new)[:, sl], f, tau)
+        if match_override is not None:
+            mt = np.asarray(match_override)[:, sl].astype(np.int64)
+        match[:, sl], listed[:, sl] = mt, ls
+        tempcache_apply_frame(st, np.asarray(k_new)[:, sl], np.asarray(v_new)[:, sl],
+                              np.asarray(codes_new)[:, :, sl], f, mt)
+    return st, match, listed
+
+
+# --------------------------------------------------------------------------
+# step 5: AnnCA pruning ([GS] 2.B mechanism; [RB] method steps, AnnCA;
+# [PL] section 5 "AnnCA")
+# --------------------------------------------------------------------------
+def annca_prune(q_codes, p_codes, F: int, n_f: int):
+    """Per (head, frame): ascending prompt ids sharing >= 1 bucket with a query.
+
+    q_codes: [H][T][F*n_f]; p_codes: [H][T][P].  A prompt token is kept
+    for frame f iff for some table t its code equals the table-t code of
+    at least one query of frame f.  Returns (kept_idx [H][F][P] padded
+    with -1, kept_cnt [H][F]).
+    """
+    q_codes = np.asarray(q_codes)
+    p_codes = np.asarray(p_codes)
+    H, T, _ = q_codes.shape
+    P = p_codes.shape[2]
+    kept_idx = np.full((H, F, P), -1, dtype=np.int32)
+    kept_cnt = np.zeros((H, F), dtype=np.int32)
+    for h in range(H):
+        for f in range(F):
+            keep = np.zeros(P, dtype=bool)
+            for t in range(T):
+                occ = np.unique(q_codes[h, t, f * n_f:(f + 1) * n_f])
+                keep |= np.isin(p_codes[h, t], occ)
+            ids = np.nonzero(keep)[0]
+            kept_idx[h, f, :ids.size] = ids
+            kept_cnt[h, f] = ids.size
+    return kept_idx, kept_cnt
+
+
+# --------------------------------------------------------------------------
+# steps 6-7: attention with an explicit allowed set and a logit bias
+# ([PL] section 3 attention formulation; appendix A, Lemma A.1)
+# --------------------------------------------------------------------------
+def masked_attention(q, k, v, allowed, bias, scale: float):
+    """o_i = sum_j softmax_j(scale q_i.k_j + bias_j | allowed_ij) v_j, in fp64.
+
+    q: [n][D], k, v: [M][D], allowed: [n][M] bool, bias: [M].
+    Rows with no allowed key give o = 0 and lse = -inf.
+    Returns (o [n][D], lse [n]) with lse = ln sum_j exp(logit_j).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n, D = q.shape
+    if k.shape[0] == 0:
+        return np.zeros((n, v.shape[1] if v.ndim == 2 else D)), np.full(n, -np.inf)
+    s = scale * (q @ k.T) + np.asarray(bias, dtype=np.float64)[None, :]
+    s = np.where(allowed, s, -np.inf)
+    M = np.max(s, axis=1)
+    anyk = np.isfinite(M)
+    Ms = np.where(anyk, M, 0.0)
+    w = np.where(allowed, np.exp(s - Ms[:, None]), 0.0)
+    lsum = np.sum(w, axis=1)
+    o = np.zeros((n, v.shape[1]))
+    o[anyk] = (w[anyk] @ v) / lsum[anyk, None]
+    lse = np.full(n, -np.inf)
+    lse[anyk] = Ms[anyk] + np.log(lsum[anyk])
+    return o, lse
+
+
+def annca_attention(q, k_p, v_p, kept_idx, kept_cnt, F: int, n_f: int, scale: float,
+                    rows=None):
+    """Cross-attention of frame f's queries over its kept prompt tokens.
+
+    q: [H][F*n_f][D]; k_p, v_p: [H][P][D]; kept_idx [H][F][P]; kept_cnt [H][F].
+    `rows` optionally restricts the output to these query indices (same for
+    every head).  Returns o [H][n][D] (n = F*n_f or len(rows)).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    H, Nq, D = q.shape
+    rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    o = np.zeros((H, rows.size, np.asarray(v_p).shape[2]))
+    for h in range(H):
+        for f in range(F):
+            sel = np.nonzero((rows >= f * n_f) & (rows < (f + 1) * n_f))[0]
+            if sel.size == 0:
+                continue
+            ids = np.asarray(kept_idx[h, f, :kept_cnt[h, f]], dtype=np.int64)
+            allowed = np.ones((sel.size, ids.size), dtype=bool)
+            o[h, sel], _ = masked_attention(q[h, rows[sel]], np.asarray(k_p)[h, ids],
+                                            np.asarray(v_p)[h, ids], allowed,
+                                            np.zeros(ids.size), scale)
+    return o
+
+
+def annsa_allowed(q_codes_h, cache_codes_h):
+    """allowed[i][s] = exists t: q_codes[t][i] == codes[t][s] (token-exact)."""
+    T = q_codes_h.shape[0]
+    allowed = np.zeros((q_codes_h.shape[1], cache_codes_h.shape[1]), dtype=bool)
+    for t in range(T):
+        allowed |= q_codes_h[t][:, None] == cache_codes_h[t][None, :]
+    return allowed
+
+
+def annsa_attention(q, q_codes, state: CacheState, scale: float, rows=None):
+    """Bucket-restricted self-attention of the chunk's queries over the cache.
+
+    A query may attend a live slot iff they share a code in some table
+    ([GS] 2.C; [RB] method steps, AnnSA); logit = scale q.K[s] + ln m[s]
+    (Lemma 5.1).  q: [H][Nq][D]; q_codes: [H][T][Nq].  `rows` optionally
+    restricts the computation to a subset of query indices (same for all
+    heads).  Returns (o [H][n][D], lse [H][n]).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    H, Nq, D = q.shape
+    rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    o = np.zeros((H, rows.size, D))
+    lse = np.zeros((H, rows.size))
+    for h in range(H):
+        size = int(state.size[h])
+        allowed = annsa_allowed(np.asarray(q_codes)[h][:, rows], state.codes[h, :, :size])
+        bias = np.log(state.m[h, :size].astype(np.float64))
+        o[h], lse[h] = masked_attention(q[h, rows], state.K[h, :size], state.V[h, :size],
+                                        allowed, bias, scale)
+    return o, lse

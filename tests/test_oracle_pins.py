@@ -1,0 +1,413 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle.
+
+Each test fixes one function of the oracle to something independent of its
+code: a fixture derived by hand from the pages' definitions
+(tests/golden/*.txt), a closed form (Lemma 5.1 / A.1 of FAST-AR,
+paperlayer.ai appendix A), a textbook law (random-hyperplane collision
+probability 1 - theta/pi, Charikar 2002), a library routine computing the
+same quantity by another route (scipy softmax / logsumexp, torch bf16
+rounding), or an invariant of the definition.  A plausible mistake in the
+oracle (a flipped bit order, a wrong sign of the log m bias, a missing
+count, a wrong candidate frame, a strict instead of inclusive threshold,
+dot products instead of cosines, a reversed eviction order) fails at least
+one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+from scipy.special import logsumexp, softmax
+
+import oracle as O
+from golden_io import load
+
+
+# ----------------------------------------------------------------- hashing
+def test_hash_fixture_axis_planes():
+    g = load("hash_axis_planes.txt")
+    D, T, B = int(g["D"]), int(g["T"]), int(g["B"])
+    R = np.stack([g[f"plane{i}"] for i in range(T * B)])
+    x = np.stack([g[f"x{i}"] for i in range(4)])[None]
+    codes, margin = O.hash_codes(x, R, T, B)
+    assert codes.shape == (1, T, 4)
+    np.testing.assert_array_equal(codes[0, 0], g["codes_t0"])
+    np.testing.assert_array_equal(codes[0, 1], g["codes_t1"])
+    np.testing.assert_array_equal(margin[0, 0], g["margin_t0"])
+    np.testing.assert_array_equal(margin[0, 1], g["margin_t1"])
+
+
+def test_hash_collision_law():
+    """P[code_t(x) == code_t(y)] = (1 - theta/pi)^B for random hyperplanes."""
+    rng = np.random.default_rng(7)
+    D, B, T = 32, 3, 1
+    n = 60000
+    theta = 1.0
+    x = rng.standard_normal((n, D))
+    x /= np.linalg.norm(x, axis=1, keepdims=True)
+    u = rng.standard_normal((n, D))
+    u -= (u * x).sum(1, keepdims=True) * x
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    y = math.cos(theta) * x + math.sin(theta) * u
+    # one fresh hyperplane set per block of 100 pairs keeps the estimate unbiased
+    hits = 0
+    for blk in range(n // 100):
+        R = rng.standard_normal((T * B, D))
+        sl = slice(blk * 100, (blk + 1) * 100)
+        cx, _ = O.hash_codes(x[None, sl], R, T, B)
+        cy, _ = O.hash_codes(y[None, sl], R, T, B)
+        hits += int((cx == cy).sum())
+    p = hits / n
+    expect = (1 - theta / math.pi) ** B
+    sd = math.sqrt(expect * (1 - expect) / n)
+    assert abs(p - expect) < 5 * sd + 0.01, (p, expect)
+
+
+def test_hash_sign_and_scale_invariants():
+    rng = np.random.default_rng(3)
+    H, N, D, T, B = 2, 200, 16, 3, 5
+    x = rng.standard_normal((H, N, D))
+    R = rng.standard_normal((T * B, D))
+    c, _ = O.hash_codes(x, R, T, B)
+    c2, _ = O.hash_codes(3.5 * x, R, T, B)
+    cn, _ = O.hash_codes(-x, R, T, B)
+    np.testing.assert_array_equal(c, c2)
+    np.testing.assert_array_equal(cn, (~c) & ((1 << B) - 1))
+    assert c.max() < (1 << B)
+
+
+def test_hash_margin_lists_near_zero_projections():
+    R = np.array([[1.0, 0.0], [0.0, 1.0]])
+    x = np.array([[[1.0, 1e-6], [1.0, 0.5]]])
+    c, m = O.hash_codes(x, R, 1, 2)
+    assert m[0, 0, 0] == 0b10 and m[0, 0, 1] == 0
+    assert c[0, 0, 0] == 0b11 and c[0, 0, 1] == 0b11
+
+
+# --------------------------------------------------------------------- CSR
+def test_csr_fixture():
+    g = load("csr_small.txt")
+    perm, offs = O.bucket_csr(g["codes"], int(g["nbuckets"]))
+    np.testing.assert_array_equal(perm, g["perm"])
+    np.testing.assert_array_equal(offs, g["offsets"])
+    perm, offs = O.bucket_csr(g["codes"], int(g["nbuckets"]), n=int(g["n_live"]))
+    np.testing.assert_array_equal(perm, g["perm_live"])
+    np.testing.assert_array_equal(offs, g["offsets_live"])
+
+
+def test_csr_invariants_random():
+    rng = np.random.default_rng(11)
+    codes = rng.integers(0, 64, size=(3, 2, 1000)).astype(np.uint32)
+    perm, offs = O.bucket_csr(codes, 64)
+    for g in range(3):
+        for t in range(2):
+            p, o, c = perm[g, t], offs[g, t], codes[g, t]
+            assert sorted(p.tolist()) == list(range(1000))
+            sc = c[p]
+            assert np.all(np.diff(sc.astype(np.int64)) >= 0)
+            for b in range(64):
+                ids = p[o[b]:o[b + 1]]
+                assert np.all(c[ids] == b)
+                assert np.all(np.diff(ids) > 0)
+            assert o[64] == 1000 and o[0] == 0
+
+
+# ------------------------------------------------------------- round bf16
+def test_round_storage_bf16_hand_values():
+    # spacing of bf16 in [1, 2) is 2^-7
+    cases = {1.0 + 2 ** -8: 1.0,                      # tie -> even (1.0)
+             1.0 + 3 * 2 ** -8: 1.0 + 2 ** -6,        # tie -> even mantissa
+             1.0 + 2 ** -8 + 2 ** -20: 1.0 + 2 ** -7,  # above the tie
+             -(2.0 + 2 ** -7): -2.0,                  # spacing 2^-6, tie -> even
+             3.0: 3.0, 0.0: 0.0}
+    for x, want in cases.items():
+        assert O.round_storage(np.array([x]), "bf16")[0] == want, x
+
+
+def test_round_storage_bf16_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(20000) * rng.choice([1e-3, 1.0, 50.0], 20000)).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_storage(x.astype(np.float64), "bf16"), ref)
+
+
+# --------------------------------------------------------------- TempCache
+def _fixture_frames(g):
+    frames = []
+    for f in range(4):
+        k = np.stack([g[f"f{f}_k0"], g[f"f{f}_k1"]])[None]
+        v = np.stack([g[f"f{f}_v0"], g[f"f{f}_v1"]])[None]
+        codes = np.asarray(g[f"f{f}_codes"], dtype=np.uint32).reshape(1, 1, 2)
+        frames.append((k, v, codes, g[f"f{f}_match"]))
+    return frames
+
+
+def test_tempcache_fixture_frame_by_frame():
+    g = load("tempcache_small.txt")
+    st = O.CacheState.empty(1, int(g["C"]), int(g["D"]), 1, "f64")
+    for f, (k, v, codes, want_match) in enumerate(_fixture_frames(g)):
+        st, match, listed = O.tempcache_merge(st, k, v, codes, 1, 2, f, float(g["tau"]))
+        np.testing.assert_array_equal(match[0], want_match)
+        assert not listed.any()
+    for s in range(3):
+        np.testing.assert_array_equal(st.K[0, s], g[f"K{s}"])
+        np.testing.assert_array_equal(st.V[0, s], g[f"V{s}"])
+    np.testing.assert_array_equal(st.m[0], g["m"])
+    np.testing.assert_array_equal(st.codes[0, 0], g["codes"])
+    np.testing.assert_array_equal(st.last_frame[0], g["last_frame"])
+    assert st.size[0] == g["size"] and st.inserted[0] == g["inserted"]
+    assert st.evicted[0] == g["evicted"]
+
+
+def test_tempcache_fixture_one_chunk_equals_frames():
+    """Merging the four frames as one chunk gives the same state."""
+    g = load("tempcache_small.txt")
+    fr = _fixture_frames(g)
+    k = np.concatenate([f[0] for f in fr], axis=1)
+    v = np.concatenate([f[1] for f in fr], axis=1)
+    c = np.concatenate([f[2] for f in fr], axis=2)
+    st = O.CacheState.empty(1, 3, 4, 1, "f64")
+    st, match, _ = O.tempcache_merge(st, k, v, c, 4, 2, 0, float(g["tau"]))
+    np.testing.assert_array_equal(match[0], np.concatenate([f[3] for f in fr]))
+    np.testing.assert_array_equal(st.m[0], g["m"])
+    np.testing.assert_array_equal(st.V[0, 2], g["V2"])
+
+
+def test_tempcache_eviction_ties_go_to_lowest_slot():
+    g = load("tempcache_evict_ties.txt")
+    st = O.CacheState.empty(1, 3, 6, 1, "f64")
+    e = np.eye(6)
+    z = lambda n: np.zeros((1, 1, n), np.uint32)  # noqa: E731
+    where = lambda row: np.nonzero((st.K[0] == row).all(1))[0].tolist()  # noqa: E731
+    st, _, _ = O.tempcache_merge(st, e[None, 0:3], np.ones((1, 3, 6)), z(3), 1, 3, 0, 0.9)
+    st, m1, _ = O.tempcache_merge(st, e[None, 3:4], np.ones((1, 1, 6)), z(1), 1, 1, 1, 0.9)
+    st, m2, _ = O.tempcache_merge(st, e[None, 4:6], np.ones((1, 2, 6)), z(2), 1, 2, 2, 0.9)
+    assert (m1 == -1).all() and (m2 == -1).all()
+    assert where(e[3]) == [g["slot_of_e3"]]
+    assert where(e[4]) == [g["slot_of_e4"]]
+    assert where(e[5]) == [g["slot_of_e5"]]
+    np.testing.assert_array_equal(st.last_frame[0], g["last_frame"])
+    assert st.evicted[0] == g["evicted"]
+
+
+def test_tempcache_tie_goes_to_lowest_slot_and_threshold_inclusive():
+    st = O.CacheState.empty(1, 8, 2, 1, "f64")
+    # frame 0: two identical keys in slots 0 and 1, and (3,4) in slot 2
+    k0 = np.array([[[1.0, 0.0], [1.0, 0.0], [3.0, 4.0]]])
+    st, _, _ = O.tempcache_merge(st, k0, np.ones((1, 3, 2)), np.zeros((1, 1, 3), np.uint32),
+                                 1, 3, 0, tau=2.0)          # tau > 1: no merging
+    assert st.size[0] == 3
+    # frame 1: (5,0) ties slots 0 and 1 at cos 1 -> slot 0;
+    #          (0,1) has cos 4/5 = 0.8 with slot 2 -> matched at tau = 0.8
+    k1 = np.array([[[5.0, 0.0], [0.0, 1.0]]])
+    _, match, _ = O.tempcache_merge(st, k1, np.ones((1, 2, 2)), np.zeros((1, 1, 2), np.uint32),
+                                    1, 2, 1, tau=0.8)
+    np.testing.assert_array_equal(match[0], [0, 2])
+    _, match, _ = O.tempcache_merge(st, k1, np.ones((1, 2, 2)), np.zeros((1, 1, 2), np.uint32),
+                                    1, 2, 1, tau=0.8000001)
+    np.testing.assert_array_equal(match[0], [0, -1])
+
+
+def test_tempcache_uses_cosine_not_dot():
+    st = O.CacheState.empty(1, 8, 2, 1, "f64")
+    # slot 0 is long but off-direction, slot 1 short and aligned
+    k0 = np.array([[[10.0, 10.0], [0.1, 0.0]]])
+    st, _, _ = O.tempcache_merge(st, k0, np.ones((1, 2, 2)), np.zeros((1, 1, 2), np.uint32),
+                                 1, 2, 0, tau=2.0)
+    _, match, _ = O.tempcache_merge(st, np.array([[[1.0, 0.05]]]), np.ones((1, 1, 2)),
+                                    np.zeros((1, 1, 1), np.uint32), 1, 1, 1, tau=0.9)
+    assert match[0, 0] == 1
+
+
+def test_tempcache_no_merge_above_one_is_append_history():
+    rng = np.random.default_rng(2)
+    H, n, D, F = 2, 5, 8, 3
+    st = O.CacheState.empty(H, 64, D, 2, "f64")
+    k = rng.standard_normal((H, F * n, D))
+    v = rng.standard_normal((H, F * n, D))
+    c = rng.integers(0, 8, size=(H, 2, F * n)).astype(np.uint32)
+    st, match, _ = O.tempcache_merge(st, k, v, c, F, n, 10, tau=1.5)
+    assert (match == -1).all()
+    np.testing.assert_array_equal(st.K[:, :F * n], k)
+    np.testing.assert_array_equal(st.V[:, :F * n], v)
+    np.testing.assert_array_equal(st.last_frame[:, :F * n],
+                                  np.repeat(np.arange(10, 10 + F), n)[None].repeat(H, 0))
+    assert (st.m[:, :F * n] == 1).all() and (st.size == F * n).all()
+
+
+def test_tempcache_lemma_end_to_end_closed_form():
+    """Exact-permutation frames: the merged cache reproduces dense attention.
+
+    Every new frame is an exact permutation of the previous one, so each key
+    lineage stays one group (m = number of frames) whose value is the mean of
+    its values.  By Lemma 5.1 attention over the merged cache with + ln m
+    equals dense attention over the full unmerged history.
+    """
+    rng = np.random.default_rng(9)
+    H, n, D, frames = 1, 12, 16, 5
+    base = rng.standard_normal((n, D))
+    st = O.CacheState.empty(H, 64, D, 1, "f64")
+    allk, allv = [], []
+    k = base
+    for f in range(frames):
+        if f:
+            k = k[rng.permutation(n)]
+        v = rng.standard_normal((n, D))
+        allk.append(k)
+        allv.append(v)
+        st, match, _ = O.tempcache_merge(st, k[None], v[None], np.zeros((1, 1, n), np.uint32),
+                                         1, n, f, tau=0.95)
+    assert st.size[0] == n and (st.m[0, :n] == frames).all()
+    q = rng.standard_normal((7, D))
+    qc = np.zeros((1, 1, 7), np.uint32)
+    o, lse = O.annsa_attention(q[None], qc, st, 1 / math.sqrt(D))
+    K = np.concatenate(allk)
+    V = np.concatenate(allv)
+    s = (q @ K.T) / math.sqrt(D)
+    ref = softmax(s, axis=1) @ V
+    np.testing.assert_allclose(o[0], ref, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse[0], logsumexp(s, axis=1), atol=1e-12, rtol=0)
+
+
+def test_tempcache_invariants_on_synthetic_layer():
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(C=300)            # small capacity: eviction happens
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    frames = d.past_k + [d.chunk_k[0]]
+    values = d.past_v + [d.chunk_v[0]]
+    inserted_keys = []
+    for f, (k, v) in enumerate(zip(frames, values)):
+        codes, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
+        st, match, listed = O.tempcache_merge(st, k, v, codes, 1, cfg.n_f, f, cfg.tau)
+        inserted_keys.append(np.asarray(k[0], dtype=np.float64))
+        assert st.m[0, :st.size[0]].sum() + st.evicted[0] == st.inserted[0]
+        assert st.inserted[0] == (f + 1) * cfg.n_f
+        assert (st.last_frame[0, :st.size[0]] <= f).all()
+    assert st.evicted[0] > 0 and st.size[0] == cfg.C
+    pool = {row.tobytes() for row in np.concatenate(inserted_keys)}
+    assert all(st.K[0, s].tobytes() in pool for s in range(st.size[0]))
+    codes, _ = O.hash_codes(st.K[:, :st.size[0]], d.planes, cfg.T, cfg.B)
+    np.testing.assert_array_equal(codes, st.codes[:, :, :st.size[0]])
+
+
+def test_tempcache_capacity_error():
+    st = O.CacheState.empty(1, 2, 2, 1, "f64")
+    k = np.array([[[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]]])
+    with pytest.raises(O.CapacityError):
+        O.tempcache_merge(st, k, np.ones((1, 3, 2)), np.zeros((1, 1, 3), np.uint32), 1, 3, 0, 0.9)
+
+
+# -------------------------------------------------------------------- AnnCA
+def test_annca_prune_fixture():
+    g = load("annca_prune_small.txt")
+    F, n_f = int(g["F"]), int(g["n_f"])
+    q = np.stack([g["q_t0"], g["q_t1"]])[None].astype(np.uint32)
+    p = np.stack([g["p_t0"], g["p_t1"]])[None].astype(np.uint32)
+    idx, cnt = O.annca_prune(q, p, F, n_f)
+    np.testing.assert_array_equal(cnt[0], [3, 4])
+    np.testing.assert_array_equal(idx[0, 0, :3], g["kept_f0"])
+    np.testing.assert_array_equal(idx[0, 1, :4], g["kept_f1"])
+    assert (idx[0, 0, 3:] == -1).all() and (idx[0, 1, 4:] == -1).all()
+
+
+def test_annca_prune_bruteforce_invariant():
+    rng = np.random.default_rng(4)
+    H, T, F, n_f, P, nb = 2, 3, 2, 7, 40, 16
+    q = rng.integers(0, nb, size=(H, T, F * n_f)).astype(np.uint32)
+    p = rng.integers(0, nb, size=(H, T, P)).astype(np.uint32)
+    idx, cnt = O.annca_prune(q, p, F, n_f)
+    for h in range(H):
+        for f in range(F):
+            kept = set(idx[h, f, :cnt[h, f]].tolist())
+            assert list(idx[h, f, :cnt[h, f]]) == sorted(kept)
+            for j in range(P):
+                shares = any(p[h, t, j] == q[h, t, f * n_f + i]
+                             for t in range(T) for i in range(n_f))
+                assert shares == (j in kept)
+
+
+def test_annca_attention_matches_softmax_over_kept():
+    rng = np.random.default_rng(8)
+    H, F, n_f, P, D = 2, 2, 5, 9, 8
+    q = rng.standard_normal((H, F * n_f, D))
+    kp = rng.standard_normal((H, P, D))
+    vp = rng.standard_normal((H, P, D))
+    idx = np.full((H, F, P), -1, np.int32)
+    cnt = np.zeros((H, F), np.int32)
+    lists = {(0, 0): [1, 4, 7], (0, 1): [], (1, 0): list(range(P)), (1, 1): [0, 8]}
+    for (h, f), ids in lists.items():
+        idx[h, f, :len(ids)] = ids
+        cnt[h, f] = len(ids)
+    o = O.annca_attention(q, kp, vp, idx, cnt, F, n_f, 0.3)
+    for (h, f), ids in lists.items():
+        qs = q[h, f * n_f:(f + 1) * n_f]
+        if not ids:
+            assert (o[h, f * n_f:(f + 1) * n_f] == 0).all()
+            continue
+        ref = softmax(0.3 * qs @ kp[h, ids].T, axis=1) @ vp[h, ids]
+        np.testing.assert_allclose(o[h, f * n_f:(f + 1) * n_f], ref, atol=1e-13, rtol=0)
+    rows = np.array([9, 0, 6])
+    o_rows = O.annca_attention(q, kp, vp, idx, cnt, F, n_f, 0.3, rows=rows)
+    np.testing.assert_array_equal(o_rows, o[:, rows])
+
+
+# ---------------------------------------------------------- attention math
+def test_lemma_5_1_merged_groups_equal_dense():
+    """Lemma 5.1 / A.1: g groups of identical keys == g reps, mean V, + ln m."""
+    rng = np.random.default_rng(1)
+    D, g = 16, 6
+    m = np.array([1, 3, 2, 7, 1, 4])
+    reps = rng.standard_normal((g, D))
+    K = np.repeat(reps, m, axis=0)
+    V = rng.standard_normal((m.sum(), D))
+    q = rng.standard_normal((5, D))
+    ref = softmax(0.25 * q @ K.T, axis=1) @ V
+    starts = np.concatenate([[0], np.cumsum(m)[:-1]])
+    Vbar = np.stack([V[s:s + c].mean(0) for s, c in zip(starts, m)])
+    o, lse = O.masked_attention(q, reps, Vbar, np.ones((5, g), bool), np.log(m), 0.25)
+    np.testing.assert_allclose(o, ref, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse, logsumexp(0.25 * q @ K.T, axis=1), atol=1e-12, rtol=0)
+    # m_t = 1 everywhere: standard attention
+    o1, _ = O.masked_attention(q, reps, Vbar, np.ones((5, g), bool), np.zeros(g), 0.25)
+    np.testing.assert_allclose(o1, softmax(0.25 * q @ reps.T, axis=1) @ Vbar, atol=1e-12)
+
+
+def test_masked_attention_equals_softmax_over_subset():
+    rng = np.random.default_rng(12)
+    n, M, D = 9, 30, 8
+    q, k, v = (rng.standard_normal((n, D)), rng.standard_normal((M, D)),
+               rng.standard_normal((M, D)))
+    bias = rng.standard_normal(M)
+    allowed = rng.random((n, M)) < 0.3
+    allowed[3] = False
+    o, lse = O.masked_attention(q, k, v, allowed, bias, 0.5)
+    for i in range(n):
+        ids = np.nonzero(allowed[i])[0]
+        if ids.size == 0:
+            assert (o[i] == 0).all() and lse[i] == -np.inf
+            continue
+        s = 0.5 * k[ids] @ q[i] + bias[ids]
+        np.testing.assert_allclose(o[i], softmax(s) @ v[ids], atol=1e-13, rtol=0)
+        np.testing.assert_allclose(lse[i], logsumexp(s), atol=1e-13)
+
+
+def test_annsa_allowed_fixture_and_single_bucket_dense():
+    g = load("annsa_allowed_small.txt")
+    qc = np.stack([g["q_t0"], g["q_t1"]]).astype(np.uint32)
+    kc = np.stack([g["k_t0"], g["k_t1"]]).astype(np.uint32)
+    al = O.annsa_allowed(qc, kc)
+    np.testing.assert_array_equal(al.astype(int), np.stack([g["allowed_q0"], g["allowed_q1"]]))
+    # B = 0 special case: every code is 0, AnnSA reduces to dense attention
+    rng = np.random.default_rng(13)
+    H, C, D, n = 1, 16, 8, 6
+    st = O.CacheState.empty(H, C, D, 2, "f64")
+    st.K[0, :10] = rng.standard_normal((10, D))
+    st.V[0, :10] = rng.standard_normal((10, D))
+    st.m[0, :10] = rng.integers(1, 5, 10)
+    st.size[0] = 10
+    q = rng.standard_normal((1, n, D))
+    o, lse = O.annsa_attention(q, np.zeros((1, 2, n), np.uint32), st, 0.35)
+    s = 0.35 * q[0] @ st.K[0, :10].T + np.log(st.m[0, :10])
+    np.testing.assert_allclose(o[0], softmax(s, axis=1) @ st.V[0, :10], atol=1e-13)
+    np.testing.assert_allclose(lse[0], logsumexp(s, axis=1), atol=1e-13)
