@@ -349,7 +349,7 @@ def test_annca_attention_matches_softmax_over_kept():
         np.testing.assert_allclose(o[h, f * n_f:(f + 1) * n_f], ref, atol=1e-13, rtol=0)
     rows = np.array([9, 0, 6])
     o_rows = O.annca_attention(q, kp, vp, idx, cnt, F, n_f, 0.3, rows=rows)
-    np.testing.assert_array_equal(o_rows, o[:, rows])
+    np.testing.assert_allclose(o_rows, o[:, rows], atol=1e-14, rtol=0)
 
 
 # ---------------------------------------------------------- attention math
