@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Per-chunk FAST-AR attention path on one GB300: latency, TFLOP/s, roofline.
+
+A step is one pass of the whole per-chunk path over one chunk of the
+configured workload (default: one attention layer at Wan-1.3B-like width,
+12 heads x D 128, 3 latent frames of 1560 tokens, 21 merged past frames,
+512 prompt tokens, 2 LSH tables x 8 bits):
+    hash(queries, new keys, prompt keys) -> TempCache merge (3 frames)
+    -> AnnCA prune -> AnnCA attention -> AnnSA attention.
+The merge mutates the cache, so the pre-chunk cache snapshot is restored
+before every step and L2 is flushed (a 256 MiB write) outside the timed
+window; CUDA events on the launch stream time each step and each stage.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  `--impl reference` times the fp64 oracle on the
+host cores instead (one head of the chunk per step, scaled to the chunk).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import CONFIGS, layer_data  # noqa: E402
+
+METRIC = "per-chunk FAST-AR attention ms, effective TFLOP/s, % of GB300 roofline"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    return ap.parse_args()
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            j = json.load(fh)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained", j["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc, self.path, self.gpu = None, None, gpu_index
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------- oracle leg
+def oracle_chunk_one_head(cfg, d, head: int, st_head):
+    """The oracle's whole per-chunk path for one head; returns seconds."""
+    import oracle as O
+    sl = slice(head, head + 1)
+    q, k, v = d.chunk_q[0][sl], d.chunk_k[0][sl], d.chunk_v[0][sl]
+    t0 = time.perf_counter()
+    qc, _ = O.hash_codes(q, d.planes, cfg.T, cfg.B)
+    O.bucket_csr(qc, 1 << cfg.B)
+    kc, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
+    pc, _ = O.hash_codes(d.prompt_k[sl], d.planes, cfg.T, cfg.B)
+    st, _, _ = O.tempcache_merge(st_head, k, v, kc, cfg.F, cfg.n_f, cfg.past_frames, cfg.tau)
+    O.bucket_csr(st.codes, 1 << cfg.B)
+    idx, cnt = O.annca_prune(qc, pc, cfg.F, cfg.n_f)
+    O.annca_attention(q, d.prompt_k[sl], d.prompt_v[sl], idx, cnt, cfg.F, cfg.n_f, cfg.scale)
+    O.annsa_attention(q, qc, st, cfg.scale)
+    return time.perf_counter() - t0
+
+
+def oracle_cache_one_head(cfg, d, head: int):
+    import oracle as O
+    sl = slice(head, head + 1)
+    st = O.CacheState.empty(1, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    f = 0
+    while f < cfg.past_frames:
+        nF = min(cfg.F, cfg.past_frames - f)
+        k = np.concatenate(d.past_k[f:f + nF], axis=1)[sl]
+        v = np.concatenate(d.past_v[f:f + nF], axis=1)[sl]
+        kc, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
+        st, _, _ = O.tempcache_merge(st, k, v, kc, nF, cfg.n_f, f, cfg.tau)
+        f += nF
+    return st
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, cfg):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    d = layer_data(cfg, chunks=1)
+    heads = [h % cfg.H for h in range(args.warmup + args.steps)]
+    states = {h: oracle_cache_one_head(cfg, d, h) for h in sorted(set(heads))}
+    times = []
+    for i, h in enumerate(heads):
+        t = oracle_chunk_one_head(cfg, d, h, states[h])
+        if i >= args.warmup:
+            times.append(t)
+    per_chunk_ms = statistics.mean(times) * cfg.H * 1e3
+    cores = host_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": per_chunk_ms, "unit": "ms/chunk",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": per_chunk_ms, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq,
+                       "P": cfg.P, "T": cfg.T, "B": cfg.B, "C": cfg.C},
+            "cpu_baseline": {"value": per_chunk_ms, "unit": "ms/chunk", "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"one head of the {cfg.H}-head chunk per step (heads in "
+                                       "turn), x H; past frames merged untimed"},
+            "e2e": {"value": per_chunk_ms, "unit": "ms/chunk", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- GPU leg
+def algorithmic(cfg, path, match, snap_size, snap_lf):
+    """Algorithmic bytes and flops of each stage of one step (see DESIGN)."""
+    import torch
+    H, D, T, Nq, P, n_f, F = cfg.H, cfg.D, cfg.T, cfg.Nq, cfg.P, cfg.n_f, cfg.F
+    e = 2 if cfg.dtype == "bf16" else 4
+    size = path.cache.size.long()
+    n_live = int(size.sum())
+    kept = int(path.kept_cnt.long().sum())
+    rows = H * (2 * Nq + P)
+    by = {}
+    by["hash"] = rows * (D * e + T * 4) + H * T * Nq * (4 + 4 + 4) + T * cfg.B * D * e
+    # merge: new k, v read; candidate K read; matched V read; K, V written for
+    # touched slots; per-slot metadata; cache CSR (codes read, perm written)
+    mt = match.view(H, F, n_f)
+    touched = 0
+    cand = []
+    prev_cnt = int(((snap_lf == cfg.past_frames - 1) & (torch.arange(cfg.C, device=snap_lf.device)[None]
+                                                         < snap_size[:, None])).sum())
+    for fi in range(F):
+        cand.append(prev_cnt)
+        m = mt[:, fi]
+        n_matched = int((m >= 0).sum())
+        n_groups = sum(int(torch.unique(m[h][m[h] >= 0]).numel()) for h in range(H))
+        t_f = n_groups + int((m < 0).sum())
+        touched += t_f
+        prev_cnt = t_f
+        by.setdefault("merge", 0)
+        by["merge"] += (2 * H * n_f * D * e + cand[-1] * D * e + n_matched * D * e
+                        + 2 * t_f * D * e + t_f * (4 * 2 + T * 4) + H * n_f * 4 * 4)
+    by["merge"] += n_live * T * (4 + 4) + H * T * ((1 << cfg.B) + 1) * 4
+    by["prune"] = H * T * (Nq + P) * 4 + H * F * P * 4
+    by["annca"] = H * Nq * D * e * 2 + kept * 2 * D * e + H * F * P * 4
+    by["annsa"] = (H * Nq * D * e * 2 + H * T * Nq * 4 + n_live * (2 * D * e + 4 + 2 * T * 4)
+                   + H * Nq * 4)
+    # flops: hash GEMM, NN GEMM, attention 4*D per allowed pair
+    fl = {"hash": 2 * rows * T * cfg.B * D,
+          "merge": sum(2 * D * n_f * c for c in cand),
+          "prune": 0,
+          "annca": 4 * D * n_f * kept}
+    pairs = 0
+    qc = path.q_codes.long()
+    for h in range(H):
+        n = int(size[h])
+        cc = path.cache.codes[h, :, :n].long()
+        for q0 in range(0, Nq, 1024):
+            allowed = torch.zeros(min(1024, Nq - q0), n, dtype=torch.bool, device=qc.device)
+            for t in range(T):
+                allowed |= qc[h, t, q0:q0 + 1024, None] == cc[t][None]
+            pairs += int(allowed.sum())
+    fl["annsa"] = 4 * D * pairs
+    return by, fl, {"n_live": n_live, "kept": kept, "allowed_pairs": pairs,
+                    "density": pairs / max(1, Nq * n_live)}
+
+
+def dense_reference_ms(cfg, d, reps=10):
+    """Dense attention of the same chunk: torch SDPA over the unmerged history."""
+    import torch
+    import torch.nn.functional as Fn
+    dt = torch.bfloat16
+    K = torch.from_numpy(np.concatenate(d.past_k + [d.chunk_k[0]], axis=1)).to("cuda", dt)
+    V = torch.from_numpy(np.concatenate(d.past_v + [d.chunk_v[0]], axis=1)).to("cuda", dt)
+    q = torch.from_numpy(d.chunk_q[0]).to("cuda", dt)
+    kp = torch.from_numpy(d.prompt_k).to("cuda", dt)
+    vp = torch.from_numpy(d.prompt_v).to("cuda", dt)
+
+    def run():
+        Fn.scaled_dot_product_attention(q[None], K[None], V[None])
+        Fn.scaled_dot_product_attention(q[None], kp[None], vp[None])
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(reps):
+        run()
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / reps
+    n_keys = K.shape[1]
+    flops = 4 * cfg.D * cfg.H * cfg.Nq * (n_keys + cfg.P)
+    return {"ms": ms, "keys": n_keys, "tflops": flops / ms / 1e9, "impl": "torch SDPA (bf16)"}
+
+
+def run_ours(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    import merged_attention_autoregressive_gb300 as fa
+    from merged_attention_autoregressive_gb300 import build as fbuild
+    from merged_attention_autoregressive_gb300.path import ChunkPath
+
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    fbuild.build()
+    fa.lib()
+    d = layer_data(cfg, chunks=1)
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", tdt)  # noqa: E731
+    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt)
+    path.planes.copy_(todev(d.planes))
+    f = 0
+    while f < cfg.past_frames:
+        nF = min(cfg.F, cfg.past_frames - f)
+        path.merge(todev(np.concatenate(d.past_k[f:f + nF], 1)),
+                   todev(np.concatenate(d.past_v[f:f + nF], 1)), f, F=nF)
+        f += nF
+    torch.cuda.synchronize()
+    snap = path.cache.snapshot()
+    q, k, v = todev(d.chunk_q[0]), todev(d.chunk_k[0]), todev(d.chunk_v[0])
+    kp, vp = todev(d.prompt_k), todev(d.prompt_v)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    first = cfg.past_frames
+    st = path.status
+    stages = ["hash", "merge", "prune", "annca", "annsa"]
+
+    def step(ev=None):
+        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
+        rec(0)
+        fa.fastar_hash(q, path.planes, cfg.T, cfg.B, path.q_codes, path.q_perm, path.q_offsets,
+                       status=st)
+        fa.fastar_hash(k, path.planes, cfg.T, cfg.B, path.k_codes, status=st)
+        fa.fastar_hash(kp, path.planes, cfg.T, cfg.B, path.p_codes, status=st)
+        rec(1)
+        fa.fastar_tempcache_merge(path.cache, k, v, path.k_codes, cfg.F, cfg.n_f, first, cfg.tau,
+                                  match_out=path.match, ws=path.ws_merge, status=st)
+        rec(2)
+        fa.fastar_annca_prune(path.q_codes, path.p_codes, cfg.F, cfg.n_f, cfg.B, path.kept_idx,
+                              path.kept_cnt, status=st)
+        rec(3)
+        fa.fastar_annca_attention(q, kp, vp, path.kept_idx, path.kept_cnt, cfg.F, cfg.n_f,
+                                  path.scale, path.o_ca, status=st)
+        rec(4)
+        fa.fastar_annsa_attention(q, path.q_codes, path.q_perm, path.q_offsets, path.cache,
+                                  path.scale, path.o_sa, path.lse, ws=path.ws_annsa, status=st)
+        rec(5)
+
+    def prep():
+        path.cache.restore(snap)
+        flush.fill_(1)
+
+    for _ in range(max(3, args.warmup)):
+        prep()
+        step()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = Clocks(local)
+    n0 = fa.fastar_launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        prep()
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    launches = fa.fastar_launch_count() - n0
+    assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))
+    step_ms = [e[0].elapsed_time(e[5]) for e in evs]
+    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs)
+                for j, s in enumerate(stages)}
+    ms = statistics.mean(step_ms)
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = total_ms / (args.steps * world)
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    hkp, hvp = kp.cpu().pin_memory(), vp.cpu().pin_memory()
+    ho_ca, ho_sa = torch.empty_like(path.o_ca, device="cpu").pin_memory(), \
+        torch.empty_like(path.o_sa, device="cpu").pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hkp, hvp))
+    d2h = ho_ca.numel() * ho_ca.element_size() + ho_sa.numel() * ho_sa.element_size()
+    e2e = []
+    for i in range(args.steps + 3):
+        prep()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for dst, src in ((q, hq), (k, hk), (v, hv), (kp, hkp), (vp, hvp)):
+            dst.copy_(src, non_blocking=True)
+        step()
+        ho_ca.copy_(path.o_ca, non_blocking=True)
+        ho_sa.copy_(path.o_sa, non_blocking=True)
+        s1.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e.append(s0.elapsed_time(s1))
+    e2e_ms = statistics.mean(e2e)
+
+    # algorithmic work of the step (from the last step's outputs)
+    by, fl, stats = algorithmic(cfg, path, path.match.clone(), snap["size"], snap["last_frame"])
+    pk = peaks()
+    dom = max(stage_ms, key=stage_ms.get)
+    if fl[dom] / (pk["bf16_tflops"] * 1e12) > by[dom] / (pk["hbm_gbs"] * 1e9):
+        bound, achieved, peak, unit = "tensor", fl[dom] / stage_ms[dom] / 1e9, pk["bf16_tflops"], "TFLOP/s"
+    else:
+        bound, achieved, peak, unit = "hbm", by[dom] / stage_ms[dom] / 1e6, pk["hbm_gbs"], "GB/s"
+    eff_tflops = sum(fl.values()) / ms / 1e9
+    line = {"metric": METRIC, "value": value, "unit": "ms/chunk", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq, "P": cfg.P,
+                       "T": cfg.T, "B": cfg.B, "C": cfg.C, "past_frames": cfg.past_frames,
+                       "l2": "flushed before every step (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "effective_tflops": eff_tflops,
+            "stages_ms": stage_ms,
+            "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": unit, "frac": achieved / peak, "traffic": None,
+                         "peak_source": pk["source"],
+                         "algorithmic_bytes": by[dom], "algorithmic_flops": fl[dom]},
+            "stage_rooflines": {s: {"GB/s": by[s] / stage_ms[s] / 1e6,
+                                    "hbm_frac": by[s] / stage_ms[s] / 1e6 / pk["hbm_gbs"],
+                                    "TFLOP/s": fl[s] / stage_ms[s] / 1e9} for s in stages},
+            "work": stats,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "wall_s_timed": t_wall,
+            "e2e": {"value": e2e_ms, "unit": "ms/chunk", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h}}
+    if not args.no_dense and rank == 0:
+        line["dense"] = dense_reference_ms(cfg, d)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        h = 0
+        st_h = oracle_cache_one_head(cfg, d, h)
+        secs = [oracle_chunk_one_head(cfg, d, h, st_h) for _ in range(2)]
+        line["cpu_baseline"] = {"value": min(secs) * cfg.H * 1e3, "unit": "ms/chunk",
+                                "cores": host_cores(), "kind": "oracle",
+                                "sample": "head 0 of the chunk (best of 2), x H heads"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+/*
+ * fastar.h -- C ABI of the FAST-AR per-chunk attention path on GB300 (sm_103a).
+ *
+ * FAST-AR ("Fast Autoregressive Video Diffusion and World Models with
+ * Temporal Cache Compression and Sparse Attention", arXiv 2602.01801) runs
+ * three training-free modules on every generated chunk of an autoregressive
+ * video diffusion model, all on one shared LSH encoding:
+ *   TempCache  merge near-duplicate cached keys across frames into groups
+ *              (newest key, count-weighted mean value, count m) and attend
+ *              with a + ln m logit bias (exact by Lemma 5.1);
+ *   AnnCA      drop prompt tokens that share no LSH bucket with a query of
+ *              the current frame, then cross-attend over the survivors;
+ *   AnnSA      self-attention of the chunk's queries over the merged cache,
+ *              each query restricted to keys sharing one of its buckets.
+ * The calls below follow that order: fastar_hash (queries, new keys, prompt
+ * keys), fastar_tempcache_merge, fastar_annca_prune, fastar_annca_attention,
+ * fastar_annsa_attention.
+ *
+ * Conventions shared by every call
+ *   - Every tensor pointer is caller-owned DEVICE memory, row-major with the
+ *     last dimension contiguous; rows of x/q/k/v are 16-byte aligned.
+ *   - The library never allocates, frees or synchronises.  Scratch memory
+ *     is the caller's workspace `ws` of at least fastar_workspace_size()
+ *     bytes (256-byte aligned); it may be NULL when that size is 0.
+ *   - Every call is asynchronous on `stream` and keeps no state between
+ *     calls, so independent calls on different streams may run at once.
+ *   - Host-detectable problems are returned as a fastar_status and nothing
+ *     is launched.  Problems found on the device are written to the
+ *     caller's `dev_status` word (int32, device memory, initialised to 0 by
+ *     the caller): the first error wins, the library never clears it, and
+ *     every later kernel that sees a non-zero status exits without writing
+ *     its outputs.  No kernel traps.
+ */
+#ifndef FASTAR_H_
+#define FASTAR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* element type of x, q, k, v, planes, the cache K/V and the outputs */
+typedef enum { FASTAR_BF16 = 0, FASTAR_F32 = 1 } fastar_dtype;
+
+typedef enum {
+  FASTAR_OK = 0,
+  FASTAR_ERR_ARG = 1,          /* null pointer, bad size, misaligned row     */
+  FASTAR_ERR_UNSUPPORTED = 2,  /* D not in {64,128}, B > 12, T*B > 64, ...   */
+  FASTAR_ERR_CUDA = 3,         /* a launch failed                            */
+  FASTAR_ERR_WORKSPACE = 4,    /* ws smaller than fastar_workspace_size()   */
+  FASTAR_ERR_CAPACITY = 16,    /* device: cache cannot take a frame's keys   */
+  FASTAR_ERR_TIMEOUT = 17,     /* device: a bounded wait ran out             */
+  FASTAR_ERR_DEVICE_ARG = 18   /* device: an index read on the device is out of range */
+} fastar_status;
+
+typedef enum {
+  FASTAR_OP_HASH = 0,
+  FASTAR_OP_MERGE = 1,
+  FASTAR_OP_PRUNE = 2,
+  FASTAR_OP_ANNCA = 3,
+  FASTAR_OP_ANNSA = 4
+} fastar_op;
+
+/* Human-readable name of a fastar_status value (static string). */
+const char* fastar_status_string(int status);
+
+/* Version of this ABI (major*10000 + minor*100 + patch). */
+int fastar_version(void);
+
+/* Number of kernels this library has launched in this process (all
+ * devices and threads; a diagnostic, e.g. to count launches per step). */
+uint64_t fastar_launch_count(void);
+
+/*
+ * Bytes of workspace a call needs.  Arguments that an op does not use are
+ * ignored.  op: FASTAR_OP_*; H heads; N rows per head (hash: N; merge:
+ * n_f, the tokens per frame; prune: P; annca: P; annsa: Nq); D head dim;
+ * T tables; B bits; C cache capacity.
+ */
+size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C);
+
+/*
+ * fastar_hash -- random-hyperplane LSH codes, optionally with bucket CSR.
+ *
+ * Passage: FAST-AR summary (paperlayer.ai) section 2, approximate nearest
+ * neighbour search (LSH with multi-table bucket probing) and section 5
+ * "ANN Attention"; FAST-AR technical summary (gist.science) 2.B (queries
+ * and prompt keys projected into one shared LSH space); FAST-AR analysis
+ * (paper.rainbus.top), technical novelty (the hash is computed once and
+ * serves all three modules).
+ *
+ *   codes[h][t][i] = sum_{b<B} [ planes[t*B+b] . x[h][i] > 0 ] << b
+ *
+ * x       [H][N][D] dt     rows to hash (queries, new keys or prompt keys)
+ * planes  [T*B][D]  dt     hyperplanes, shared by every head and every caller
+ * codes   [H][T][N] uint32 output
+ * perm    [H][T][N] int32  optional (NULL): ids 0..N-1 grouped by code,
+ *                          stable (ascending id inside a bucket)
+ * offsets [H][T][2^B+1] int32 optional, with perm: offsets[c] = number of
+ *                          ids whose code is < c
+ * Limits: D in {64, 128}; 1 <= T*B <= 64; B <= 12 when perm is requested.
+ * Products are exact in fp32 and accumulated in fp32; a bit whose
+ * projection is within fp32 rounding of 0 may take either value.
+ */
+int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D,
+                const void* planes, int T, int B, uint32_t* codes,
+                int32_t* perm, int32_t* offsets, void* ws, size_t ws_bytes,
+                int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * The merged cache of one layer: fixed capacity C per head, all buffers
+ * caller-owned device memory, allocated once.  Initialise last_frame to -1
+ * and every other buffer to 0.  Checkpointing the cache means copying
+ * these buffers.
+ *   K, V        [H][C][D] dt   representative key / mean value of a group
+ *   m           [H][C] int32   group count (multiplicity)
+ *   codes       [H][T][C] uint32 LSH codes of K
+ *   last_frame  [H][C] int32   frame that last refreshed the group, -1 empty
+ *   size        [H] int32      live slots; slots >= size are empty
+ *   inserted    [H] int64      keys ever merged in
+ *   evicted     [H] int64      sum of m over evicted groups
+ *   perm        [H][T][C] int32  CSR of the live codes (first size entries)
+ *   offsets     [H][T][2^B+1] int32
+ * Invariant: sum of m over live slots + evicted == inserted.
+ */
+typedef struct {
+  int H, D, C, T, B;
+  fastar_dtype dt;
+  void* K;
+  void* V;
+  int32_t* m;
+  uint32_t* codes;
+  int32_t* last_frame;
+  int32_t* size;
+  int64_t* inserted;
+  int64_t* evicted;
+  int32_t* perm;
+  int32_t* offsets;
+} fastar_cache;
+
+/*
+ * fastar_tempcache_merge -- merge the F frames of a chunk into the cache.
+ *
+ * Passage: FAST-AR summary (paperlayer.ai) section 5 "TempCache" (top-1
+ * ANN correspondence, recent representatives, mean values and + log m_t)
+ * and appendix A (Lemma A.1); FAST-AR technical summary (gist.science) 2.A
+ * (merging bounds the cache, so memory and latency stay constant); FAST-AR
+ * analysis (paper.rainbus.top), method steps, TempCache.
+ *
+ * Frame f = first_frame + i (i = 0..F-1) is merged after frame f-1:
+ *   1. every key k_j of frame f is matched to the live group s with
+ *      last_frame[s] == f-1 of largest cosine(k_j, K[s]) (ties: lowest s);
+ *      it joins s iff that cosine >= tau;
+ *   2. a group joined by the keys S gets m' = m + |S|,
+ *      V' = (m V + sum_{j in S} v_j) / m' (fp32, rounded to dt), and K,
+ *      codes and last_frame of the lowest j in S;
+ *   3. unmatched keys (ascending j) become groups of count 1 in the free
+ *      slots size, size+1, ... and then in evicted slots: the groups with
+ *      the smallest (last_frame, slot) among those with last_frame < f, in
+ *      ascending slot order; evicted += their m; inserted += n_f.
+ * Afterwards the CSR (perm, offsets) of the live codes is rebuilt.
+ *
+ * k_new, v_new [H][F*n_f][D] dt; codes_new [H][T][F*n_f] uint32 (from
+ * fastar_hash of k_new with the cache's planes); match_out optional
+ * [H][F*n_f] int32: the slot each key joined, or -1.
+ * Requires n_f <= C (then step 3 always finds room).
+ */
+int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
+                           const void* v_new, const uint32_t* codes_new,
+                           int F, int n_f, int32_t first_frame, float tau,
+                           int32_t* match_out, void* ws, size_t ws_bytes,
+                           int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * fastar_annca_prune -- per-frame prompt-token selection for AnnCA.
+ *
+ * Passage: FAST-AR technical summary (gist.science) 2.B AnnCA mechanism
+ * (a prompt token is kept for a frame iff it shares a bucket with at least
+ * one query of that frame); FAST-AR analysis (paper.rainbus.top), method
+ * steps, AnnCA; FAST-AR summary (paperlayer.ai) section 5 "AnnCA".
+ *
+ * q_codes [H][T][F*n_f], p_codes [H][T][P] uint32 (codes < 2^B).
+ * kept_idx [H][F][P] int32: ascending kept prompt ids of (head, frame),
+ * padded with -1; kept_cnt [H][F] int32.  Multi-table = union over tables.
+ */
+int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes,
+                       int H, int F, int n_f, int P, int T, int B,
+                       int32_t* kept_idx, int32_t* kept_cnt, void* ws,
+                       size_t ws_bytes, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * fastar_annca_attention -- cross-attention over the kept prompt tokens.
+ *
+ * Passage: FAST-AR technical summary (gist.science) 2.B; FAST-AR summary
+ * (paperlayer.ai) section 3, attention formulation (cross-attention keys are
+ * the projected prompt tokens).
+ *
+ *   out[h][i] = sum_{p in kept(h, i / n_f)} softmax_p(scale q_i.k_p) v_p
+ *   (0 when the kept set is empty)
+ *
+ * q [H][F*n_f][D], k_p, v_p [H][P][D] dt; kept_idx/kept_cnt from
+ * fastar_annca_prune (or any ascending id list); out [H][F*n_f][D] dt.
+ * fp32 accumulation.  Passing kept = 0..P-1 gives dense attention.
+ */
+int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p,
+                           const void* v_p, const int32_t* kept_idx,
+                           const int32_t* kept_cnt, int H, int F, int n_f,
+                           int P, int D, float scale, void* out, void* ws,
+                           size_t ws_bytes, int32_t* dev_status,
+                           cudaStream_t stream);
+
+/*
+ * fastar_annsa_attention -- bucket-restricted self-attention over the cache.
+ *
+ * Passage: FAST-AR technical summary (gist.science) 2.C (each query attends
+ * only keys in its own semantic bucket(s)); FAST-AR analysis
+ * (paper.rainbus.top), method steps, AnnSA; FAST-AR summary (paperlayer.ai)
+ * appendix A, Lemma A.1 (+ log m_t bias of merged groups).
+ *
+ *   allowed(i, s) <=> s < size and exists t: q_codes[t][i] == codes[t][s]
+ *   out[h][i] = sum_{allowed s} softmax_s(scale q_i.K[s] + ln m[s]) V[s]
+ *   lse[h][i] = ln sum_{allowed s} exp(scale q_i.K[s] + ln m[s])
+ *   (out = 0 and lse = -inf when nothing is allowed)
+ *
+ * q [H][Nq][D] dt; q_codes [H][T][Nq]; q_perm [H][T][Nq] and q_offsets
+ * [H][T][2^B+1] from fastar_hash of q; the cache after the chunk's merge;
+ * out [H][Nq][D] dt; lse optional [H][Nq] float.  fp32 accumulation.
+ */
+int fastar_annsa_attention(fastar_dtype dt, const void* q,
+                           const uint32_t* q_codes, const int32_t* q_perm,
+                           const int32_t* q_offsets, int Nq,
+                           const fastar_cache* cache, float scale, void* out,
+                           float* lse, void* ws, size_t ws_bytes,
+                           int32_t* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FASTAR_H_ */

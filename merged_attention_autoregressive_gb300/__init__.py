@@ -1,0 +1,203 @@
+"""Python binding of libfastar, the FAST-AR per-chunk attention library.
+
+Argument marshalling only: every function reads shapes from torch tensors,
+passes their device pointers and the current CUDA stream to the C ABI of
+include/fastar.h, and raises FastarError on a non-zero status.  All work
+runs in the library's CUDA kernels; there is no fallback.  If the library
+has not been built, loading it raises (build it with
+`python -m merged_attention_autoregressive_gb300.build`).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfastar.so")
+
+BF16, F32 = 0, 1
+OP_HASH, OP_MERGE, OP_PRUNE, OP_ANNCA, OP_ANNSA = 0, 1, 2, 3, 4
+STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "FASTAR_ERR_CUDA",
+          4: "FASTAR_ERR_WORKSPACE", 16: "FASTAR_ERR_CAPACITY", 17: "FASTAR_ERR_TIMEOUT",
+          18: "FASTAR_ERR_DEVICE_ARG"}
+EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
+           "fastar_workspace_size", "fastar_hash",
+           "fastar_tempcache_merge", "fastar_annca_prune", "fastar_annca_attention",
+           "fastar_annsa_attention"]
+
+
+class FastarError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({lib().fastar_status_string(code).decode()})")
+        self.code = code
+
+
+class CacheStruct(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int), ("D", ctypes.c_int), ("C", ctypes.c_int),
+                ("T", ctypes.c_int), ("B", ctypes.c_int), ("dt", ctypes.c_int),
+                ("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("m", ctypes.c_void_p),
+                ("codes", ctypes.c_void_p), ("last_frame", ctypes.c_void_p),
+                ("size", ctypes.c_void_p), ("inserted", ctypes.c_void_p),
+                ("evicted", ctypes.c_void_p), ("perm", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p)]
+
+
+_lib = None
+_VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+def lib() -> ctypes.CDLL:
+    """Load the in-tree libfastar.so (raises OSError when it is missing)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with "
+                          "`python -m merged_attention_autoregressive_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        L.fastar_status_string.restype = ctypes.c_char_p
+        L.fastar_status_string.argtypes = [_I]
+        L.fastar_version.restype = _I
+        L.fastar_launch_count.restype = ctypes.c_uint64
+        L.fastar_workspace_size.restype = _SZ
+        L.fastar_workspace_size.argtypes = [_I] * 7
+        L.fastar_hash.argtypes = [_I, _VP, _I, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_tempcache_merge.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
+                                             ctypes.c_int32, _F, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_annca_prune.argtypes = [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_annca_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F,
+                                             _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_annsa_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _I, ctypes.POINTER(CacheStruct),
+                                             _F, _VP, _VP, _VP, _SZ, _VP, _VP]
+        for name in EXPORTS[4:]:
+            getattr(L, name).restype = _I
+        _lib = L
+    return _lib
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise FastarError(rc, where)
+
+
+def fastar_launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().fastar_launch_count())
+
+
+def fastar_workspace_size(op: int, H: int, N: int, D: int, T: int, B: int, C: int) -> int:
+    return int(lib().fastar_workspace_size(op, H, N, D, T, B, C))
+
+
+def _ws(op, H, N, D, T, B, C, ws, device):
+    need = fastar_workspace_size(op, H, N, D, T, B, C)
+    if need == 0:
+        return None, 0
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def fastar_hash(x, planes, T, B, codes, perm=None, offsets=None, status=None, stream=None):
+    """codes [H][T][N] (and optional CSR perm/offsets) of x [H][N][D]."""
+    H, N, D = x.shape
+    _check(lib().fastar_hash(_dt(x), _p(x), H, N, D, _p(planes), T, B, _p(codes), _p(perm),
+                             _p(offsets), None, 0, _p(status), _stream(stream)), "fastar_hash")
+
+
+class Cache:
+    """Device buffers of one layer's merged cache (allocated once, torch-owned)."""
+
+    def __init__(self, H, C, D, T, B, dtype=torch.bfloat16, device="cuda"):
+        self.H, self.C, self.D, self.T, self.B, self.dtype = H, C, D, T, B, dtype
+        dev = torch.device(device)
+        self.K = torch.zeros(H, C, D, dtype=dtype, device=dev)
+        self.V = torch.zeros(H, C, D, dtype=dtype, device=dev)
+        self.m = torch.zeros(H, C, dtype=torch.int32, device=dev)
+        self.codes = torch.zeros(H, T, C, dtype=torch.int32, device=dev)
+        self.last_frame = torch.full((H, C), -1, dtype=torch.int32, device=dev)
+        self.size = torch.zeros(H, dtype=torch.int32, device=dev)
+        self.inserted = torch.zeros(H, dtype=torch.int64, device=dev)
+        self.evicted = torch.zeros(H, dtype=torch.int64, device=dev)
+        self.perm = torch.zeros(H, T, C, dtype=torch.int32, device=dev)
+        self.offsets = torch.zeros(H, T, (1 << B) + 1, dtype=torch.int32, device=dev)
+
+    BUFFERS = ("K", "V", "m", "codes", "last_frame", "size", "inserted", "evicted", "perm", "offsets")
+
+    def struct(self) -> CacheStruct:
+        return CacheStruct(self.H, self.D, self.C, self.T, self.B,
+                           BF16 if self.dtype == torch.bfloat16 else F32,
+                           *[getattr(self, n).data_ptr() for n in self.BUFFERS])
+
+    def snapshot(self) -> dict:
+        return {n: getattr(self, n).clone() for n in self.BUFFERS}
+
+    def restore(self, snap: dict):
+        for n in self.BUFFERS:
+            getattr(self, n).copy_(snap[n], non_blocking=True)
+
+    def nbytes(self) -> int:
+        return sum(getattr(self, n).numel() * getattr(self, n).element_size() for n in self.BUFFERS)
+
+
+def fastar_tempcache_merge(cache: Cache, k_new, v_new, codes_new, F, n_f, first_frame, tau,
+                           match_out=None, ws=None, status=None, stream=None):
+    """Merge the F frames of a chunk (k_new/v_new [H][F*n_f][D]) into `cache`."""
+    ws, nbytes = _ws(OP_MERGE, cache.H, n_f, cache.D, cache.T, cache.B, cache.C, ws, k_new.device)
+    cs = cache.struct()
+    _check(lib().fastar_tempcache_merge(ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F,
+                                        n_f, first_frame, tau, _p(match_out), _p(ws), nbytes,
+                                        _p(status), _stream(stream)), "fastar_tempcache_merge")
+
+
+def fastar_annca_prune(q_codes, p_codes, F, n_f, B, kept_idx, kept_cnt, status=None, stream=None):
+    """kept_idx [H][F][P] / kept_cnt [H][F] of the prompt tokens per frame."""
+    H, T, _ = q_codes.shape
+    P = p_codes.shape[2]
+    _check(lib().fastar_annca_prune(_p(q_codes), _p(p_codes), H, F, n_f, P, T, B, _p(kept_idx),
+                                    _p(kept_cnt), None, 0, _p(status), _stream(stream)),
+           "fastar_annca_prune")
+
+
+def fastar_annca_attention(q, k_p, v_p, kept_idx, kept_cnt, F, n_f, scale, out, status=None,
+                           stream=None):
+    """out [H][F*n_f][D]: cross-attention of each frame over its kept tokens."""
+    H, Nq, D = q.shape
+    P = k_p.shape[1]
+    _check(lib().fastar_annca_attention(_dt(q), _p(q), _p(k_p), _p(v_p), _p(kept_idx),
+                                        _p(kept_cnt), H, F, n_f, P, D, scale, _p(out), None, 0,
+                                        _p(status), _stream(stream)), "fastar_annca_attention")
+
+
+def fastar_annsa_attention(q, q_codes, q_perm, q_offsets, cache: Cache, scale, out, lse=None,
+                           ws=None, status=None, stream=None):
+    """out [H][Nq][D] (and lse [H][Nq]): bucket-restricted attention over `cache`."""
+    H, Nq, D = q.shape
+    ws, nbytes = _ws(OP_ANNSA, cache.H, Nq, cache.D, cache.T, cache.B, cache.C, ws, q.device)
+    cs = cache.struct()
+    _check(lib().fastar_annsa_attention(_dt(q), _p(q), _p(q_codes), _p(q_perm), _p(q_offsets), Nq,
+                                        ctypes.byref(cs), scale, _p(out), _p(lse), _p(ws), nbytes,
+                                        _p(status), _stream(stream)), "fastar_annsa_attention")

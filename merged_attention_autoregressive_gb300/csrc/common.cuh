@@ -1,0 +1,156 @@
+// Shared device helpers of the FAST-AR kernels: element access for bf16/fp32,
+// the sticky device status word, warp/block scans.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fastar.h"
+
+namespace fastar {
+
+constexpr int kMaxTB = 64;      // T*B hyperplanes per hash call
+constexpr int kMaxCsrBits = 12; // bucket CSR supports up to 4096 buckets
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static __device__ __forceinline__ float ld(const float* p) { return *p; }
+  static __device__ __forceinline__ void st(float* p, float v) { *p = v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float ld(const __nv_bfloat16* p) {
+    return __bfloat162float(*p);
+  }
+  static __device__ __forceinline__ void st(__nv_bfloat16* p, float v) {
+    *p = __float2bfloat16_rn(v);
+  }
+};
+
+// ---- sticky device status: first error wins, kernels exit once it is set
+__device__ __forceinline__ bool status_bad(const int32_t* st) {
+  return st != nullptr && *((volatile const int32_t*)st) != 0;
+}
+__device__ __forceinline__ void status_set(int32_t* st, int32_t code) {
+  if (st) atomicCAS(st, 0, code);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
+// Exclusive scan over the block (blockDim.x a multiple of 32, <= 1024).
+// `sh` holds at least 33 ints.  Returns the exclusive prefix; *total gets
+// the block sum.  Every thread must call it.
+__device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  int inc = warp_incl_scan(v);
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? sh[lane] : 0;
+    int wi = warp_incl_scan(w);
+    if (lane < nw) sh[lane] = wi - w;
+    if (lane == nw - 1) sh[32] = wi;
+  }
+  __syncthreads();
+  int res = sh[warp] + inc - v;
+  if (total) *total = sh[32];
+  __syncthreads();
+  return res;
+}
+
+__device__ __forceinline__ int block_min_int(int v, int* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? sh[lane] : 0x7fffffff;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w = min(w, __shfl_xor_sync(0xffffffffu, w, o));
+    if (lane == 0) sh[32] = w;
+  }
+  __syncthreads();
+  int r = sh[32];
+  __syncthreads();
+  return r;
+}
+
+__device__ __forceinline__ long long block_sum_ll(long long v, long long* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nw ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+    if (lane == 0) sh[32] = w;
+  }
+  __syncthreads();
+  long long r = sh[32];
+  __syncthreads();
+  return r;
+}
+
+}  // namespace fastar
+
+// ---- host-side launch helpers (declared here, defined per .cu file)
+namespace fastar {
+int launch_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes,
+                int T, int B, uint32_t* codes, int32_t* st, cudaStream_t s);
+int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_div, int nb,
+               int32_t* perm, int32_t* offsets, int32_t* st, cudaStream_t s);
+int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
+                 const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                 int32_t* match_out, void* ws, int32_t* st, cudaStream_t s);
+size_t merge_ws_bytes(int H, int n_f, int C);
+int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,
+                 int P, int T, int B, int32_t* kept_idx, int32_t* kept_cnt, int32_t* st,
+                 cudaStream_t s);
+int launch_annca(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
+                 const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f,
+                 int P, int D, float scale, void* out, int32_t* st, cudaStream_t s);
+int launch_annsa(fastar_dtype dt, const void* q, const uint32_t* q_codes,
+                 const int32_t* q_perm, const int32_t* q_offsets, int Nq,
+                 const fastar_cache* c, float scale, void* out, float* lse, void* ws,
+                 int32_t* st, cudaStream_t s);
+size_t annsa_ws_bytes(int H, int Nq, int D, int T);
+}  // namespace fastar
+
+namespace fastar {
+void count_launch();
+}
+
+#define FASTAR_LAUNCH_CHECK()                                   \
+  do {                                                          \
+    fastar::count_launch();                                     \
+    if (cudaPeekAtLastError() != cudaSuccess) {                 \
+      (void)cudaGetLastError();                                 \
+      return FASTAR_ERR_CUDA;                                   \
+    }                                                           \
+  } while (0)

@@ -1,0 +1,187 @@
+// C ABI of the FAST-AR per-chunk attention path: argument checks, workspace
+// sizing and dispatch to the kernels.  Nothing here allocates, frees or
+// synchronises; every launch goes to the caller's stream.
+#include <string.h>
+
+#include <atomic>
+
+#include "common.cuh"
+
+namespace fastar {
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+int launch_hash_simt(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes,
+                     int T, int B, uint32_t* codes, int32_t* st, cudaStream_t s);
+int launch_hash_tc(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes,
+                   int T, int B, uint32_t* codes, int32_t* st, cudaStream_t s);
+int launch_annca_simt(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
+                      const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P,
+                      int D, float scale, void* out, int32_t* st, cudaStream_t s);
+int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
+                    const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P,
+                    int D, float scale, void* out, int32_t* st, cudaStream_t s);
+int launch_annsa_simt(fastar_dtype dt, const void* q, const uint32_t* q_codes, int Nq,
+                      const fastar_cache* c, float scale, void* out, float* lse, int32_t* st,
+                      cudaStream_t s);
+int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
+                    const int32_t* q_offsets, int Nq, const fastar_cache* c, float scale, void* out,
+                    float* lse, void* ws, int32_t* st, cudaStream_t s);
+size_t annsa_tc_ws_bytes(int H, int Nq, int D, int T);
+
+int launch_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes, int T,
+                int B, uint32_t* codes, int32_t* st, cudaStream_t s) {
+  int rc = launch_hash_tc(dt, x, H, N, D, planes, T, B, codes, st, s);
+  if (rc != FASTAR_ERR_UNSUPPORTED) return rc;
+  return launch_hash_simt(dt, x, H, N, D, planes, T, B, codes, st, s);
+}
+
+int launch_annca(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
+                 const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P,
+                 int D, float scale, void* out, int32_t* st, cudaStream_t s) {
+  int rc = launch_annca_tc(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, st, s);
+  if (rc != FASTAR_ERR_UNSUPPORTED) return rc;
+  return launch_annca_simt(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, st, s);
+}
+
+int launch_annsa(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
+                 const int32_t* q_offsets, int Nq, const fastar_cache* c, float scale, void* out,
+                 float* lse, void* ws, int32_t* st, cudaStream_t s) {
+  int rc = launch_annsa_tc(dt, q, q_codes, q_perm, q_offsets, Nq, c, scale, out, lse, ws, st, s);
+  if (rc != FASTAR_ERR_UNSUPPORTED) return rc;
+  return launch_annsa_simt(dt, q, q_codes, Nq, c, scale, out, lse, st, s);
+}
+
+size_t annsa_ws_bytes(int H, int Nq, int D, int T) { return annsa_tc_ws_bytes(H, Nq, D, T); }
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+static bool dtype_ok(int dt) { return dt == FASTAR_BF16 || dt == FASTAR_F32; }
+static bool dim_ok(int D) { return D == 64 || D == 128; }
+
+}  // namespace fastar
+
+using namespace fastar;
+
+extern "C" {
+
+const char* fastar_status_string(int status) {
+  switch (status) {
+    case FASTAR_OK: return "ok";
+    case FASTAR_ERR_ARG: return "invalid argument";
+    case FASTAR_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case FASTAR_ERR_CUDA: return "CUDA launch error";
+    case FASTAR_ERR_WORKSPACE: return "workspace too small";
+    case FASTAR_ERR_CAPACITY: return "cache capacity exhausted (device)";
+    case FASTAR_ERR_TIMEOUT: return "bounded device wait expired (device)";
+    case FASTAR_ERR_DEVICE_ARG: return "out-of-range index found on the device";
+    default: return "unknown status";
+  }
+}
+
+int fastar_version(void) { return 100; }
+
+uint64_t fastar_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C) {
+  (void)B;
+  if (H < 0 || N < 0 || C < 0) return 0;
+  switch (op) {
+    case FASTAR_OP_MERGE: return merge_ws_bytes(H, N, C);
+    case FASTAR_OP_ANNSA: return annsa_ws_bytes(H, N, D, T);
+    default: return 0;
+  }
+}
+
+int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes, int T,
+                int B, uint32_t* codes, int32_t* perm, int32_t* offsets, void* ws, size_t ws_bytes,
+                int32_t* dev_status, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
+  if (H < 0 || N < 0 || T < 1 || B < 1 || T > 8) return FASTAR_ERR_ARG;
+  if (!dim_ok(D) || T * B > kMaxTB) return FASTAR_ERR_UNSUPPORTED;
+  if ((perm == nullptr) != (offsets == nullptr)) return FASTAR_ERR_ARG;
+  if (perm && B > kMaxCsrBits) return FASTAR_ERR_UNSUPPORTED;
+  if ((size_t)H * N == 0) return FASTAR_OK;
+  if (!x || !planes || !codes || !aligned16(x) || !aligned16(planes)) return FASTAR_ERR_ARG;
+  int rc = launch_hash(dt, x, H, N, D, planes, T, B, codes, dev_status, stream);
+  if (rc != FASTAR_OK || !perm) return rc;
+  return launch_csr(codes, H * T, N, nullptr, 1, 1 << B, perm, offsets, dev_status, stream);
+}
+
+static int check_cache(const fastar_cache* c) {
+  if (!c) return FASTAR_ERR_ARG;
+  if (!dtype_ok(c->dt)) return FASTAR_ERR_UNSUPPORTED;
+  if (c->H < 0 || c->C < 1 || c->T < 1 || c->T > 8 || c->B < 1) return FASTAR_ERR_ARG;
+  if (!dim_ok(c->D) || c->B > kMaxCsrBits) return FASTAR_ERR_UNSUPPORTED;
+  if (!c->K || !c->V || !c->m || !c->codes || !c->last_frame || !c->size || !c->inserted ||
+      !c->evicted || !c->perm || !c->offsets)
+    return FASTAR_ERR_ARG;
+  if (!aligned16(c->K) || !aligned16(c->V)) return FASTAR_ERR_ARG;
+  return FASTAR_OK;
+}
+
+int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const void* v_new,
+                           const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                           int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                           cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc != FASTAR_OK) return rc;
+  if (F < 0 || n_f < 0 || n_f > cache->C) return FASTAR_ERR_ARG;
+  if (F == 0 || n_f == 0 || cache->H == 0) return FASTAR_OK;
+  if (!k_new || !v_new || !codes_new || !aligned16(k_new) || !aligned16(v_new)) return FASTAR_ERR_ARG;
+  if (first_frame < 0 || (int64_t)first_frame + F > 0x7fffff00) return FASTAR_ERR_ARG;
+  if (tau != tau) return FASTAR_ERR_ARG;
+  const size_t need = merge_ws_bytes(cache->H, n_f, cache->C);
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
+  return launch_merge(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws,
+                      dev_status, stream);
+}
+
+int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,
+                       int P, int T, int B, int32_t* kept_idx, int32_t* kept_cnt, void* ws,
+                       size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (H < 0 || F < 0 || n_f < 0 || P < 0 || T < 1 || T > 8 || B < 1) return FASTAR_ERR_ARG;
+  if (B > 16) return FASTAR_ERR_UNSUPPORTED;
+  if (H == 0 || F == 0) return FASTAR_OK;
+  if (!kept_cnt || (P > 0 && !kept_idx) || (n_f > 0 && !q_codes) || (P > 0 && !p_codes))
+    return FASTAR_ERR_ARG;
+  return launch_prune(q_codes, p_codes, H, F, n_f, P, T, B, kept_idx, kept_cnt, dev_status, stream);
+}
+
+int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
+                           const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f,
+                           int P, int D, float scale, void* out, void* ws, size_t ws_bytes,
+                           int32_t* dev_status, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
+  if (H < 0 || F < 0 || n_f < 0 || P < 0) return FASTAR_ERR_ARG;
+  if (!dim_ok(D)) return FASTAR_ERR_UNSUPPORTED;
+  if ((size_t)H * F * n_f == 0) return FASTAR_OK;
+  if (!q || !out || !kept_cnt || !aligned16(q) || !aligned16(out)) return FASTAR_ERR_ARG;
+  if (P > 0 && (!k_p || !v_p || !kept_idx || !aligned16(k_p) || !aligned16(v_p))) return FASTAR_ERR_ARG;
+  return launch_annca(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, dev_status,
+                      stream);
+}
+
+int fastar_annsa_attention(fastar_dtype dt, const void* q, const uint32_t* q_codes,
+                           const int32_t* q_perm, const int32_t* q_offsets, int Nq,
+                           const fastar_cache* cache, float scale, void* out, float* lse, void* ws,
+                           size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc != FASTAR_OK) return rc;
+  if (dt != cache->dt) return FASTAR_ERR_ARG;
+  if (Nq < 0) return FASTAR_ERR_ARG;
+  if (Nq == 0 || cache->H == 0) return FASTAR_OK;
+  if (!q || !q_codes || !q_perm || !q_offsets || !out || !aligned16(q) || !aligned16(out))
+    return FASTAR_ERR_ARG;
+  const size_t need = annsa_ws_bytes(cache->H, Nq, cache->D, cache->T);
+  if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255))) return FASTAR_ERR_WORKSPACE;
+  return launch_annsa(dt, q, q_codes, q_perm, q_offsets, Nq, cache, scale, out, lse, ws,
+                      dev_status, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,446 @@
+// TempCache: merge the frames of a chunk into the fixed-capacity cache.
+//
+// FAST-AR summary (paperlayer.ai) section 5 "TempCache" and appendix A,
+// Lemma A.1; gist.science technical summary 2.A; paper.rainbus.top method
+// steps, TempCache.  For each frame f of the chunk, in order:
+//   nn     each new key is matched to the group refreshed in frame f-1 of
+//          largest cosine (ties: lowest slot); it joins iff cosine >= tau;
+//   plan   one CTA per head groups the matches (lowest index = new
+//          representative), ranks the unmatched keys and assigns them free
+//          slots, then evicted slots (smallest (last_frame, slot) among the
+//          groups not refreshed in frame f); updates size / inserted /
+//          evicted and writes the next frame's candidate list;
+//   apply  one warp per key writes K, V (count-weighted mean, fp32, rounded
+//          to the storage type), m, codes and last_frame.
+// The candidates of frame f are exactly the groups that frame f-1 refreshed,
+// so each plan writes the candidate list of the next frame; the first frame
+// of a call compacts the slots with last_frame == first_frame - 1.
+//
+// Workspace (caller-owned, no initialisation needed):
+//   cand[2][H][C], ncand[2][H], rep_j[H][C], gcnt[H][C],
+//   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], evict[H][n_f]
+// rep_j/gcnt are indexed by slot and reset for the candidate slots of each
+// frame before use (only candidates can be matched).
+#include <math.h>
+
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace fastar {
+
+constexpr int kPlanThreads = 1024;
+enum : int { KIND_MEMBER = 0, KIND_LEADER = 1, KIND_INSERT = 2 };
+
+struct MergeWs {
+  int32_t* cand[2];
+  int32_t* ncand[2];
+  int32_t* rep_j;
+  int32_t* gcnt;
+  int32_t* match;
+  int32_t* plan_slot;
+  int32_t* plan_kind;
+  int32_t* evict;
+};
+
+static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t merge_ws_bytes(int H, int n_f, int C) {
+  size_t b = 0;
+  b += 2 * align256((size_t)H * C * 4);   // cand
+  b += 2 * align256((size_t)H * 4);       // ncand
+  b += 2 * align256((size_t)H * C * 4);   // rep_j, gcnt
+  b += 4 * align256((size_t)H * n_f * 4); // match, plan_slot, plan_kind, evict
+  return b;
+}
+
+static MergeWs carve(void* ws, int H, int n_f, int C) {
+  char* p = (char*)ws;
+  MergeWs w;
+  auto take = [&](size_t bytes) { char* r = p; p += align256(bytes); return (int32_t*)r; };
+  w.cand[0] = take((size_t)H * C * 4);
+  w.cand[1] = take((size_t)H * C * 4);
+  w.ncand[0] = take((size_t)H * 4);
+  w.ncand[1] = take((size_t)H * 4);
+  w.rep_j = take((size_t)H * C * 4);
+  w.gcnt = take((size_t)H * C * 4);
+  w.match = take((size_t)H * n_f * 4);
+  w.plan_slot = take((size_t)H * n_f * 4);
+  w.plan_kind = take((size_t)H * n_f * 4);
+  w.evict = take((size_t)H * n_f * 4);
+  return w;
+}
+
+// ---------------------------------------------------------------- cand init
+__global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* __restrict__ last_frame,
+                                                                 const int32_t* __restrict__ size, int C,
+                                                                 int32_t prev_frame, int32_t* cand,
+                                                                 int32_t* ncand, int32_t* st) {
+  __shared__ int sh[33];
+  if (status_bad(st)) return;
+  const int h = blockIdx.x;
+  const int n = min(max(size[h], 0), C);
+  const int32_t* lf = last_frame + (size_t)h * C;
+  int32_t* out = cand + (size_t)h * C;
+  int base = 0;
+  for (int s0 = 0; s0 < n; s0 += blockDim.x) {
+    const int s = s0 + threadIdx.x;
+    const int hit = (s < n && lf[s] == prev_frame) ? 1 : 0;
+    int tot;
+    const int pos = block_excl_scan(hit, sh, &tot);
+    if (hit) out[base + pos] = s;
+    base += tot;
+  }
+  if (threadIdx.x == 0) ncand[h] = base;
+}
+
+// ---------------------------------------------------------------- NN (SIMT)
+template <typename T, int D>
+__global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_frame, int n_f, int row_stride_keys,
+                                                      const T* __restrict__ K, int C,
+                                                      const int32_t* __restrict__ cand,
+                                                      const int32_t* __restrict__ ncand, float tau,
+                                                      int32_t* __restrict__ match, int32_t* match_out,
+                                                      int match_out_stride, int32_t* st) {
+  constexpr int PER = D / 32;
+  if (status_bad(st)) return;
+  const int h = blockIdx.y;
+  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= n_f) return;
+  const T* kj = k_frame + ((size_t)h * row_stride_keys + j) * D;
+  float kv[PER];
+  float nk = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    kv[i] = Elem<T>::ld(kj + lane + 32 * i);
+    nk = fmaf(kv[i], kv[i], nk);
+  }
+  nk = warp_sum(nk);
+  const int nc = ncand[h];
+  const int32_t* ch = cand + (size_t)h * C;
+  float best = -INFINITY;
+  int best_slot = 0x7fffffff;
+  if (nk > 0.f) {
+    const float sk = sqrtf(nk);
+    for (int c = 0; c < nc; ++c) {
+      const int s = ch[c];
+      const T* ks = K + ((size_t)h * C + s) * D;
+      float dot = 0.f, nn = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const float v = Elem<T>::ld(ks + lane + 32 * i);
+        dot = fmaf(kv[i], v, dot);
+        nn = fmaf(v, v, nn);
+      }
+      dot = warp_sum(dot);
+      nn = warp_sum(nn);
+      if (nn > 0.f) {
+        const float cs = dot / (sk * sqrtf(nn));
+        if (cs > best || (cs == best && s < best_slot)) {
+          best = cs;
+          best_slot = s;
+        }
+      }
+    }
+  }
+  if (lane == 0) {
+    const int m = (best >= tau) ? best_slot : -1;
+    match[(size_t)h * n_f + j] = m;
+    if (match_out) match_out[(size_t)h * match_out_stride + j] = m;
+  }
+}
+
+// ---------------------------------------------------------------- plan
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int32_t f,
+                                                            const int32_t* __restrict__ match,
+                                                            const int32_t* __restrict__ cand_cur,
+                                                            const int32_t* __restrict__ ncand_cur,
+                                                            int32_t* __restrict__ cand_next,
+                                                            int32_t* __restrict__ ncand_next,
+                                                            int32_t* rep_j, int32_t* gcnt,
+                                                            int32_t* __restrict__ plan_slot,
+                                                            int32_t* __restrict__ plan_kind,
+                                                            int32_t* __restrict__ evict,
+                                                            const int32_t* __restrict__ last_frame,
+                                                            const int32_t* __restrict__ m,
+                                                            int32_t* size, int64_t* inserted,
+                                                            int64_t* evicted, int32_t* st) {
+  __shared__ int sh[33];
+  __shared__ long long shl[33];
+  __shared__ int hist[2048];
+  __shared__ int s_lstar, s_nlt, s_found;
+  if (status_bad(st)) return;
+  const int h = blockIdx.x;
+  const int32_t* mt = match + (size_t)h * n_f;
+  const int32_t* cc = cand_cur + (size_t)h * C;
+  int32_t* rj = rep_j + (size_t)h * C;
+  int32_t* gc = gcnt + (size_t)h * C;
+  const int32_t* lf = last_frame + (size_t)h * C;
+  const int nc = ncand_cur[h];
+  // 1. reset the group accumulators of the candidate slots
+  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
+    const int s = cc[c];
+    rj[s] = 0x7fffffff;
+    gc[s] = 0;
+  }
+  __syncthreads();
+  // 2. group the matched keys: count and lowest index per slot
+  for (int j = threadIdx.x; j < n_f; j += blockDim.x) {
+    const int s = mt[j];
+    if (s >= 0) {
+      atomicMin(&rj[s], j);
+      atomicAdd(&gc[s], 1);
+    }
+  }
+  __syncthreads();
+  // 3. unmatched keys: count
+  int U = 0;
+  {
+    int loc = 0;
+    for (int j = threadIdx.x; j < n_f; j += blockDim.x) loc += (mt[j] < 0);
+    int tot;
+    block_excl_scan(loc, sh, &tot);
+    U = tot;
+  }
+  const int size0 = min(max(size[h], 0), C);
+  const int freeslots = C - size0;
+  const int n_app = min(freeslots, U);
+  const int E = U - n_app;
+  // 4. eviction: the E smallest (last_frame, slot) among slots with
+  //    last_frame < f that no key of this frame joined
+  if (E > 0) {
+    // eligible: lf < f, and not a slot matched now (only lf == f-1 can be)
+    auto eligible = [&](int s) -> bool {
+      const int l = lf[s];
+      if (l >= f) return false;
+      if (l == f - 1 && gc[s] > 0) return false;
+      return true;
+    };
+    int lo = 0x7fffffff;
+    for (int s = threadIdx.x; s < size0; s += blockDim.x)
+      if (eligible(s)) lo = min(lo, lf[s]);
+    lo = block_min_int(lo, sh);
+    if (threadIdx.x == 0) s_found = 0;
+    __syncthreads();
+    long long below = 0;
+    for (long long base = lo; base < (long long)f && lo != 0x7fffffff; base += 2048) {
+      for (int i = threadIdx.x; i < 2048; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      for (int s = threadIdx.x; s < size0; s += blockDim.x) {
+        if (!eligible(s)) continue;
+        const long long d = (long long)lf[s] - base;
+        if (d >= 0 && d < 2048) atomicAdd(&hist[(int)d], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        long long cum = below;
+        for (int b = 0; b < 2048; ++b) {
+          if (cum + hist[b] >= E) {
+            s_lstar = (int)(base + b);
+            s_nlt = (int)cum;
+            s_found = 1;
+            break;
+          }
+          cum += hist[b];
+        }
+        if (!s_found) s_nlt = (int)cum;
+      }
+      __syncthreads();
+      if (s_found) break;
+      below = s_nlt;
+      __syncthreads();
+    }
+    if (!s_found) {
+      if (threadIdx.x == 0) status_set(st, FASTAR_ERR_CAPACITY);
+      return;
+    }
+    const int lstar = s_lstar, eq_take = E - s_nlt;
+    // ordered selection over slots: chunk of consecutive slots per thread
+    const int per = (size0 + blockDim.x - 1) / blockDim.x;
+    const int s0 = min(size0, (int)threadIdx.x * per), s1 = min(size0, s0 + per);
+    int nlt = 0, neq = 0;
+    for (int s = s0; s < s1; ++s) {
+      if (!eligible(s)) continue;
+      nlt += lf[s] < lstar;
+      neq += lf[s] == lstar;
+    }
+    int tlt, teq;
+    int lt_before = block_excl_scan(nlt, sh, &tlt);
+    int eq_before = block_excl_scan(neq, sh, &teq);
+    int32_t* ev = evict + (size_t)h * n_f;
+    for (int s = s0; s < s1; ++s) {
+      if (!eligible(s)) continue;
+      const int l = lf[s];
+      if (l < lstar) {
+        ev[lt_before + min(eq_before, eq_take)] = s;
+        ++lt_before;
+      } else if (l == lstar) {
+        if (eq_before < eq_take) ev[lt_before + eq_before] = s;
+        ++eq_before;
+      }
+    }
+    __syncthreads();
+    // evicted += sum of m over the evicted groups
+    long long em = 0;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) em += m[(size_t)h * C + ev[e]];
+    em = block_sum_ll(em, shl);
+    if (threadIdx.x == 0) evicted[h] += em;
+  }
+  // 5. per-key plan (ascending j), and the next frame's candidate list
+  const int32_t* ev = evict + (size_t)h * n_f;
+  int urank_base = 0, cand_base = 0;
+  for (int j0 = 0; j0 < n_f; j0 += blockDim.x) {
+    const int j = j0 + threadIdx.x;
+    const bool in = j < n_f;
+    const int s = in ? mt[j] : 0;
+    const int unm = (in && s < 0) ? 1 : 0;
+    int utot;
+    const int ur = block_excl_scan(unm, sh, &utot) + urank_base;
+    int kind = KIND_MEMBER, slot = -1;
+    if (in) {
+      if (s >= 0) {
+        slot = s;
+        kind = (rj[s] == j) ? KIND_LEADER : KIND_MEMBER;
+      } else {
+        slot = ur < n_app ? size0 + ur : ev[ur - n_app];
+        kind = KIND_INSERT;
+      }
+      plan_slot[(size_t)h * n_f + j] = slot;
+      plan_kind[(size_t)h * n_f + j] = kind;
+    }
+    const int isc = (in && kind != KIND_MEMBER) ? 1 : 0;
+    int ctot;
+    const int cp = block_excl_scan(isc, sh, &ctot) + cand_base;
+    if (isc) cand_next[(size_t)h * C + cp] = slot;
+    urank_base += utot;
+    cand_base += ctot;
+  }
+  if (threadIdx.x == 0) {
+    ncand_next[h] = cand_base;
+    size[h] = size0 + n_app;
+    inserted[h] += n_f;
+  }
+}
+
+// ---------------------------------------------------------------- apply
+template <typename T, int D>
+__global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
+                                                    const uint32_t* __restrict__ codes_frame, int n_f,
+                                                    int row_stride_keys, int Tt, int32_t f,
+                                                    const int32_t* __restrict__ match,
+                                                    const int32_t* __restrict__ plan_slot,
+                                                    const int32_t* __restrict__ plan_kind,
+                                                    const int32_t* __restrict__ gcnt, T* K, T* V,
+                                                    int32_t* m, uint32_t* codes, int32_t* last_frame,
+                                                    int C, int32_t* st) {
+  constexpr int PER = D / 32;
+  if (status_bad(st)) return;
+  const int h = blockIdx.y;
+  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (j >= n_f) return;
+  const int kind = plan_kind[(size_t)h * n_f + j];
+  if (kind == KIND_MEMBER) return;
+  const int s = plan_slot[(size_t)h * n_f + j];
+  const size_t krow = ((size_t)h * row_stride_keys + j) * D;
+  const size_t crow = ((size_t)h * C + s) * D;
+  int m_new = 1;
+  if (kind == KIND_LEADER) {
+    const int cnt = gcnt[(size_t)h * C + s];
+    const int m_old = m[(size_t)h * C + s];
+    m_new = m_old + cnt;
+    float acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      acc[i] = (float)m_old * Elem<T>::ld(V + crow + lane + 32 * i);
+    if (cnt == 1) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += Elem<T>::ld(v_frame + krow + lane + 32 * i);
+    } else {
+      const int32_t* mt = match + (size_t)h * n_f;
+      for (int jj = j; jj < n_f; ++jj) {
+        if (mt[jj] != s) continue;
+        const size_t r = ((size_t)h * row_stride_keys + jj) * D;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] += Elem<T>::ld(v_frame + r + lane + 32 * i);
+      }
+    }
+    const float mf = (float)m_new;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) Elem<T>::st(V + crow + lane + 32 * i, acc[i] / mf);
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      V[crow + lane + 32 * i] = v_frame[krow + lane + 32 * i];
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) K[crow + lane + 32 * i] = k_frame[krow + lane + 32 * i];
+  if (lane == 0) {
+    m[(size_t)h * C + s] = m_new;
+    last_frame[(size_t)h * C + s] = f;
+  }
+  for (int t = lane; t < Tt; t += 32)
+    codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
+}
+
+int launch_nn_tc(fastar_dtype dt, const void* k_frame, int n_f, int row_stride_keys, int H,
+                 const void* K, int C, int D, const int32_t* cand, const int32_t* ncand, float tau,
+                 int32_t* match, int32_t* match_out, int match_out_stride, int32_t* st,
+                 cudaStream_t s);
+
+template <typename T, int D>
+static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
+                      const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                      int32_t* match_out, void* ws, int32_t* st, cudaStream_t s) {
+  const int H = c->H, C = c->C, Tt = c->T;
+  MergeWs w = carve(ws, H, n_f, C);
+  const int Nrow = F * n_f;
+  cand_init_kernel<<<H, kPlanThreads, 0, s>>>(c->last_frame, c->size, C, first_frame - 1,
+                                              w.cand[0], w.ncand[0], st);
+  FASTAR_LAUNCH_CHECK();
+  const dim3 wgrid((n_f + 7) / 8, H), wblock(256);
+  for (int fi = 0; fi < F; ++fi) {
+    const int cur = fi & 1, nxt = cur ^ 1;
+    const int32_t f = first_frame + fi;
+    const T* kf = (const T*)k_new + (size_t)fi * n_f * D;
+    const T* vf = (const T*)v_new + (size_t)fi * n_f * D;
+    const uint32_t* cf = codes_new + (size_t)fi * n_f;
+    int32_t* mo = match_out ? match_out + (size_t)fi * n_f : nullptr;
+    int rc = launch_nn_tc(std::is_same<T, float>::value ? FASTAR_F32 : FASTAR_BF16, kf, n_f, Nrow,
+                          H, c->K, C, D, w.cand[cur], w.ncand[cur], tau, w.match, mo, Nrow, st, s);
+    if (rc == FASTAR_ERR_UNSUPPORTED) {
+      nn_simt_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
+                                                    w.ncand[cur], tau, w.match, mo, Nrow, st);
+      FASTAR_LAUNCH_CHECK();
+    } else if (rc != FASTAR_OK) {
+      return rc;
+    }
+    plan_kernel<<<H, kPlanThreads, 0, s>>>(n_f, C, f, w.match, w.cand[cur], w.ncand[cur],
+                                           w.cand[nxt], w.ncand[nxt], w.rep_j, w.gcnt, w.plan_slot,
+                                           w.plan_kind, w.evict, c->last_frame, c->m, c->size,
+                                           c->inserted, c->evicted, st);
+    FASTAR_LAUNCH_CHECK();
+    apply_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
+                                                w.plan_kind, w.gcnt, (T*)c->K, (T*)c->V, c->m,
+                                                c->codes, c->last_frame, C, st);
+    FASTAR_LAUNCH_CHECK();
+  }
+  return launch_csr(c->codes, H * Tt, C, c->size, Tt, 1 << c->B, c->perm, c->offsets, st, s);
+}
+
+int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
+                 const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                 int32_t* match_out, void* ws, int32_t* st, cudaStream_t s) {
+  if (c->dt == FASTAR_F32 && c->D == 64)
+    return merge_impl<float, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+  if (c->dt == FASTAR_F32 && c->D == 128)
+    return merge_impl<float, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+  if (c->dt == FASTAR_BF16 && c->D == 64)
+    return merge_impl<__nv_bfloat16, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+  if (c->dt == FASTAR_BF16 && c->D == 128)
+    return merge_impl<__nv_bfloat16, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+  return FASTAR_ERR_UNSUPPORTED;
+}
+
+}  // namespace fastar

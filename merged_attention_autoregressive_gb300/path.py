@@ -1,0 +1,85 @@
+"""One chunk of the FAST-AR attention path on preallocated device buffers.
+
+The order follows the method: hash the chunk's queries, its new keys and
+the prompt keys once (FAST-AR analysis, paper.rainbus.top: the encoding is
+computed once and serves all three modules); merge the new frames into the
+TempCache; prune the prompt per frame (AnnCA); cross-attend; then
+self-attend over the merged cache with the bucket restriction (AnnSA).
+Every step is one C-ABI call; this class only owns the buffers.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import (Cache, OP_ANNSA, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
+               fastar_annsa_attention, fastar_hash, fastar_tempcache_merge,
+               fastar_workspace_size)
+
+
+class ChunkPath:
+    """Buffers and calls of one layer's per-chunk path."""
+
+    def __init__(self, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda"):
+        self.H, self.D, self.n_f, self.F, self.P = H, D, n_f, F, P
+        self.T, self.B, self.C, self.tau, self.dtype = T, B, C, tau, dtype
+        self.Nq = F * n_f
+        self.scale = D ** -0.5
+        dev = torch.device(device)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.cache = Cache(H, C, D, T, B, dtype, dev)
+        self.planes = torch.zeros(T * B, D, dtype=dtype, device=dev)
+        Nq = self.Nq
+        self.q_codes = torch.zeros(H, T, Nq, **i32)
+        self.q_perm = torch.zeros(H, T, Nq, **i32)
+        self.q_offsets = torch.zeros(H, T, (1 << B) + 1, **i32)
+        self.k_codes = torch.zeros(H, T, Nq, **i32)
+        self.p_codes = torch.zeros(H, T, max(P, 1), **i32)
+        self.kept_idx = torch.zeros(H, F, max(P, 1), **i32)
+        self.kept_cnt = torch.zeros(H, F, **i32)
+        self.match = torch.zeros(H, Nq, **i32)
+        self.o_ca = torch.zeros(H, Nq, D, dtype=dtype, device=dev)
+        self.o_sa = torch.zeros(H, Nq, D, dtype=dtype, device=dev)
+        self.lse = torch.zeros(H, Nq, dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, **i32)
+        self.ws_merge = torch.empty(max(1, fastar_workspace_size(OP_MERGE, H, n_f, D, T, B, C)),
+                                    dtype=torch.uint8, device=dev)
+        self.ws_annsa = torch.empty(max(1, fastar_workspace_size(OP_ANNSA, H, Nq, D, T, B, C)),
+                                    dtype=torch.uint8, device=dev)
+
+    # -- pieces -----------------------------------------------------------
+    def merge(self, k, v, first_frame, F=None, stream=None):
+        """Hash new keys k [H][F*n_f][D] and merge them (cache building).
+
+        Returns (codes [H][T][F*n_f], match [H][F*n_f]) of this call.
+        """
+        F = self.F if F is None else F
+        n = F * self.n_f
+        if F == self.F:
+            codes, match = self.k_codes, self.match
+        else:
+            codes = torch.empty(self.H, self.T, n, dtype=torch.int32, device=k.device)
+            match = torch.empty(self.H, n, dtype=torch.int32, device=k.device)
+        fastar_hash(k, self.planes, self.T, self.B, codes, status=self.status, stream=stream)
+        fastar_tempcache_merge(self.cache, k, v, codes, F, self.n_f, first_frame, self.tau,
+                               match_out=match, ws=self.ws_merge, status=self.status,
+                               stream=stream)
+        return codes, match
+
+    def step(self, q, k, v, kp, vp, first_frame, stream=None):
+        """The whole path for one chunk: q, k, v [H][F*n_f][D]; kp, vp [H][P][D]."""
+        st = self.status
+        fastar_hash(q, self.planes, self.T, self.B, self.q_codes, self.q_perm, self.q_offsets,
+                    status=st, stream=stream)
+        fastar_hash(k, self.planes, self.T, self.B, self.k_codes, status=st, stream=stream)
+        if self.P:
+            fastar_hash(kp, self.planes, self.T, self.B, self.p_codes, status=st, stream=stream)
+        fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
+                               self.tau, match_out=self.match, ws=self.ws_merge, status=st,
+                               stream=stream)
+        fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
+                           self.kept_idx, self.kept_cnt, status=st, stream=stream)
+        fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
+                               self.scale, self.o_ca, status=st, stream=stream)
+        fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
+                               self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
+                               stream=stream)

@@ -1,0 +1,102 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every declared call.
+
+No compute is launched here: only calls that the host-side checks reject
+(before any CUDA call) and the pure-host helpers are exercised, so these
+tests run without a GPU.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fastar.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from merged_attention_autoregressive_gb300 import build, lib
+    build.build()
+    return lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fastar_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("fastar_hash", "fastar_tempcache_merge", "fastar_annca_prune",
+              "fastar_annca_attention", "fastar_annsa_attention", "fastar_workspace_size",
+              "fastar_status_string", "fastar_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+    assert L.fastar_version() >= 100
+
+
+def test_binding_exports_match_header():
+    import merged_attention_autoregressive_gb300 as m
+    assert set(m.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(L):
+    for code in (0, 1, 2, 3, 4, 16, 17, 18):
+        assert L.fastar_status_string(code)
+    assert L.fastar_status_string(12345) == b"unknown status"
+
+
+def test_workspace_sizes(L):
+    from merged_attention_autoregressive_gb300 import OP_HASH, OP_MERGE, OP_PRUNE
+    assert L.fastar_workspace_size(OP_HASH, 12, 4680, 128, 2, 8, 32768) == 0
+    assert L.fastar_workspace_size(OP_PRUNE, 12, 512, 128, 2, 8, 32768) == 0
+    w1 = L.fastar_workspace_size(OP_MERGE, 12, 1560, 128, 2, 8, 32768)
+    w2 = L.fastar_workspace_size(OP_MERGE, 24, 1560, 128, 2, 8, 32768)
+    assert w1 >= 12 * 32768 * 16 and w2 >= 2 * w1 - 4096
+
+
+def test_host_argument_errors_need_no_gpu(L):
+    vp = ctypes.c_void_p
+    fake = vp(0x1000)       # never dereferenced: the checks reject the call first
+    # unsupported head dim
+    assert L.fastar_hash(0, fake, 1, 8, 96, fake, 1, 4, fake, None, None, None, 0, None, None) == 2
+    # T*B above 64
+    assert L.fastar_hash(0, fake, 1, 8, 128, fake, 8, 9, fake, None, None, None, 0, None, None) == 2
+    # perm without offsets
+    assert L.fastar_hash(0, fake, 1, 8, 128, fake, 1, 4, fake, fake, None, None, 0, None, None) == 1
+    # null input
+    assert L.fastar_hash(0, None, 1, 8, 128, fake, 1, 4, fake, None, None, None, 0, None, None) == 1
+    # misaligned rows
+    assert L.fastar_hash(0, vp(0x1004), 1, 8, 128, fake, 1, 4, fake, None, None, None, 0, None,
+                         None) == 1
+    # empty input: nothing to do, OK without touching the device
+    assert L.fastar_hash(0, None, 0, 8, 128, None, 1, 4, None, None, None, None, 0, None, None) == 0
+    # prune: bad tables
+    assert L.fastar_annca_prune(fake, fake, 1, 1, 4, 4, 0, 4, fake, fake, None, 0, None, None) == 1
+    # attention: bad dtype
+    assert L.fastar_annca_attention(7, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
+                                    ctypes.c_float(0.1), fake, None, 0, None, None) == 2
+    # merge: null cache
+    assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
+                                    None, 0, None, None) == 1
+
+
+def test_merge_rejects_small_workspace(L):
+    import merged_attention_autoregressive_gb300 as m
+    fake = 0x1000
+    cs = m.CacheStruct(2, 128, 64, 2, 8, 0, *([fake] * 10))
+    rc = L.fastar_tempcache_merge(ctypes.byref(cs), ctypes.c_void_p(fake), ctypes.c_void_p(fake),
+                                  ctypes.c_void_p(fake), 1, 16, 0, ctypes.c_float(0.9), None,
+                                  ctypes.c_void_p(4096), 16, None, None)
+    assert rc == 4
+    # n_f above the capacity
+    rc = L.fastar_tempcache_merge(ctypes.byref(cs), ctypes.c_void_p(fake), ctypes.c_void_p(fake),
+                                  ctypes.c_void_p(fake), 1, 65, 0, ctypes.c_float(0.9), None,
+                                  ctypes.c_void_p(4096), 1 << 30, None, None)
+    assert rc == 1

@@ -1,0 +1,195 @@
+"""GPU parity of the whole per-chunk path against the fp64 oracle (cascaded).
+
+Runs the library through its C ABI (via the ctypes binding) on seeded
+synthetic layers: the past frames are merged call by call, then one chunk
+runs hash -> merge -> prune -> AnnCA -> AnnSA.  Every stage is compared with
+the oracle as described in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from parity import Report, cache_to_oracle, check_att, check_codes, check_csr, check_merge, dev, host
+from workloads import CONFIGS, layer_data
+
+pytestmark = pytest.mark.gpu
+
+
+def _path(cfg):
+    from merged_attention_autoregressive_gb300.path import ChunkPath
+    return ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau,
+                     dtype={"bf16": torch.bfloat16, "f32": torch.float32}[cfg.dtype])
+
+
+def build_cache(cfg, d, path, rep, check=True):
+    """Merge the past frames in calls of cfg.F frames; returns the oracle state."""
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    f = 0
+    while f < cfg.past_frames:
+        nF = min(cfg.F, cfg.past_frames - f)
+        k = np.concatenate(d.past_k[f:f + nF], axis=1)
+        v = np.concatenate(d.past_v[f:f + nF], axis=1)
+        codes, match = path.merge(dev(k, cfg.dtype), dev(v, cfg.dtype), f, F=nF)
+        torch.cuda.synchronize()
+        if check:
+            gc = check_codes(codes, k, d.planes, cfg.T, cfg.B, rep, f"past {f} key codes")
+            st = check_merge(path, st, k, v, gc, match, nF, cfg.n_f, f, cfg.tau, cfg.dtype, rep,
+                             f"past frames {f}..{f + nF - 1}")
+            check_csr(path.cache.perm, path.cache.offsets, st.codes, 1 << cfg.B, st.size,
+                      f"cache CSR after frame {f + nF - 1}")
+        f += nF
+    return st if check else cache_to_oracle(path.cache, cfg.dtype)
+
+
+def run_chunk(cfg, d, path, st, rep, chunk=0, rows=None):
+    q, k, v = d.chunk_q[chunk], d.chunk_k[chunk], d.chunk_v[chunk]
+    first = cfg.past_frames + chunk * cfg.F
+    qd, kd, vd = dev(q, cfg.dtype), dev(k, cfg.dtype), dev(v, cfg.dtype)
+    kp, vp = dev(d.prompt_k, cfg.dtype), dev(d.prompt_v, cfg.dtype)
+    path.step(qd, kd, vd, kp, vp, first)
+    torch.cuda.synchronize()
+    assert int(path.status.item()) == 0
+    qc = check_codes(path.q_codes, q, d.planes, cfg.T, cfg.B, rep, "query codes")
+    check_csr(path.q_perm, path.q_offsets, qc, 1 << cfg.B, what="query CSR")
+    kc = check_codes(path.k_codes, k, d.planes, cfg.T, cfg.B, rep, "new key codes")
+    pc = check_codes(path.p_codes[:, :, :cfg.P], d.prompt_k, d.planes, cfg.T, cfg.B, rep,
+                     "prompt codes")
+    st = check_merge(path, st, k, v, kc, path.match, cfg.F, cfg.n_f, first, cfg.tau, cfg.dtype,
+                     rep, "chunk merge")
+    check_csr(path.cache.perm, path.cache.offsets, st.codes, 1 << cfg.B, st.size, "cache CSR")
+    idx, cnt = O.annca_prune(qc, pc, cfg.F, cfg.n_f)
+    np.testing.assert_array_equal(host(path.kept_cnt), cnt)
+    np.testing.assert_array_equal(host(path.kept_idx), idx)
+    o_ca = O.annca_attention(q, d.prompt_k, d.prompt_v, idx, cnt, cfg.F, cfg.n_f, cfg.scale,
+                             rows=rows)
+    o_sa, lse = O.annsa_attention(q, qc, st, cfg.scale, rows=rows)
+    sel = slice(None) if rows is None else rows
+    check_att(path.o_ca[:, sel], o_ca, "AnnCA", rep)
+    check_att(path.o_sa[:, sel], o_sa, "AnnSA", rep)
+    gl = host(path.lse[:, sel]).astype(np.float64)
+    fin = np.isfinite(lse)
+    np.testing.assert_array_equal(np.isfinite(gl), fin)
+    assert np.abs(gl[fin] - lse[fin]).max(initial=0) <= 1e-3
+    return st
+
+
+@pytest.mark.parametrize("C", [1024, 300])
+def test_tiny_fp32_chain(C):
+    """4 past frames + one 256-token frame, fp32; C = 300 forces eviction."""
+    cfg = CONFIGS[0].replace(C=C)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    run_chunk(cfg, d, path, st, rep)
+    if C == 300:
+        assert int(host(path.cache.evicted).sum()) > 0
+
+
+def test_tiny_bf16_chain():
+    cfg = CONFIGS[0].replace(dtype="bf16", C=300)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    run_chunk(cfg, d, path, st, rep)
+
+
+def test_ragged_bf16_chain():
+    """Sizes off every tile multiple: n_f = 197, 2 frames, P = 77, T = 3, B = 7."""
+    cfg = CONFIGS[0].replace(dtype="bf16", n_f=197, F=2, past_frames=5, P=77, T=3, B=7, C=700,
+                             D=128, H=3, redraw=0.3)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    run_chunk(cfg, d, path, st, rep)
+
+
+def test_wan_layer_chain():
+    """Bench workload: 12 heads, D 128, 3 x 1560 queries, 21 merged past frames."""
+    cfg = CONFIGS[1]
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    run_chunk(cfg, d, path, st, rep)
+    print("report", rep)
+
+
+def test_long_prompt_prune_and_cross_attention():
+    """4096-token prompt from 256 clusters, T = 4 x B = 10 (AnnCA stress)."""
+    cfg = CONFIGS[3]
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    from merged_attention_autoregressive_gb300 import (fastar_annca_attention, fastar_annca_prune,
+                                                       fastar_hash)
+    q = d.chunk_q[0]
+    qd, kp, vp = dev(q, cfg.dtype), dev(d.prompt_k, cfg.dtype), dev(d.prompt_v, cfg.dtype)
+    fastar_hash(qd, path.planes, cfg.T, cfg.B, path.q_codes, status=path.status)
+    fastar_hash(kp, path.planes, cfg.T, cfg.B, path.p_codes, status=path.status)
+    fastar_annca_prune(path.q_codes, path.p_codes, cfg.F, cfg.n_f, cfg.B, path.kept_idx,
+                       path.kept_cnt, status=path.status)
+    fastar_annca_attention(qd, kp, vp, path.kept_idx, path.kept_cnt, cfg.F, cfg.n_f, cfg.scale,
+                           path.o_ca, status=path.status)
+    torch.cuda.synchronize()
+    assert int(path.status.item()) == 0
+    qc = check_codes(path.q_codes, q, d.planes, cfg.T, cfg.B, rep, "query codes")
+    pc = check_codes(path.p_codes, d.prompt_k, d.planes, cfg.T, cfg.B, rep, "prompt codes")
+    idx, cnt = O.annca_prune(qc, pc, cfg.F, cfg.n_f)
+    np.testing.assert_array_equal(host(path.kept_cnt), cnt)
+    np.testing.assert_array_equal(host(path.kept_idx), idx)
+    ref = O.annca_attention(q, d.prompt_k, d.prompt_v, idx, cnt, cfg.F, cfg.n_f, cfg.scale)
+    check_att(path.o_ca, ref, "AnnCA long prompt", rep)
+
+
+def test_empty_sets_give_zero_output():
+    """Empty kept sets and queries with no allowed slot give zeros (and lse -inf)."""
+    cfg = CONFIGS[0].replace(dtype="bf16", H=2, D=128, n_f=64, F=2, past_frames=1, P=16, T=1, B=10)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    from merged_attention_autoregressive_gb300 import (fastar_annca_attention, fastar_annca_prune,
+                                                       fastar_annsa_attention)
+    # crafted codes: prompt code 9 everywhere; queries code 5, except head 1 frame 1 (code 9)
+    qc = torch.full((cfg.H, cfg.T, cfg.Nq), 5, dtype=torch.int32, device="cuda")
+    pc = torch.full((cfg.H, cfg.T, cfg.P), 9, dtype=torch.int32, device="cuda")
+    qc[1, :, cfg.n_f:] = 9
+    fastar_annca_prune(qc, pc, cfg.F, cfg.n_f, cfg.B, path.kept_idx, path.kept_cnt,
+                       status=path.status)
+    q = dev(d.chunk_q[0], cfg.dtype)
+    kp, vp = dev(d.prompt_k, cfg.dtype), dev(d.prompt_v, cfg.dtype)
+    fastar_annca_attention(q, kp, vp, path.kept_idx, path.kept_cnt, cfg.F, cfg.n_f, cfg.scale,
+                           path.o_ca, status=path.status)
+    torch.cuda.synchronize()
+    cnt = host(path.kept_cnt)
+    assert cnt.tolist() == [[0, 0], [0, cfg.P]]
+    o = host(path.o_ca)
+    assert (o[0] == 0).all() and (o[1, :cfg.n_f] == 0).all()
+    ref = O.annca_attention(d.chunk_q[0], d.prompt_k, d.prompt_v, host(path.kept_idx), cnt,
+                            cfg.F, cfg.n_f, cfg.scale)
+    check_att(path.o_ca, ref, "AnnCA crafted", rep)
+    # AnnSA: half of the queries carry a code that no cache slot has
+    used = set(st.codes[:, 0, :int(st.size.max())].ravel().tolist())
+    absent = next(c for c in range(1 << cfg.B) if c not in used)
+    qcodes = np.array(O.hash_codes(d.chunk_q[0], d.planes, cfg.T, cfg.B)[0])
+    qcodes[:, :, ::2] = absent
+    perm, offs = O.bucket_csr(qcodes, 1 << cfg.B)
+    tq = lambda a: torch.from_numpy(np.ascontiguousarray(a).astype(np.int32)).cuda()  # noqa: E731
+    fastar_annsa_attention(q, tq(qcodes), tq(perm), tq(offs), path.cache, cfg.scale, path.o_sa,
+                           path.lse, ws=path.ws_annsa, status=path.status)
+    torch.cuda.synchronize()
+    assert int(path.status.item()) == 0
+    o_sa, lse = O.annsa_attention(d.chunk_q[0], qcodes, st, cfg.scale)
+    assert (host(path.o_sa)[:, ::2] == 0).all()
+    assert np.isneginf(host(path.lse)[:, ::2]).all()
+    check_att(path.o_sa, o_sa, "AnnSA crafted", rep)
