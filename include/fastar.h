@@ -175,6 +175,31 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
                            int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * fastar_tempcache_merge_noalloc -- fastar_tempcache_merge without a
+ * caller workspace.  The paper has no counterpart: this is a convenience of
+ * this library for callers that cannot allocate device memory, such as a
+ * plugin inside a host application that owns the GPU's memory budget, or a
+ * C/FFI caller that holds only the pointers handed to it.
+ *
+ * Same arguments and results as fastar_tempcache_merge, minus ws/ws_bytes.
+ * The scratch is a fixed array of FASTAR_NOALLOC_SCRATCH_BYTES inside the
+ * library's device memory, held by every GPU that loads the library until
+ * the process exits.  Returns FASTAR_ERR_WORKSPACE when the merge needs more
+ * (fastar_workspace_size(FASTAR_OP_MERGE, ...) > FASTAR_NOALLOC_SCRATCH_BYTES;
+ * e.g. 12 heads x C 32768 x n_f 1560 needs 6.3 MiB and fits).  All calls
+ * share the array, so calls that overlap on the GPU race and must be ordered
+ * by the caller; it keeps the last call's contents (the merge needs none of
+ * it zeroed).  The first call on a device looks up the array's address with
+ * that device current; make it before any stream capture.
+ */
+#define FASTAR_NOALLOC_SCRATCH_BYTES (8u << 20)
+int fastar_tempcache_merge_noalloc(const fastar_cache* cache, const void* k_new,
+                                   const void* v_new, const uint32_t* codes_new,
+                                   int F, int n_f, int32_t first_frame, float tau,
+                                   int32_t* match_out, int32_t* dev_status,
+                                   cudaStream_t stream);
+
+/*
  * fastar_annca_prune -- per-frame prompt-token selection for AnnCA.
  *
  * Passage: FAST-AR technical summary (gist.science) 2.B AnnCA mechanism
