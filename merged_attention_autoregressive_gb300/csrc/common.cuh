@@ -34,6 +34,16 @@ __device__ __forceinline__ bool status_bad(const int32_t* st) {
 __device__ __forceinline__ void status_set(int32_t* st, int32_t code) {
   if (st) atomicCAS(st, 0, code);
 }
+// Block-uniform status check: thread 0 reads the word, every thread gets the
+// same answer (a block never splits at a later barrier).  Call from all threads.
+__device__ __forceinline__ bool block_status_bad(const int32_t* st) {
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = status_bad(st) ? 1 : 0;
+  __syncthreads();
+  const bool bad = s_bad != 0;
+  __syncthreads();
+  return bad;
+}
 
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;

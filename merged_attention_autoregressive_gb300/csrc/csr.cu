@@ -22,7 +22,7 @@ __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __rest
                                                           int32_t* __restrict__ offsets, int32_t* st) {
   extern __shared__ int cnt[];  // [W][nb]
   __shared__ int scan_sh[33];
-  if (status_bad(st)) return;
+  if (block_status_bad(st)) return;
   const int g = blockIdx.x;
   int n = N;
   if (n_dev) n = min(max(n_dev[g / n_div], 0), N);

@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(256) hash_warp_kernel(const T* __restrict__ x,
   constexpr int PER = D / 32;
   __shared__ float R[kMaxTB * D];
   const int TB = T_ * B;
-  if (status_bad(st)) return;
+  if (block_status_bad(st)) return;
   for (int i = threadIdx.x; i < TB * D; i += blockDim.x) R[i] = Elem<T>::ld(planes + i);
   __syncthreads();
   const int lane = threadIdx.x & 31;

@@ -19,7 +19,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const uint32_t* __
                                                               int32_t* __restrict__ kept_cnt, int32_t* st) {
   extern __shared__ uint32_t occ[];  // [T][2^B / 32]
   __shared__ int sh[33];
-  if (status_bad(st)) return;
+  if (block_status_bad(st)) return;
   const int f = blockIdx.x, h = blockIdx.y;
   const int words = ((1 << B) + 31) >> 5;
   const uint32_t mask = (B >= 32) ? 0xffffffffu : ((1u << B) - 1u);

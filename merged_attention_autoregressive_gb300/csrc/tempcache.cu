@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* 
                                                                  int32_t prev_frame, int32_t* cand,
                                                                  int32_t* ncand, int32_t* st) {
   __shared__ int sh[33];
-  if (status_bad(st)) return;
+  if (block_status_bad(st)) return;
   const int h = blockIdx.x;
   const int n = min(max(size[h], 0), C);
   const int32_t* lf = last_frame + (size_t)h * C;
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
   __shared__ long long shl[33];
   __shared__ int hist[2048];
   __shared__ int s_lstar, s_nlt, s_found;
-  if (status_bad(st)) return;
+  if (block_status_bad(st)) return;
   const int h = blockIdx.x;
   const int32_t* mt = match + (size_t)h * n_f;
   const int32_t* cc = cand_cur + (size_t)h * C;
@@ -384,9 +384,9 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
     codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
 }
 
-int launch_nn_tc(fastar_dtype dt, const void* k_frame, int n_f, int row_stride_keys, int H,
-                 const void* K, int C, int D, const int32_t* cand, const int32_t* ncand, float tau,
-                 int32_t* match, int32_t* match_out, int match_out_stride, int32_t* st,
+int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
+                 int C, int D, const int32_t* cand, const int32_t* ncand, const int32_t* prev_slot,
+                 const int32_t* prev_kind, float tau, int32_t* match, int32_t* match_out, int32_t* st,
                  cudaStream_t s);
 
 template <typename T, int D>
@@ -407,8 +407,9 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     const T* vf = (const T*)v_new + (size_t)fi * n_f * D;
     const uint32_t* cf = codes_new + (size_t)fi * n_f;
     int32_t* mo = match_out ? match_out + (size_t)fi * n_f : nullptr;
-    int rc = launch_nn_tc(std::is_same<T, float>::value ? FASTAR_F32 : FASTAR_BF16, kf, n_f, Nrow,
-                          H, c->K, C, D, w.cand[cur], w.ncand[cur], tau, w.match, mo, Nrow, st, s);
+    int rc = launch_nn_tc(std::is_same<T, float>::value ? FASTAR_F32 : FASTAR_BF16, k_new, n_f, Nrow,
+                          H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.plan_slot, w.plan_kind, tau,
+                          w.match, match_out, st, s);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       nn_simt_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], tau, w.match, mo, Nrow, st);
