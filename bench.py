@@ -40,8 +40,8 @@ METRIC = "per-chunk FAST-AR attention ms, effective TFLOP/s, % of GB300 roofline
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -68,7 +68,7 @@ def peaks():
 
 # ----------------------------------------------------------------- clocks
 class Clocks:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -82,12 +82,22 @@ class Clocks:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # wait for the first sample so that the sampler runs before timing starts
+        for _ in range(100):
+            time.sleep(0.05)
+            if os.path.getsize(self.path) > 0:
+                break
+
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
 
     def stop(self):
+        """Median SM clock and active throttle reasons of the samples taken in window()."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -96,24 +106,33 @@ class Clocks:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], None, set()
+        import datetime as _dt
+        sm_in, sm_all, smax, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
         with open(self.path) as fh:
             for line in fh:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax = float(parts[2])
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    sm = float(parts[2])
+                    smax = float(parts[3])
                 except ValueError:
                     continue
-                for n, v in zip(names, parts[5:9]):
+                inside = t0 is None or (t0 - 0.05 <= ts <= t1 + 0.05)
+                sm_all.append(sm)
+                if not inside:
+                    continue
+                sm_in.append(sm)
+                for n, v in zip(names, parts[6:10]):
                     if v.lower().startswith("active"):
                         reasons.add(n)
         os.unlink(self.path)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        use = sm_in if sm_in else sm_all
+        return {"sm_mhz": statistics.median(use) if use else None, "sm_max_mhz": smax,
+                "samples": len(sm_in), "samples_run": len(sm_all), "reasons": sorted(reasons)}
 
 
 # ----------------------------------------------------------------- oracle leg
@@ -162,12 +181,16 @@ def run_reference(args, cfg):
     if rank != 0:
         return
     d = layer_data(cfg, chunks=1)
-    heads = [h % cfg.H for h in range(args.warmup + args.steps)]
+    # one head of the chunk per step; the sample is capped at 24 heads so the
+    # CPU run stays within a few minutes whatever --steps says
+    n_meas = min(args.steps, 24)
+    n_warm = min(args.warmup, 2)
+    heads = [h % cfg.H for h in range(n_warm + n_meas)]
     states = {h: oracle_cache_one_head(cfg, d, h) for h in sorted(set(heads))}
     times = []
     for i, h in enumerate(heads):
         t = oracle_chunk_one_head(cfg, d, h, states[h])
-        if i >= args.warmup:
+        if i >= n_warm:
             times.append(t)
     per_chunk_ms = statistics.mean(times) * cfg.H * 1e3
     cores = host_cores()
@@ -179,8 +202,9 @@ def run_reference(args, cfg):
                        "P": cfg.P, "T": cfg.T, "B": cfg.B, "C": cfg.C},
             "cpu_baseline": {"value": per_chunk_ms, "unit": "ms/chunk", "cores": cores,
                              "kind": "oracle",
-                             "sample": f"one head of the {cfg.H}-head chunk per step (heads in "
-                                       "turn), x H; past frames merged untimed"},
+                             "sample": f"{n_meas} single-head samples of the {cfg.H}-head chunk "
+                                       f"(heads in turn, after {n_warm} warm-up samples), mean x H; "
+                                       "past frames merged untimed"},
             "e2e": {"value": per_chunk_ms, "unit": "ms/chunk", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -342,12 +366,14 @@ def run_ours(args, cfg):
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
+    t0 = time.time()
     t_wall = time.perf_counter()
     for i in range(args.steps):
         prep()
         step(evs[i])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    clocks.window(t0, time.time())
     clk = clocks.stop()
     launches = fa.fastar_launch_count() - n0
     assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))

@@ -45,6 +45,22 @@ __device__ __forceinline__ bool block_status_bad(const int32_t* st) {
   return bad;
 }
 
+// A nearest-neighbour candidate (cosine, slot) packed into one 64-bit word
+// whose unsigned order is: larger cosine first, then lower slot.  The best
+// candidate of several partial searches is their atomicMax; 0 means none.
+__device__ __forceinline__ unsigned long long pack_best(float cos, int slot) {
+  uint32_t b = __float_as_uint(cos);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)b << 32) | (unsigned long long)(0xffffffffu - (uint32_t)slot);
+}
+__device__ __forceinline__ float best_cos(unsigned long long key) {
+  const uint32_t b = (uint32_t)(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7fffffffu) : ~b);
+}
+__device__ __forceinline__ int best_slot(unsigned long long key) {
+  return (int)(0xffffffffu - (uint32_t)key);
+}
+
 __device__ __forceinline__ unsigned lanemask_lt() {
   unsigned m;
   asm volatile("mov.u32 %0, %%lanemask_lt;" : "=r"(m));

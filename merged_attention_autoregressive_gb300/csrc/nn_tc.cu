@@ -6,16 +6,29 @@
 // the previous frame) by cosine, and matched to the best one (ties: lowest
 // slot) iff the cosine reaches tau.
 //
-// One CTA (4 warps) owns 128 new keys of one head.  The keys arrive by TMA
-// (two 64-column boxes, 128-byte swizzle).  Candidate rows are gathered with
-// cp.async into the same swizzled layout, 128 at a time, double-buffered so
-// the next gather overlaps the current MMA: for the first frame of a call
-// they are the cache rows listed by the candidate compaction; for later
-// frames they are the previous frame's representative rows of k_new (the
-// rows the previous merge step stored into the cache).  One thread issues
-// 8 MMAs (M 128, N 128, K 16) into a 128-column fp32 TMEM accumulator; each
-// thread then reads its key's 128 dot products from TMEM, scales them by the
-// two inverse norms and keeps the best (cosine, slot).
+// One CTA owns 128 new keys of one head and one slice of the candidates (the
+// candidates are split over gridDim.y CTAs so that about two CTAs run per
+// SM).  The new keys arrive by TMA (two 64-column boxes, 128-byte swizzle).
+// The slots and inverse norms of the CTA's candidates are staged in shared
+// memory once.  The CTA is warp-specialised:
+//   warp 0     producer: fills a 4-stage ring of 64-row candidate tiles.
+//              After the first frame of a call the candidates are the rows of
+//              the previous frame, contiguous in k_new, and come by TMA; for
+//              the first frame they are scattered cache rows, gathered with
+//              cp.async into the same swizzled layout;
+//   warp 1     one thread issues 8 MMAs (M 128, N 64, K 16) per tile into one
+//              of four 64-column fp32 TMEM accumulators; the MMA commit frees
+//              the tile's stage;
+//   warps 2-9  epilogue: two warps per TMEM lane quarter, 32 columns each;
+//              a thread scales its key's dot products by the candidates'
+//              inverse norms (NaN for a candidate with a zero norm, which
+//              drops out of every comparison) and keeps the best
+//              (cosine, slot) among the candidates that are groups.
+// At the end the two halves of a row are merged and the CTA's best of each
+// key is folded into a packed 64-bit word with atomicMax (larger cosine
+// first, then lower slot), so the result does not depend on CTA order.  The
+// epilogue also writes the new keys' inverse norms, which are the candidate
+// norms of the next frame.
 #include <math.h>
 
 #include "common.cuh"
@@ -25,15 +38,21 @@ namespace fastar {
 
 namespace {
 
-constexpr int kM = 128, kN = 128, kD = 128;
-constexpr int kMember = 0;  // plan kind of a key that joined a group it does not represent
+constexpr int kM = 128, kN = 64, kD = 128, kStages = 4, kAcc = 4;
+constexpr int kThreads = 320;  // 10 warps
+constexpr int kMember = 0;     // plan kind of a key that joined a group it does not represent
+constexpr int kMetaCap = 1408; // candidates whose slot / inverse norm are staged per CTA
 
 struct NnSmem {
   uint8_t A[kM * kD * 2];
-  uint8_t B[2][kN * kD * 2];
-  float inv_nb[2][kN];
-  int slot[2][kN];
-  uint64_t bar_a, bar_mma;
+  uint8_t B[kStages][kN * kD * 2];
+  int mslot[kMetaCap];
+  float minv[kMetaCap];
+  float half_best[kM];
+  int half_slot[kM];
+  uint64_t bar_a;
+  uint64_t full[kStages], empty[kStages];
+  uint64_t tfull[kAcc], tempty[kAcc];
   uint32_t tmem;
 };
 
@@ -53,161 +72,303 @@ __device__ __forceinline__ float row_sq_norm(const uint8_t* tile, int r, int row
   return s;
 }
 
-__global__ void __launch_bounds__(128) nn_tc_kernel(const __grid_constant__ CUtensorMap mapA,
-                                                    const __nv_bfloat16* __restrict__ k_new, int n_f,
-                                                    int Nrow, int fi, const __nv_bfloat16* __restrict__ K,
-                                                    int C, const int32_t* __restrict__ cand,
-                                                    const int32_t* __restrict__ ncand,
-                                                    const int32_t* __restrict__ prev_slot,
-                                                    const int32_t* __restrict__ prev_kind, float tau,
-                                                    int32_t* __restrict__ match, int32_t* match_out,
-                                                    int32_t* st) {
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+struct NnArgs {
+  const __nv_bfloat16* k_new;  // [H][Nrow][D]
+  const __nv_bfloat16* K;      // cache keys [H][C][D]
+  int n_f, Nrow, fi, C;
+  // first frame of a call: candidates = cache slots cand[h][c] (c < ncand[h]),
+  // inverse norms cinv[h][c] (stride C)
+  const int32_t* cand;
+  const int32_t* ncand;
+  const float* cinv;
+  // later frames: candidates = rows of the previous frame, a group iff its
+  // plan kind is not "member"; inverse norms invn_prev[h][j] (stride n_f)
+  const int32_t* prev_slot;
+  const int32_t* prev_kind;
+  const float* invn_prev;
+  float* invn_out;                 // inverse norms of this frame's keys [H][n_f]
+  unsigned long long* best_out;    // packed best candidate [H][n_f]
+};
+
+__device__ __forceinline__ void cand_meta(const NnArgs& a, int h, int c, int& slot, float& inv) {
+  if (a.fi == 0) {
+    slot = a.cand[(size_t)h * a.C + c];
+    inv = a.cinv[(size_t)h * a.C + c];
+  } else {
+    slot = a.prev_kind[(size_t)h * a.n_f + c] != kMember ? a.prev_slot[(size_t)h * a.n_f + c] : -1;
+    inv = a.invn_prev[(size_t)h * a.n_f + c];
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constant__ CUtensorMap mapA,
+                                                           const __grid_constant__ CUtensorMap mapB,
+                                                           NnArgs a, int32_t* st) {
   extern __shared__ uint8_t smem_raw[];
   NnSmem& sm = *reinterpret_cast<NnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
-  const int h = blockIdx.y, m0 = blockIdx.x * kM;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int nc = (fi == 0) ? min(max(ncand[h], 0), C) : n_f;
-  const int ntiles = (nc + kN - 1) / kN;
+  const int h = blockIdx.z, m0 = blockIdx.x * kM;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nc = (a.fi == 0) ? min(max(a.ncand[h], 0), a.C) : a.n_f;
+  const int ttot = (nc + kN - 1) / kN;
+  const int tb0 = (int)((long long)ttot * blockIdx.y / gridDim.y);
+  const int tb1 = (int)((long long)ttot * (blockIdx.y + 1) / gridDim.y);
+  const int ntiles = tb1 - tb0;
+  const int cbase = tb0 * kN, cend = min(nc, tb1 * kN);
 
   if (tid == 0) {
     tc::mbar_init(&sm.bar_a, 1);
-    tc::mbar_init(&sm.bar_mma, 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&sm.full[s], 1);   // producer lane 0 (with the TMA bytes, or after the gather)
+      tc::mbar_init(&sm.empty[s], 1);  // MMA commit
+    }
+    for (int b = 0; b < kAcc; ++b) {
+      tc::mbar_init(&sm.tfull[b], 1);   // MMA commit
+      tc::mbar_init(&sm.tempty[b], 8);  // 8 epilogue warps
+    }
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&mapA);
+    tc::prefetch_tensormap(&mapB);
+    const int row0 = h * a.Nrow + a.fi * a.n_f + m0;
+    tc::mbar_arrive_expect_tx(&sm.bar_a, kM * kD * 2);
+    tc::tma_load_2d(sm.A, &mapA, &sm.bar_a, 0, row0);
+    tc::tma_load_2d(sm.A + kM * 128, &mapA, &sm.bar_a, 64, row0);
   }
-  if (warp == 0) {
-    tc::tmem_alloc(&sm.tmem, 128);
+  if (warp == 1) {
+    tc::tmem_alloc(&sm.tmem, kAcc * kN);
     tc::tmem_relinquish();
+  }
+  // stage the candidates' slots and inverse norms (all threads, one pass)
+  for (int c = cbase + tid; c < cbase + ntiles * kN && c - cbase < kMetaCap; c += kThreads) {
+    int sl = -1;
+    float inv = __int_as_float(0x7fc00000);
+    if (c < cend) cand_meta(a, h, c, sl, inv);
+    sm.mslot[c - cbase] = sl;
+    sm.minv[c - cbase] = sl >= 0 ? inv : __int_as_float(0x7fc00000);
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem;
+  bool ok = true;
 
-  if (tid == 0) {
-    const int row0 = h * Nrow + fi * n_f + m0;
-    tc::mbar_arrive_expect_tx(&sm.bar_a, kM * kD * 2);
-    tc::tma_load_2d(sm.A, &mapA, &sm.bar_a, 0, row0);
-    tc::tma_load_2d(sm.A + kM * 128, &mapA, &sm.bar_a, 64, row0);
-  }
-
-  auto issue_b = [&](int t, int buf) {
-    const int c0 = t * kN;
-    tc::gather_rows_sw128(
-        tc::smem_u32(sm.B[buf]), kN,
-        [&](int r) -> const void* {
-          const int c = c0 + r;
-          if (c >= nc) return nullptr;
-          if (fi == 0) return K + ((size_t)h * C + cand[(size_t)h * C + c]) * kD;
-          return k_new + ((size_t)h * Nrow + (size_t)(fi - 1) * n_f + c) * kD;
-        },
-        tid, 128, K);
-    tc::cp_async_commit();
-    for (int r = tid; r < kN; r += 128) {
-      const int c = c0 + r;
-      int s = -1;
-      if (c < nc) {
-        if (fi == 0)
-          s = cand[(size_t)h * C + c];
-        else
-          s = prev_kind[(size_t)h * n_f + c] != kMember ? prev_slot[(size_t)h * n_f + c] : -1;
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (a.fi > 0) {
+      // contiguous candidate rows: one TMA per 64-column half of a tile
+      if (lane == 0) {
+        for (int t = 0; t < ntiles && ok; ++t) {
+          const int s = t % kStages;
+          if (t >= kStages) ok = tc::mbar_wait(&sm.empty[s], (uint32_t)((t / kStages) - 1) & 1u);
+          if (!ok) break;
+          const int row = h * a.Nrow + (a.fi - 1) * a.n_f + (tb0 + t) * kN;
+          tc::mbar_arrive_expect_tx(&sm.full[s], kN * kD * 2);
+          tc::tma_load_2d(sm.B[s], &mapB, &sm.full[s], 0, row);
+          tc::tma_load_2d(sm.B[s] + kN * 128, &mapB, &sm.full[s], 64, row);
+        }
       }
-      sm.slot[buf][r] = s;
-    }
-  };
-  if (ntiles > 0) issue_b(0, 0);
-
-  bool ok = tc::mbar_wait(&sm.bar_a, 0);
-  const float na2 = row_sq_norm(sm.A, tid, kM);
-  const float ia = na2 > 0.f ? 1.f / sqrtf(na2) : 0.f;
-  float best = -INFINITY;
-  int best_slot = 0x7fffffff;
-  constexpr uint32_t idesc = tc::idesc_bf16_f32(kM, kN, 0, 0);
-  uint32_t phase = 0;
-
-  for (int t = 0; t < ntiles; ++t) {
-    const int buf = t & 1;
-    tc::cp_async_wait_all();
-    tc::fence_proxy_async_smem();
-    __syncthreads();
-    const float nb2 = row_sq_norm(sm.B[buf], tid, kN);
-    sm.inv_nb[buf][tid] = nb2 > 0.f ? 1.f / sqrtf(nb2) : 0.f;
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    if (tid == 0 && ok) {
-      const uint32_t a0 = tc::smem_u32(sm.A), b0 = tc::smem_u32(sm.B[buf]);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off_a = (kk >> 2) * kM * 128 + (kk & 3) * 32;
-        const uint32_t off_b = (kk >> 2) * kN * 128 + (kk & 3) * 32;
-        tc::mma_bf16(tmem, tc::sdesc_kmajor_sw128(a0 + off_a), tc::sdesc_kmajor_sw128(b0 + off_b), idesc,
-                     kk > 0 ? 1u : 0u);
-      }
-      tc::mma_commit(&sm.bar_mma);
-    }
-    if (t + 1 < ntiles) issue_b(t + 1, buf ^ 1);
-    if (ok) ok = tc::mbar_wait(&sm.bar_mma, phase);
-    phase ^= 1;
-    tc::tc_fence_after();
-    if (ok) {
-#pragma unroll 1
-      for (int q = 0; q < kN / 32; ++q) {
-        float v[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + q * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int r = q * 32 + i;
-          const int s = sm.slot[buf][r];
-          const float ib = sm.inv_nb[buf][r];
-          if (s < 0 || ib == 0.f) continue;
-          const float cs = v[i] * ia * ib;
-          if (cs > best || (cs == best && s < best_slot)) {
-            best = cs;
-            best_slot = s;
+    } else {
+      // scattered cache rows: cp.async gather, a stage is released once its
+      // copies have landed (kStages - 1 tiles later in the issue order)
+      for (int t = 0; t < ntiles + kStages - 1; ++t) {
+        if (t < ntiles) {
+          const int s = t % kStages;
+          if (t >= kStages) ok = ok && tc::mbar_wait(&sm.empty[s], (uint32_t)((t / kStages) - 1) & 1u);
+          const int c0 = (tb0 + t) * kN;
+          const uint32_t tile = tc::smem_u32(sm.B[s]);
+#pragma unroll 4
+          for (int i = 0; i < kN * 16 / 32; ++i) {
+            const int e = lane + 32 * i, r = e >> 4, ch = e & 15;
+            const int c = c0 + r;
+            const char* src = nullptr;
+            if (c < nc) {
+              int sl = -1;
+              if (c - cbase < kMetaCap) {
+                sl = sm.mslot[c - cbase];
+              } else {
+                float unused;
+                cand_meta(a, h, c, sl, unused);
+              }
+              if (sl >= 0) src = (const char*)(a.K + ((size_t)h * a.C + sl) * kD);
+            }
+            tc::cp_async16(tile + tc::sw128_offset(r, ch, kN), src ? (const void*)(src + ch * 16) : (const void*)a.K,
+                           src ? 16u : 0u);
           }
+        }
+        tc::cp_async_commit();  // one group per iteration (empty past the last tile)
+        if (t >= kStages - 1) {
+          asm volatile("cp.async.wait_group %0;" ::"n"(kStages - 1) : "memory");
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&sm.full[(t - (kStages - 1)) % kStages]);
         }
       }
     }
-    tc::tc_fence_before();
-    __syncthreads();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    const uint32_t idesc = tc::idesc_bf16_f32(kM, kN, 0, 0);
+    if (ntiles > 0) ok = tc::mbar_wait(&sm.bar_a, 0);
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int s = t % kStages, b = t % kAcc;
+      ok = tc::mbar_wait(&sm.full[s], (uint32_t)(t / kStages) & 1u);
+      if (ok && t >= kAcc) ok = tc::mbar_wait(&sm.tempty[b], (uint32_t)((t / kAcc) - 1) & 1u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = tc::smem_u32(sm.A), b0 = tc::smem_u32(sm.B[s]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off_a = (kk >> 2) * kM * 128 + (kk & 3) * 32;
+          const uint32_t off_b = (kk >> 2) * kN * 128 + (kk & 3) * 32;
+          tc::mma_bf16(tmem + b * kN, tc::sdesc_kmajor_sw128(a0 + off_a), tc::sdesc_kmajor_sw128(b0 + off_b),
+                       idesc, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&sm.tfull[b]);
+        tc::mma_commit(&sm.empty[s]);
+      }
+      __syncwarp();
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.bar_a, 0));
+    const float na2 = row_sq_norm(sm.A, row, kM);
+    const float ia = na2 > 0.f ? 1.f / sqrtf(na2) : 0.f;
+    const int j = m0 + row;
+    if (half == 0 && blockIdx.y == 0 && j < a.n_f && a.invn_out)
+      a.invn_out[(size_t)h * a.n_f + j] = na2 > 0.f ? ia : __int_as_float(0x7fc00000);
+    float best = -INFINITY;
+    int best_slot = 0x7fffffff;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const int b = t % kAcc;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.tfull[b], (uint32_t)(t / kAcc) & 1u));
+      if (!ok) break;
+      tc::tc_fence_after();
+      const int c0 = (tb0 + t) * kN;
+      const int nval = min(kN, nc - c0);
+      const int col0 = half * 32;
+      if (col0 < nval) {
+        float v[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + b * kN + col0, v);
+        const int m_off = c0 + col0 - cbase;  // index of column col0 in the staged metadata
+        float cs[32];
+        if (m_off + 32 <= kMetaCap) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 ib = *reinterpret_cast<const float4*>(&sm.minv[m_off + i]);
+            cs[i] = v[i] * ib.x;
+            cs[i + 1] = v[i + 1] * ib.y;
+            cs[i + 2] = v[i + 2] * ib.z;
+            cs[i + 3] = v[i + 3] * ib.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            int sl = -1;
+            float ib = __int_as_float(0x7fc00000);
+            if (col0 + i < nval) cand_meta(a, h, c0 + col0 + i, sl, ib);
+            cs[i] = sl >= 0 ? v[i] * ib : __int_as_float(0x7fc00000);
+          }
+        }
+        // phase 1: the tile's largest cosine (NaN columns are ignored)
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, cs[i]);
+        // phase 2 (only when it can change the answer): the slot attaining it;
+        // several equal columns in one tile take the lowest slot
+        if (tmax >= best) {
+          int first = 0, neq = 0;
+#pragma unroll
+          for (int i = 31; i >= 0; --i) {
+            const bool e = cs[i] == tmax;
+            first = e ? i : first;
+            neq += e ? 1 : 0;
+          }
+          auto slot_at = [&](int i) -> int {
+            if (m_off + i < kMetaCap) return sm.mslot[m_off + i];
+            int sl;
+            float unused;
+            cand_meta(a, h, c0 + col0 + i, sl, unused);
+            return sl;
+          };
+          int smin = 0x7fffffff;
+          if (neq == 1) {
+            smin = slot_at(first);
+          } else if (neq > 1) {
+            for (int i = 0; i < 32; ++i)
+              if (cs[i] == tmax) smin = min(smin, slot_at(i));
+          }
+          if (neq > 0 && (tmax > best || smin < best_slot)) {
+            best = tmax;
+            best_slot = smin;
+          }
+        }
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.tempty[b]);
+    }
+    // merge the two column halves of each row (epilogue warps only)
+    if (half == 1) {
+      sm.half_best[row] = best;
+      sm.half_slot[row] = best_slot;
+    }
+    named_bar_sync(1, 256);
+    if (half == 0) {
+      const float b2 = sm.half_best[row];
+      const int s2 = sm.half_slot[row];
+      if (b2 > best || (b2 == best && s2 < best_slot)) {
+        best = b2;
+        best_slot = s2;
+      }
+      if (ok && j < a.n_f && na2 > 0.f && best_slot != 0x7fffffff)
+        atomicMax(a.best_out + (size_t)h * a.n_f + j, pack_best(best * ia, best_slot));
+    }
   }
-  tc::cp_async_wait_all();
-  const int j = m0 + tid;
-  if (!ok) {
-    if (tid == 0) status_set(st, FASTAR_ERR_TIMEOUT);
-  } else if (j < n_f) {
-    const int m = (na2 > 0.f && best >= tau) ? best_slot : -1;
-    match[(size_t)h * n_f + j] = m;
-    if (match_out) match_out[(size_t)h * Nrow + fi * n_f + j] = m;
-  }
+  if (!ok) status_set(st, FASTAR_ERR_TIMEOUT);
+  if (warp == 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  if (warp == 1) tc::tmem_dealloc(tmem, kAcc * kN);
 }
 
 }  // namespace
 
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
-                 int C, int D, const int32_t* cand, const int32_t* ncand, const int32_t* prev_slot,
-                 const int32_t* prev_kind, float tau, int32_t* match, int32_t* match_out, int32_t* st,
-                 cudaStream_t s) {
+                 int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
+                 const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
+                 float* invn_out, unsigned long long* best_out, int32_t* st, cudaStream_t s) {
   if (dt != FASTAR_BF16 || D != kD) return FASTAR_ERR_UNSUPPORTED;
   if (n_f == 0 || H == 0) return FASTAR_OK;
-  CUtensorMap mapA;
+  CUtensorMap mapA, mapB;
   if (make_tmap_bf16_2d(&mapA, k_new, (uint64_t)H * Nrow, kD, kM, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(&mapB, k_new, (uint64_t)H * Nrow, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   const size_t smem = sizeof(NnSmem) + 1024;
   if (cudaFuncSetAttribute(nn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  dim3 grid((n_f + kM - 1) / kM, H);
-  nn_tc_kernel<<<grid, 128, smem, s>>>(mapA, (const __nv_bfloat16*)k_new, n_f, Nrow, fi,
-                                       (const __nv_bfloat16*)K, C, cand, ncand, prev_slot, prev_kind,
-                                       tau, match, match_out, st);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  (void)cudaGetLastError();
+  // split the candidates so that about two CTAs run per SM and each CTA's
+  // candidate metadata fits its staging area (the expected candidate count
+  // is n_f: the groups the previous frame refreshed)
+  const int atiles = (n_f + kM - 1) / kM;
+  const int btiles = (n_f + kN - 1) / kN;
+  int split = (2 * sms + atiles * H - 1) / (atiles * H);
+  split = max(split, (btiles * kN + kMetaCap - 1) / kMetaCap);
+  split = max(1, min(split, min(16, btiles)));
+  NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, n_f, Nrow, fi, C, cand, ncand, cinv,
+           prev_slot, prev_kind, invn_prev, invn_out, best_out};
+  nn_tc_kernel<<<dim3(atiles, split, H), kThreads, smem, s>>>(mapA, mapB, a, st);
   FASTAR_LAUNCH_CHECK();
   return FASTAR_OK;
 }

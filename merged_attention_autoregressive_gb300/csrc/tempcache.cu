@@ -18,9 +18,13 @@
 //
 // Workspace (caller-owned, no initialisation needed):
 //   cand[2][H][C], ncand[2][H], rep_j[H][C], gcnt[H][C],
-//   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], evict[H][n_f]
+//   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], evict[H][n_f],
+//   best[H][n_f] (packed best candidate per key, see pack_best),
+//   cinv[H][C] (inverse norms of the first frame's candidates),
+//   invn[2][H][n_f] (inverse norms of the keys of the last two frames)
 // rep_j/gcnt are indexed by slot and reset for the candidate slots of each
-// frame before use (only candidates can be matched).
+// frame before use (only candidates can be matched); best is zeroed when a
+// call starts and again by each plan after it has read it.
 #include <math.h>
 
 #include <type_traits>
@@ -41,6 +45,9 @@ struct MergeWs {
   int32_t* plan_slot;
   int32_t* plan_kind;
   int32_t* evict;
+  unsigned long long* best;
+  float* cinv;
+  float* invn[2];
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -51,6 +58,9 @@ size_t merge_ws_bytes(int H, int n_f, int C) {
   b += 2 * align256((size_t)H * 4);       // ncand
   b += 2 * align256((size_t)H * C * 4);   // rep_j, gcnt
   b += 4 * align256((size_t)H * n_f * 4); // match, plan_slot, plan_kind, evict
+  b += align256((size_t)H * n_f * 8);     // best
+  b += align256((size_t)H * C * 4);       // cinv
+  b += 2 * align256((size_t)H * n_f * 4); // invn
   return b;
 }
 
@@ -68,6 +78,10 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
   w.plan_slot = take((size_t)H * n_f * 4);
   w.plan_kind = take((size_t)H * n_f * 4);
   w.evict = take((size_t)H * n_f * 4);
+  w.best = (unsigned long long*)take((size_t)H * n_f * 8);
+  w.cinv = (float*)take((size_t)H * C * 4);
+  w.invn[0] = (float*)take((size_t)H * n_f * 4);
+  w.invn[1] = (float*)take((size_t)H * n_f * 4);
   return w;
 }
 
@@ -75,7 +89,8 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
 __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* __restrict__ last_frame,
                                                                  const int32_t* __restrict__ size, int C,
                                                                  int32_t prev_frame, int32_t* cand,
-                                                                 int32_t* ncand, int32_t* st) {
+                                                                 int32_t* ncand, unsigned long long* best,
+                                                                 int n_f, int32_t* st) {
   __shared__ int sh[33];
   if (block_status_bad(st)) return;
   const int h = blockIdx.x;
@@ -92,6 +107,26 @@ __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* 
     base += tot;
   }
   if (threadIdx.x == 0) ncand[h] = base;
+  for (int j = threadIdx.x; j < n_f; j += blockDim.x) best[(size_t)h * n_f + j] = 0ull;
+}
+
+// Inverse norms of the first frame's candidates (bf16 rows of 128), one warp
+// per candidate, grid-stride over the device-side candidate count.
+__global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __restrict__ K, int C,
+                                                        const int32_t* __restrict__ cand,
+                                                        const int32_t* __restrict__ ncand, float* cinv,
+                                                        int32_t* st) {
+  if (status_bad(st)) return;
+  const int h = blockIdx.y, lane = threadIdx.x & 31;
+  const int nc = min(max(ncand[h], 0), C);
+  for (int c = blockIdx.x * 8 + (threadIdx.x >> 5); c < nc; c += gridDim.x * 8) {
+    const int s = cand[(size_t)h * C + c];
+    const uint2 u = *reinterpret_cast<const uint2*>(K + ((size_t)h * C + s) * 128 + lane * 4);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    const float n2 = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
+    if (lane == 0) cinv[(size_t)h * C + c] = n2 > 0.f ? 1.f / sqrtf(n2) : __int_as_float(0x7fc00000);
+  }
 }
 
 // ---------------------------------------------------------------- NN (SIMT)
@@ -99,9 +134,8 @@ template <typename T, int D>
 __global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_frame, int n_f, int row_stride_keys,
                                                       const T* __restrict__ K, int C,
                                                       const int32_t* __restrict__ cand,
-                                                      const int32_t* __restrict__ ncand, float tau,
-                                                      int32_t* __restrict__ match, int32_t* match_out,
-                                                      int match_out_stride, int32_t* st) {
+                                                      const int32_t* __restrict__ ncand,
+                                                      unsigned long long* __restrict__ best_out, int32_t* st) {
   constexpr int PER = D / 32;
   if (status_bad(st)) return;
   const int h = blockIdx.y;
@@ -144,16 +178,14 @@ __global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_fr
       }
     }
   }
-  if (lane == 0) {
-    const int m = (best >= tau) ? best_slot : -1;
-    match[(size_t)h * n_f + j] = m;
-    if (match_out) match_out[(size_t)h * match_out_stride + j] = m;
-  }
+  if (lane == 0) best_out[(size_t)h * n_f + j] = best_slot != 0x7fffffff ? pack_best(best, best_slot) : 0ull;
 }
 
 // ---------------------------------------------------------------- plan
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int32_t f,
-                                                            const int32_t* __restrict__ match,
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int32_t f, float tau,
+                                                            unsigned long long* __restrict__ best,
+                                                            int32_t* __restrict__ match_out, int match_off,
+                                                            int match_stride, int32_t* __restrict__ match,
                                                             const int32_t* __restrict__ cand_cur,
                                                             const int32_t* __restrict__ ncand_cur,
                                                             int32_t* __restrict__ cand_next,
@@ -178,6 +210,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
   int32_t* gc = gcnt + (size_t)h * C;
   const int32_t* lf = last_frame + (size_t)h * C;
   const int nc = ncand_cur[h];
+  // 0. the NN decision of every key: best candidate if its cosine reaches tau
+  for (int j = threadIdx.x; j < n_f; j += blockDim.x) {
+    unsigned long long* bp = best + (size_t)h * n_f + j;
+    const unsigned long long key = *bp;
+    const int mj = (key != 0ull && best_cos(key) >= tau) ? best_slot(key) : -1;
+    match[(size_t)h * n_f + j] = mj;
+    if (match_out) match_out[(size_t)h * match_stride + match_off + j] = mj;
+    *bp = 0ull;
+  }
+  __syncthreads();
   // 1. reset the group accumulators of the candidate slots
   for (int c = threadIdx.x; c < nc; c += blockDim.x) {
     const int s = cc[c];
@@ -385,9 +427,9 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
 }
 
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
-                 int C, int D, const int32_t* cand, const int32_t* ncand, const int32_t* prev_slot,
-                 const int32_t* prev_kind, float tau, int32_t* match, int32_t* match_out, int32_t* st,
-                 cudaStream_t s);
+                 int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
+                 const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
+                 float* invn_out, unsigned long long* best_out, int32_t* st, cudaStream_t s);
 
 template <typename T, int D>
 static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
@@ -397,30 +439,36 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
   MergeWs w = carve(ws, H, n_f, C);
   const int Nrow = F * n_f;
   cand_init_kernel<<<H, kPlanThreads, 0, s>>>(c->last_frame, c->size, C, first_frame - 1,
-                                              w.cand[0], w.ncand[0], st);
+                                              w.cand[0], w.ncand[0], w.best, n_f, st);
   FASTAR_LAUNCH_CHECK();
   const dim3 wgrid((n_f + 7) / 8, H), wblock(256);
+  const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
+  if (tc_nn) {
+    cand_norm_kernel<<<wgrid, wblock, 0, s>>>((const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
+                                              st);
+    FASTAR_LAUNCH_CHECK();
+  }
   for (int fi = 0; fi < F; ++fi) {
     const int cur = fi & 1, nxt = cur ^ 1;
     const int32_t f = first_frame + fi;
     const T* kf = (const T*)k_new + (size_t)fi * n_f * D;
     const T* vf = (const T*)v_new + (size_t)fi * n_f * D;
     const uint32_t* cf = codes_new + (size_t)fi * n_f;
-    int32_t* mo = match_out ? match_out + (size_t)fi * n_f : nullptr;
-    int rc = launch_nn_tc(std::is_same<T, float>::value ? FASTAR_F32 : FASTAR_BF16, k_new, n_f, Nrow,
-                          H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.plan_slot, w.plan_kind, tau,
-                          w.match, match_out, st, s);
+    int rc = FASTAR_ERR_UNSUPPORTED;
+    if (tc_nn)
+      rc = launch_nn_tc(FASTAR_BF16, k_new, n_f, Nrow, H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.cinv,
+                        w.plan_slot, w.plan_kind, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.best, st, s);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       nn_simt_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
-                                                    w.ncand[cur], tau, w.match, mo, Nrow, st);
+                                                    w.ncand[cur], w.best, st);
       FASTAR_LAUNCH_CHECK();
     } else if (rc != FASTAR_OK) {
       return rc;
     }
-    plan_kernel<<<H, kPlanThreads, 0, s>>>(n_f, C, f, w.match, w.cand[cur], w.ncand[cur],
-                                           w.cand[nxt], w.ncand[nxt], w.rep_j, w.gcnt, w.plan_slot,
-                                           w.plan_kind, w.evict, c->last_frame, c->m, c->size,
-                                           c->inserted, c->evicted, st);
+    plan_kernel<<<H, kPlanThreads, 0, s>>>(n_f, C, f, tau, w.best, match_out, fi * n_f, Nrow, w.match,
+                                           w.cand[cur], w.ncand[cur], w.cand[nxt], w.ncand[nxt], w.rep_j,
+                                           w.gcnt, w.plan_slot, w.plan_kind, w.evict, c->last_frame, c->m,
+                                           c->size, c->inserted, c->evicted, st);
     FASTAR_LAUNCH_CHECK();
     apply_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
                                                 w.plan_kind, w.gcnt, (T*)c->K, (T*)c->V, c->m,
