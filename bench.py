@@ -212,7 +212,14 @@ def run_reference(args, cfg):
 
 # ----------------------------------------------------------------- GPU leg
 def algorithmic(cfg, path, match, snap_size, snap_lf):
-    """Algorithmic bytes and flops of each stage of one step (see DESIGN)."""
+    """Algorithmic bytes and flops of one step, per stage and per kernel.
+
+    Bytes count each input read once and each output written once; flops
+    are 2*M*N*K for a GEMM and 4*D per (query, key) pair of attention.
+    Returns (bytes per stage, flops per stage, per-kernel models, stats);
+    a per-kernel model gives the bytes and flops of one launch (averaged over
+    the launches of that kernel in a step).
+    """
     import torch
     H, D, T, Nq, P, n_f, F = cfg.H, cfg.D, cfg.T, cfg.Nq, cfg.P, cfg.n_f, cfg.F
     e = 2 if cfg.dtype == "bf16" else 4
@@ -225,19 +232,17 @@ def algorithmic(cfg, path, match, snap_size, snap_lf):
     # merge: new k, v read; candidate K read; matched V read; K, V written for
     # touched slots; per-slot metadata; cache CSR (codes read, perm written)
     mt = match.view(H, F, n_f)
-    touched = 0
     cand = []
     prev_cnt = int(((snap_lf == cfg.past_frames - 1) & (torch.arange(cfg.C, device=snap_lf.device)[None]
                                                          < snap_size[:, None])).sum())
+    by["merge"] = 0
     for fi in range(F):
         cand.append(prev_cnt)
         m = mt[:, fi]
         n_matched = int((m >= 0).sum())
         n_groups = sum(int(torch.unique(m[h][m[h] >= 0]).numel()) for h in range(H))
         t_f = n_groups + int((m < 0).sum())
-        touched += t_f
         prev_cnt = t_f
-        by.setdefault("merge", 0)
         by["merge"] += (2 * H * n_f * D * e + cand[-1] * D * e + n_matched * D * e
                         + 2 * t_f * D * e + t_f * (4 * 2 + T * 4) + H * n_f * 4 * 4)
     by["merge"] += n_live * T * (4 + 4) + H * T * ((1 << cfg.B) + 1) * 4
@@ -245,24 +250,63 @@ def algorithmic(cfg, path, match, snap_size, snap_lf):
     by["annca"] = H * Nq * D * e * 2 + kept * 2 * D * e + H * F * P * 4
     by["annsa"] = (H * Nq * D * e * 2 + H * T * Nq * 4 + n_live * (2 * D * e + 4 + 2 * T * 4)
                    + H * Nq * 4)
-    # flops: hash GEMM, NN GEMM, attention 4*D per allowed pair
-    fl = {"hash": 2 * rows * T * cfg.B * D,
-          "merge": sum(2 * D * n_f * c for c in cand),
-          "prune": 0,
-          "annca": 4 * D * n_f * kept}
-    pairs = 0
+    # allowed pairs, split by the first table in which they collide
+    pairs_t = [0] * T
     qc = path.q_codes.long()
     for h in range(H):
         n = int(size[h])
         cc = path.cache.codes[h, :, :n].long()
         for q0 in range(0, Nq, 1024):
-            allowed = torch.zeros(min(1024, Nq - q0), n, dtype=torch.bool, device=qc.device)
+            seen = torch.zeros(min(1024, Nq - q0), n, dtype=torch.bool, device=qc.device)
             for t in range(T):
-                allowed |= qc[h, t, q0:q0 + 1024, None] == cc[t][None]
-            pairs += int(allowed.sum())
-    fl["annsa"] = 4 * D * pairs
-    return by, fl, {"n_live": n_live, "kept": kept, "allowed_pairs": pairs,
-                    "density": pairs / max(1, Nq * n_live)}
+                hit = (qc[h, t, q0:q0 + 1024, None] == cc[t][None]) & ~seen
+                pairs_t[t] += int(hit.sum())
+                seen |= hit
+    pairs = sum(pairs_t)
+    nn_flops = [2 * D * n_f * c for c in cand]
+    fl = {"hash": 2 * rows * T * cfg.B * D, "merge": sum(nn_flops), "prune": 0,
+          "annca": 4 * D * n_f * kept, "annsa": 4 * D * pairs}
+    kern = {
+        "nn_tc": {"flops": sum(nn_flops) / F,
+                  "bytes": sum((H * n_f + c) * D * e for c in cand) / F},
+        "annca_tc": {"flops": fl["annca"], "bytes": by["annca"]},
+        "annsa_tc": {"flops": fl["annsa"] / T,
+                     "bytes": (H * Nq * D * e + n_live * (2 * D * e + 4 + 2 * T * 4)) / 1.0 + H * Nq * D * 4},
+        "hash_tc": {"flops": 2 * rows * T * cfg.B * D / 3, "bytes": (rows * (D * e + T * 4)) / 3},
+        "apply": {"flops": 0, "bytes": by["merge"] / F * 0.5},
+    }
+    return by, fl, kern, {"n_live": n_live, "kept": kept, "allowed_pairs": pairs,
+                          "allowed_pairs_by_table": pairs_t,
+                          "density": pairs / max(1, Nq * n_live)}
+
+
+KERNEL_SOURCES = {"nn_tc": "nn_tc.cu", "annca_tc": "attention_tc.cu", "annsa_tc": "attention_tc.cu",
+                  "hash_tc": "hash_tc.cu"}
+
+
+def profiled_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/traffic_<kernel>.txt), or None when there is none or the
+    kernel's source has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}.txt")
+    src = KERNEL_SOURCES.get(kernel)
+    if not src or not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    with open(os.path.join(ROOT, "merged_attention_autoregressive_gb300", "csrc", src), "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()[:16]
+    if vals.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def dense_reference_ms(cfg, d, reps=10):
@@ -388,6 +432,20 @@ def run_ours(args, cfg):
         total_ms = float(t.item())
     value = total_ms / (args.steps * world)
 
+    # per-kernel durations: a separate pass with the library's launch timer
+    # (same restore + L2 flush protocol), events on the launch stream
+    timer = fa.LaunchTimer(64)
+    per_kernel = {}
+    n_tsteps = min(args.steps, 50)
+    for i in range(n_tsteps):
+        prep()
+        timer.begin()
+        step()
+        for name, ms_k in timer.end():
+            per_kernel.setdefault(name, []).append(ms_k)
+    kernels = {k: {"launches_per_step": len(v) / n_tsteps, "avg_ms": statistics.mean(v),
+                   "ms_per_step": sum(v) / n_tsteps} for k, v in per_kernel.items()}
+
     # end to end through the C ABI with host buffers (pinned), copies timed
     hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
     hkp, hvp = kp.cpu().pin_memory(), vp.cpu().pin_memory()
@@ -412,13 +470,19 @@ def run_ours(args, cfg):
     e2e_ms = statistics.mean(e2e)
 
     # algorithmic work of the step (from the last step's outputs)
-    by, fl, stats = algorithmic(cfg, path, path.match.clone(), snap["size"], snap["last_frame"])
+    by, fl, kern, stats = algorithmic(cfg, path, path.match.clone(), snap["size"], snap["last_frame"])
     pk = peaks()
-    dom = max(stage_ms, key=stage_ms.get)
-    if fl[dom] / (pk["bf16_tflops"] * 1e12) > by[dom] / (pk["hbm_gbs"] * 1e9):
-        bound, achieved, peak, unit = "tensor", fl[dom] / stage_ms[dom] / 1e9, pk["bf16_tflops"], "TFLOP/s"
+    # roofline of the kernel with the largest device time per step
+    dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
+    km = kern.get(dom, {"flops": 0, "bytes": 0})
+    kms = kernels[dom]["avg_ms"]
+    t_tc = km["flops"] / (pk["bf16_tflops"] * 1e12)
+    t_bw = km["bytes"] / (pk["hbm_gbs"] * 1e9)
+    if t_tc >= t_bw:
+        bound, achieved, peak, unit = "tensor", km["flops"] / kms / 1e9, pk["bf16_tflops"], "TFLOP/s"
     else:
-        bound, achieved, peak, unit = "hbm", by[dom] / stage_ms[dom] / 1e6, pk["hbm_gbs"], "GB/s"
+        bound, achieved, peak, unit = "hbm", km["bytes"] / kms / 1e6, pk["hbm_gbs"], "GB/s"
+    traffic = profiled_traffic(dom)
     eff_tflops = sum(fl.values()) / ms / 1e9
     line = {"metric": METRIC, "value": value, "unit": "ms/chunk", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -431,9 +495,12 @@ def run_ours(args, cfg):
             "effective_tflops": eff_tflops,
             "stages_ms": stage_ms,
             "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
-                         "unit": unit, "frac": achieved / peak, "traffic": None,
-                         "peak_source": pk["source"],
-                         "algorithmic_bytes": by[dom], "algorithmic_flops": fl[dom]},
+                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
+                         "peak_source": pk["source"] + " (burst)",
+                         "avg_launch_ms": kms, "launches_per_step": kernels[dom]["launches_per_step"],
+                         "algorithmic_bytes_per_launch": km["bytes"],
+                         "algorithmic_flops_per_launch": km["flops"]},
+            "kernels": kernels,
             "stage_rooflines": {s: {"GB/s": by[s] / stage_ms[s] / 1e6,
                                     "hbm_frac": by[s] / stage_ms[s] / 1e6 / pk["hbm_gbs"],
                                     "TFLOP/s": fl[s] / stage_ms[s] / 1e9} for s in stages},

@@ -74,6 +74,20 @@ int fastar_version(void);
  * devices and threads; a diagnostic, e.g. to count launches per step). */
 uint64_t fastar_launch_count(void);
 
+/* Per-kernel launch timing (a diagnostic).  fastar_timing_begin hands the
+ * library `capacity` events the caller created (cudaEventCreate, timing
+ * enabled); until fastar_timing_end, the library records the next unused
+ * event on the launch stream right after each kernel it launches, so the
+ * time between consecutive events of one stream is the duration of the
+ * kernel in between (the caller records its own event before the first
+ * call).  fastar_timing_end stops recording and returns how many events were
+ * recorded; fastar_timing_name(i) names the kernel that event i follows
+ * (a static string; "" out of range).  Timing is process-wide: use it from
+ * one thread.  NULL/0 disables it.  The library allocates nothing for it. */
+int fastar_timing_begin(cudaEvent_t* events, int capacity);
+int fastar_timing_end(void);
+const char* fastar_timing_name(int i);
+
 /*
  * Bytes of workspace a call needs.  Arguments that an op does not use are
  * ignored.  op: FASTAR_OP_*; H heads; N rows per head (hash: N; merge:
@@ -186,13 +200,14 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
  * library's device memory, held by every GPU that loads the library until
  * the process exits.  Returns FASTAR_ERR_WORKSPACE when the merge needs more
  * (fastar_workspace_size(FASTAR_OP_MERGE, ...) > FASTAR_NOALLOC_SCRATCH_BYTES;
- * e.g. 12 heads x C 32768 x n_f 1560 needs 6.3 MiB and fits).  All calls
+ * e.g. 12 heads x C 32768 x n_f 1560 needs about 8.1 MiB and fits, 40 heads
+ * x n_f 3600 needs about 29 MiB and is refused).  All calls
  * share the array, so calls that overlap on the GPU race and must be ordered
  * by the caller; it keeps the last call's contents (the merge needs none of
  * it zeroed).  The first call on a device looks up the array's address with
  * that device current; make it before any stream capture.
  */
-#define FASTAR_NOALLOC_SCRATCH_BYTES (8u << 20)
+#define FASTAR_NOALLOC_SCRATCH_BYTES (16u << 20)
 int fastar_tempcache_merge_noalloc(const fastar_cache* cache, const void* k_new,
                                    const void* v_new, const uint32_t* codes_new,
                                    int F, int n_f, int32_t first_frame, float tau,

@@ -23,6 +23,7 @@ STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "
           4: "FASTAR_ERR_WORKSPACE", 16: "FASTAR_ERR_CAPACITY", 17: "FASTAR_ERR_TIMEOUT",
           18: "FASTAR_ERR_DEVICE_ARG"}
 EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
+           "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
            "fastar_workspace_size", "fastar_hash",
            "fastar_tempcache_merge", "fastar_annca_prune", "fastar_annca_attention",
            "fastar_annsa_attention"]
@@ -60,6 +61,11 @@ def lib() -> ctypes.CDLL:
         L.fastar_status_string.argtypes = [_I]
         L.fastar_version.restype = _I
         L.fastar_launch_count.restype = ctypes.c_uint64
+        L.fastar_timing_begin.argtypes = [_VP, _I]
+        L.fastar_timing_begin.restype = _I
+        L.fastar_timing_end.restype = _I
+        L.fastar_timing_name.argtypes = [_I]
+        L.fastar_timing_name.restype = ctypes.c_char_p
         L.fastar_workspace_size.restype = _SZ
         L.fastar_workspace_size.argtypes = [_I] * 7
         L.fastar_hash.argtypes = [_I, _VP, _I, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
@@ -70,7 +76,7 @@ def lib() -> ctypes.CDLL:
                                              _VP, _VP, _SZ, _VP, _VP]
         L.fastar_annsa_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _I, ctypes.POINTER(CacheStruct),
                                              _F, _VP, _VP, _VP, _SZ, _VP, _VP]
-        for name in EXPORTS[4:]:
+        for name in EXPORTS[7:]:
             getattr(L, name).restype = _I
         _lib = L
     return _lib
@@ -106,6 +112,37 @@ def _check(rc: int, where: str):
 def fastar_launch_count() -> int:
     """Kernels launched by the library so far in this process."""
     return int(lib().fastar_launch_count())
+
+
+class LaunchTimer:
+    """Per-kernel device durations of the library's launches (diagnostic).
+
+    Usage: t = LaunchTimer(n); t.begin(); <calls on the current stream>;
+    t.end() -> [(kernel name, ms), ...] in launch order.
+    """
+
+    def __init__(self, capacity: int):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.events:          # create the underlying CUDA events now
+            e.record()
+        self.start = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        self._handles = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.events])
+
+    def begin(self):
+        self.start.record()
+        _check(lib().fastar_timing_begin(ctypes.cast(self._handles, ctypes.c_void_p), len(self.events)),
+               "fastar_timing_begin")
+
+    def end(self):
+        n = int(lib().fastar_timing_end())
+        names = [lib().fastar_timing_name(i).decode() for i in range(n)]
+        torch.cuda.synchronize()
+        out, prev = [], self.start
+        for i in range(n):
+            out.append((names[i], prev.elapsed_time(self.events[i])))
+            prev = self.events[i]
+        return out
 
 
 def fastar_workspace_size(op: int, H: int, N: int, D: int, T: int, B: int, C: int) -> int:

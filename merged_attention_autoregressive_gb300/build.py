@@ -71,11 +71,7 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + ".tmp"
-    stubs = "/usr/local/cuda/lib64/stubs"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static"]
-    if os.path.isdir(stubs):
-        cmd += ["-L", stubs]
-    cmd += ["-lcuda", "-lpthread", "-ldl", "-lrt"]
+    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lpthread", "-ldl", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

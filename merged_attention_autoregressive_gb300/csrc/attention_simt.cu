@@ -141,7 +141,7 @@ int launch_annca_simt(fastar_dtype dt, const void* q, const void* k_p, const voi
   else if (dt == FASTAR_BF16 && D == 128) ANNCA_CASE(__nv_bfloat16, 128);
   else return FASTAR_ERR_UNSUPPORTED;
 #undef ANNCA_CASE
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "annca_simt");
   return FASTAR_OK;
 }
 
@@ -162,7 +162,7 @@ int launch_annsa_simt(fastar_dtype dt, const void* q, const uint32_t* q_codes, i
   else if (dt == FASTAR_BF16 && c->D == 128) ANNSA_CASE(__nv_bfloat16, 128);
   else return FASTAR_ERR_UNSUPPORTED;
 #undef ANNSA_CASE
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "annsa_simt");
   return FASTAR_OK;
 }
 

@@ -436,7 +436,7 @@ int launch_attn(const CUtensorMap& map, dim3 grid, int H, int Nq, float scale, c
     return FASTAR_ERR_CUDA;
   }
   attn_tc_kernel<kT><<<grid, 128, smem, s>>>(map, H, Nq, scale, ca, sa, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, kT < 0 ? "annca_tc" : "annsa_tc");
   return FASTAR_OK;
 }
 
@@ -490,7 +490,7 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   if (rc != FASTAR_OK) return rc;
   annsa_combine_kernel<<<dim3((Nq + 7) / 8, c->H), 256, 0, s>>>(sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "annsa_combine");
   return FASTAR_OK;
 }
 

@@ -169,12 +169,15 @@ size_t annsa_ws_bytes(int H, int Nq, int D, int T);
 }  // namespace fastar
 
 namespace fastar {
-void count_launch();
+// Called after every kernel launch of the library: counts it and, while
+// launch timing is on (fastar_timing_begin), records the next caller event
+// on the launch stream, tagged with the kernel's name.
+void after_launch(cudaStream_t s, const char* name);
 }
 
-#define FASTAR_LAUNCH_CHECK()                                   \
+#define FASTAR_LAUNCHED(stream, name)                           \
   do {                                                          \
-    fastar::count_launch();                                     \
+    fastar::after_launch((stream), (name));                     \
     if (cudaPeekAtLastError() != cudaSuccess) {                 \
       (void)cudaGetLastError();                                 \
       return FASTAR_ERR_CUDA;                                   \

@@ -98,7 +98,7 @@ int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_d
   }
   csr_kernel<<<G, kCsrThreads, smem, s>>>(keys, N, n_dev, n_div > 0 ? n_div : 1, nb, W, perm,
                                           offsets, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "csr");
   return FASTAR_OK;
 }
 

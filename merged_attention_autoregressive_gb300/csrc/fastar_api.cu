@@ -4,12 +4,29 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "common.cuh"
 
 namespace fastar {
 static std::atomic<uint64_t> g_launches{0};
-void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// launch timing: caller-created events, recorded after each launch
+static std::mutex g_tmu;
+static std::atomic<int> g_timing{0};
+static cudaEvent_t* g_tev = nullptr;
+static int g_tcap = 0, g_tn = 0;
+static const char* g_tname[4096];
+
+void after_launch(cudaStream_t s, const char* name) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_timing.load(std::memory_order_acquire)) return;
+  std::lock_guard<std::mutex> lock(g_tmu);
+  if (g_tev && g_tn < g_tcap && g_tn < 4096) {
+    if (cudaEventRecord(g_tev[g_tn], s) == cudaSuccess) g_tname[g_tn++] = name;
+    else (void)cudaGetLastError();
+  }
+}
 
 int launch_hash_simt(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes,
                      int T, int B, uint32_t* codes, int32_t* st, cudaStream_t s);
@@ -81,6 +98,29 @@ const char* fastar_status_string(int status) {
 int fastar_version(void) { return 100; }
 
 uint64_t fastar_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int fastar_timing_begin(cudaEvent_t* events, int capacity) {
+  if (capacity < 0 || (capacity > 0 && !events)) return FASTAR_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_tmu);
+  g_tev = events;
+  g_tcap = capacity;
+  g_tn = 0;
+  g_timing.store(capacity > 0 ? 1 : 0, std::memory_order_release);
+  return FASTAR_OK;
+}
+
+int fastar_timing_end(void) {
+  std::lock_guard<std::mutex> lock(g_tmu);
+  g_timing.store(0, std::memory_order_release);
+  g_tev = nullptr;
+  g_tcap = 0;
+  return g_tn;
+}
+
+const char* fastar_timing_name(int i) {
+  std::lock_guard<std::mutex> lock(g_tmu);
+  return (i >= 0 && i < g_tn) ? g_tname[i] : "";
+}
 
 size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C) {
   (void)B;

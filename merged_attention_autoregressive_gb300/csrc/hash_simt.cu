@@ -58,7 +58,7 @@ int launch_hash_simt(fastar_dtype dt, const void* x, int H, int N, int D, const 
     hash_warp_kernel<__nv_bfloat16, 128><<<grid, block, 0, s>>>((const __nv_bfloat16*)x, rows, (const __nv_bfloat16*)planes, T, B, N, codes, st);
   else
     return FASTAR_ERR_UNSUPPORTED;
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "hash_warp");
   return FASTAR_OK;
 }
 

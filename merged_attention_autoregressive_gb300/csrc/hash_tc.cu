@@ -158,7 +158,7 @@ int launch_hash_tc(fastar_dtype dt, const void* x, int H, int N, int D, const vo
   }
   hash_tc_kernel<<<grid, 128, smem, s>>>(mapX, (const __nv_bfloat16*)planes, TB, NP, T, B, N, rows, ntiles,
                                          codes, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "hash_tc");
   return FASTAR_OK;
 }
 

@@ -11,7 +11,7 @@
 // identical.
 //
 // Costs and limits:
-//   * the array is FASTAR_NOALLOC_SCRATCH_BYTES (8 MiB) of device memory,
+//   * the array is FASTAR_NOALLOC_SCRATCH_BYTES (16 MiB) of device memory,
 //     held by every GPU that loads this library until the process exits;
 //   * problems whose merge workspace (fastar_workspace_size with
 //     FASTAR_OP_MERGE) exceeds it are rejected with FASTAR_ERR_WORKSPACE;

@@ -369,7 +369,7 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
   NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, n_f, Nrow, fi, C, cand, ncand, cinv,
            prev_slot, prev_kind, invn_prev, invn_out, best_out};
   nn_tc_kernel<<<dim3(atiles, split, H), kThreads, smem, s>>>(mapA, mapB, a, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "nn_tc");
   return FASTAR_OK;
 }
 

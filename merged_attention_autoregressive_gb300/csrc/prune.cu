@@ -61,7 +61,7 @@ int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F,
   if (smem > 48 * 1024) return FASTAR_ERR_UNSUPPORTED;
   prune_kernel<<<dim3(F, H), kPruneThreads, smem, s>>>(q_codes, p_codes, F, n_f, P, T, B, kept_idx,
                                                        kept_cnt, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "prune");
   return FASTAR_OK;
 }
 

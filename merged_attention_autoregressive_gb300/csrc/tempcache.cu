@@ -440,13 +440,13 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
   const int Nrow = F * n_f;
   cand_init_kernel<<<H, kPlanThreads, 0, s>>>(c->last_frame, c->size, C, first_frame - 1,
                                               w.cand[0], w.ncand[0], w.best, n_f, st);
-  FASTAR_LAUNCH_CHECK();
+  FASTAR_LAUNCHED(s, "cand_init");
   const dim3 wgrid((n_f + 7) / 8, H), wblock(256);
   const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
   if (tc_nn) {
     cand_norm_kernel<<<wgrid, wblock, 0, s>>>((const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
                                               st);
-    FASTAR_LAUNCH_CHECK();
+    FASTAR_LAUNCHED(s, "cand_norm");
   }
   for (int fi = 0; fi < F; ++fi) {
     const int cur = fi & 1, nxt = cur ^ 1;
@@ -461,7 +461,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       nn_simt_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], w.best, st);
-      FASTAR_LAUNCH_CHECK();
+      FASTAR_LAUNCHED(s, "nn_simt");
     } else if (rc != FASTAR_OK) {
       return rc;
     }
@@ -469,11 +469,11 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
                                            w.cand[cur], w.ncand[cur], w.cand[nxt], w.ncand[nxt], w.rep_j,
                                            w.gcnt, w.plan_slot, w.plan_kind, w.evict, c->last_frame, c->m,
                                            c->size, c->inserted, c->evicted, st);
-    FASTAR_LAUNCH_CHECK();
+    FASTAR_LAUNCHED(s, "plan");
     apply_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
                                                 w.plan_kind, w.gcnt, (T*)c->K, (T*)c->V, c->m,
                                                 c->codes, c->last_frame, C, st);
-    FASTAR_LAUNCH_CHECK();
+    FASTAR_LAUNCHED(s, "apply");
   }
   return launch_csr(c->codes, H * Tt, C, c->size, Tt, 1 << c->B, c->perm, c->offsets, st, s);
 }

@@ -41,6 +41,8 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     cs = fa.CacheStruct(40, 128, 32768, 2, 10, 0, *([fake] * 10))
     rc = f(ctypes.byref(cs), fake, fake, fake, 3, 3600, 0, 0.95, None, None, None)
     assert rc == ERR_WORKSPACE
+    # the one-layer workload (12 heads, C 32768, 1560 tokens per frame) fits
+    assert fa.fastar_workspace_size(fa.OP_MERGE, 12, 1560, 128, 2, 8, 32768) <= 16 << 20
 
 
 @pytest.mark.gpu
