@@ -11,11 +11,13 @@
 // SM).  The new keys arrive by TMA (two 64-column boxes, 128-byte swizzle).
 // The slots and inverse norms of the CTA's candidates are staged in shared
 // memory once.  The CTA is warp-specialised:
-//   warp 0     producer: fills a 4-stage ring of 64-row candidate tiles.
-//              After the first frame of a call the candidates are the rows of
-//              the previous frame, contiguous in k_new, and come by TMA; for
-//              the first frame they are scattered cache rows, gathered with
-//              cp.async into the same swizzled layout;
+//   warp 0     producer: fills a 4-stage ring of 64-row candidate tiles by
+//              TMA.  After the first frame of a call the candidates are the
+//              rows of the previous frame, contiguous in k_new; for the first
+//              frame they are cache rows that an earlier kernel copied, in
+//              candidate order, into a contiguous staging buffer.  A head
+//              with more first-frame candidates than the staging buffer holds
+//              gathers its scattered cache rows with cp.async instead;
 //   warp 1     one thread issues 8 MMAs (M 128, N 64, K 16) per tile into one
 //              of four 64-column fp32 TMEM accumulators; the MMA commit frees
 //              the tile's stage;
@@ -106,6 +108,7 @@ __device__ __forceinline__ void cand_meta(const NnArgs& a, int h, int c, int& sl
 
 __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constant__ CUtensorMap mapA,
                                                            const __grid_constant__ CUtensorMap mapB,
+                                                           const __grid_constant__ CUtensorMap mapS,
                                                            NnArgs a, int32_t* st) {
   extern __shared__ uint8_t smem_raw[];
   NnSmem& sm = *reinterpret_cast<NnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
     tc::fence_mbar_init();
     tc::prefetch_tensormap(&mapA);
     tc::prefetch_tensormap(&mapB);
+    if (a.fi == 0) tc::prefetch_tensormap(&mapS);
     const int row0 = h * a.Nrow + a.fi * a.n_f + m0;
     tc::mbar_arrive_expect_tx(&sm.bar_a, kM * kD * 2);
     tc::tma_load_2d(sm.A, &mapA, &sm.bar_a, 0, row0);
@@ -157,17 +161,21 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
-    if (a.fi > 0) {
-      // contiguous candidate rows: one TMA per 64-column half of a tile
+    if (a.fi > 0 || nc <= a.n_f) {
+      // contiguous candidate rows (k_new of the previous frame, or the
+      // staging copy of the first frame's candidates): one TMA per 64-column
+      // half of a tile
+      const CUtensorMap* map = a.fi > 0 ? &mapB : &mapS;
+      const int rbase = a.fi > 0 ? h * a.Nrow + (a.fi - 1) * a.n_f : h * a.n_f;
       if (lane == 0) {
         for (int t = 0; t < ntiles && ok; ++t) {
           const int s = t % kStages;
           if (t >= kStages) ok = tc::mbar_wait(&sm.empty[s], (uint32_t)((t / kStages) - 1) & 1u);
           if (!ok) break;
-          const int row = h * a.Nrow + (a.fi - 1) * a.n_f + (tb0 + t) * kN;
+          const int row = rbase + (tb0 + t) * kN;
           tc::mbar_arrive_expect_tx(&sm.full[s], kN * kD * 2);
-          tc::tma_load_2d(sm.B[s], &mapB, &sm.full[s], 0, row);
-          tc::tma_load_2d(sm.B[s] + kN * 128, &mapB, &sm.full[s], 64, row);
+          tc::tma_load_2d(sm.B[s], map, &sm.full[s], 0, row);
+          tc::tma_load_2d(sm.B[s] + kN * 128, map, &sm.full[s], 64, row);
         }
       }
     } else {
@@ -343,12 +351,14 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
                  int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
                  const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
-                 float* invn_out, unsigned long long* best_out, int32_t* st, cudaStream_t s) {
+                 float* invn_out, unsigned long long* best_out, const void* stage, int32_t* st,
+                 cudaStream_t s) {
   if (dt != FASTAR_BF16 || D != kD) return FASTAR_ERR_UNSUPPORTED;
   if (n_f == 0 || H == 0) return FASTAR_OK;
-  CUtensorMap mapA, mapB;
+  CUtensorMap mapA, mapB, mapS;
   if (make_tmap_bf16_2d(&mapA, k_new, (uint64_t)H * Nrow, kD, kM, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   if (make_tmap_bf16_2d(&mapB, k_new, (uint64_t)H * Nrow, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(&mapS, stage, (uint64_t)H * n_f, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   const size_t smem = sizeof(NnSmem) + 1024;
   if (cudaFuncSetAttribute(nn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
@@ -368,7 +378,7 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
   split = max(1, min(split, min(16, btiles)));
   NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, n_f, Nrow, fi, C, cand, ncand, cinv,
            prev_slot, prev_kind, invn_prev, invn_out, best_out};
-  nn_tc_kernel<<<dim3(atiles, split, H), kThreads, smem, s>>>(mapA, mapB, a, st);
+  nn_tc_kernel<<<dim3(atiles, split, H), kThreads, smem, s>>>(mapA, mapB, mapS, a, st);
   FASTAR_LAUNCHED(s, "nn_tc");
   return FASTAR_OK;
 }

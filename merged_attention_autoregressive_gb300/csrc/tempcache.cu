@@ -21,6 +21,8 @@
 //   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], evict[H][n_f],
 //   best[H][n_f] (packed best candidate per key, see pack_best),
 //   cinv[H][C] (inverse norms of the first frame's candidates),
+//   stage[H][n_f][128] bf16 (copies of the first n_f first-frame candidate
+//   rows, contiguous, so that the NN kernel can load them by TMA),
 //   invn[2][H][n_f] (inverse norms of the keys of the last two frames)
 // rep_j/gcnt are indexed by slot and reset for the candidate slots of each
 // frame before use (only candidates can be matched); best is zeroed when a
@@ -48,6 +50,7 @@ struct MergeWs {
   unsigned long long* best;
   float* cinv;
   float* invn[2];
+  __nv_bfloat16* stage;
 };
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -61,6 +64,7 @@ size_t merge_ws_bytes(int H, int n_f, int C) {
   b += align256((size_t)H * n_f * 8);     // best
   b += align256((size_t)H * C * 4);       // cinv
   b += 2 * align256((size_t)H * n_f * 4); // invn
+  b += align256((size_t)H * n_f * 128 * 2); // stage
   return b;
 }
 
@@ -82,6 +86,7 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
   w.cinv = (float*)take((size_t)H * C * 4);
   w.invn[0] = (float*)take((size_t)H * n_f * 4);
   w.invn[1] = (float*)take((size_t)H * n_f * 4);
+  w.stage = (__nv_bfloat16*)take((size_t)H * n_f * 128 * 2);
   return w;
 }
 
@@ -111,17 +116,19 @@ __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* 
 }
 
 // Inverse norms of the first frame's candidates (bf16 rows of 128), one warp
-// per candidate, grid-stride over the device-side candidate count.
+// per candidate, grid-stride over the device-side candidate count; the first
+// n_f candidate rows are also copied, in candidate order, into `stage`.
 __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __restrict__ K, int C,
                                                         const int32_t* __restrict__ cand,
                                                         const int32_t* __restrict__ ncand, float* cinv,
-                                                        int32_t* st) {
+                                                        __nv_bfloat16* stage, int n_f, int32_t* st) {
   if (status_bad(st)) return;
   const int h = blockIdx.y, lane = threadIdx.x & 31;
   const int nc = min(max(ncand[h], 0), C);
   for (int c = blockIdx.x * 8 + (threadIdx.x >> 5); c < nc; c += gridDim.x * 8) {
     const int s = cand[(size_t)h * C + c];
     const uint2 u = *reinterpret_cast<const uint2*>(K + ((size_t)h * C + s) * 128 + lane * 4);
+    if (c < n_f) *reinterpret_cast<uint2*>(stage + ((size_t)h * n_f + c) * 128 + lane * 4) = u;
     const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
     const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
     const float n2 = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
@@ -429,7 +436,8 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
                  int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
                  const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
-                 float* invn_out, unsigned long long* best_out, int32_t* st, cudaStream_t s);
+                 float* invn_out, unsigned long long* best_out, const void* stage, int32_t* st,
+                 cudaStream_t s);
 
 template <typename T, int D>
 static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
@@ -445,7 +453,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
   const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
   if (tc_nn) {
     cand_norm_kernel<<<wgrid, wblock, 0, s>>>((const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
-                                              st);
+                                              w.stage, n_f, st);
     FASTAR_LAUNCHED(s, "cand_norm");
   }
   for (int fi = 0; fi < F; ++fi) {
@@ -457,7 +465,8 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     int rc = FASTAR_ERR_UNSUPPORTED;
     if (tc_nn)
       rc = launch_nn_tc(FASTAR_BF16, k_new, n_f, Nrow, H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.cinv,
-                        w.plan_slot, w.plan_kind, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.best, st, s);
+                        w.plan_slot, w.plan_kind, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.best, w.stage,
+                        st, s);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       nn_simt_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], w.best, st);
