@@ -1,22 +1,26 @@
 // AnnCA and AnnSA attention on the tensor cores (tcgen05 + TMEM, bf16).
 //
-// One CTA (4 warps, one thread per query row) owns 128 queries and walks
-// their keys 128 at a time:
-//   S = Q K^T            8 MMAs (M 128, N 128, K 16) into TMEM columns 0..127
-//   softmax              each thread reads its row of S from TMEM, applies
-//                        the scale, the + ln m bias and the mask, updates its
-//                        running max / sum (base-2 online softmax) and writes
-//                        P (bf16) into shared memory over the spent K tile
-//   O_tile = P V         8 MMAs, V as an MN-major operand, TMEM columns
-//                        128..255; the thread rescales its fp32 accumulator
-//                        row in registers and adds O_tile.
-// Keys and values are gathered row by row with cp.async into the 128-byte
-// swizzled layout; the value tile uses the same physical layout, read by the
-// MMA as an MN-major operand.
+// One CTA owns 128 queries (one per softmax thread) and walks their keys 64
+// at a time through a warp-specialised pipeline:
+//   warp 0     producer: the queries (AnnCA: one TMA box pair; AnnSA: a
+//              cp.async row gather), then for every key tile the key and
+//              value rows (cp.async gathers into the 128-byte swizzled
+//              layout, 2-stage ring) and the tile's mask metadata;
+//   warp 1     MMA issuer: S_j = Q K_j^T (M 128, N 64, K 128) into one of two
+//              TMEM S buffers, issued one tile ahead of the softmax, and
+//              O += P_j V_j (M 128, N 128, K 64; V read as an MN-major operand)
+//              into the TMEM accumulator;
+//   warps 2-5  softmax, one thread per query row: read S_j from TMEM, apply
+//              the scale, the + ln m bias and the mask, keep a running max
+//              and sum in base 2, write P_j (bf16) over the spent key tile.
+//              The running max is only raised (and O in TMEM rescaled) when a
+//              tile's maximum exceeds it by more than 2^8, so P stays <= 256
+//              and rescaling is rare.
+// At the end the softmax threads read O from TMEM and write the output.
 //
 // AnnCA (gist.science technical summary 2.B): the CTA owns 128 queries of
-// one frame (loaded by TMA, two 64-column boxes) and walks the frame's kept
-// prompt tokens; it writes the normalised output.
+// one frame and walks the frame's kept prompt tokens; it writes the
+// normalised output.
 // AnnSA (gist.science 2.C; paper.rainbus.top method steps; + ln m from
 // paperlayer.ai appendix A, Lemma A.1): one launch per LSH table t.  The CTA
 // owns 128 consecutive queries of the chunk in the bucket order of table t
@@ -37,18 +41,21 @@ namespace fastar {
 
 namespace {
 
-constexpr int kM = 128, kN = 128, kD = 128, kMaxT = 4;
+constexpr int kM = 128, kN = 64, kD = 128, kMaxT = 4, kStages = 2;
+constexpr int kThreads = 192;  // producer, MMA issuer, 4 softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.f;  // raise the running max only when exceeded by more than this (log2)
 
 struct AttnSmem {
   uint8_t Q[kM * kD * 2];
-  uint8_t K[kN * kD * 2];  // key tile, then P (bf16, K-major over keys)
-  uint8_t V[kN * kD * 2];
-  float bias[kN];
-  uint32_t kcodes[kMaxT][kN];
-  int rows[kM];
-  uint64_t bar_q, bar_mma;
+  uint8_t K[kStages][kN * kD * 2];  // key tile, then P_j (bf16, 128 rows x 64 keys)
+  uint8_t V[kStages][kN * kD * 2];
+  float bias[kStages][kN];
+  uint32_t kcodes[kStages][kMaxT][kN];
+  uint64_t bar_q;
+  uint64_t full[kStages], empty[kStages];
+  uint64_t sfull[2], sfree[2], pready[2], fin;
   uint32_t tmem;
 };
 
@@ -77,221 +84,42 @@ struct SaArgs {
   float2* ws_ml; // [T][H][Nq] (running max in log2 units, sum)
 };
 
-// One 128-key step of the online softmax for the calling thread's row.
-// kT: AnnSA table (the mask compares kT + 1 codes); -1 for AnnCA.
-// qlo/qhi: code range of the warp's queries in table kT (AnnSA).
-// Returns false when a bounded wait expired.
-template <int kT>
-__device__ __forceinline__ bool attend_tile(AttnSmem& sm, uint32_t tmem, int nvalid, float scale2,
-                                            const uint32_t* qcode, uint32_t qlo, uint32_t qhi, float& m_run,
-                                            float& l_run, float* acc, uint32_t& phase, bool ok) {
-  constexpr bool kSA = kT >= 0;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kM, kN, 0, 0);
-  constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kM, kD, 0, 1);
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  if (tid == 0 && ok) {
-    const uint32_t q0 = tc::smem_u32(sm.Q), k0 = tc::smem_u32(sm.K);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t oq = (kk >> 2) * kM * 128 + (kk & 3) * 32;
-      const uint32_t okk = (kk >> 2) * kN * 128 + (kk & 3) * 32;
-      tc::mma_bf16(tmem, tc::sdesc_kmajor_sw128(q0 + oq), tc::sdesc_kmajor_sw128(k0 + okk), idesc_qk,
-                   kk > 0 ? 1u : 0u);
-    }
-    tc::mma_commit(&sm.bar_mma);
-  }
-  if (ok) ok = tc::mbar_wait(&sm.bar_mma, phase);
-  ok = __all_sync(0xffffffffu, ok);
-  phase ^= 1;
-  tc::tc_fence_after();
-
-  // which 32-key chunks can hold an allowed key for some query of this warp
-  bool live[kN / 32];
-#pragma unroll
-  for (int q = 0; q < kN / 32; ++q) {
-    live[q] = q * 32 < nvalid;
-    if constexpr (kSA) {
-      if (live[q]) {
-        const uint32_t klo = sm.kcodes[kT][q * 32];
-        const uint32_t khi = sm.kcodes[kT][min(q * 32 + 31, nvalid - 1)];
-        live[q] = !(khi < qlo || klo > qhi);
-      }
-    }
-  }
-
-  // pass 1: masked maximum of the row and the allowed bits
-  uint32_t allow_bits[kN / 32];
-  float tmax = -INFINITY;
-#pragma unroll
-  for (int q = 0; q < kN / 32; ++q) {
-    allow_bits[q] = 0u;
-    if (!ok || !live[q]) continue;
-    float v[32];
-    tc::tmem_ld32(tmem + lane_base + q * 32, v);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int c = q * 32 + i;
-      bool allow = c < nvalid;
-      float s = v[i] * scale2;
-      if constexpr (kSA) {
-        allow = allow && sm.kcodes[kT][c] == qcode[kT];
-#pragma unroll
-        for (int u = 0; u < kT; ++u) allow = allow && sm.kcodes[u][c] != qcode[u];
-        s += sm.bias[c];
-      }
-      allow_bits[q] |= (allow ? 1u : 0u) << i;
-      tmax = allow ? fmaxf(tmax, s) : tmax;
-    }
-  }
-  const float m_new = fmaxf(m_run, tmax);
-  const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-  // pass 2: P = 2^(s - m_new) written as bf16 over the spent key tile
-  float psum = 0.f;
-#pragma unroll
-  for (int q = 0; q < kN / 32; ++q) {
-    uint32_t packed[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) packed[i] = 0u;
-    if (ok && live[q]) {
-      // the warp loads the chunk collectively, even for rows that allow nothing in it
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + q * 32, v);
-      if (allow_bits[q]) {
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = q * 32 + i + e;
-            float s = v[i + e] * scale2;
-            if constexpr (kSA) s += sm.bias[c];
-            p2[e] = ((allow_bits[q] >> (i + e)) & 1u) ? exp2f(s - m_new) : 0.f;
-          }
-          const __nv_bfloat162 b = __floats2bfloat162_rn(p2[0], p2[1]);
-          psum += p2[0] + p2[1];
-          packed[i >> 1] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-      }
-    }
-    // 32 keys = 4 chunks of 8 keys; chunk index over 128 keys is q*4 + k
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint4 u = make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
-      *reinterpret_cast<uint4*>(sm.K + tc::sw128_offset(tid, q * 4 + k, kM)) = u;
-    }
-  }
-  l_run = l_run * alpha + psum;
-  m_run = m_new;
-  tc::fence_proxy_async_smem();
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  if (tid == 0 && ok) {
-    const uint32_t p0 = tc::smem_u32(sm.K), v0 = tc::smem_u32(sm.V);
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t op = (kk >> 2) * kM * 128 + (kk & 3) * 32;
-      tc::mma_bf16(tmem + 128, tc::sdesc_kmajor_sw128(p0 + op),
-                   tc::sdesc_mnmajor_sw128(v0 + kk * 16 * 128, kN * 128), idesc_pv, kk > 0 ? 1u : 0u);
-    }
-    tc::mma_commit(&sm.bar_mma);
-  }
-  if (ok) ok = tc::mbar_wait(&sm.bar_mma, phase);
-  ok = __all_sync(0xffffffffu, ok);
-  phase ^= 1;
-  tc::tc_fence_after();
-  if (ok) {
-#pragma unroll
-    for (int q = 0; q < kD / 32; ++q) {
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + 128 + q * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[q * 32 + i] = fmaf(acc[q * 32 + i], alpha, v[i]);
-    }
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  return ok;
+// Wait until the PV product of key tile j has landed in O (and, since one
+// thread issues every MMA in order, all products before it).  The commit
+// after PV_j arrives on empty[j % kStages].  A parity wait is only sound
+// while the barrier is at most one phase behind the awaited one: here the
+// previous phase on that barrier (PV_{j-2}) has completed, because the
+// producer waited for it before loading tile j, whose arrival on full[] the
+// caller has already seen; and the next phase (PV_{j+2}) cannot complete
+// before the caller has released P_{j+2}.
+__device__ __forceinline__ bool wait_pv(AttnSmem& sm, int j) {
+  return tc::mbar_wait(&sm.empty[j % kStages], (uint32_t)(j / kStages) & 1u);
 }
 
 // kT = -1: AnnCA (grid: query tiles x frames x heads); kT >= 0: AnnSA table
 // kT (grid: query tiles x 1 x heads).
 template <int kT>
-__global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, int H,
-                                                      int Nq, float scale, CaArgs ca, SaArgs sa,
-                                                      int32_t* st) {
+__global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, int H,
+                                                             int Nq, float scale, CaArgs ca, SaArgs sa,
+                                                             int32_t* st) {
   constexpr bool kSA = kT >= 0;
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * kM;
   const int h = blockIdx.z;
+  const int g = blockIdx.y;  // AnnCA: frame
   const float scale2 = scale * kLog2e;
 
-  if (tid == 0) {
-    tc::mbar_init(&sm.bar_q, 1);
-    tc::mbar_init(&sm.bar_mma, 1);
-    tc::fence_mbar_init();
-  }
-  if (warp == 0) {
-    tc::tmem_alloc(&sm.tmem, 256);
-    tc::tmem_relinquish();
-  }
-  tc::tc_fence_before();
-  __syncthreads();
-  tc::tc_fence_after();
-  const uint32_t tmem = sm.tmem;
-  bool ok = true;
-  bool bad_index = false;
-
-  // ---- queries and the key list
+  // ---- the key list of this CTA (every thread computes it)
   int nkeys = 0, kbeg = 0;
-  uint32_t qcode[kMaxT] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-  uint32_t qlo = 0xffffffffu, qhi = 0u;
-  int my_row = -1;  // query index of this thread's row (-1: padding)
+  bool bad_index = false;
   if constexpr (!kSA) {
-    const int f = blockIdx.y;
-    if (tid == 0) {
-      tc::prefetch_tensormap(&mapQ);
-      tc::mbar_arrive_expect_tx(&sm.bar_q, kM * kD * 2);
-      const int row0 = h * Nq + f * ca.n_f + m0;
-      tc::tma_load_2d(sm.Q, &mapQ, &sm.bar_q, 0, row0);
-      tc::tma_load_2d(sm.Q + kM * 128, &mapQ, &sm.bar_q, 64, row0);
-    }
-    nkeys = min(max(ca.kept_cnt[(size_t)h * ca.F + f], 0), ca.P);
-    if (m0 + tid < ca.n_f) my_row = f * ca.n_f + m0 + tid;
-    ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.bar_q, 0));
+    nkeys = min(max(ca.kept_cnt[(size_t)h * ca.F + g], 0), ca.P);
   } else {
     const int32_t* qp = sa.q_perm + ((size_t)h * sa.T + kT) * Nq;
     const int nrow = min(kM, Nq - m0);
-    if (tid < nrow) {
-      const int qi = qp[m0 + tid];
-      if (qi >= 0 && qi < Nq) my_row = qi; else bad_index = true;
-    }
-    sm.rows[tid] = my_row;
-    __syncthreads();
-    tc::gather_rows_sw128(tc::smem_u32(sm.Q), kM,
-                          [&](int r) -> const void* {
-                            const int qi = sm.rows[r];
-                            return qi >= 0 ? (const void*)(sa.q + ((size_t)h * Nq + qi) * kD) : nullptr;
-                          },
-                          tid, 128, sa.q);
-    tc::cp_async_commit();
-#pragma unroll
-    for (int u = 0; u <= kT; ++u)
-      qcode[u] = my_row >= 0 ? sa.q_codes[((size_t)h * sa.T + u) * Nq + my_row] : 0xffffffffu;
-    // code range of the warp's queries (padding rows excluded)
-    uint32_t lo = my_row >= 0 ? qcode[kT] : 0xffffffffu, hi = my_row >= 0 ? qcode[kT] : 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-      hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    qlo = lo;
-    qhi = hi;
-    // key range: the cache buckets spanned by this tile's table-kT codes
     const int first = qp[m0], last = qp[m0 + nrow - 1];
     const uint32_t c_lo = (first >= 0 && first < Nq) ? sa.q_codes[((size_t)h * sa.T + kT) * Nq + first] : 0u;
     const uint32_t c_hi = (last >= 0 && last < Nq) ? sa.q_codes[((size_t)h * sa.T + kT) * Nq + last] : 0u;
@@ -300,91 +128,357 @@ __global__ void __launch_bounds__(128) attn_tc_kernel(const __grid_constant__ CU
       const int32_t* off = sa.offsets + ((size_t)h * sa.T + kT) * (sa.nb + 1);
       kbeg = min(max(off[c_lo], 0), n_live);
       nkeys = min(max(off[c_hi + 1], kbeg), n_live) - kbeg;
-    } else if (tid == 0) {
+    } else {
       bad_index = true;
     }
-    tc::cp_async_wait_all();
   }
+  const int ntiles = (nkeys + kN - 1) / kN;
 
-  float m_run = -INFINITY, l_run = 0.f;
-  float acc[kD];
-#pragma unroll
-  for (int i = 0; i < kD; ++i) acc[i] = 0.f;
-  uint32_t phase = 0;
-
-  for (int k0 = 0; k0 < nkeys && ok; k0 += kN) {
-    const int nvalid = min(kN, nkeys - k0);
-    // row sources of this key tile (AnnCA: kept prompt ids; AnnSA: cache slots)
-    int src = -1;
-    if (tid < nvalid) {
-      if constexpr (!kSA) {
-        const int p = ca.kept_idx[((size_t)h * ca.F + blockIdx.y) * ca.P + k0 + tid];
-        if (p >= 0 && p < ca.P) src = p; else bad_index = true;
-      } else {
-        const int s = sa.perm[((size_t)h * sa.T + kT) * sa.C + kbeg + k0 + tid];
-        if (s >= 0 && s < sa.C) src = s; else bad_index = true;
-      }
+  if (tid == 0) {
+    tc::mbar_init(&sm.bar_q, kSA ? 32 : 1);
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&sm.full[s], 32 + 1);  // 32 cp.async lanes + the metadata arrive
+      tc::mbar_init(&sm.empty[s], 1);      // PV commit (also: O holds this tile's product)
     }
-    sm.rows[tid] = src;  // reuse: key source per row of this tile
-    if constexpr (kSA) {
-#pragma unroll
-      for (int u = 0; u <= kT; ++u)
-        sm.kcodes[u][tid] = src >= 0 ? sa.codes[((size_t)h * sa.T + u) * sa.C + src] : 0xfffffffeu;
-      sm.bias[tid] = src >= 0 ? log2f((float)max(sa.m[(size_t)h * sa.C + src], 1)) : 0.f;
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&sm.sfull[b], 1);      // QK commit
+      tc::mbar_init(&sm.sfree[b], 4);      // softmax warps
+      tc::mbar_init(&sm.pready[b], 4);     // softmax warps
     }
-    __syncthreads();
-    const __nv_bfloat16* kbase = kSA ? sa.K : ca.k_p;
-    const __nv_bfloat16* vbase = kSA ? sa.V : ca.v_p;
-    const size_t rows_per_head = kSA ? (size_t)sa.C : (size_t)ca.P;
-    auto krow = [&](int r) -> const void* {
-      const int s = sm.rows[r];
-      return s >= 0 ? (const void*)(kbase + ((size_t)h * rows_per_head + s) * kD) : nullptr;
-    };
-    auto vrow = [&](int r) -> const void* {
-      const int s = sm.rows[r];
-      return s >= 0 ? (const void*)(vbase + ((size_t)h * rows_per_head + s) * kD) : nullptr;
-    };
-    tc::gather_rows_sw128(tc::smem_u32(sm.K), kN, krow, tid, 128, kbase);
-    tc::gather_rows_sw128(tc::smem_u32(sm.V), kN, vrow, tid, 128, vbase);
-    tc::cp_async_commit();
-    tc::cp_async_wait_all();
-    tc::fence_proxy_async_smem();
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    ok = attend_tile<kT>(sm, tmem, nvalid, scale2, qcode, qlo, qhi, m_run, l_run, acc, phase, ok);
+    tc::mbar_init(&sm.fin, 1);             // last commit of the MMA issuer
+    tc::fence_mbar_init();
   }
-
-  if (bad_index) status_set(st, FASTAR_ERR_DEVICE_ARG);
-  if (!ok) {
-    if (tid == 0) status_set(st, FASTAR_ERR_TIMEOUT);
-  } else if (my_row >= 0) {
-    if constexpr (!kSA) {
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-      __nv_bfloat16* o = ca.out + ((size_t)h * Nq + my_row) * kD;
-#pragma unroll
-      for (int i = 0; i < kD; i += 8) {
-        uint4 u;
-        uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 b = __floats2bfloat162_rn(acc[i + 2 * e] * inv, acc[i + 2 * e + 1] * inv);
-          w[e] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        *reinterpret_cast<uint4*>(o + i) = u;
-      }
-    } else {
-      const size_t r = ((size_t)kT * H + h) * Nq + my_row;
-      float* o = sa.ws_o + r * kD;
-#pragma unroll
-      for (int i = 0; i < kD; i += 4) *reinterpret_cast<float4*>(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-      sa.ws_ml[r] = make_float2(m_run, l_run);
-    }
+  if (warp == 1) {
+    tc::tmem_alloc(&sm.tmem, 256);
+    tc::tmem_relinquish();
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+  const uint32_t tmem = sm.tmem;  // S buffers at columns 0 and 64, O at 128
+  bool ok = true;
+
+  if (warp == 0) {
+    // ================================================= producer
+    if (ntiles > 0) {
+      if constexpr (!kSA) {
+        if (lane == 0) {
+          tc::prefetch_tensormap(&mapQ);
+          tc::mbar_arrive_expect_tx(&sm.bar_q, kM * kD * 2);
+          const int row0 = h * Nq + g * ca.n_f + m0;
+          tc::tma_load_2d(sm.Q, &mapQ, &sm.bar_q, 0, row0);
+          tc::tma_load_2d(sm.Q + kM * 128, &mapQ, &sm.bar_q, 64, row0);
+        }
+      } else {
+        // query rows lane, lane + 32, lane + 64, lane + 96 of the tile
+        const int32_t* qp = sa.q_perm + ((size_t)h * sa.T + kT) * Nq;
+        int qi[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = lane + 32 * u;
+          qi[u] = -1;
+          if (m0 + r < Nq) {
+            const int x = qp[m0 + r];
+            if (x >= 0 && x < Nq) qi[u] = x; else bad_index = true;
+          }
+        }
+        const uint32_t q0 = tc::smem_u32(sm.Q);
+#pragma unroll
+        for (int i = 0; i < kM * 16 / 32; ++i) {
+          const int r = 2 * i + (lane >> 4), ch = lane & 15;
+          const int x = __shfl_sync(0xffffffffu, qi[r >> 5], r & 31);
+          const char* src = x >= 0 ? (const char*)(sa.q + ((size_t)h * Nq + x) * kD) + ch * 16 : (const char*)sa.q;
+          tc::cp_async16(q0 + tc::sw128_offset(r, ch, kM), src, x >= 0 ? 16u : 0u);
+        }
+        tc::cp_async_arrive_noinc(&sm.bar_q);
+      }
+    }
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int s = j % kStages;
+      if (j >= kStages) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.empty[s], (uint32_t)((j / kStages) - 1) & 1u));
+      if (!ok) break;
+      const int k0 = j * kN;
+      const int nvalid = min(kN, nkeys - k0);
+      // row sources of rows lane and lane + 32 (AnnCA: prompt ids; AnnSA: slots)
+      int src[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = lane + 32 * u;
+        src[u] = -1;
+        if (r < nvalid) {
+          int x;
+          if constexpr (!kSA) x = ca.kept_idx[((size_t)h * ca.F + g) * ca.P + k0 + r];
+          else x = sa.perm[((size_t)h * sa.T + kT) * sa.C + kbeg + k0 + r];
+          const int lim = kSA ? sa.C : ca.P;
+          if (x >= 0 && x < lim) src[u] = x; else bad_index = true;
+        }
+        if constexpr (kSA) {
+#pragma unroll
+          for (int w = 0; w <= kT; ++w)
+            sm.kcodes[s][w][r] = src[u] >= 0 ? sa.codes[((size_t)h * sa.T + w) * sa.C + src[u]] : 0xfffffffeu;
+          sm.bias[s][r] = src[u] >= 0 ? log2f((float)max(sa.m[(size_t)h * sa.C + src[u]], 1)) : 0.f;
+        }
+      }
+      const __nv_bfloat16* kb = kSA ? sa.K : ca.k_p;
+      const __nv_bfloat16* vb = kSA ? sa.V : ca.v_p;
+      const size_t rows_per_head = kSA ? (size_t)sa.C : (size_t)ca.P;
+      const uint32_t kt = tc::smem_u32(sm.K[s]), vt = tc::smem_u32(sm.V[s]);
+#pragma unroll
+      for (int i = 0; i < kN * 16 / 32; ++i) {
+        const int r = 2 * i + (lane >> 4), ch = lane & 15;
+        const int sr = __shfl_sync(0xffffffffu, src[r >> 5], r & 31);
+        const uint32_t off = tc::sw128_offset(r, ch, kN);
+        if (sr >= 0) {
+          const size_t row = ((size_t)h * rows_per_head + sr) * kD;
+          tc::cp_async16(kt + off, (const char*)(kb + row) + ch * 16, 16u);
+          tc::cp_async16(vt + off, (const char*)(vb + row) + ch * 16, 16u);
+        } else {
+          tc::cp_async16(kt + off, kb, 0u);
+          tc::cp_async16(vt + off, vb, 0u);
+        }
+      }
+      tc::cp_async_arrive_noinc(&sm.full[s]);
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.full[s]);  // the metadata written above
+    }
+  } else if (warp == 1) {
+    // ================================================= MMA issuer
+    constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kM, kN, 0, 0);
+    constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kM, kD, 0, 1);
+    if (ntiles > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.bar_q, 0));
+    auto issue_qk = [&](int j) -> bool {
+      const int s = j % kStages, b = j & 1;
+      bool good = tc::mbar_wait(&sm.full[s], (uint32_t)(j / kStages) & 1u);
+      if (good && j >= 2) good = tc::mbar_wait(&sm.sfree[b], (uint32_t)((j >> 1) - 1) & 1u);
+      good = __all_sync(0xffffffffu, good);
+      if (!good) return false;
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t q0 = tc::smem_u32(sm.Q), k0 = tc::smem_u32(sm.K[s]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t oq = (kk >> 2) * kM * 128 + (kk & 3) * 32;
+          const uint32_t okk = (kk >> 2) * kN * 128 + (kk & 3) * 32;
+          tc::mma_bf16(tmem + b * kN, tc::sdesc_kmajor_sw128(q0 + oq), tc::sdesc_kmajor_sw128(k0 + okk),
+                       idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(&sm.sfull[b]);
+      }
+      __syncwarp();
+      return true;
+    };
+    if (ok && ntiles > 0) ok = issue_qk(0);
+    for (int j = 0; j < ntiles && ok; ++j) {
+      if (j + 1 < ntiles) {
+        ok = issue_qk(j + 1);
+        if (!ok) break;
+      }
+      const int s = j % kStages, b = j & 1;
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.pready[b], (uint32_t)(j >> 1) & 1u));
+      if (!ok) break;
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_after();
+      if (lane == 0) {
+        const uint32_t p0 = tc::smem_u32(sm.K[s]), v0 = tc::smem_u32(sm.V[s]);
+#pragma unroll
+        for (int kk = 0; kk < kN / 16; ++kk)
+          tc::mma_bf16(tmem + 128, tc::sdesc_kmajor_sw128(p0 + kk * 32),
+                       tc::sdesc_mnmajor_sw128(v0 + kk * 16 * 128, kN * 128), idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
+        tc::mma_commit(&sm.empty[s]);
+      }
+      __syncwarp();
+    }
+    // every MMA this warp issued has finished before TMEM is freed (also on
+    // an expired wait, where nobody else may wait for them)
+    if (ntiles > 0) {
+      if (lane == 0) tc::mma_commit(&sm.fin);
+      __syncwarp();
+      if (!tc::mbar_wait(&sm.fin, 0)) ok = false;
+    }
+  } else {
+    // ================================================= softmax (warps 2-5)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    int my_row = -1;
+    uint32_t qcode[kMaxT] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
+    uint32_t qlo = 0xffffffffu, qhi = 0u;
+    if constexpr (!kSA) {
+      if (m0 + r < ca.n_f) my_row = g * ca.n_f + m0 + r;
+    } else {
+      if (m0 + r < Nq) {
+        const int qi = sa.q_perm[((size_t)h * sa.T + kT) * Nq + m0 + r];
+        if (qi >= 0 && qi < Nq) my_row = qi;
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxT; ++u)
+        if (u <= kT && my_row >= 0) qcode[u] = sa.q_codes[((size_t)h * sa.T + u) * Nq + my_row];
+      uint32_t lo = my_row >= 0 ? qcode[kT] : 0xffffffffu, hi = my_row >= 0 ? qcode[kT] : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+      }
+      qlo = lo;
+      qhi = hi;
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int s = j % kStages, b = j & 1;
+      const int nvalid = min(kN, nkeys - j * kN);
+      ok = tc::mbar_wait(&sm.full[s], (uint32_t)(j / kStages) & 1u);  // metadata of the tile
+      ok = ok && tc::mbar_wait(&sm.sfull[b], (uint32_t)(j >> 1) & 1u);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc::tc_fence_after();
+      // which 32-key chunks can hold an allowed key for some query of this warp
+      bool live[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        live[q] = q * 32 < nvalid;
+        if constexpr (kSA) {
+          if (live[q]) {
+            const uint32_t klo = sm.kcodes[s][kT][q * 32];
+            const uint32_t khi = sm.kcodes[s][kT][min(q * 32 + 31, nvalid - 1)];
+            live[q] = !(khi < qlo || klo > qhi);
+          }
+        }
+      }
+      float v[2][32];
+      uint32_t bits[2] = {0u, 0u};
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (!live[q]) continue;
+        tc::tmem_ld32(tmem + lane_base + b * kN + q * 32, v[q]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = q * 32 + i;
+          bool allow = c < nvalid;
+          float sc = v[q][i] * scale2;
+          if constexpr (kSA) {
+            allow = allow && sm.kcodes[s][kT][c] == qcode[kT];
+#pragma unroll
+            for (int w = 0; w < kT; ++w) allow = allow && sm.kcodes[s][w][c] != qcode[w];
+            sc += sm.bias[s][c];
+          }
+          v[q][i] = sc;
+          bits[q] |= (allow ? 1u : 0u) << i;
+          tmax = allow ? fmaxf(tmax, sc) : tmax;
+        }
+      }
+      // S_j is in registers: release the S buffer
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.sfree[b]);
+      // raise the running max (and rescale O) only for a large increase
+      const bool raise = tmax > m_run + kRescale;
+      const float m_new = raise ? tmax : m_run;
+      const float alpha = (raise && m_run != -INFINITY) ? exp2f(m_run - m_new) : 1.f;
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // wait until O holds P_0 V_0 .. P_{j-1} V_{j-1}
+        ok = __all_sync(0xffffffffu, wait_pv(sm, j - 1));
+        if (!ok) break;
+        tc::tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < kD / 32; ++q) {
+          float o[32];
+          tc::tmem_ld32(tmem + lane_base + 128 + q * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= alpha;
+          tc::tmem_st32(tmem + lane_base + 128 + q * 32, o);
+        }
+      }
+      l_run *= alpha;
+      m_run = m_new;
+      // P_j (bf16) over the spent key tile: 128 rows x 64 keys, one swizzle atom per row
+      float psum = 0.f;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t packed[16];
+        if (live[q]) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const float p0 = ((bits[q] >> i) & 1u) ? exp2f(v[q][i] - m_run) : 0.f;
+            const float p1 = ((bits[q] >> (i + 1)) & 1u) ? exp2f(v[q][i + 1] - m_run) : 0.f;
+            psum += p0 + p1;
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            packed[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) packed[i] = 0u;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<uint4*>(sm.K[s] + tc::sw128_offset(r, q * 4 + k, kM)) =
+              make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
+      }
+      l_run += psum;
+      tc::fence_proxy_async_smem();
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&sm.pready[b]);
+    }
+    // ---- output: O (TMEM) / l
+    if (ok && ntiles > 0) {
+      ok = __all_sync(0xffffffffu, wait_pv(sm, ntiles - 1));
+      tc::tc_fence_after();
+    }
+    if (ok) {
+      float o[kD / 32][32];
+      if (ntiles > 0) {
+#pragma unroll
+        for (int q = 0; q < kD / 32; ++q) tc::tmem_ld32(tmem + lane_base + 128 + q * 32, o[q]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < kD / 32; ++q)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[q][i] = 0.f;
+      }
+      if (my_row >= 0) {
+        if constexpr (!kSA) {
+          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+          __nv_bfloat16* dst = ca.out + ((size_t)h * Nq + my_row) * kD;
+#pragma unroll
+          for (int q = 0; q < kD / 32; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              uint4 u;
+              uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 pb = __floats2bfloat162_rn(o[q][i + 2 * e] * inv, o[q][i + 2 * e + 1] * inv);
+                w[e] = *reinterpret_cast<const uint32_t*>(&pb);
+              }
+              *reinterpret_cast<uint4*>(dst + q * 32 + i) = u;
+            }
+        } else {
+          const size_t row = ((size_t)kT * H + h) * Nq + my_row;
+          float* dst = sa.ws_o + row * kD;
+#pragma unroll
+          for (int q = 0; q < kD / 32; ++q)
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              *reinterpret_cast<float4*>(dst + q * 32 + i) = make_float4(o[q][i], o[q][i + 1], o[q][i + 2], o[q][i + 3]);
+          sa.ws_ml[row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
+        }
+      }
+    }
+  }
+  if (bad_index) status_set(st, FASTAR_ERR_DEVICE_ARG);
+  if (!ok) status_set(st, FASTAR_ERR_TIMEOUT);
+  if (warp == 0) {
+    // the producer's copies have landed before the CTA exits
+    tc::cp_async_wait_all();
+    if (!kSA && ntiles > 0 && lane == 0 && !tc::mbar_wait(&sm.bar_q, 0)) status_set(st, FASTAR_ERR_TIMEOUT);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, 256);
 }
 
 // Merge the T per-table partials of each query (warp per query).
@@ -435,7 +529,7 @@ int launch_attn(const CUtensorMap& map, dim3 grid, int H, int Nq, float scale, c
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  attn_tc_kernel<kT><<<grid, 128, smem, s>>>(map, H, Nq, scale, ca, sa, st);
+  attn_tc_kernel<kT><<<grid, kThreads, smem, s>>>(map, H, Nq, scale, ca, sa, st);
   FASTAR_LAUNCHED(s, kT < 0 ? "annca_tc" : "annsa_tc");
   return FASTAR_OK;
 }
