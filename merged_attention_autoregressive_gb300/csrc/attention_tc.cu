@@ -46,18 +46,22 @@ constexpr int kThreads = 192;  // producer, MMA issuer, 4 softmax warps
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.f;  // raise the running max only when exceeded by more than this (log2)
+constexpr uint32_t kIdlePolls = 1u << 22;  // MMA issuer: bound on polls that find nothing ready
 
 struct AttnSmem {
   uint8_t Q[kM * kD * 2];
   uint8_t K[kStages][kN * kD * 2];  // key tile, then P_j (bf16, 128 rows x 64 keys)
   uint8_t V[kStages][kN * kD * 2];
-  float bias[kStages][kN];
-  uint32_t kcodes[kStages][kMaxT][kN];
+  float bias[kStages][kN];                      // AnnSA: log2 m of the tile's slots
+  uint32_t kcodes[kStages][kMaxT - 1][kN];      // AnnSA: slot codes of the tables before t
   uint64_t bar_q;
   uint64_t full[kStages], empty[kStages];
   uint64_t sfull[2], sfree[2], pready[2], fin;
   uint32_t tmem;
 };
+// At the end the output rows are staged through Q and K (free by then):
+// 16 KB per softmax warp.
+static_assert(sizeof(((AttnSmem*)0)->Q) + sizeof(((AttnSmem*)0)->K) >= 4 * 32 * kD * 4, "staging space");
 
 struct CaArgs {
   const __nv_bfloat16* k_p;
@@ -89,11 +93,21 @@ struct SaArgs {
 // after PV_j arrives on empty[j % kStages].  A parity wait is only sound
 // while the barrier is at most one phase behind the awaited one: here the
 // previous phase on that barrier (PV_{j-2}) has completed, because the
-// producer waited for it before loading tile j, whose arrival on full[] the
-// caller has already seen; and the next phase (PV_{j+2}) cannot complete
-// before the caller has released P_{j+2}.
+// producer waited for it before loading tile j, whose QK product the caller
+// has already seen; and the next phase (PV_{j+2}) cannot complete before the
+// caller has released P_{j+2}.
 __device__ __forceinline__ bool wait_pv(AttnSmem& sm, int j) {
   return tc::mbar_wait(&sm.empty[j % kStages], (uint32_t)(j / kStages) & 1u);
+}
+
+// Bits c (0..63) of the key tile with lo <= c < hi.
+__device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
+  lo = max(lo, 0);
+  hi = min(hi, 64);
+  if (hi <= lo) return 0ull;
+  const uint64_t below_hi = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+  const uint64_t below_lo = (1ull << lo) - 1ull;
+  return below_hi & ~below_lo;
 }
 
 // kT = -1: AnnCA (grid: query tiles x frames x heads); kT >= 0: AnnSA table
@@ -103,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
                                                              int Nq, float scale, CaArgs ca, SaArgs sa,
                                                              int32_t* st) {
   constexpr bool kSA = kT >= 0;
+  constexpr int kPrev = kSA ? kT : 0;  // AnnSA: earlier tables whose collisions are excluded
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
@@ -112,30 +127,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   const int g = blockIdx.y;  // AnnCA: frame
   const float scale2 = scale * kLog2e;
 
-  // ---- the key list of this CTA (every thread computes it)
-  int nkeys = 0, kbeg = 0;
-  bool bad_index = false;
-  if constexpr (!kSA) {
-    nkeys = min(max(ca.kept_cnt[(size_t)h * ca.F + g], 0), ca.P);
-  } else {
-    const int32_t* qp = sa.q_perm + ((size_t)h * sa.T + kT) * Nq;
-    const int nrow = min(kM, Nq - m0);
-    const int first = qp[m0], last = qp[m0 + nrow - 1];
-    const uint32_t c_lo = (first >= 0 && first < Nq) ? sa.q_codes[((size_t)h * sa.T + kT) * Nq + first] : 0u;
-    const uint32_t c_hi = (last >= 0 && last < Nq) ? sa.q_codes[((size_t)h * sa.T + kT) * Nq + last] : 0u;
-    const int n_live = min(max(sa.size[h], 0), sa.C);
-    if (c_lo < (uint32_t)sa.nb && c_hi < (uint32_t)sa.nb && c_lo <= c_hi) {
-      const int32_t* off = sa.offsets + ((size_t)h * sa.T + kT) * (sa.nb + 1);
-      kbeg = min(max(off[c_lo], 0), n_live);
-      nkeys = min(max(off[c_hi + 1], kbeg), n_live) - kbeg;
-    } else {
-      bad_index = true;
-    }
-  }
-  const int ntiles = (nkeys + kN - 1) / kN;
-
   if (tid == 0) {
-    tc::mbar_init(&sm.bar_q, kSA ? 32 : 1);
+    tc::mbar_init(&sm.bar_q, kSA ? 128 : 1);  // AnnSA: every softmax thread gathers its query row
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&sm.full[s], 32 + 1);  // 32 cp.async lanes + the metadata arrive
       tc::mbar_init(&sm.empty[s], 1);      // PV commit (also: O holds this tile's product)
@@ -157,77 +150,117 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem;  // S buffers at columns 0 and 64, O at 128
   bool ok = true;
+  bool bad_index = false;
+
+  // ---- AnnSA: the softmax threads gather their query rows right away
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;  // softmax warps: query row of the tile = TMEM lane
+  int my_row = -1;
+  if constexpr (kSA) {
+    if (warp >= 2) {
+      if (m0 + r < Nq) {
+        const int x = sa.q_perm[((size_t)h * sa.T + kT) * Nq + m0 + r];
+        if (x >= 0 && x < Nq) my_row = x; else bad_index = true;
+      }
+      const uint32_t q0 = tc::smem_u32(sm.Q);
+      const char* src = my_row >= 0 ? (const char*)(sa.q + ((size_t)h * Nq + my_row) * kD) : (const char*)sa.q;
+#pragma unroll
+      for (int ch = 0; ch < 16; ++ch)
+        tc::cp_async16(q0 + tc::sw128_offset(r, ch, kM), src + (my_row >= 0 ? ch * 16 : 0), my_row >= 0 ? 16u : 0u);
+      tc::cp_async_arrive_noinc(&sm.bar_q);
+    }
+  } else {
+    if (warp >= 2 && m0 + r < ca.n_f) my_row = g * ca.n_f + m0 + r;
+  }
+
+  // ---- the key list of this CTA (every thread computes it)
+  int nkeys = 0, kbeg = 0, n_live = 0;
+  const int32_t* toff = nullptr;  // AnnSA: cache CSR offsets of table kT
+  if constexpr (!kSA) {
+    nkeys = min(max(ca.kept_cnt[(size_t)h * ca.F + g], 0), ca.P);
+  } else {
+    const int32_t* qp = sa.q_perm + ((size_t)h * sa.T + kT) * Nq;
+    const int nrow = min(kM, Nq - m0);
+    const int first = qp[m0], last = qp[m0 + nrow - 1];
+    const uint32_t c_lo = (first >= 0 && first < Nq) ? sa.q_codes[((size_t)h * sa.T + kT) * Nq + first] : 0u;
+    const uint32_t c_hi = (last >= 0 && last < Nq) ? sa.q_codes[((size_t)h * sa.T + kT) * Nq + last] : 0u;
+    n_live = min(max(sa.size[h], 0), sa.C);
+    toff = sa.offsets + ((size_t)h * sa.T + kT) * (sa.nb + 1);
+    if (c_lo < (uint32_t)sa.nb && c_hi < (uint32_t)sa.nb && c_lo <= c_hi) {
+      kbeg = min(max(toff[c_lo], 0), n_live);
+      nkeys = min(max(toff[c_hi + 1], kbeg), n_live) - kbeg;
+    } else {
+      bad_index = true;
+    }
+  }
+  const int ntiles = (nkeys + kN - 1) / kN;
 
   if (warp == 0) {
     // ================================================= producer
-    if (ntiles > 0) {
-      if constexpr (!kSA) {
-        if (lane == 0) {
-          tc::prefetch_tensormap(&mapQ);
-          tc::mbar_arrive_expect_tx(&sm.bar_q, kM * kD * 2);
-          const int row0 = h * Nq + g * ca.n_f + m0;
-          tc::tma_load_2d(sm.Q, &mapQ, &sm.bar_q, 0, row0);
-          tc::tma_load_2d(sm.Q + kM * 128, &mapQ, &sm.bar_q, 64, row0);
-        }
-      } else {
-        // query rows lane, lane + 32, lane + 64, lane + 96 of the tile
-        const int32_t* qp = sa.q_perm + ((size_t)h * sa.T + kT) * Nq;
-        int qi[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int r = lane + 32 * u;
-          qi[u] = -1;
-          if (m0 + r < Nq) {
-            const int x = qp[m0 + r];
-            if (x >= 0 && x < Nq) qi[u] = x; else bad_index = true;
-          }
-        }
-        const uint32_t q0 = tc::smem_u32(sm.Q);
-#pragma unroll
-        for (int i = 0; i < kM * 16 / 32; ++i) {
-          const int r = 2 * i + (lane >> 4), ch = lane & 15;
-          const int x = __shfl_sync(0xffffffffu, qi[r >> 5], r & 31);
-          const char* src = x >= 0 ? (const char*)(sa.q + ((size_t)h * Nq + x) * kD) + ch * 16 : (const char*)sa.q;
-          tc::cp_async16(q0 + tc::sw128_offset(r, ch, kM), src, x >= 0 ? 16u : 0u);
-        }
-        tc::cp_async_arrive_noinc(&sm.bar_q);
+    if constexpr (!kSA) {
+      if (ntiles > 0 && lane == 0) {
+        tc::prefetch_tensormap(&mapQ);
+        tc::mbar_arrive_expect_tx(&sm.bar_q, kM * kD * 2);
+        const int row0 = h * Nq + g * ca.n_f + m0;
+        tc::tma_load_2d(sm.Q, &mapQ, &sm.bar_q, 0, row0);
+        tc::tma_load_2d(sm.Q + kM * 128, &mapQ, &sm.bar_q, 64, row0);
       }
     }
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int s = j % kStages;
-      if (j >= kStages) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.empty[s], (uint32_t)((j / kStages) - 1) & 1u));
-      if (!ok) break;
-      const int k0 = j * kN;
-      const int nvalid = min(kN, nkeys - k0);
-      // row sources of rows lane and lane + 32 (AnnCA: prompt ids; AnnSA: slots)
-      int src[2];
+    // row sources of tile j, rows lane and lane + 32 (AnnCA: prompt ids; AnnSA: slots)
+    auto fetch_src = [&](int j, int* out) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int r = lane + 32 * u;
-        src[u] = -1;
-        if (r < nvalid) {
+        const int rr = lane + 32 * u, k = j * kN + rr;
+        out[u] = -1;
+        if (k < nkeys) {
           int x;
-          if constexpr (!kSA) x = ca.kept_idx[((size_t)h * ca.F + g) * ca.P + k0 + r];
-          else x = sa.perm[((size_t)h * sa.T + kT) * sa.C + kbeg + k0 + r];
+          if constexpr (!kSA) x = ca.kept_idx[((size_t)h * ca.F + g) * ca.P + k];
+          else x = sa.perm[((size_t)h * sa.T + kT) * sa.C + kbeg + k];
           const int lim = kSA ? sa.C : ca.P;
-          if (x >= 0 && x < lim) src[u] = x; else bad_index = true;
-        }
-        if constexpr (kSA) {
-#pragma unroll
-          for (int w = 0; w <= kT; ++w)
-            sm.kcodes[s][w][r] = src[u] >= 0 ? sa.codes[((size_t)h * sa.T + w) * sa.C + src[u]] : 0xfffffffeu;
-          sm.bias[s][r] = src[u] >= 0 ? log2f((float)max(sa.m[(size_t)h * sa.C + src[u]], 1)) : 0.f;
+          if (x >= 0 && x < lim) out[u] = x; else bad_index = true;
         }
       }
-      const __nv_bfloat16* kb = kSA ? sa.K : ca.k_p;
-      const __nv_bfloat16* vb = kSA ? sa.V : ca.v_p;
-      const size_t rows_per_head = kSA ? (size_t)sa.C : (size_t)ca.P;
+    };
+    // AnnSA metadata of those rows: codes of the earlier tables and log2 m
+    uint32_t kc[kMaxT - 1][2];
+    float bs[2];
+    auto fetch_meta = [&](const int* src) {
+      if constexpr (kSA) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+          for (int w = 0; w < kPrev; ++w)
+            kc[w][u] = src[u] >= 0 ? sa.codes[((size_t)h * sa.T + w) * sa.C + src[u]] : 0xfffffffeu;
+          bs[u] = src[u] >= 0 ? log2f((float)max(sa.m[(size_t)h * sa.C + src[u]], 1)) : 0.f;
+        }
+      }
+    };
+    int src[2];
+    fetch_src(0, src);
+    fetch_meta(src);
+    const __nv_bfloat16* kb = kSA ? sa.K : ca.k_p;
+    const __nv_bfloat16* vb = kSA ? sa.V : ca.v_p;
+    const size_t rows_per_head = kSA ? (size_t)sa.C : (size_t)ca.P;
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int s = j % kStages;
+      int nsrc[2] = {-1, -1};
+      if (j + 1 < ntiles) fetch_src(j + 1, nsrc);  // in flight during the wait below
+      if (j >= kStages) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.empty[s], (uint32_t)((j / kStages) - 1) & 1u));
+      if (!ok) break;
+      if constexpr (kSA) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+#pragma unroll
+          for (int w = 0; w < kPrev; ++w) sm.kcodes[s][w][lane + 32 * u] = kc[w][u];
+          sm.bias[s][lane + 32 * u] = bs[u];
+        }
+      }
       const uint32_t kt = tc::smem_u32(sm.K[s]), vt = tc::smem_u32(sm.V[s]);
 #pragma unroll
       for (int i = 0; i < kN * 16 / 32; ++i) {
-        const int r = 2 * i + (lane >> 4), ch = lane & 15;
-        const int sr = __shfl_sync(0xffffffffu, src[r >> 5], r & 31);
-        const uint32_t off = tc::sw128_offset(r, ch, kN);
+        const int rr = 2 * i + (lane >> 4), ch = lane & 15;
+        const int sr = __shfl_sync(0xffffffffu, src[rr >> 5], rr & 31);
+        const uint32_t off = tc::sw128_offset(rr, ch, kN);
         if (sr >= 0) {
           const size_t row = ((size_t)h * rows_per_head + sr) * kD;
           tc::cp_async16(kt + off, (const char*)(kb + row) + ch * 16, 16u);
@@ -240,139 +273,167 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       tc::cp_async_arrive_noinc(&sm.full[s]);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.full[s]);  // the metadata written above
+      src[0] = nsrc[0];
+      src[1] = nsrc[1];
+      if (j + 1 < ntiles) fetch_meta(src);  // lands while tile j is consumed
     }
   } else if (warp == 1) {
     // ================================================= MMA issuer
+    // Issues QK_j (S_j = Q K_j^T into S buffer j & 1) and PV_j (O += P_j V_j)
+    // in whichever order their inputs become ready, with QK at most one tile
+    // ahead of PV.
     constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kM, kN, 0, 0);
     constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kM, kD, 0, 1);
     if (ntiles > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.bar_q, 0));
-    auto issue_qk = [&](int j) -> bool {
-      const int s = j % kStages, b = j & 1;
-      bool good = tc::mbar_wait(&sm.full[s], (uint32_t)(j / kStages) & 1u);
-      if (good && j >= 2) good = tc::mbar_wait(&sm.sfree[b], (uint32_t)((j >> 1) - 1) & 1u);
-      good = __all_sync(0xffffffffu, good);
-      if (!good) return false;
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_after();
-      if (lane == 0) {
-        const uint32_t q0 = tc::smem_u32(sm.Q), k0 = tc::smem_u32(sm.K[s]);
+    int jq = 0, jp = 0;
+    uint32_t idle = 0;
+    while (ok && jp < ntiles) {
+      bool did = false;
+      if (jp < jq) {
+        const int b = jp & 1;
+        int ready = lane == 0 ? (int)tc::mbar_test_wait(&sm.pready[b], (uint32_t)(jp >> 1) & 1u) : 0;
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          tc::fence_proxy_async_smem();
+          tc::tc_fence_after();
+          if (lane == 0) {
+            const int s = jp % kStages;
+            const uint32_t p0 = tc::smem_u32(sm.K[s]), v0 = tc::smem_u32(sm.V[s]);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t oq = (kk >> 2) * kM * 128 + (kk & 3) * 32;
-          const uint32_t okk = (kk >> 2) * kN * 128 + (kk & 3) * 32;
-          tc::mma_bf16(tmem + b * kN, tc::sdesc_kmajor_sw128(q0 + oq), tc::sdesc_kmajor_sw128(k0 + okk),
-                       idesc_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kN / 16; ++kk)
+              tc::mma_bf16(tmem + 128, tc::sdesc_kmajor_sw128(p0 + kk * 32),
+                           tc::sdesc_mnmajor_sw128(v0 + kk * 16 * 128, kN * 128), idesc_pv,
+                           (jp > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_commit(&sm.empty[s]);
+          }
+          __syncwarp();
+          ++jp;
+          did = true;
         }
-        tc::mma_commit(&sm.sfull[b]);
       }
-      __syncwarp();
-      return true;
-    };
-    if (ok && ntiles > 0) ok = issue_qk(0);
-    for (int j = 0; j < ntiles && ok; ++j) {
-      if (j + 1 < ntiles) {
-        ok = issue_qk(j + 1);
-        if (!ok) break;
-      }
-      const int s = j % kStages, b = j & 1;
-      ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.pready[b], (uint32_t)(j >> 1) & 1u));
-      if (!ok) break;
-      tc::fence_proxy_async_smem();
-      tc::tc_fence_after();
-      if (lane == 0) {
-        const uint32_t p0 = tc::smem_u32(sm.K[s]), v0 = tc::smem_u32(sm.V[s]);
+      if (!did && jq < ntiles && jq <= jp + 1) {
+        const int s = jq % kStages, b = jq & 1;
+        int ready = 0;
+        if (lane == 0)
+          ready = tc::mbar_test_wait(&sm.full[s], (uint32_t)(jq / kStages) & 1u) &&
+                  (jq < 2 || tc::mbar_test_wait(&sm.sfree[b], (uint32_t)((jq >> 1) - 1) & 1u));
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          tc::fence_proxy_async_smem();
+          tc::tc_fence_after();
+          if (lane == 0) {
+            const uint32_t q0 = tc::smem_u32(sm.Q), k0 = tc::smem_u32(sm.K[s]);
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_bf16(tmem + 128, tc::sdesc_kmajor_sw128(p0 + kk * 32),
-                       tc::sdesc_mnmajor_sw128(v0 + kk * 16 * 128, kN * 128), idesc_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_commit(&sm.empty[s]);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t oq = (kk >> 2) * kM * 128 + (kk & 3) * 32;
+              const uint32_t okk = (kk >> 2) * kN * 128 + (kk & 3) * 32;
+              tc::mma_bf16(tmem + b * kN, tc::sdesc_kmajor_sw128(q0 + oq), tc::sdesc_kmajor_sw128(k0 + okk),
+                           idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(&sm.sfull[b]);
+          }
+          __syncwarp();
+          ++jq;
+          did = true;
+        }
       }
-      __syncwarp();
+      if (did) {
+        idle = 0;
+      } else if (++idle > kIdlePolls) {
+        ok = false;
+      } else {
+        __nanosleep(32);
+      }
     }
     // every MMA this warp issued has finished before TMEM is freed (also on
     // an expired wait, where nobody else may wait for them)
-    if (ntiles > 0) {
+    if (jq > 0) {
       if (lane == 0) tc::mma_commit(&sm.fin);
       __syncwarp();
       if (!tc::mbar_wait(&sm.fin, 0)) ok = false;
     }
   } else {
     // ================================================= softmax (warps 2-5)
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // query row of the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    int my_row = -1;
-    uint32_t qcode[kMaxT] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};
-    uint32_t qlo = 0xffffffffu, qhi = 0u;
-    if constexpr (!kSA) {
-      if (m0 + r < ca.n_f) my_row = g * ca.n_f + m0 + r;
-    } else {
-      if (m0 + r < Nq) {
-        const int qi = sa.q_perm[((size_t)h * sa.T + kT) * Nq + m0 + r];
-        if (qi >= 0 && qi < Nq) my_row = qi;
-      }
+    uint32_t qprev[kMaxT - 1] = {0xffffffffu, 0xffffffffu, 0xffffffffu};
+    // keys of this row's bucket in table kT, in CTA key coordinates
+    int run_a = 0, run_b = nkeys;
+    if constexpr (kSA) {
+      run_b = 0;
+      if (my_row >= 0) {
 #pragma unroll
-      for (int u = 0; u < kMaxT; ++u)
-        if (u <= kT && my_row >= 0) qcode[u] = sa.q_codes[((size_t)h * sa.T + u) * Nq + my_row];
-      uint32_t lo = my_row >= 0 ? qcode[kT] : 0xffffffffu, hi = my_row >= 0 ? qcode[kT] : 0u;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        for (int w = 0; w < kPrev; ++w) qprev[w] = sa.q_codes[((size_t)h * sa.T + w) * Nq + my_row];
+        const uint32_t qk = sa.q_codes[((size_t)h * sa.T + kT) * Nq + my_row];
+        if (qk < (uint32_t)sa.nb) {
+          const int a = min(max(toff[qk], 0), n_live);
+          const int b = min(max(toff[qk + 1], a), n_live);
+          run_a = min(max(a - kbeg, 0), nkeys);
+          run_b = min(max(b - kbeg, run_a), nkeys);
+        } else {
+          bad_index = true;
+        }
       }
-      qlo = lo;
-      qhi = hi;
     }
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int s = j % kStages, b = j & 1;
-      const int nvalid = min(kN, nkeys - j * kN);
-      ok = tc::mbar_wait(&sm.full[s], (uint32_t)(j / kStages) & 1u);  // metadata of the tile
+      if constexpr (kSA) ok = tc::mbar_wait(&sm.full[s], (uint32_t)(j / kStages) & 1u);  // metadata
       ok = ok && tc::mbar_wait(&sm.sfull[b], (uint32_t)(j >> 1) & 1u);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc::tc_fence_after();
-      // which 32-key chunks can hold an allowed key for some query of this warp
+      const uint64_t run = range_bits(run_a - j * kN, run_b - j * kN);
+      uint32_t bits[2] = {(uint32_t)run, (uint32_t)(run >> 32)};
       bool live[2];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        live[q] = q * 32 < nvalid;
-        if constexpr (kSA) {
-          if (live[q]) {
-            const uint32_t klo = sm.kcodes[s][kT][q * 32];
-            const uint32_t khi = sm.kcodes[s][kT][min(q * 32 + 31, nvalid - 1)];
-            live[q] = !(khi < qlo || klo > qhi);
-          }
-        }
-      }
+      for (int q = 0; q < 2; ++q) live[q] = __any_sync(0xffffffffu, bits[q] != 0u);
       float v[2][32];
-      uint32_t bits[2] = {0u, 0u};
-      float tmax = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        if (!live[q]) continue;
-        tc::tmem_ld32(tmem + lane_base + b * kN + q * 32, v[q]);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = q * 32 + i;
-          bool allow = c < nvalid;
-          float sc = v[q][i] * scale2;
-          if constexpr (kSA) {
-            allow = allow && sm.kcodes[s][kT][c] == qcode[kT];
-#pragma unroll
-            for (int w = 0; w < kT; ++w) allow = allow && sm.kcodes[s][w][c] != qcode[w];
-            sc += sm.bias[s][c];
-          }
-          v[q][i] = sc;
-          bits[q] |= (allow ? 1u : 0u) << i;
-          tmax = allow ? fmaxf(tmax, sc) : tmax;
-        }
-      }
+      for (int q = 0; q < 2; ++q)
+        if (live[q]) tc::tmem_ld32(tmem + lane_base + b * kN + q * 32, v[q]);
       // S_j is in registers: release the S buffer
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.sfree[b]);
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        if (!live[q]) continue;
+        if constexpr (kSA) {
+          // drop slots an earlier table already admitted for this query
+#pragma unroll
+          for (int w = 0; w < kPrev; ++w) {
+            if (bits[q]) {
+#pragma unroll
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const uint4 c4 = *reinterpret_cast<const uint4*>(&sm.kcodes[s][w][q * 32 + i4 * 4]);
+                const uint32_t eq = (c4.x == qprev[w] ? 1u : 0u) | (c4.y == qprev[w] ? 2u : 0u) |
+                                    (c4.z == qprev[w] ? 4u : 0u) | (c4.w == qprev[w] ? 8u : 0u);
+                bits[q] &= ~(eq << (i4 * 4));
+              }
+            }
+          }
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 b4 = *reinterpret_cast<const float4*>(&sm.bias[s][q * 32 + i4 * 4]);
+            const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int i = i4 * 4 + e;
+              const float sc = ((bits[q] >> i) & 1u) ? fmaf(v[q][i], scale2, bb[e]) : -INFINITY;
+              v[q][i] = sc;
+              tmax = fmaxf(tmax, sc);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float sc = ((bits[q] >> i) & 1u) ? v[q][i] * scale2 : -INFINITY;
+            v[q][i] = sc;
+            tmax = fmaxf(tmax, sc);
+          }
+        }
+      }
       // raise the running max (and rescale O) only for a large increase
       const bool raise = tmax > m_run + kRescale;
       const float m_new = raise ? tmax : m_run;
@@ -393,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       }
       l_run *= alpha;
       m_run = m_new;
-      // P_j (bf16) over the spent key tile: 128 rows x 64 keys, one swizzle atom per row
+      // P_j (bf16) over the spent key tile: 128 rows x 64 keys, one swizzle
+      // atom per row; masked scores are -inf and give 0
+      const float m_sub = m_run == -INFINITY ? 0.f : m_run;
       float psum = 0.f;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -401,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         if (live[q]) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = ((bits[q] >> i) & 1u) ? exp2f(v[q][i] - m_run) : 0.f;
-            const float p1 = ((bits[q] >> (i + 1)) & 1u) ? exp2f(v[q][i + 1] - m_run) : 0.f;
+            const float p0 = exp2f(v[q][i] - m_sub);
+            const float p1 = exp2f(v[q][i + 1] - m_sub);
             psum += p0 + p1;
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             packed[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
@@ -422,48 +485,72 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.pready[b]);
     }
-    // ---- output: O (TMEM) / l
+    // ---- output: O (TMEM) staged per warp through shared memory (Q and K
+    // are free once the last PV product has landed), then written one row
+    // per warp instruction
     if (ok && ntiles > 0) {
       ok = __all_sync(0xffffffffu, wait_pv(sm, ntiles - 1));
       tc::tc_fence_after();
     }
+    if constexpr (kSA) tc::cp_async_wait_all();  // the query rows (no key tile may have waited for them)
     if (ok) {
-      float o[kD / 32][32];
-      if (ntiles > 0) {
+      uint8_t* wbase = sm.Q + quarter * (32 * kD * 4);
+      if constexpr (kSA) {
+        // fp32 rows of 512 bytes; chunk i of row `lane` at position (i + lane) % 32
 #pragma unroll
-        for (int q = 0; q < kD / 32; ++q) tc::tmem_ld32(tmem + lane_base + 128 + q * 32, o[q]);
+        for (int q = 0; q < kD / 32; ++q) {
+          float o[32];
+          if (ntiles > 0) {
+            tc::tmem_ld32(tmem + lane_base + 128 + q * 32, o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(wbase + lane * 512 + (((q * 8 + k) + lane) & 31) * 16) =
+                make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+        }
+        __syncwarp();
+        for (int rr = 0; rr < 32; ++rr) {
+          const int row = __shfl_sync(0xffffffffu, my_row, rr);
+          if (row < 0) continue;
+          const float4 x = *reinterpret_cast<const float4*>(wbase + rr * 512 + ((lane + rr) & 31) * 16);
+          *reinterpret_cast<float4*>(sa.ws_o + (((size_t)kT * H + h) * Nq + row) * kD + lane * 4) = x;
+        }
+        if (my_row >= 0)
+          sa.ws_ml[((size_t)kT * H + h) * Nq + my_row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
       } else {
+        // normalised bf16 rows of 256 bytes; chunk i of row `lane` at position (i + lane) % 16
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-        for (int q = 0; q < kD / 32; ++q)
+        for (int q = 0; q < kD / 32; ++q) {
+          float o[32];
+          if (ntiles > 0) {
+            tc::tmem_ld32(tmem + lane_base + 128 + q * 32, o);
+          } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[q][i] = 0.f;
-      }
-      if (my_row >= 0) {
-        if constexpr (!kSA) {
-          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-          __nv_bfloat16* dst = ca.out + ((size_t)h * Nq + my_row) * kD;
+            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+          }
 #pragma unroll
-          for (int q = 0; q < kD / 32; ++q)
+          for (int k = 0; k < 4; ++k) {
+            uint4 u;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&u);
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 u;
-              uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(o[q][i + 2 * e] * inv, o[q][i + 2 * e + 1] * inv);
-                w[e] = *reinterpret_cast<const uint32_t*>(&pb);
-              }
-              *reinterpret_cast<uint4*>(dst + q * 32 + i) = u;
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 pb = __floats2bfloat162_rn(o[8 * k + 2 * e] * inv, o[8 * k + 2 * e + 1] * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&pb);
             }
-        } else {
-          const size_t row = ((size_t)kT * H + h) * Nq + my_row;
-          float* dst = sa.ws_o + row * kD;
-#pragma unroll
-          for (int q = 0; q < kD / 32; ++q)
-#pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              *reinterpret_cast<float4*>(dst + q * 32 + i) = make_float4(o[q][i], o[q][i + 1], o[q][i + 2], o[q][i + 3]);
-          sa.ws_ml[row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
+            *reinterpret_cast<uint4*>(wbase + lane * 256 + (((q * 4 + k) + lane) & 15) * 16) = u;
+          }
+        }
+        __syncwarp();
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int rw = rr + (lane >> 4), c = lane & 15;
+          const int row = __shfl_sync(0xffffffffu, my_row, rw);
+          if (row < 0) continue;
+          const uint4 x = *reinterpret_cast<const uint4*>(wbase + rw * 256 + ((c + rw) & 15) * 16);
+          *reinterpret_cast<uint4*>(ca.out + ((size_t)h * Nq + row) * kD + c * 8) = x;
         }
       }
     }
