@@ -270,8 +270,13 @@ def algorithmic(cfg, path, match, snap_size, snap_lf):
         "nn_tc": {"flops": sum(nn_flops) / F,
                   "bytes": sum((H * n_f + c) * D * e for c in cand) / F},
         "annca_tc": {"flops": fl["annca"], "bytes": by["annca"]},
-        "annsa_tc": {"flops": fl["annsa"] / T,
-                     "bytes": (H * Nq * D * e + n_live * (2 * D * e + 4 + 2 * T * 4)) / 1.0 + H * Nq * D * 4},
+        # one launch for all tables; per table the queries and the live
+        # slots (K, V, m, codes); with T > 1 each table writes an fp32
+        # partial (o, max, sum) that the combine kernel reads back
+        "annsa_tc": {"flops": fl["annsa"],
+                     "bytes": (T * (H * Nq * D * e + n_live * (2 * D * e + 4 + 2 * T * 4))
+                               + (T * H * Nq * (D * 4 + 8) if T > 1 else H * Nq * (D * e + 4)))},
+        "annsa_combine": {"flops": 0, "bytes": T * H * Nq * (D * 4 + 8) + H * Nq * (D * e + 4)},
         "hash_tc": {"flops": 2 * rows * T * cfg.B * D / 3, "bytes": (rows * (D * e + T * 4)) / 3},
         "apply": {"flops": 0, "bytes": by["merge"] / F * 0.5},
     }

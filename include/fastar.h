@@ -243,6 +243,7 @@ int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes,
  *
  * q [H][F*n_f][D], k_p, v_p [H][P][D] dt; kept_idx/kept_cnt from
  * fastar_annca_prune (or any ascending id list); out [H][F*n_f][D] dt.
+ * scale must be positive and finite (FASTAR_ERR_ARG otherwise).
  * fp32 accumulation.  Passing kept = 0..P-1 gives dense attention.
  */
 int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p,
@@ -267,7 +268,8 @@ int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p,
  *
  * q [H][Nq][D] dt; q_codes [H][T][Nq]; q_perm [H][T][Nq] and q_offsets
  * [H][T][2^B+1] from fastar_hash of q; the cache after the chunk's merge;
- * out [H][Nq][D] dt; lse optional [H][Nq] float.  fp32 accumulation.
+ * out [H][Nq][D] dt; lse optional [H][Nq] float.  scale must be positive
+ * and finite (FASTAR_ERR_ARG otherwise).  fp32 accumulation.
  */
 int fastar_annsa_attention(fastar_dtype dt, const void* q,
                            const uint32_t* q_codes, const int32_t* q_perm,

@@ -2,36 +2,40 @@
 //
 // One CTA owns 128 queries (one per softmax thread) and walks their keys 64
 // at a time through a warp-specialised pipeline:
-//   warp 0     producer: the queries (AnnCA: one TMA box pair; AnnSA: a
-//              cp.async row gather), then for every key tile the key and
-//              value rows (cp.async gathers into the 128-byte swizzled
-//              layout, 2-stage ring) and the tile's mask metadata;
+//   warp 0     producer: AnnCA's queries (one TMA box pair), then for every
+//              key tile the key and value rows (cp.async gathers into the
+//              128-byte swizzled layout, 2-stage ring) and the tile's mask
+//              metadata, fetched one tile ahead;
 //   warp 1     MMA issuer: S_j = Q K_j^T (M 128, N 64, K 128) into one of two
-//              TMEM S buffers, issued one tile ahead of the softmax, and
-//              O += P_j V_j (M 128, N 128, K 64; V read as an MN-major operand)
-//              into the TMEM accumulator;
-//   warps 2-5  softmax, one thread per query row: read S_j from TMEM, apply
-//              the scale, the + ln m bias and the mask, keep a running max
-//              and sum in base 2, write P_j (bf16) over the spent key tile.
-//              The running max is only raised (and O in TMEM rescaled) when a
-//              tile's maximum exceeds it by more than 2^8, so P stays <= 256
-//              and rescaling is rare.
-// At the end the softmax threads read O from TMEM and write the output.
+//              TMEM S buffers and O += P_j V_j (M 128, N 128, K 64; V read as
+//              an MN-major operand) into the TMEM accumulator, each as soon as
+//              its inputs are ready (QK at most one tile ahead of PV);
+//   warps 2-5  softmax, one thread per query row (AnnSA: each also gathers
+//              its query row): read S_j from TMEM, apply the scale, the
+//              + ln m bias and the mask, keep a running max and sum in base 2,
+//              write P_j (bf16) over the spent key tile.  The running max is
+//              only raised (and O in TMEM rescaled) when a tile's maximum
+//              exceeds it by more than 2^8, so P stays <= 256 and rescaling
+//              is rare.
+// At the end the softmax threads read O from TMEM, stage their rows in shared
+// memory and write them out one row per warp instruction.
 //
 // AnnCA (gist.science technical summary 2.B): the CTA owns 128 queries of
 // one frame and walks the frame's kept prompt tokens; it writes the
 // normalised output.
 // AnnSA (gist.science 2.C; paper.rainbus.top method steps; + ln m from
-// paperlayer.ai appendix A, Lemma A.1): one launch per LSH table t.  The CTA
-// owns 128 consecutive queries of the chunk in the bucket order of table t
-// (the query CSR) and walks the cache slots of the buckets they span (the
-// cache CSR, sorted by code too).  A slot is allowed for a query iff their
-// table-t codes agree and no earlier table already allowed it, so every
-// allowed pair is visited exactly once over the T tables.  Because both
-// sides are bucket-sorted, a warp skips every 32-key chunk whose code range
-// does not meet the code range of its 32 queries.  Each table writes an
-// unnormalised partial (o, running max, sum); a combine kernel merges the T
-// partials per query.
+// paperlayer.ai appendix A, Lemma A.1): one launch covers every LSH table
+// t (grid y).  The CTA owns 128 consecutive queries of the chunk in the
+// bucket order of table t (the query CSR) and walks the cache slots of the
+// buckets they span (the cache CSR, sorted by code too).  A slot is allowed
+// for a query iff their table-t codes agree and no earlier table already
+// allowed it, so every allowed pair is visited exactly once over the T
+// tables.  The slots of a query's own table-t bucket form one run of the
+// CTA's key list (from the cache CSR offsets); a warp skips every 32-key
+// chunk that no run of its queries meets.  With one table the CTA writes the
+// normalised output and the log-sum-exp; with more, each table writes an
+// unnormalised partial (o, running max, sum) and a combine kernel merges the
+// T partials of each query.
 #include <math.h>
 
 #include "common.cuh"
@@ -84,8 +88,10 @@ struct SaArgs {
   const int32_t* perm;
   const int32_t* offsets;
   int C, T, nb;
-  float* ws_o;   // [T][H][Nq][D] unnormalised accumulators
-  float2* ws_ml; // [T][H][Nq] (running max in log2 units, sum)
+  float* ws_o;   // [T][H][Nq][D] per-table unnormalised partials (T >= 2)
+  float2* ws_ml; // [T][H][Nq] their (max in log2 units, sum)
+  __nv_bfloat16* out;
+  float* lse;
 };
 
 // Wait until the PV product of key tile j has landed in O (and, since one
@@ -100,6 +106,14 @@ __device__ __forceinline__ bool wait_pv(AttnSmem& sm, int j) {
   return tc::mbar_wait(&sm.empty[j % kStages], (uint32_t)(j / kStages) & 1u);
 }
 
+// 2^x by the SFU instruction (relative error about 2^-22; results below
+// 2^-126 flush to 0, and 2^-inf is 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Bits c (0..63) of the key tile with lo <= c < hi.
 __device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
   lo = max(lo, 0);
@@ -110,14 +124,12 @@ __device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
   return below_hi & ~below_lo;
 }
 
-// kT = -1: AnnCA (grid: query tiles x frames x heads); kT >= 0: AnnSA table
-// kT (grid: query tiles x 1 x heads).
-template <int kT>
+// AnnCA: grid (query tiles, frames, heads); AnnSA: grid (query tiles,
+// tables, heads).
+template <bool kSA>
 __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, int H,
                                                              int Nq, float scale, CaArgs ca, SaArgs sa,
                                                              int32_t* st) {
-  constexpr bool kSA = kT >= 0;
-  constexpr int kPrev = kSA ? kT : 0;  // AnnSA: earlier tables whose collisions are excluded
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
@@ -125,6 +137,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   const int m0 = blockIdx.x * kM;
   const int h = blockIdx.z;
   const int g = blockIdx.y;  // AnnCA: frame
+  const int kT = kSA ? (int)blockIdx.y : 0;  // AnnSA: table (the earlier tables' collisions are excluded)
   const float scale2 = scale * kLog2e;
 
   if (tid == 0) {
@@ -229,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
 #pragma unroll
-          for (int w = 0; w < kPrev; ++w)
-            kc[w][u] = src[u] >= 0 ? sa.codes[((size_t)h * sa.T + w) * sa.C + src[u]] : 0xfffffffeu;
+          for (int w = 0; w < kMaxT - 1; ++w)
+            kc[w][u] = (w < kT && src[u] >= 0) ? sa.codes[((size_t)h * sa.T + w) * sa.C + src[u]] : 0xfffffffeu;
           bs[u] = src[u] >= 0 ? log2f((float)max(sa.m[(size_t)h * sa.C + src[u]], 1)) : 0.f;
         }
       }
@@ -251,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
 #pragma unroll
-          for (int w = 0; w < kPrev; ++w) sm.kcodes[s][w][lane + 32 * u] = kc[w][u];
+          for (int w = 0; w < kMaxT - 1; ++w)
+            if (w < kT) sm.kcodes[s][w][lane + 32 * u] = kc[w][u];
           sm.bias[s][lane + 32 * u] = bs[u];
         }
       }
@@ -362,7 +376,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       run_b = 0;
       if (my_row >= 0) {
 #pragma unroll
-        for (int w = 0; w < kPrev; ++w) qprev[w] = sa.q_codes[((size_t)h * sa.T + w) * Nq + my_row];
+        for (int w = 0; w < kMaxT - 1; ++w)
+          if (w < kT) qprev[w] = sa.q_codes[((size_t)h * sa.T + w) * Nq + my_row];
         const uint32_t qk = sa.q_codes[((size_t)h * sa.T + kT) * Nq + my_row];
         if (qk < (uint32_t)sa.nb) {
           const int a = min(max(toff[qk], 0), n_live);
@@ -395,15 +410,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.sfree[b]);
-      float tmax = -INFINITY;
+      // scores in log2 units (masked: -inf) and their maximum; AnnCA keeps
+      // the raw products and scales the maximum (scale > 0)
+      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         if (!live[q]) continue;
         if constexpr (kSA) {
           // drop slots an earlier table already admitted for this query
 #pragma unroll
-          for (int w = 0; w < kPrev; ++w) {
-            if (bits[q]) {
+          for (int w = 0; w < kMaxT - 1; ++w) {
+            if (w < kT && bits[q]) {
 #pragma unroll
               for (int i4 = 0; i4 < 8; ++i4) {
                 const uint4 c4 = *reinterpret_cast<const uint4*>(&sm.kcodes[s][w][q * 32 + i4 * 4]);
@@ -422,18 +439,20 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
               const int i = i4 * 4 + e;
               const float sc = ((bits[q] >> i) & 1u) ? fmaf(v[q][i], scale2, bb[e]) : -INFINITY;
               v[q][i] = sc;
-              tmax = fmaxf(tmax, sc);
+              tm[e] = fmaxf(tm[e], sc);
             }
           }
         } else {
+          if (!__all_sync(0xffffffffu, bits[q] == 0xffffffffu)) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float sc = ((bits[q] >> i) & 1u) ? v[q][i] * scale2 : -INFINITY;
-            v[q][i] = sc;
-            tmax = fmaxf(tmax, sc);
+            for (int i = 0; i < 32; ++i) v[q][i] = ((bits[q] >> i) & 1u) ? v[q][i] : -INFINITY;
           }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) tm[i & 3] = fmaxf(tm[i & 3], v[q][i]);
         }
       }
+      float tmax = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+      if constexpr (!kSA) tmax *= scale2;
       // raise the running max (and rescale O) only for a large increase
       const bool raise = tmax > m_run + kRescale;
       const float m_new = raise ? tmax : m_run;
@@ -455,18 +474,25 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       l_run *= alpha;
       m_run = m_new;
       // P_j (bf16) over the spent key tile: 128 rows x 64 keys, one swizzle
-      // atom per row; masked scores are -inf and give 0
+      // atom per row; masked scores are -inf and give 0 (scale > 0)
       const float m_sub = m_run == -INFINITY ? 0.f : m_run;
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         uint32_t packed[16];
         if (live[q]) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = exp2f(v[q][i] - m_sub);
-            const float p1 = exp2f(v[q][i + 1] - m_sub);
-            psum += p0 + p1;
+            float p0, p1;
+            if constexpr (kSA) {
+              p0 = ex2(v[q][i] - m_sub);
+              p1 = ex2(v[q][i + 1] - m_sub);
+            } else {
+              p0 = ex2(fmaf(v[q][i], scale2, -m_sub));
+              p1 = ex2(fmaf(v[q][i + 1], scale2, -m_sub));
+            }
+            ps[i & 3] += p0;
+            ps[(i & 3) + 1] += p1;
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             packed[i >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
           }
@@ -479,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
           *reinterpret_cast<uint4*>(sm.K[s] + tc::sw128_offset(r, q * 4 + k, kM)) =
               make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
       }
+      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
       l_run += psum;
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
@@ -512,14 +539,34 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
                 make_float4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
         }
         __syncwarp();
-        for (int rr = 0; rr < 32; ++rr) {
-          const int row = __shfl_sync(0xffffffffu, my_row, rr);
-          if (row < 0) continue;
-          const float4 x = *reinterpret_cast<const float4*>(wbase + rr * 512 + ((lane + rr) & 31) * 16);
-          *reinterpret_cast<float4*>(sa.ws_o + (((size_t)kT * H + h) * Nq + row) * kD + lane * 4) = x;
+        const size_t ri = (size_t)h * Nq + my_row;
+        if (sa.T == 1) {
+          // a single table: the partial is the result
+          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+          if (my_row >= 0 && sa.lse) sa.lse[ri] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+          for (int rr = 0; rr < 32; ++rr) {
+            const int row = __shfl_sync(0xffffffffu, my_row, rr);
+            const float iv = __shfl_sync(0xffffffffu, inv, rr);
+            if (row < 0) continue;
+            const float4 x = *reinterpret_cast<const float4*>(wbase + rr * 512 + ((lane + rr) & 31) * 16);
+            const __nv_bfloat162 b0 = __floats2bfloat162_rn(x.x * iv, x.y * iv);
+            const __nv_bfloat162 b1 = __floats2bfloat162_rn(x.z * iv, x.w * iv);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t*>(&b0);
+            u.y = *reinterpret_cast<const uint32_t*>(&b1);
+            *reinterpret_cast<uint2*>(sa.out + ((size_t)h * Nq + row) * kD + lane * 4) = u;
+          }
+        } else {
+          // this table's partial; the combine kernel merges the tables
+          for (int rr = 0; rr < 32; ++rr) {
+            const int row = __shfl_sync(0xffffffffu, my_row, rr);
+            if (row < 0) continue;
+            const float4 x = *reinterpret_cast<const float4*>(wbase + rr * 512 + ((lane + rr) & 31) * 16);
+            *reinterpret_cast<float4*>(sa.ws_o + (((size_t)kT * H + h) * Nq + row) * kD + lane * 4) = x;
+          }
+          if (my_row >= 0)
+            sa.ws_ml[((size_t)kT * H + h) * Nq + my_row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
         }
-        if (my_row >= 0)
-          sa.ws_ml[((size_t)kT * H + h) * Nq + my_row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
       } else {
         // normalised bf16 rows of 256 bytes; chunk i of row `lane` at position (i + lane) % 16
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
@@ -568,7 +615,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   if (warp == 1) tc::tmem_dealloc(tmem, 256);
 }
 
-// Merge the T per-table partials of each query (warp per query).
+// Merge the T per-table partials of each query: one warp per query, four
+// dimensions per lane; every table's (max, sum) and partial row are loaded
+// before any is used.
 __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restrict__ ws_o,
                                                             const float2* __restrict__ ws_ml, int T, int H,
                                                             int Nq, __nv_bfloat16* __restrict__ out,
@@ -578,46 +627,53 @@ __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restr
   const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (i >= Nq) return;
-  float M = -INFINITY;
-  for (int t = 0; t < T; ++t) M = fmaxf(M, ws_ml[((size_t)t * H + h) * Nq + i].x);
-  float L = 0.f;
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int t = 0; t < T; ++t) {
+  float2 ml[kMaxT];
+  float4 o[kMaxT];
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) {
+    ml[t] = make_float2(-INFINITY, 0.f);
+    o[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (t < T) {
       const size_t r = ((size_t)t * H + h) * Nq + i;
-      const float2 ml = ws_ml[r];
-      if (ml.x == -INFINITY) continue;
-      const float w = exp2f(ml.x - M);
-      L = fmaf(ml.y, w, L);
-      const float4 a = *reinterpret_cast<const float4*>(ws_o + r * kD + lane * 4);
-      o.x = fmaf(a.x, w, o.x);
-      o.y = fmaf(a.y, w, o.y);
-      o.z = fmaf(a.z, w, o.z);
-      o.w = fmaf(a.w, w, o.w);
+      ml[t] = __ldcs(ws_ml + r);
+      o[t] = __ldcs(reinterpret_cast<const float4*>(ws_o + r * kD) + lane);
     }
   }
+  float M = -INFINITY;
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) M = fmaxf(M, ml[t].x);
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) {
+    const float w = ml[t].x == -INFINITY ? 0.f : exp2f(ml[t].x - M);
+    L = fmaf(ml[t].y, w, L);
+    acc.x = fmaf(o[t].x, w, acc.x);
+    acc.y = fmaf(o[t].y, w, acc.y);
+    acc.z = fmaf(o[t].z, w, acc.z);
+    acc.w = fmaf(o[t].w, w, acc.w);
+  }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  __nv_bfloat16* dst = out + ((size_t)h * Nq + i) * kD + lane * 4;
-  const __nv_bfloat162 b0 = __floats2bfloat162_rn(o.x * inv, o.y * inv);
-  const __nv_bfloat162 b1 = __floats2bfloat162_rn(o.z * inv, o.w * inv);
+  const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+  const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   uint2 u;
   u.x = *reinterpret_cast<const uint32_t*>(&b0);
   u.y = *reinterpret_cast<const uint32_t*>(&b1);
-  *reinterpret_cast<uint2*>(dst) = u;
+  *reinterpret_cast<uint2*>(out + ((size_t)h * Nq + i) * kD + lane * 4) = u;
   if (lse && lane == 0) lse[(size_t)h * Nq + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
 }
 
-template <int kT>
+template <bool kSA>
 int launch_attn(const CUtensorMap& map, dim3 grid, int H, int Nq, float scale, const CaArgs& ca,
                 const SaArgs& sa, int32_t* st, cudaStream_t s) {
   const size_t smem = sizeof(AttnSmem) + 1024;
-  if (cudaFuncSetAttribute(attn_tc_kernel<kT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  if (cudaFuncSetAttribute(attn_tc_kernel<kSA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  attn_tc_kernel<kT><<<grid, kThreads, smem, s>>>(map, H, Nq, scale, ca, sa, st);
-  FASTAR_LAUNCHED(s, kT < 0 ? "annca_tc" : "annsa_tc");
+  attn_tc_kernel<kSA><<<grid, kThreads, smem, s>>>(map, H, Nq, scale, ca, sa, st);
+  FASTAR_LAUNCHED(s, kSA ? "annsa_tc" : "annca_tc");
   return FASTAR_OK;
 }
 
@@ -625,6 +681,7 @@ int launch_attn(const CUtensorMap& map, dim3 grid, int H, int Nq, float scale, c
 
 size_t annsa_tc_ws_bytes(int H, int Nq, int D, int T) {
   if (D != kD || T > kMaxT) return 0;
+  if (T == 1) return 0;  // a single table writes the output directly
   const size_t o = (size_t)T * H * Nq * kD * sizeof(float);
   const size_t ml = (size_t)T * H * Nq * sizeof(float2);
   return ((o + 255) & ~(size_t)255) + ((ml + 255) & ~(size_t)255);
@@ -641,7 +698,7 @@ int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void*
   CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P,
             (__nv_bfloat16*)out};
   SaArgs sa{};
-  return launch_attn<-1>(mapQ, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
+  return launch_attn<false>(mapQ, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
 }
 
 int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
@@ -650,25 +707,17 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   (void)q_offsets;
   if (dt != FASTAR_BF16 || c->D != kD || c->T > kMaxT) return FASTAR_ERR_UNSUPPORTED;
   if (Nq == 0 || c->H == 0) return FASTAR_OK;
-  if (!ws) return FASTAR_ERR_WORKSPACE;
+  if (c->T > 1 && !ws) return FASTAR_ERR_WORKSPACE;
   const size_t o_bytes = ((size_t)c->T * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
   SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
-            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes)};
+            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse};
   CaArgs ca{};
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
-  const dim3 grid((Nq + kM - 1) / kM, 1, c->H);
-  int rc = FASTAR_OK;
-  for (int t = 0; t < c->T && rc == FASTAR_OK; ++t) {
-    switch (t) {
-      case 0: rc = launch_attn<0>(dummy, grid, c->H, Nq, scale, ca, sa, st, s); break;
-      case 1: rc = launch_attn<1>(dummy, grid, c->H, Nq, scale, ca, sa, st, s); break;
-      case 2: rc = launch_attn<2>(dummy, grid, c->H, Nq, scale, ca, sa, st, s); break;
-      default: rc = launch_attn<3>(dummy, grid, c->H, Nq, scale, ca, sa, st, s); break;
-    }
-  }
-  if (rc != FASTAR_OK) return rc;
+  // every table in one launch: the tables' CTAs fill each other's waves
+  const int rc = launch_attn<true>(dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa, st, s);
+  if (rc != FASTAR_OK || c->T == 1) return rc;
   annsa_combine_kernel<<<dim3((Nq + 7) / 8, c->H), 256, 0, s>>>(sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");

@@ -199,6 +199,7 @@ int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p, cons
   (void)ws_bytes;
   if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
   if (H < 0 || F < 0 || n_f < 0 || P < 0) return FASTAR_ERR_ARG;
+  if (!(scale > 0.f && scale < INFINITY)) return FASTAR_ERR_ARG;
   if (!dim_ok(D)) return FASTAR_ERR_UNSUPPORTED;
   if ((size_t)H * F * n_f == 0) return FASTAR_OK;
   if (!q || !out || !kept_cnt || !aligned16(q) || !aligned16(out)) return FASTAR_ERR_ARG;
@@ -215,6 +216,7 @@ int fastar_annsa_attention(fastar_dtype dt, const void* q, const uint32_t* q_cod
   if (rc != FASTAR_OK) return rc;
   if (dt != cache->dt) return FASTAR_ERR_ARG;
   if (Nq < 0) return FASTAR_ERR_ARG;
+  if (!(scale > 0.f && scale < INFINITY)) return FASTAR_ERR_ARG;
   if (Nq == 0 || cache->H == 0) return FASTAR_OK;
   if (!q || !q_codes || !q_perm || !q_offsets || !out || !aligned16(q) || !aligned16(out))
     return FASTAR_ERR_ARG;

@@ -82,6 +82,10 @@ def test_host_argument_errors_need_no_gpu(L):
     # attention: bad dtype
     assert L.fastar_annca_attention(7, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
                                     ctypes.c_float(0.1), fake, None, 0, None, None) == 2
+    # attention: scale must be positive and finite
+    for bad in (0.0, -0.1, float("inf"), float("nan")):
+        assert L.fastar_annca_attention(0, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
+                                        ctypes.c_float(bad), fake, None, 0, None, None) == 1
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
