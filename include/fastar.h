@@ -180,7 +180,8 @@ typedef struct {
  * k_new, v_new [H][F*n_f][D] dt; codes_new [H][T][F*n_f] uint32 (from
  * fastar_hash of k_new with the cache's planes); match_out optional
  * [H][F*n_f] int32: the slot each key joined, or -1.
- * Requires n_f <= C (then step 3 always finds room).
+ * Requires n_f <= C (then step 3 always finds room) and
+ * n_f <= FASTAR_MAX_FRAME_KEYS (FASTAR_ERR_UNSUPPORTED otherwise).
  */
 int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
                            const void* v_new, const uint32_t* codes_new,
@@ -207,6 +208,10 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
  * it zeroed).  The first call on a device looks up the array's address with
  * that device current; make it before any stream capture.
  */
+/* Largest frame (keys per frame) the merge accepts: the per-frame plan keeps
+ * one 32-bit word per key in shared memory. */
+#define FASTAR_MAX_FRAME_KEYS 49152
+
 #define FASTAR_NOALLOC_SCRATCH_BYTES (16u << 20)
 int fastar_tempcache_merge_noalloc(const fastar_cache* cache, const void* k_new,
                                    const void* v_new, const uint32_t* codes_new,

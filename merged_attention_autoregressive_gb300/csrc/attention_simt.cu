@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(256) annca_simt_kernel(const T* __restrict__ q
                                                          const int32_t* __restrict__ kept_cnt, int F, int n_f,
                                                          int P, float scale, T* __restrict__ out,
                                                          int32_t* st) {
+  pdl_wait();
   constexpr int PER = D / 32;
   if (status_bad(st)) return;
   const int h = blockIdx.y;
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(256) annca_simt_kernel(const T* __restrict__ q
   T* orow = out + ((size_t)h * Nq + i) * D;
 #pragma unroll
   for (int k = 0; k < PER; ++k) Elem<T>::st(orow + lane + 32 * k, os.acc[k] * inv);
+  pdl_trigger();
 }
 
 template <typename T, int D>
@@ -84,6 +86,7 @@ __global__ void __launch_bounds__(256) annsa_simt_kernel(const T* __restrict__ q
                                                          const int32_t* __restrict__ offsets, int C, int Tt,
                                                          int nb, float scale, T* __restrict__ out,
                                                          float* __restrict__ lse, int32_t* st) {
+  pdl_wait();
   constexpr int PER = D / 32;
   if (status_bad(st)) return;
   const int h = blockIdx.y;
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(256) annsa_simt_kernel(const T* __restrict__ q
 #pragma unroll
   for (int k = 0; k < PER; ++k) Elem<T>::st(orow + lane + 32 * k, os.acc[k] * inv);
   if (lse && lane == 0) lse[(size_t)h * Nq + i] = os.l > 0.f ? os.mx + logf(os.l) : -INFINITY;
+  pdl_trigger();
 }
 
 int launch_annca_simt(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
@@ -133,7 +137,7 @@ int launch_annca_simt(fastar_dtype dt, const void* q, const void* k_p, const voi
   if (Nq == 0 || H == 0) return FASTAR_OK;
   dim3 grid((Nq + 7) / 8, H), block(256);
 #define ANNCA_CASE(TT, DD)                                                                      \
-  annca_simt_kernel<TT, DD><<<grid, block, 0, s>>>((const TT*)q, (const TT*)k_p, (const TT*)v_p, \
+  fastar::launch_pdl((annca_simt_kernel<TT, DD>), grid, block, 0, s, (const TT*)q, (const TT*)k_p, (const TT*)v_p, \
                                                    kept_idx, kept_cnt, F, n_f, P, scale, (TT*)out, st)
   if (dt == FASTAR_F32 && D == 64) ANNCA_CASE(float, 64);
   else if (dt == FASTAR_F32 && D == 128) ANNCA_CASE(float, 128);
@@ -152,7 +156,7 @@ int launch_annsa_simt(fastar_dtype dt, const void* q, const uint32_t* q_codes, i
   dim3 grid((Nq + 7) / 8, c->H), block(256);
   const int nb = 1 << c->B;
 #define ANNSA_CASE(TT, DD)                                                                        \
-  annsa_simt_kernel<TT, DD><<<grid, block, 0, s>>>((const TT*)q, q_codes, Nq, (const TT*)c->K,    \
+  fastar::launch_pdl((annsa_simt_kernel<TT, DD>), grid, block, 0, s, (const TT*)q, q_codes, Nq, (const TT*)c->K,    \
                                                    (const TT*)c->V, c->m, c->codes, c->size,      \
                                                    c->perm, c->offsets, c->C, c->T, nb, scale,    \
                                                    (TT*)out, lse, st)

@@ -130,6 +130,7 @@ template <bool kSA>
 __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, int H,
                                                              int Nq, float scale, CaArgs ca, SaArgs sa,
                                                              int32_t* st) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   AttnSmem& sm = *reinterpret_cast<AttnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
@@ -613,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, 256);
+  pdl_trigger();
 }
 
 // Merge the T per-table partials of each query: one warp per query, four
@@ -622,6 +624,7 @@ __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restr
                                                             const float2* __restrict__ ws_ml, int T, int H,
                                                             int Nq, __nv_bfloat16* __restrict__ out,
                                                             float* __restrict__ lse, int32_t* st) {
+  pdl_wait();
   if (status_bad(st)) return;
   const int h = blockIdx.y;
   const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -661,6 +664,7 @@ __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restr
   u.y = *reinterpret_cast<const uint32_t*>(&b1);
   *reinterpret_cast<uint2*>(out + ((size_t)h * Nq + i) * kD + lane * 4) = u;
   if (lse && lane == 0) lse[(size_t)h * Nq + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  pdl_trigger();
 }
 
 template <bool kSA>
@@ -672,7 +676,7 @@ int launch_attn(const CUtensorMap& map, dim3 grid, int H, int Nq, float scale, c
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  attn_tc_kernel<kSA><<<grid, kThreads, smem, s>>>(map, H, Nq, scale, ca, sa, st);
+  fastar::launch_pdl((attn_tc_kernel<kSA>), grid, kThreads, smem, s, map, H, Nq, scale, ca, sa, st);
   FASTAR_LAUNCHED(s, kSA ? "annsa_tc" : "annca_tc");
   return FASTAR_OK;
 }
@@ -718,7 +722,7 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   // every table in one launch: the tables' CTAs fill each other's waves
   const int rc = launch_attn<true>(dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa, st, s);
   if (rc != FASTAR_OK || c->T == 1) return rc;
-  annsa_combine_kernel<<<dim3((Nq + 7) / 8, c->H), 256, 0, s>>>(sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
+  fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 7) / 8, c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");
   return FASTAR_OK;

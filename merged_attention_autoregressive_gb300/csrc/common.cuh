@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "fastar.h"
 
 namespace fastar {
@@ -26,6 +28,30 @@ template <> struct Elem<__nv_bfloat16> {
     *p = __float2bfloat16_rn(v);
   }
 };
+
+// N consecutive elements of a row as floats (one vector access; the address
+// is aligned to N * sizeof(T), which must be 4, 8 or 16 bytes).
+template <typename T, int N>
+__device__ __forceinline__ void ld_vec(const T* p, float* out) {
+  constexpr int B = N * (int)sizeof(T);
+  static_assert(B == 4 || B == 8 || B == 16, "vector width");
+  using V = typename std::conditional<B == 4, uint32_t, typename std::conditional<B == 8, uint2, uint4>::type>::type;
+  const V v = *reinterpret_cast<const V*>(p);
+  const T* e = reinterpret_cast<const T*>(&v);
+#pragma unroll
+  for (int i = 0; i < N; ++i) out[i] = Elem<T>::ld(e + i);
+}
+template <typename T, int N>
+__device__ __forceinline__ void st_vec(T* p, const float* in) {
+  constexpr int B = N * (int)sizeof(T);
+  static_assert(B == 4 || B == 8 || B == 16, "vector width");
+  using V = typename std::conditional<B == 4, uint32_t, typename std::conditional<B == 8, uint2, uint4>::type>::type;
+  V v;
+  T* e = reinterpret_cast<T*>(&v);
+#pragma unroll
+  for (int i = 0; i < N; ++i) Elem<T>::st(e + i, in[i]);
+  *reinterpret_cast<V*>(p) = v;
+}
 
 // ---- sticky device status: first error wins, kernels exit once it is set
 __device__ __forceinline__ bool status_bad(const int32_t* st) {
@@ -173,6 +199,32 @@ namespace fastar {
 // launch timing is on (fastar_timing_begin), records the next caller event
 // on the launch stream, tagged with the kernel's name.
 void after_launch(cudaStream_t s, const char* name);
+
+// Every kernel of the library is a programmatic dependent launch: it may be
+// scheduled while the previous kernel of the stream is still finishing, so
+// its launch and CTA ramp-up overlap that kernel's tail.  Each kernel starts
+// with pdl_wait(), which returns once the previous grid has completed and its
+// writes are visible (so it must come before any other access, TMEM
+// allocation included), and calls pdl_trigger() when its main work is done:
+// the next grid is launched once every CTA of this one has triggered or
+// exited, so its waiting CTAs only share the SMs with this grid's last ones.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 }
 
 #define FASTAR_LAUNCHED(stream, name)                           \

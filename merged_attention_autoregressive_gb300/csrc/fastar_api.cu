@@ -168,6 +168,7 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const v
   int rc = check_cache(cache);
   if (rc != FASTAR_OK) return rc;
   if (F < 0 || n_f < 0 || n_f > cache->C) return FASTAR_ERR_ARG;
+  if (n_f > FASTAR_MAX_FRAME_KEYS) return FASTAR_ERR_UNSUPPORTED;
   if (F == 0 || n_f == 0 || cache->H == 0) return FASTAR_OK;
   if (!k_new || !v_new || !codes_new || !aligned16(k_new) || !aligned16(v_new)) return FASTAR_ERR_ARG;
   if (first_frame < 0 || (int64_t)first_frame + F > 0x7fffff00) return FASTAR_ERR_ARG;

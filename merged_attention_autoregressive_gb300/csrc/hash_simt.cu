@@ -15,6 +15,7 @@ __global__ void __launch_bounds__(256) hash_warp_kernel(const T* __restrict__ x,
                                                         const T* __restrict__ planes, int T_,
                                                         int B, int N, uint32_t* __restrict__ codes,
                                                         int32_t* st) {
+  pdl_wait();
   constexpr int PER = D / 32;
   __shared__ float R[kMaxTB * D];
   const int TB = T_ * B;
@@ -41,6 +42,7 @@ __global__ void __launch_bounds__(256) hash_warp_kernel(const T* __restrict__ x,
     }
     if (lane == 0) codes[((size_t)h * T_ + t) * N + i] = code;
   }
+  pdl_trigger();
 }
 
 int launch_hash_simt(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes,
@@ -49,13 +51,13 @@ int launch_hash_simt(fastar_dtype dt, const void* x, int H, int N, int D, const 
   if (rows == 0) return FASTAR_OK;
   dim3 grid((rows + 7) / 8), block(256);
   if (dt == FASTAR_F32 && D == 64)
-    hash_warp_kernel<float, 64><<<grid, block, 0, s>>>((const float*)x, rows, (const float*)planes, T, B, N, codes, st);
+    fastar::launch_pdl((hash_warp_kernel<float, 64>), grid, block, 0, s, (const float*)x, rows, (const float*)planes, T, B, N, codes, st);
   else if (dt == FASTAR_F32 && D == 128)
-    hash_warp_kernel<float, 128><<<grid, block, 0, s>>>((const float*)x, rows, (const float*)planes, T, B, N, codes, st);
+    fastar::launch_pdl((hash_warp_kernel<float, 128>), grid, block, 0, s, (const float*)x, rows, (const float*)planes, T, B, N, codes, st);
   else if (dt == FASTAR_BF16 && D == 64)
-    hash_warp_kernel<__nv_bfloat16, 64><<<grid, block, 0, s>>>((const __nv_bfloat16*)x, rows, (const __nv_bfloat16*)planes, T, B, N, codes, st);
+    fastar::launch_pdl((hash_warp_kernel<__nv_bfloat16, 64>), grid, block, 0, s, (const __nv_bfloat16*)x, rows, (const __nv_bfloat16*)planes, T, B, N, codes, st);
   else if (dt == FASTAR_BF16 && D == 128)
-    hash_warp_kernel<__nv_bfloat16, 128><<<grid, block, 0, s>>>((const __nv_bfloat16*)x, rows, (const __nv_bfloat16*)planes, T, B, N, codes, st);
+    fastar::launch_pdl((hash_warp_kernel<__nv_bfloat16, 128>), grid, block, 0, s, (const __nv_bfloat16*)x, rows, (const __nv_bfloat16*)planes, T, B, N, codes, st);
   else
     return FASTAR_ERR_UNSUPPORTED;
   FASTAR_LAUNCHED(s, "hash_warp");

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(128, 1) hash_tc_kernel(const __grid_constant__
                                                          const __nv_bfloat16* __restrict__ planes, int TB,
                                                          int NP, int T, int B, int N, long long rows, int ntiles,
                                                          uint32_t* __restrict__ codes, int32_t* st) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   HashSmem& sm = *reinterpret_cast<HashSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(128, 1) hash_tc_kernel(const __grid_constant__
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, 128);
+  pdl_trigger();
 }
 
 }  // namespace
@@ -156,7 +158,7 @@ int launch_hash_tc(fastar_dtype dt, const void* x, int H, int N, int D, const vo
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  hash_tc_kernel<<<grid, 128, smem, s>>>(mapX, (const __nv_bfloat16*)planes, TB, NP, T, B, N, rows, ntiles,
+  fastar::launch_pdl((hash_tc_kernel), grid, 128, smem, s, mapX, (const __nv_bfloat16*)planes, TB, NP, T, B, N, rows, ntiles,
                                          codes, st);
   FASTAR_LAUNCHED(s, "hash_tc");
   return FASTAR_OK;

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
                                                            const __grid_constant__ CUtensorMap mapB,
                                                            const __grid_constant__ CUtensorMap mapS,
                                                            NnArgs a, int32_t* st) {
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   NnSmem& sm = *reinterpret_cast<NnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   if (block_status_bad(st)) return;
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
   __syncthreads();
   tc::tc_fence_after();
   if (warp == 1) tc::tmem_dealloc(tmem, kAcc * kN);
+  pdl_trigger();
 }
 
 }  // namespace
@@ -378,7 +380,7 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
   split = max(1, min(split, min(16, btiles)));
   NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, n_f, Nrow, fi, C, cand, ncand, cinv,
            prev_slot, prev_kind, invn_prev, invn_out, best_out};
-  nn_tc_kernel<<<dim3(atiles, split, H), kThreads, smem, s>>>(mapA, mapB, mapS, a, st);
+  fastar::launch_pdl((nn_tc_kernel), dim3(atiles, split, H), kThreads, smem, s, mapA, mapB, mapS, a, st);
   FASTAR_LAUNCHED(s, "nn_tc");
   return FASTAR_OK;
 }

@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const uint32_t* __
                                                               int n_f, int P, int Tt, int B,
                                                               int32_t* __restrict__ kept_idx,
                                                               int32_t* __restrict__ kept_cnt, int32_t* st) {
+  pdl_wait();
   extern __shared__ uint32_t occ[];  // [T][2^B / 32]
   __shared__ int sh[33];
   if (block_status_bad(st)) return;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(kPruneThreads) prune_kernel(const uint32_t* __
   }
   for (int i = base + threadIdx.x; i < P; i += blockDim.x) out[i] = -1;
   if (threadIdx.x == 0) kept_cnt[(size_t)h * F + f] = base;
+  pdl_trigger();
 }
 
 int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f, int P,
@@ -59,7 +61,7 @@ int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F,
   if (H == 0 || F == 0) return FASTAR_OK;
   const size_t smem = (size_t)T * (((1 << B) + 31) >> 5) * sizeof(uint32_t);
   if (smem > 48 * 1024) return FASTAR_ERR_UNSUPPORTED;
-  prune_kernel<<<dim3(F, H), kPruneThreads, smem, s>>>(q_codes, p_codes, F, n_f, P, T, B, kept_idx,
+  fastar::launch_pdl((prune_kernel), dim3(F, H), kPruneThreads, smem, s, q_codes, p_codes, F, n_f, P, T, B, kept_idx,
                                                        kept_cnt, st);
   FASTAR_LAUNCHED(s, "prune");
   return FASTAR_OK;

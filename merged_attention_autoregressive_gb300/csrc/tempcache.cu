@@ -18,15 +18,17 @@
 //
 // Workspace (caller-owned, no initialisation needed):
 //   cand[2][H][C], ncand[2][H], rep_j[H][C], gcnt[H][C],
-//   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], evict[H][n_f],
+//   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], plan_cnt[H][n_f],
+//   evict[H][n_f],
 //   best[H][n_f] (packed best candidate per key, see pack_best),
 //   cinv[H][C] (inverse norms of the first frame's candidates),
 //   stage[H][n_f][128] bf16 (copies of the first n_f first-frame candidate
 //   rows, contiguous, so that the NN kernel can load them by TMA),
 //   invn[2][H][n_f] (inverse norms of the keys of the last two frames)
-// rep_j/gcnt are indexed by slot and reset for the candidate slots of each
-// frame before use (only candidates can be matched); best is zeroed when a
-// call starts and again by each plan after it has read it.
+// rep_j/gcnt are indexed by slot; they are clean for every candidate slot
+// when a plan starts (only candidates can be matched): cand_init cleans the
+// first frame's candidates and each plan the slots it refreshed.  best is
+// zeroed when a call starts and again by each plan after it has read it.
 #include <math.h>
 
 #include <type_traits>
@@ -46,6 +48,7 @@ struct MergeWs {
   int32_t* match;
   int32_t* plan_slot;
   int32_t* plan_kind;
+  int32_t* plan_cnt;
   int32_t* evict;
   unsigned long long* best;
   float* cinv;
@@ -60,7 +63,7 @@ size_t merge_ws_bytes(int H, int n_f, int C) {
   b += 2 * align256((size_t)H * C * 4);   // cand
   b += 2 * align256((size_t)H * 4);       // ncand
   b += 2 * align256((size_t)H * C * 4);   // rep_j, gcnt
-  b += 4 * align256((size_t)H * n_f * 4); // match, plan_slot, plan_kind, evict
+  b += 5 * align256((size_t)H * n_f * 4); // match, plan_slot, plan_kind, plan_cnt, evict
   b += align256((size_t)H * n_f * 8);     // best
   b += align256((size_t)H * C * 4);       // cinv
   b += 2 * align256((size_t)H * n_f * 4); // invn
@@ -81,6 +84,7 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
   w.match = take((size_t)H * n_f * 4);
   w.plan_slot = take((size_t)H * n_f * 4);
   w.plan_kind = take((size_t)H * n_f * 4);
+  w.plan_cnt = take((size_t)H * n_f * 4);
   w.evict = take((size_t)H * n_f * 4);
   w.best = (unsigned long long*)take((size_t)H * n_f * 8);
   w.cinv = (float*)take((size_t)H * C * 4);
@@ -91,28 +95,44 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
 }
 
 // ---------------------------------------------------------------- cand init
+// The slots refreshed in frame prev_frame, in slot order (thread t owns a
+// contiguous run of slots, so one load round and one block scan suffice);
+// their group accumulators are cleaned for the first plan.
 __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* __restrict__ last_frame,
                                                                  const int32_t* __restrict__ size, int C,
                                                                  int32_t prev_frame, int32_t* cand,
                                                                  int32_t* ncand, unsigned long long* best,
-                                                                 int n_f, int32_t* st) {
+                                                                 int32_t* rep_j, int32_t* gcnt, int n_f,
+                                                                 int32_t* st) {
+  pdl_wait();
+  constexpr int kPer = 16;  // slots per thread and round
   __shared__ int sh[33];
   if (block_status_bad(st)) return;
   const int h = blockIdx.x;
   const int n = min(max(size[h], 0), C);
   const int32_t* lf = last_frame + (size_t)h * C;
   int32_t* out = cand + (size_t)h * C;
+  for (int j = threadIdx.x; j < n_f; j += blockDim.x) best[(size_t)h * n_f + j] = 0ull;
   int base = 0;
-  for (int s0 = 0; s0 < n; s0 += blockDim.x) {
-    const int s = s0 + threadIdx.x;
-    const int hit = (s < n && lf[s] == prev_frame) ? 1 : 0;
+  for (int r0 = 0; r0 < n; r0 += kPer * kPlanThreads) {
+    const int s0 = r0 + threadIdx.x * kPer;
+    uint32_t hits = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (s0 + i < n && lf[s0 + i] == prev_frame) hits |= 1u << i;
     int tot;
-    const int pos = block_excl_scan(hit, sh, &tot);
-    if (hit) out[base + pos] = s;
+    int pos = base + block_excl_scan(__popc(hits), sh, &tot);
+    while (hits) {
+      const int i = __ffs(hits) - 1;
+      hits &= hits - 1;
+      out[pos++] = s0 + i;
+      rep_j[(size_t)h * C + s0 + i] = 0x7fffffff;  // the first plan's group accumulators
+      gcnt[(size_t)h * C + s0 + i] = 0;
+    }
     base += tot;
   }
   if (threadIdx.x == 0) ncand[h] = base;
-  for (int j = threadIdx.x; j < n_f; j += blockDim.x) best[(size_t)h * n_f + j] = 0ull;
+  pdl_trigger();
 }
 
 // Inverse norms of the first frame's candidates (bf16 rows of 128), one warp
@@ -122,6 +142,7 @@ __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __r
                                                         const int32_t* __restrict__ cand,
                                                         const int32_t* __restrict__ ncand, float* cinv,
                                                         __nv_bfloat16* stage, int n_f, int32_t* st) {
+  pdl_wait();
   if (status_bad(st)) return;
   const int h = blockIdx.y, lane = threadIdx.x & 31;
   const int nc = min(max(ncand[h], 0), C);
@@ -134,6 +155,7 @@ __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __r
     const float n2 = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
     if (lane == 0) cinv[(size_t)h * C + c] = n2 > 0.f ? 1.f / sqrtf(n2) : __int_as_float(0x7fc00000);
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- NN (SIMT)
@@ -143,6 +165,7 @@ __global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_fr
                                                       const int32_t* __restrict__ cand,
                                                       const int32_t* __restrict__ ncand,
                                                       unsigned long long* __restrict__ best_out, int32_t* st) {
+  pdl_wait();
   constexpr int PER = D / 32;
   if (status_bad(st)) return;
   const int h = blockIdx.y;
@@ -186,77 +209,65 @@ __global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_fr
     }
   }
   if (lane == 0) best_out[(size_t)h * n_f + j] = best_slot != 0x7fffffff ? pack_best(best, best_slot) : 0ull;
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- plan
+// rep_j / gcnt are clean (INT_MAX / 0) for the candidate slots when a plan
+// starts: cand_init cleans the first frame's candidates, and every plan
+// cleans the slots its frame refreshed, which are the next frame's
+// candidates.  The matches of the frame stay in shared memory.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int32_t f, float tau,
                                                             unsigned long long* __restrict__ best,
                                                             int32_t* __restrict__ match_out, int match_off,
                                                             int match_stride, int32_t* __restrict__ match,
-                                                            const int32_t* __restrict__ cand_cur,
-                                                            const int32_t* __restrict__ ncand_cur,
                                                             int32_t* __restrict__ cand_next,
                                                             int32_t* __restrict__ ncand_next,
                                                             int32_t* rep_j, int32_t* gcnt,
                                                             int32_t* __restrict__ plan_slot,
                                                             int32_t* __restrict__ plan_kind,
+                                                            int32_t* __restrict__ plan_cnt,
                                                             int32_t* __restrict__ evict,
                                                             const int32_t* __restrict__ last_frame,
                                                             const int32_t* __restrict__ m,
                                                             int32_t* size, int64_t* inserted,
                                                             int64_t* evicted, int32_t* st) {
+  pdl_wait();
+  extern __shared__ int s_key[];  // [n_f]: matched slot (or -1), later the planned slot
   __shared__ int sh[33];
   __shared__ long long shl[33];
   __shared__ int hist[2048];
   __shared__ int s_lstar, s_nlt, s_found;
   if (block_status_bad(st)) return;
   const int h = blockIdx.x;
-  const int32_t* mt = match + (size_t)h * n_f;
-  const int32_t* cc = cand_cur + (size_t)h * C;
   int32_t* rj = rep_j + (size_t)h * C;
   int32_t* gc = gcnt + (size_t)h * C;
   const int32_t* lf = last_frame + (size_t)h * C;
-  const int nc = ncand_cur[h];
-  // 0. the NN decision of every key: best candidate if its cosine reaches tau
+  // 0. the NN decision of every key (best candidate if its cosine reaches
+  //    tau), and the groups: count and lowest key index per matched slot
+  int unm_local = 0;
   for (int j = threadIdx.x; j < n_f; j += blockDim.x) {
     unsigned long long* bp = best + (size_t)h * n_f + j;
     const unsigned long long key = *bp;
     const int mj = (key != 0ull && best_cos(key) >= tau) ? best_slot(key) : -1;
+    s_key[j] = mj;
     match[(size_t)h * n_f + j] = mj;
     if (match_out) match_out[(size_t)h * match_stride + match_off + j] = mj;
     *bp = 0ull;
-  }
-  __syncthreads();
-  // 1. reset the group accumulators of the candidate slots
-  for (int c = threadIdx.x; c < nc; c += blockDim.x) {
-    const int s = cc[c];
-    rj[s] = 0x7fffffff;
-    gc[s] = 0;
-  }
-  __syncthreads();
-  // 2. group the matched keys: count and lowest index per slot
-  for (int j = threadIdx.x; j < n_f; j += blockDim.x) {
-    const int s = mt[j];
-    if (s >= 0) {
-      atomicMin(&rj[s], j);
-      atomicAdd(&gc[s], 1);
+    if (mj >= 0) {
+      atomicMin(&rj[mj], j);
+      atomicAdd(&gc[mj], 1);
+    } else {
+      ++unm_local;
     }
   }
-  __syncthreads();
-  // 3. unmatched keys: count
-  int U = 0;
-  {
-    int loc = 0;
-    for (int j = threadIdx.x; j < n_f; j += blockDim.x) loc += (mt[j] < 0);
-    int tot;
-    block_excl_scan(loc, sh, &tot);
-    U = tot;
-  }
+  int U;
+  block_excl_scan(unm_local, sh, &U);  // its barriers also order the atomics above
   const int size0 = min(max(size[h], 0), C);
   const int freeslots = C - size0;
   const int n_app = min(freeslots, U);
   const int E = U - n_app;
-  // 4. eviction: the E smallest (last_frame, slot) among slots with
+  // 1. eviction: the E smallest (last_frame, slot) among slots with
   //    last_frame < f that no key of this frame joined
   if (E > 0) {
     // eligible: lf < f, and not a slot matched now (only lf == f-1 can be)
@@ -336,43 +347,56 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
     em = block_sum_ll(em, shl);
     if (threadIdx.x == 0) evicted[h] += em;
   }
-  // 5. per-key plan (ascending j), and the next frame's candidate list
+  // 2. per-key plan (ascending j), and the next frame's candidate list; one
+  //    block scan counts the unmatched keys (low half) and the candidates
+  //    (high half) before each key
   const int32_t* ev = evict + (size_t)h * n_f;
   int urank_base = 0, cand_base = 0;
   for (int j0 = 0; j0 < n_f; j0 += blockDim.x) {
     const int j = j0 + threadIdx.x;
     const bool in = j < n_f;
-    const int s = in ? mt[j] : 0;
+    const int s = in ? s_key[j] : 0;
+    bool leader = false;
+    int cnt = 0;
+    if (in && s >= 0) {
+      leader = rj[s] == j;
+      if (leader) cnt = gc[s];
+    }
     const int unm = (in && s < 0) ? 1 : 0;
-    int utot;
-    const int ur = block_excl_scan(unm, sh, &utot) + urank_base;
-    int kind = KIND_MEMBER, slot = -1;
+    const int isc = (in && (s < 0 || leader)) ? 1 : 0;
+    int tot;
+    const int both = block_excl_scan(unm | (isc << 16), sh, &tot);
+    const int ur = (both & 0xffff) + urank_base, cp = (both >> 16) + cand_base;
     if (in) {
-      if (s >= 0) {
-        slot = s;
-        kind = (rj[s] == j) ? KIND_LEADER : KIND_MEMBER;
-      } else {
-        slot = ur < n_app ? size0 + ur : ev[ur - n_app];
-        kind = KIND_INSERT;
-      }
+      const int slot = s >= 0 ? s : (ur < n_app ? size0 + ur : ev[ur - n_app]);
+      const int kind = s < 0 ? KIND_INSERT : (leader ? KIND_LEADER : KIND_MEMBER);
       plan_slot[(size_t)h * n_f + j] = slot;
       plan_kind[(size_t)h * n_f + j] = kind;
+      plan_cnt[(size_t)h * n_f + j] = cnt;
+      if (isc) cand_next[(size_t)h * C + cp] = slot;
+      s_key[j] = slot;
     }
-    const int isc = (in && kind != KIND_MEMBER) ? 1 : 0;
-    int ctot;
-    const int cp = block_excl_scan(isc, sh, &ctot) + cand_base;
-    if (isc) cand_next[(size_t)h * C + cp] = slot;
-    urank_base += utot;
-    cand_base += ctot;
+    urank_base += tot & 0xffff;
+    cand_base += tot >> 16;
+  }
+  __syncthreads();
+  // 3. clean the group accumulators of every slot this frame refreshed
+  for (int j = threadIdx.x; j < n_f; j += blockDim.x) {
+    const int slot = s_key[j];
+    rj[slot] = 0x7fffffff;
+    gc[slot] = 0;
   }
   if (threadIdx.x == 0) {
     ncand_next[h] = cand_base;
     size[h] = size0 + n_app;
     inserted[h] += n_f;
   }
+  pdl_trigger();
 }
 
 // ---------------------------------------------------------------- apply
+// One warp per key; lane l handles the D/32 consecutive dimensions starting
+// at l * D/32 (one vector access per row).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
                                                     const uint32_t* __restrict__ codes_frame, int n_f,
@@ -380,9 +404,10 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
                                                     const int32_t* __restrict__ match,
                                                     const int32_t* __restrict__ plan_slot,
                                                     const int32_t* __restrict__ plan_kind,
-                                                    const int32_t* __restrict__ gcnt, T* K, T* V,
+                                                    const int32_t* __restrict__ plan_cnt, T* K, T* V,
                                                     int32_t* m, uint32_t* codes, int32_t* last_frame,
                                                     int C, int32_t* st) {
+  pdl_wait();
   constexpr int PER = D / 32;
   if (status_bad(st)) return;
   const int h = blockIdx.y;
@@ -392,45 +417,48 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
   const int kind = plan_kind[(size_t)h * n_f + j];
   if (kind == KIND_MEMBER) return;
   const int s = plan_slot[(size_t)h * n_f + j];
-  const size_t krow = ((size_t)h * row_stride_keys + j) * D;
-  const size_t crow = ((size_t)h * C + s) * D;
+  const size_t krow = ((size_t)h * row_stride_keys + j) * D + lane * PER;
+  const size_t crow = ((size_t)h * C + s) * D + lane * PER;
+  float kv[PER], vv[PER];
+  ld_vec<T, PER>(k_frame + krow, kv);
+  ld_vec<T, PER>(v_frame + krow, vv);
   int m_new = 1;
   if (kind == KIND_LEADER) {
-    const int cnt = gcnt[(size_t)h * C + s];
+    const int cnt = plan_cnt[(size_t)h * n_f + j];
     const int m_old = m[(size_t)h * C + s];
     m_new = m_old + cnt;
     float acc[PER];
+    ld_vec<T, PER>(V + crow, acc);
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
-      acc[i] = (float)m_old * Elem<T>::ld(V + crow + lane + 32 * i);
-    if (cnt == 1) {
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += Elem<T>::ld(v_frame + krow + lane + 32 * i);
-    } else {
+    for (int i = 0; i < PER; ++i) acc[i] = (float)m_old * acc[i] + vv[i];
+    if (cnt > 1) {
+      // the other members of the group, in ascending key order
       const int32_t* mt = match + (size_t)h * n_f;
-      for (int jj = j; jj < n_f; ++jj) {
+      int left = cnt - 1;
+      for (int jj = j + 1; jj < n_f && left > 0; ++jj) {
         if (mt[jj] != s) continue;
-        const size_t r = ((size_t)h * row_stride_keys + jj) * D;
+        float x[PER];
+        ld_vec<T, PER>(v_frame + ((size_t)h * row_stride_keys + jj) * D + lane * PER, x);
 #pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] += Elem<T>::ld(v_frame + r + lane + 32 * i);
+        for (int i = 0; i < PER; ++i) acc[i] += x[i];
+        --left;
       }
     }
     const float mf = (float)m_new;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) Elem<T>::st(V + crow + lane + 32 * i, acc[i] / mf);
+    for (int i = 0; i < PER; ++i) acc[i] = acc[i] / mf;
+    st_vec<T, PER>(V + crow, acc);
   } else {
-#pragma unroll
-    for (int i = 0; i < PER; ++i)
-      V[crow + lane + 32 * i] = v_frame[krow + lane + 32 * i];
+    st_vec<T, PER>(V + crow, vv);
   }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) K[crow + lane + 32 * i] = k_frame[krow + lane + 32 * i];
+  st_vec<T, PER>(K + crow, kv);
   if (lane == 0) {
     m[(size_t)h * C + s] = m_new;
     last_frame[(size_t)h * C + s] = f;
   }
   for (int t = lane; t < Tt; t += 32)
     codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
+  pdl_trigger();
 }
 
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
@@ -445,14 +473,21 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
                       int32_t* match_out, void* ws, int32_t* st, cudaStream_t s) {
   const int H = c->H, C = c->C, Tt = c->T;
   MergeWs w = carve(ws, H, n_f, C);
+  // the plan keeps one int per key of a frame in shared memory
+  const size_t plan_smem = (size_t)n_f * sizeof(int);
+  if (plan_smem > 48 * 1024 &&
+      cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return FASTAR_ERR_UNSUPPORTED;
+  }
   const int Nrow = F * n_f;
-  cand_init_kernel<<<H, kPlanThreads, 0, s>>>(c->last_frame, c->size, C, first_frame - 1,
-                                              w.cand[0], w.ncand[0], w.best, n_f, st);
+  fastar::launch_pdl((cand_init_kernel), H, kPlanThreads, 0, s, c->last_frame, c->size, C, first_frame - 1,
+                                              w.cand[0], w.ncand[0], w.best, w.rep_j, w.gcnt, n_f, st);
   FASTAR_LAUNCHED(s, "cand_init");
   const dim3 wgrid((n_f + 7) / 8, H), wblock(256);
   const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
   if (tc_nn) {
-    cand_norm_kernel<<<wgrid, wblock, 0, s>>>((const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
+    fastar::launch_pdl((cand_norm_kernel), wgrid, wblock, 0, s, (const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
                                               w.stage, n_f, st);
     FASTAR_LAUNCHED(s, "cand_norm");
   }
@@ -468,19 +503,19 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
                         w.plan_slot, w.plan_kind, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.best, w.stage,
                         st, s);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
-      nn_simt_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
+      fastar::launch_pdl((nn_simt_kernel<T, D>), wgrid, wblock, 0, s, kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], w.best, st);
       FASTAR_LAUNCHED(s, "nn_simt");
     } else if (rc != FASTAR_OK) {
       return rc;
     }
-    plan_kernel<<<H, kPlanThreads, 0, s>>>(n_f, C, f, tau, w.best, match_out, fi * n_f, Nrow, w.match,
-                                           w.cand[cur], w.ncand[cur], w.cand[nxt], w.ncand[nxt], w.rep_j,
-                                           w.gcnt, w.plan_slot, w.plan_kind, w.evict, c->last_frame, c->m,
-                                           c->size, c->inserted, c->evicted, st);
+    fastar::launch_pdl((plan_kernel), H, kPlanThreads, (size_t)n_f * sizeof(int), s, 
+        n_f, C, f, tau, w.best, match_out, fi * n_f, Nrow, w.match, w.cand[nxt], w.ncand[nxt], w.rep_j,
+        w.gcnt, w.plan_slot, w.plan_kind, w.plan_cnt, w.evict, c->last_frame, c->m, c->size, c->inserted,
+        c->evicted, st);
     FASTAR_LAUNCHED(s, "plan");
-    apply_kernel<T, D><<<wgrid, wblock, 0, s>>>(kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
-                                                w.plan_kind, w.gcnt, (T*)c->K, (T*)c->V, c->m,
+    fastar::launch_pdl((apply_kernel<T, D>), wgrid, wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
+                                                w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m,
                                                 c->codes, c->last_frame, C, st);
     FASTAR_LAUNCHED(s, "apply");
   }
