@@ -25,7 +25,8 @@
 //              a thread scales its key's dot products by the candidates'
 //              inverse norms (NaN for a candidate with a zero norm, which
 //              drops out of every comparison) and keeps the best
-//              (cosine, slot) among the candidates that are groups.
+//              (cosine, slot) among the candidates that are groups and
+//              reach the join threshold (no others can be matched).
 // At the end the two halves of a row are merged and the CTA's best of each
 // key is folded into a packed 64-bit word with atomicMax (larger cosine
 // first, then lower slot), so the result does not depend on CTA order.  The
@@ -94,6 +95,7 @@ struct NnArgs {
   const float* invn_prev;
   float* invn_out;                 // inverse norms of this frame's keys [H][n_f]
   unsigned long long* best_out;    // packed best candidate [H][n_f]
+  float tau;                       // join threshold on the cosine
 };
 
 __device__ __forceinline__ void cand_meta(const NnArgs& a, int h, int c, int& slot, float& inv) {
@@ -251,7 +253,13 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
     const int j = m0 + row;
     if (half == 0 && blockIdx.y == 0 && j < a.n_f && a.invn_out)
       a.invn_out[(size_t)h * a.n_f + j] = na2 > 0.f ? ia : __int_as_float(0x7fc00000);
-    float best = -INFINITY;
+    // Only candidates that can reach tau matter: a key whose best cosine is
+    // below tau joins no group, whatever the best candidate.  So the running
+    // best starts at the row's threshold, in the units of cs (cosine * |k_j|),
+    // lowered by 1e-5 so that rounding cannot drop a candidate the plan's
+    // exact test (cosine >= tau) would accept; the plan still decides.  The
+    // slot search below then only runs for tiles holding such a candidate.
+    float best = na2 > 0.f ? (a.tau - 1e-5f) * sqrtf(na2) : INFINITY;
     int best_slot = 0x7fffffff;
     for (int t = 0; t < ntiles && ok; ++t) {
       const int b = t % kAcc;
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
                  int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
                  const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
-                 float* invn_out, unsigned long long* best_out, const void* stage, int32_t* st,
+                 float* invn_out, unsigned long long* best_out, const void* stage, float tau, int32_t* st,
                  cudaStream_t s) {
   if (dt != FASTAR_BF16 || D != kD) return FASTAR_ERR_UNSUPPORTED;
   if (n_f == 0 || H == 0) return FASTAR_OK;
@@ -379,7 +387,7 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
   split = max(split, (btiles * kN + kMetaCap - 1) / kMetaCap);
   split = max(1, min(split, min(16, btiles)));
   NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, n_f, Nrow, fi, C, cand, ncand, cinv,
-           prev_slot, prev_kind, invn_prev, invn_out, best_out};
+           prev_slot, prev_kind, invn_prev, invn_out, best_out, tau};
   fastar::launch_pdl((nn_tc_kernel), dim3(atiles, split, H), kThreads, smem, s, mapA, mapB, mapS, a, st);
   FASTAR_LAUNCHED(s, "nn_tc");
   return FASTAR_OK;

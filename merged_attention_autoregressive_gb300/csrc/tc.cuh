@@ -15,7 +15,11 @@
 namespace fastar {
 namespace tc {
 
-constexpr uint32_t kWaitPolls = 1u << 20;  // bounded wait: each try_wait suspends up to its time limit
+// Bounded waits: each try_wait suspends the thread for up to kSuspendNs (it
+// resumes as soon as the phase completes), so a wait gives up after about
+// kWaitPolls * kSuspendNs = 2 s.
+constexpr uint32_t kSuspendNs = 2000;
+constexpr uint32_t kWaitPolls = 1u << 20;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -39,10 +43,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -58,9 +62,9 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete; false on timeout.
-// try_wait suspends the thread in hardware until the phase completes or a
-// short time limit passes, so waiting warps leave the issue slots to the
-// warps that compute; the loop bounds the total wait.
+// try_wait suspends the thread in hardware until the phase completes or the
+// suspend hint passes, so waiting warps leave the issue slots to the warps
+// that compute instead of spinning; the loop bounds the total wait.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;

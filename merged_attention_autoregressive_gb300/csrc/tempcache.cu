@@ -464,7 +464,7 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
                  int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
                  const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
-                 float* invn_out, unsigned long long* best_out, const void* stage, int32_t* st,
+                 float* invn_out, unsigned long long* best_out, const void* stage, float tau, int32_t* st,
                  cudaStream_t s);
 
 template <typename T, int D>
@@ -501,7 +501,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     if (tc_nn)
       rc = launch_nn_tc(FASTAR_BF16, k_new, n_f, Nrow, H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.cinv,
                         w.plan_slot, w.plan_kind, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.best, w.stage,
-                        st, s);
+                        tau, st, s);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       fastar::launch_pdl((nn_simt_kernel<T, D>), wgrid, wblock, 0, s, kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], w.best, st);
