@@ -7,10 +7,11 @@
 // slot) iff the cosine reaches tau.
 //
 // One CTA owns 128 new keys of one head and one slice of the candidates (the
-// candidates are split over gridDim.y CTAs so that about two CTAs run per
-// SM).  The new keys arrive by TMA (two 64-column boxes, 128-byte swizzle).
-// The slots and inverse norms of the CTA's candidates are staged in shared
-// memory once.  The CTA is warp-specialised:
+// candidates are split over gridDim.y CTAs; the split minimises the launch's
+// rounds of SM slots times the CTA cost).  The new keys arrive by TMA (two
+// 64-column boxes, 128-byte swizzle).  The slots and inverse norms of the
+// CTA's candidates are staged in shared memory once, by the epilogue warps
+// while the first tiles load.  The CTA is warp-specialised:
 //   warp 0     producer: fills a 4-stage ring of 64-row candidate tiles by
 //              TMA.  After the first frame of a call the candidates are the
 //              rows of the previous frame, contiguous in k_new; for the first
@@ -77,6 +78,9 @@ __device__ __forceinline__ float row_sq_norm(const uint8_t* tile, int r, int row
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 struct NnArgs {
@@ -148,17 +152,27 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
     tc::tmem_alloc(&sm.tmem, kAcc * kN);
     tc::tmem_relinquish();
   }
-  // stage the candidates' slots and inverse norms (all threads, one pass)
-  for (int c = cbase + tid; c < cbase + ntiles * kN && c - cbase < kMetaCap; c += kThreads) {
-    int sl = -1;
-    float inv = __int_as_float(0x7fc00000);
-    if (c < cend) cand_meta(a, h, c, sl, inv);
-    sm.mslot[c - cbase] = sl;
-    sm.minv[c - cbase] = sl >= 0 ? inv : __int_as_float(0x7fc00000);
-  }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // The epilogue warps stage the candidates' slots and inverse norms while
+  // the producer and the MMA issuer already start on the first tiles; named
+  // barrier 2 (epilogue + producer) publishes them.  The producer needs the
+  // slots only when it gathers scattered cache rows, otherwise it just
+  // arrives.
+  if (warp >= 2) {
+    for (int c = cbase + tid - 64; c < cbase + ntiles * kN && c - cbase < kMetaCap; c += kThreads - 64) {
+      int sl = -1;
+      float inv = __int_as_float(0x7fc00000);
+      if (c < cend) cand_meta(a, h, c, sl, inv);
+      sm.mslot[c - cbase] = sl;
+      sm.minv[c - cbase] = sl >= 0 ? inv : __int_as_float(0x7fc00000);
+    }
+    named_bar_sync(2, kThreads - 32);
+  } else if (warp == 0) {
+    if (a.fi > 0 || nc <= a.n_f) named_bar_arrive(2, kThreads - 32);
+    else named_bar_sync(2, kThreads - 32);
+  }
   const uint32_t tmem = sm.tmem;
   bool ok = true;
 
@@ -273,15 +287,16 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
         float v[32];
         tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + b * kN + col0, v);
         const int m_off = c0 + col0 - cbase;  // index of column col0 in the staged metadata
-        float cs[32];
+        // cs = dot * inverse candidate norm, in place (NaN: not a group)
+        float* cs = v;
         if (m_off + 32 <= kMetaCap) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 ib = *reinterpret_cast<const float4*>(&sm.minv[m_off + i]);
-            cs[i] = v[i] * ib.x;
-            cs[i + 1] = v[i + 1] * ib.y;
-            cs[i + 2] = v[i + 2] * ib.z;
-            cs[i + 3] = v[i + 3] * ib.w;
+            cs[i] *= ib.x;
+            cs[i + 1] *= ib.y;
+            cs[i + 2] *= ib.z;
+            cs[i + 3] *= ib.w;
           }
         } else {
 #pragma unroll
@@ -289,23 +304,22 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
             int sl = -1;
             float ib = __int_as_float(0x7fc00000);
             if (col0 + i < nval) cand_meta(a, h, c0 + col0 + i, sl, ib);
-            cs[i] = sl >= 0 ? v[i] * ib : __int_as_float(0x7fc00000);
+            cs[i] = sl >= 0 ? cs[i] * ib : __int_as_float(0x7fc00000);
           }
         }
-        // phase 1: the tile's largest cosine (NaN columns are ignored)
-        float tmax = -INFINITY;
+        // phase 1: the tile's largest cosine (NaN columns are ignored); four
+        // independent chains keep the dependency depth short
+        float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tmax = fmaxf(tmax, cs[i]);
-        // phase 2 (only when it can change the answer): the slot attaining it;
-        // several equal columns in one tile take the lowest slot
+        for (int i = 0; i < 32; ++i) t4[i & 3] = fmaxf(t4[i & 3], cs[i]);
+        const float tmax = fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3]));
+        // phase 2 (only when it can change the answer): the columns attaining
+        // it as a bit mask; several equal columns take the lowest slot
         if (tmax >= best) {
-          int first = 0, neq = 0;
+          uint32_t e4[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-          for (int i = 31; i >= 0; --i) {
-            const bool e = cs[i] == tmax;
-            first = e ? i : first;
-            neq += e ? 1 : 0;
-          }
+          for (int i = 0; i < 32; ++i) e4[i & 3] |= (cs[i] == tmax ? 1u : 0u) << i;
+          uint32_t eq = (e4[0] | e4[1]) | (e4[2] | e4[3]);
           auto slot_at = [&](int i) -> int {
             if (m_off + i < kMetaCap) return sm.mslot[m_off + i];
             int sl;
@@ -314,13 +328,12 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
             return sl;
           };
           int smin = 0x7fffffff;
-          if (neq == 1) {
-            smin = slot_at(first);
-          } else if (neq > 1) {
-            for (int i = 0; i < 32; ++i)
-              if (cs[i] == tmax) smin = min(smin, slot_at(i));
+          const bool any = eq != 0u;
+          while (eq) {
+            smin = min(smin, slot_at(__ffs(eq) - 1));
+            eq &= eq - 1u;
           }
-          if (neq > 0 && (tmax > best || smin < best_slot)) {
+          if (any && (tmax > best || smin < best_slot)) {
             best = tmax;
             best_slot = smin;
           }
@@ -378,14 +391,28 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   (void)cudaGetLastError();
-  // split the candidates so that about two CTAs run per SM and each CTA's
-  // candidate metadata fits its staging area (the expected candidate count
-  // is n_f: the groups the previous frame refreshed)
+  // split the candidates over gridDim.y CTAs (the expected candidate count is
+  // n_f: the groups the previous frame refreshed)
   const int atiles = (n_f + kM - 1) / kM;
   const int btiles = (n_f + kN - 1) / kN;
-  int split = (2 * sms + atiles * H - 1) / (atiles * H);
-  split = max(split, (btiles * kN + kMetaCap - 1) / kMetaCap);
-  split = max(1, min(split, min(16, btiles)));
+  // Two CTAs fit an SM.  A CTA costs a fixed start (A tile, metadata,
+  // TMEM; about kStartTiles tile times) plus its tiles, and the launch takes
+  // as many rounds as the CTAs need SM slots: pick the split with the least
+  // rounds x CTA cost among those whose metadata fits the staging area.
+  constexpr int kStartTiles = 6;
+  const int min_split = max(1, (btiles * kN + kMetaCap - 1) / kMetaCap);
+  const long long slots = 2LL * sms;
+  int split = min_split;
+  long long best_cost = -1;
+  for (int sp = min_split; sp <= min(16, btiles); ++sp) {
+    const long long rounds = ((long long)atiles * H * sp + slots - 1) / slots;
+    const long long cost = rounds * (kStartTiles + (btiles + sp - 1) / sp);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      split = sp;
+    }
+  }
+  split = max(1, min(split, btiles));
   NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, n_f, Nrow, fi, C, cand, ncand, cinv,
            prev_slot, prev_kind, invn_prev, invn_out, best_out, tau};
   fastar::launch_pdl((nn_tc_kernel), dim3(atiles, split, H), kThreads, smem, s, mapA, mapB, mapS, a, st);
