@@ -201,16 +201,16 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
  * library's device memory, held by every GPU that loads the library until
  * the process exits.  Returns FASTAR_ERR_WORKSPACE when the merge needs more
  * (fastar_workspace_size(FASTAR_OP_MERGE, ...) > FASTAR_NOALLOC_SCRATCH_BYTES;
- * e.g. 12 heads x C 32768 x n_f 1560 needs about 12.6 MiB and fits, 40 heads
- * x n_f 3600 needs about 65 MiB and is refused).  All calls
+ * e.g. 12 heads x C 32768 x n_f 1560 needs about 9.7 MiB and fits, 40 heads
+ * x n_f 3600 needs about 55 MiB and is refused).  All calls
  * share the array, so calls that overlap on the GPU race and must be ordered
  * by the caller; it keeps the last call's contents (the merge needs none of
  * it zeroed).  The first call on a device looks up the array's address with
  * that device current; make it before any stream capture.
  */
 /* Largest frame (keys per frame) the merge accepts: the per-frame plan keeps
- * one 32-bit word per key in shared memory. */
-#define FASTAR_MAX_FRAME_KEYS 49152
+ * each key's match and a hash table of the frame's groups in shared memory. */
+#define FASTAR_MAX_FRAME_KEYS 6144
 
 #define FASTAR_NOALLOC_SCRATCH_BYTES (16u << 20)
 int fastar_tempcache_merge_noalloc(const fastar_cache* cache, const void* k_new,

@@ -617,9 +617,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   pdl_trigger();
 }
 
-// Merge the T per-table partials of each query: one warp per query, four
-// dimensions per lane; every table's (max, sum) and partial row are loaded
-// before any is used.
+// Merge the T per-table partials of each query: a warp handles kCombineQ
+// queries, four dimensions per lane; every (max, sum) and partial row of its
+// queries is loaded before any is used.
+constexpr int kCombineQ = 4;
 __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restrict__ ws_o,
                                                             const float2* __restrict__ ws_ml, int T, int H,
                                                             int Nq, __nv_bfloat16* __restrict__ out,
@@ -627,43 +628,50 @@ __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restr
   pdl_wait();
   if (status_bad(st)) return;
   const int h = blockIdx.y;
-  const int i = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int i0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * kCombineQ;
   const int lane = threadIdx.x & 31;
-  if (i >= Nq) return;
-  float2 ml[kMaxT];
-  float4 o[kMaxT];
+  float2 ml[kCombineQ][kMaxT];
+  float4 o[kCombineQ][kMaxT];
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) {
-    ml[t] = make_float2(-INFINITY, 0.f);
-    o[t] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t < T) {
-      const size_t r = ((size_t)t * H + h) * Nq + i;
-      ml[t] = __ldcs(ws_ml + r);
-      o[t] = __ldcs(reinterpret_cast<const float4*>(ws_o + r * kD) + lane);
+  for (int k = 0; k < kCombineQ; ++k) {
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+      ml[k][t] = make_float2(-INFINITY, 0.f);
+      o[k][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < T && i0 + k < Nq) {
+        const size_t r = ((size_t)t * H + h) * Nq + i0 + k;
+        ml[k][t] = __ldcs(ws_ml + r);
+        o[k][t] = __ldcs(reinterpret_cast<const float4*>(ws_o + r * kD) + lane);
+      }
     }
   }
-  float M = -INFINITY;
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) M = fmaxf(M, ml[t].x);
-  float L = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < kCombineQ; ++k) {
+    const int i = i0 + k;
+    if (i >= Nq) break;
+    float M = -INFINITY;
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) {
-    const float w = ml[t].x == -INFINITY ? 0.f : exp2f(ml[t].x - M);
-    L = fmaf(ml[t].y, w, L);
-    acc.x = fmaf(o[t].x, w, acc.x);
-    acc.y = fmaf(o[t].y, w, acc.y);
-    acc.z = fmaf(o[t].z, w, acc.z);
-    acc.w = fmaf(o[t].w, w, acc.w);
+    for (int t = 0; t < kMaxT; ++t) M = fmaxf(M, ml[k][t].x);
+    float L = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+      const float w = ml[k][t].x == -INFINITY ? 0.f : exp2f(ml[k][t].x - M);
+      L = fmaf(ml[k][t].y, w, L);
+      acc.x = fmaf(o[k][t].x, w, acc.x);
+      acc.y = fmaf(o[k][t].y, w, acc.y);
+      acc.z = fmaf(o[k][t].z, w, acc.z);
+      acc.w = fmaf(o[k][t].w, w, acc.w);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t*>(&b0);
+    u.y = *reinterpret_cast<const uint32_t*>(&b1);
+    *reinterpret_cast<uint2*>(out + ((size_t)h * Nq + i) * kD + lane * 4) = u;
+    if (lse && lane == 0) lse[(size_t)h * Nq + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-  const __nv_bfloat162 b1 = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  uint2 u;
-  u.x = *reinterpret_cast<const uint32_t*>(&b0);
-  u.y = *reinterpret_cast<const uint32_t*>(&b1);
-  *reinterpret_cast<uint2*>(out + ((size_t)h * Nq + i) * kD + lane * 4) = u;
-  if (lse && lane == 0) lse[(size_t)h * Nq + i] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
   pdl_trigger();
 }
 
@@ -722,7 +730,7 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   // every table in one launch: the tables' CTAs fill each other's waves
   const int rc = launch_attn<true>(dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa, st, s);
   if (rc != FASTAR_OK || c->T == 1) return rc;
-  fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 7) / 8, c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
+  fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");
   return FASTAR_OK;

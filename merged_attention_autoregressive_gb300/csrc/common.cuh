@@ -29,28 +29,40 @@ template <> struct Elem<__nv_bfloat16> {
   }
 };
 
-// N consecutive elements of a row as floats (one vector access; the address
-// is aligned to N * sizeof(T), which must be 4, 8 or 16 bytes).
+// N consecutive elements of a row moved as one vector (the address is
+// aligned to N * sizeof(T), which must be 4, 8 or 16 bytes): raw loads and
+// stores, and conversion to / from floats.
 template <typename T, int N>
-__device__ __forceinline__ void ld_vec(const T* p, float* out) {
-  constexpr int B = N * (int)sizeof(T);
+struct VecOf {
+  static constexpr int B = N * (int)sizeof(T);
   static_assert(B == 4 || B == 8 || B == 16, "vector width");
-  using V = typename std::conditional<B == 4, uint32_t, typename std::conditional<B == 8, uint2, uint4>::type>::type;
-  const V v = *reinterpret_cast<const V*>(p);
+  using type = typename std::conditional<B == 4, uint32_t, typename std::conditional<B == 8, uint2, uint4>::type>::type;
+};
+template <typename T, int N>
+__device__ __forceinline__ typename VecOf<T, N>::type ld_raw(const T* p) {
+  return *reinterpret_cast<const typename VecOf<T, N>::type*>(p);
+}
+template <typename T, int N>
+__device__ __forceinline__ void st_raw(T* p, const typename VecOf<T, N>::type& v) {
+  *reinterpret_cast<typename VecOf<T, N>::type*>(p) = v;
+}
+template <typename T, int N>
+__device__ __forceinline__ void raw_to_float(const typename VecOf<T, N>::type& v, float* out) {
   const T* e = reinterpret_cast<const T*>(&v);
 #pragma unroll
   for (int i = 0; i < N; ++i) out[i] = Elem<T>::ld(e + i);
 }
 template <typename T, int N>
+__device__ __forceinline__ void ld_vec(const T* p, float* out) {
+  raw_to_float<T, N>(ld_raw<T, N>(p), out);
+}
+template <typename T, int N>
 __device__ __forceinline__ void st_vec(T* p, const float* in) {
-  constexpr int B = N * (int)sizeof(T);
-  static_assert(B == 4 || B == 8 || B == 16, "vector width");
-  using V = typename std::conditional<B == 4, uint32_t, typename std::conditional<B == 8, uint2, uint4>::type>::type;
-  V v;
+  typename VecOf<T, N>::type v;
   T* e = reinterpret_cast<T*>(&v);
 #pragma unroll
   for (int i = 0; i < N; ++i) Elem<T>::st(e + i, in[i]);
-  *reinterpret_cast<V*>(p) = v;
+  st_raw<T, N>(p, v);
 }
 
 // ---- sticky device status: first error wins, kernels exit once it is set

@@ -5,8 +5,8 @@
 // steps, TempCache.  For each frame f of the chunk, in order:
 //   nn     each new key is matched to the group refreshed in frame f-1 of
 //          largest cosine (ties: lowest slot); it joins iff cosine >= tau;
-//   plan   one CTA per head groups the matches (lowest index = new
-//          representative), ranks the unmatched keys and assigns them free
+//   plan   one CTA per head groups the matches in shared memory (lowest
+//          index = new representative), ranks the unmatched keys and assigns them free
 //          slots, then evicted slots (smallest (last_frame, slot) among the
 //          groups not refreshed in frame f); updates size / inserted /
 //          evicted and writes the next frame's candidate list;
@@ -17,7 +17,7 @@
 // of a call compacts the slots with last_frame == first_frame - 1.
 //
 // Workspace (caller-owned, no initialisation needed):
-//   cand[2][H][C], ncand[2][H], rep_j[H][C], gcnt[H][C],
+//   cand[2][H][C], ncand[2][H],
 //   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], plan_cnt[H][n_f],
 //   evict[H][n_f],
 //   best[H][n_f] (packed best candidate per key, see pack_best),
@@ -25,10 +25,8 @@
 //   stage[H][n_f][128] bf16 (copies of the first n_f first-frame candidate
 //   rows, contiguous, so that the NN kernel can load them by TMA),
 //   invn[2][H][n_f] (inverse norms of the keys of the last two frames)
-// rep_j/gcnt are indexed by slot; they are clean for every candidate slot
-// when a plan starts (only candidates can be matched): cand_init cleans the
-// first frame's candidates and each plan the slots it refreshed.  best is
-// zeroed when a call starts and again by each plan after it has read it.
+// best is zeroed when a call starts and again by each plan after it has
+// read it.
 #include <math.h>
 
 #include <type_traits>
@@ -43,8 +41,6 @@ enum : int { KIND_MEMBER = 0, KIND_LEADER = 1, KIND_INSERT = 2 };
 struct MergeWs {
   int32_t* cand[2];
   int32_t* ncand[2];
-  int32_t* rep_j;
-  int32_t* gcnt;
   int32_t* match;
   int32_t* plan_slot;
   int32_t* plan_kind;
@@ -62,7 +58,6 @@ size_t merge_ws_bytes(int H, int n_f, int C) {
   size_t b = 0;
   b += 2 * align256((size_t)H * C * 4);   // cand
   b += 2 * align256((size_t)H * 4);       // ncand
-  b += 2 * align256((size_t)H * C * 4);   // rep_j, gcnt
   b += 5 * align256((size_t)H * n_f * 4); // match, plan_slot, plan_kind, plan_cnt, evict
   b += align256((size_t)H * n_f * 8);     // best
   b += align256((size_t)H * C * 4);       // cinv
@@ -79,8 +74,6 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
   w.cand[1] = take((size_t)H * C * 4);
   w.ncand[0] = take((size_t)H * 4);
   w.ncand[1] = take((size_t)H * 4);
-  w.rep_j = take((size_t)H * C * 4);
-  w.gcnt = take((size_t)H * C * 4);
   w.match = take((size_t)H * n_f * 4);
   w.plan_slot = take((size_t)H * n_f * 4);
   w.plan_kind = take((size_t)H * n_f * 4);
@@ -96,13 +89,12 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
 
 // ---------------------------------------------------------------- cand init
 // The slots refreshed in frame prev_frame, in slot order (thread t owns a
-// contiguous run of slots, so one load round and one block scan suffice);
-// their group accumulators are cleaned for the first plan.
+// contiguous run of slots, so one load round and one block scan suffice).
 __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* __restrict__ last_frame,
                                                                  const int32_t* __restrict__ size, int C,
                                                                  int32_t prev_frame, int32_t* cand,
                                                                  int32_t* ncand, unsigned long long* best,
-                                                                 int32_t* rep_j, int32_t* gcnt, int n_f,
+                                                                 int n_f,
                                                                  int32_t* st) {
   pdl_wait();
   constexpr int kPer = 16;  // slots per thread and round
@@ -126,8 +118,6 @@ __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* 
       const int i = __ffs(hits) - 1;
       hits &= hits - 1;
       out[pos++] = s0 + i;
-      rep_j[(size_t)h * C + s0 + i] = 0x7fffffff;  // the first plan's group accumulators
-      gcnt[(size_t)h * C + s0 + i] = 0;
     }
     base += tot;
   }
@@ -135,9 +125,11 @@ __global__ void __launch_bounds__(kPlanThreads) cand_init_kernel(const int32_t* 
   pdl_trigger();
 }
 
-// Inverse norms of the first frame's candidates (bf16 rows of 128), one warp
-// per candidate, grid-stride over the device-side candidate count; the first
-// n_f candidate rows are also copied, in candidate order, into `stage`.
+// Inverse norms of the first frame's candidates (bf16 rows of 128): a warp
+// handles kNormCands consecutive candidates (all rows loaded first), over a
+// grid-stride range of the device-side candidate count; the first n_f
+// candidate rows are also copied, in candidate order, into `stage`.
+constexpr int kNormCands = 4;
 __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __restrict__ K, int C,
                                                         const int32_t* __restrict__ cand,
                                                         const int32_t* __restrict__ ncand, float* cinv,
@@ -146,14 +138,25 @@ __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __r
   if (status_bad(st)) return;
   const int h = blockIdx.y, lane = threadIdx.x & 31;
   const int nc = min(max(ncand[h], 0), C);
-  for (int c = blockIdx.x * 8 + (threadIdx.x >> 5); c < nc; c += gridDim.x * 8) {
-    const int s = cand[(size_t)h * C + c];
-    const uint2 u = *reinterpret_cast<const uint2*>(K + ((size_t)h * C + s) * 128 + lane * 4);
-    if (c < n_f) *reinterpret_cast<uint2*>(stage + ((size_t)h * n_f + c) * 128 + lane * 4) = u;
-    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-    const float n2 = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
-    if (lane == 0) cinv[(size_t)h * C + c] = n2 > 0.f ? 1.f / sqrtf(n2) : __int_as_float(0x7fc00000);
+  const int step = gridDim.x * 8 * kNormCands;
+  for (int c0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * kNormCands; c0 < nc; c0 += step) {
+    int sl[kNormCands];
+#pragma unroll
+    for (int u = 0; u < kNormCands; ++u) sl[u] = c0 + u < nc ? cand[(size_t)h * C + c0 + u] : -1;
+    uint2 row[kNormCands];
+#pragma unroll
+    for (int u = 0; u < kNormCands; ++u)
+      if (sl[u] >= 0) row[u] = *reinterpret_cast<const uint2*>(K + ((size_t)h * C + sl[u]) * 128 + lane * 4);
+#pragma unroll
+    for (int u = 0; u < kNormCands; ++u) {
+      if (sl[u] < 0) continue;
+      const int c = c0 + u;
+      if (c < n_f) *reinterpret_cast<uint2*>(stage + ((size_t)h * n_f + c) * 128 + lane * 4) = row[u];
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&row[u].x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&row[u].y));
+      const float n2 = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
+      if (lane == 0) cinv[(size_t)h * C + c] = n2 > 0.f ? 1.f / sqrtf(n2) : __int_as_float(0x7fc00000);
+    }
   }
   pdl_trigger();
 }
@@ -213,17 +216,43 @@ __global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_fr
 }
 
 // ---------------------------------------------------------------- plan
-// rep_j / gcnt are clean (INT_MAX / 0) for the candidate slots when a plan
-// starts: cand_init cleans the first frame's candidates, and every plan
-// cleans the slots its frame refreshed, which are the next frame's
-// candidates.  The matches of the frame stay in shared memory.
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int32_t f, float tau,
+// The frame's matches and groups live in shared memory: s_key[n_f] holds
+// each key's matched slot (later its planned slot), and an open-addressing
+// hash table of 2^lg_tab entries (at least 4/3 of n_f, so it never fills)
+// maps each matched slot to its group: lowest key index and count.
+__device__ __forceinline__ int plan_hash(int slot, int lg_tab) {
+  return (int)(((uint32_t)slot * 2654435761u) >> (32 - lg_tab));
+}
+// Entry of `slot`, inserting it when absent.
+__device__ __forceinline__ int plan_insert(int* tab_slot, int slot, int lg_tab) {
+  const int mask = (1 << lg_tab) - 1;
+  int e = plan_hash(slot, lg_tab);
+  for (int i = 0; i <= mask; ++i) {
+    const int prev = atomicCAS(&tab_slot[e], -1, slot);
+    if (prev == -1 || prev == slot) return e;
+    e = (e + 1) & mask;
+  }
+  return -1;  // cannot happen: the table has more entries than keys
+}
+// Entry of `slot`, or -1 when no key of the frame matched it.
+__device__ __forceinline__ int plan_find(const int* tab_slot, int slot, int lg_tab) {
+  const int mask = (1 << lg_tab) - 1;
+  int e = plan_hash(slot, lg_tab);
+  for (int i = 0; i <= mask; ++i) {
+    const int v = tab_slot[e];
+    if (v == slot) return e;
+    if (v == -1) return -1;
+    e = (e + 1) & mask;
+  }
+  return -1;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int32_t f, float tau, int lg_tab,
                                                             unsigned long long* __restrict__ best,
                                                             int32_t* __restrict__ match_out, int match_off,
                                                             int match_stride, int32_t* __restrict__ match,
                                                             int32_t* __restrict__ cand_next,
                                                             int32_t* __restrict__ ncand_next,
-                                                            int32_t* rep_j, int32_t* gcnt,
                                                             int32_t* __restrict__ plan_slot,
                                                             int32_t* __restrict__ plan_kind,
                                                             int32_t* __restrict__ plan_cnt,
@@ -233,16 +262,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
                                                             int32_t* size, int64_t* inserted,
                                                             int64_t* evicted, int32_t* st) {
   pdl_wait();
-  extern __shared__ int s_key[];  // [n_f]: matched slot (or -1), later the planned slot
+  extern __shared__ int plan_smem[];
+  const int ntab = 1 << lg_tab;
+  int* s_key = plan_smem;              // [n_f]
+  int* tab_slot = s_key + n_f;         // [ntab], -1 = empty
+  int* tab_min = tab_slot + ntab;      // [ntab] lowest key index of the group
+  int* tab_cnt = tab_min + ntab;       // [ntab] keys in the group
   __shared__ int sh[33];
   __shared__ long long shl[33];
   __shared__ int hist[2048];
   __shared__ int s_lstar, s_nlt, s_found;
   if (block_status_bad(st)) return;
   const int h = blockIdx.x;
-  int32_t* rj = rep_j + (size_t)h * C;
-  int32_t* gc = gcnt + (size_t)h * C;
   const int32_t* lf = last_frame + (size_t)h * C;
+  for (int e = threadIdx.x; e < ntab; e += blockDim.x) {
+    tab_slot[e] = -1;
+    tab_min[e] = 0x7fffffff;
+    tab_cnt[e] = 0;
+  }
+  __syncthreads();
   // 0. the NN decision of every key (best candidate if its cosine reaches
   //    tau), and the groups: count and lowest key index per matched slot
   int unm_local = 0;
@@ -255,8 +293,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
     if (match_out) match_out[(size_t)h * match_stride + match_off + j] = mj;
     *bp = 0ull;
     if (mj >= 0) {
-      atomicMin(&rj[mj], j);
-      atomicAdd(&gc[mj], 1);
+      const int e = plan_insert(tab_slot, mj, lg_tab);
+      atomicMin(&tab_min[e], j);
+      atomicAdd(&tab_cnt[e], 1);
     } else {
       ++unm_local;
     }
@@ -274,7 +313,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
     auto eligible = [&](int s) -> bool {
       const int l = lf[s];
       if (l >= f) return false;
-      if (l == f - 1 && gc[s] > 0) return false;
+      if (l == f - 1 && plan_find(tab_slot, s, lg_tab) >= 0) return false;
       return true;
     };
     int lo = 0x7fffffff;
@@ -359,8 +398,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
     bool leader = false;
     int cnt = 0;
     if (in && s >= 0) {
-      leader = rj[s] == j;
-      if (leader) cnt = gc[s];
+      const int e = plan_find(tab_slot, s, lg_tab);
+      leader = tab_min[e] == j;
+      if (leader) cnt = tab_cnt[e];
     }
     const int unm = (in && s < 0) ? 1 : 0;
     const int isc = (in && (s < 0 || leader)) ? 1 : 0;
@@ -374,17 +414,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
       plan_kind[(size_t)h * n_f + j] = kind;
       plan_cnt[(size_t)h * n_f + j] = cnt;
       if (isc) cand_next[(size_t)h * C + cp] = slot;
-      s_key[j] = slot;
     }
     urank_base += tot & 0xffff;
     cand_base += tot >> 16;
-  }
-  __syncthreads();
-  // 3. clean the group accumulators of every slot this frame refreshed
-  for (int j = threadIdx.x; j < n_f; j += blockDim.x) {
-    const int slot = s_key[j];
-    rj[slot] = 0x7fffffff;
-    gc[slot] = 0;
   }
   if (threadIdx.x == 0) {
     ncand_next[h] = cand_base;
@@ -395,10 +427,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
 }
 
 // ---------------------------------------------------------------- apply
-// One warp per key; lane l handles the D/32 consecutive dimensions starting
-// at l * D/32 (one vector access per row).
+// One warp per kApplyKeys consecutive keys (their plan records, then all of
+// their rows, are loaded before any is used); lane l handles the D/32
+// consecutive dimensions starting at l * D/32 (one vector access per row).
+constexpr int kApplyKeys = 4;
 template <typename T, int D>
-__global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
+__global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
                                                     const uint32_t* __restrict__ codes_frame, int n_f,
                                                     int row_stride_keys, int Tt, int32_t f,
                                                     const int32_t* __restrict__ match,
@@ -411,53 +445,75 @@ __global__ void __launch_bounds__(256) apply_kernel(const T* __restrict__ k_fram
   constexpr int PER = D / 32;
   if (status_bad(st)) return;
   const int h = blockIdx.y;
-  const int j = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int j0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kApplyKeys;
   const int lane = threadIdx.x & 31;
-  if (j >= n_f) return;
-  const int kind = plan_kind[(size_t)h * n_f + j];
-  if (kind == KIND_MEMBER) return;
-  const int s = plan_slot[(size_t)h * n_f + j];
-  const size_t krow = ((size_t)h * row_stride_keys + j) * D + lane * PER;
-  const size_t crow = ((size_t)h * C + s) * D + lane * PER;
-  float kv[PER], vv[PER];
-  ld_vec<T, PER>(k_frame + krow, kv);
-  ld_vec<T, PER>(v_frame + krow, vv);
-  int m_new = 1;
-  if (kind == KIND_LEADER) {
-    const int cnt = plan_cnt[(size_t)h * n_f + j];
-    const int m_old = m[(size_t)h * C + s];
-    m_new = m_old + cnt;
-    float acc[PER];
-    ld_vec<T, PER>(V + crow, acc);
+  int kind[kApplyKeys], slot[kApplyKeys], cnt[kApplyKeys], m_old[kApplyKeys];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = (float)m_old * acc[i] + vv[i];
-    if (cnt > 1) {
-      // the other members of the group, in ascending key order
-      const int32_t* mt = match + (size_t)h * n_f;
-      int left = cnt - 1;
-      for (int jj = j + 1; jj < n_f && left > 0; ++jj) {
-        if (mt[jj] != s) continue;
-        float x[PER];
-        ld_vec<T, PER>(v_frame + ((size_t)h * row_stride_keys + jj) * D + lane * PER, x);
-#pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] += x[i];
-        --left;
-      }
+  for (int u = 0; u < kApplyKeys; ++u) {
+    const int j = j0 + u;
+    kind[u] = KIND_MEMBER;
+    slot[u] = 0;
+    cnt[u] = 0;
+    if (j < n_f) {
+      kind[u] = plan_kind[(size_t)h * n_f + j];
+      slot[u] = plan_slot[(size_t)h * n_f + j];
+      cnt[u] = plan_cnt[(size_t)h * n_f + j];
     }
-    const float mf = (float)m_new;
+  }
+  using Raw = typename VecOf<T, PER>::type;
+  Raw kv[kApplyKeys], vv[kApplyKeys], vo[kApplyKeys];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = acc[i] / mf;
-    st_vec<T, PER>(V + crow, acc);
-  } else {
-    st_vec<T, PER>(V + crow, vv);
+  for (int u = 0; u < kApplyKeys; ++u) {
+    m_old[u] = 0;
+    if (kind[u] == KIND_MEMBER) continue;
+    const size_t krow = ((size_t)h * row_stride_keys + j0 + u) * D + lane * PER;
+    kv[u] = ld_raw<T, PER>(k_frame + krow);
+    vv[u] = ld_raw<T, PER>(v_frame + krow);
+    if (kind[u] == KIND_LEADER) {
+      m_old[u] = m[(size_t)h * C + slot[u]];
+      vo[u] = ld_raw<T, PER>(V + ((size_t)h * C + slot[u]) * D + lane * PER);
+    }
   }
-  st_vec<T, PER>(K + crow, kv);
-  if (lane == 0) {
-    m[(size_t)h * C + s] = m_new;
-    last_frame[(size_t)h * C + s] = f;
+#pragma unroll
+  for (int u = 0; u < kApplyKeys; ++u) {
+    if (kind[u] == KIND_MEMBER) continue;
+    const int j = j0 + u, s = slot[u];
+    const size_t crow = ((size_t)h * C + s) * D + lane * PER;
+    int m_new = 1;
+    if (kind[u] == KIND_LEADER) {
+      m_new = m_old[u] + cnt[u];
+      float acc[PER], x[PER];
+      raw_to_float<T, PER>(vo[u], acc);
+      raw_to_float<T, PER>(vv[u], x);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = (float)m_old[u] * acc[i] + x[i];
+      if (cnt[u] > 1) {
+        // the other members of the group, in ascending key order
+        const int32_t* mt = match + (size_t)h * n_f;
+        int left = cnt[u] - 1;
+        for (int jj = j + 1; jj < n_f && left > 0; ++jj) {
+          if (mt[jj] != s) continue;
+          ld_vec<T, PER>(v_frame + ((size_t)h * row_stride_keys + jj) * D + lane * PER, x);
+#pragma unroll
+          for (int i = 0; i < PER; ++i) acc[i] += x[i];
+          --left;
+        }
+      }
+      const float mf = (float)m_new;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = acc[i] / mf;
+      st_vec<T, PER>(V + crow, acc);
+    } else {
+      st_raw<T, PER>(V + crow, vv[u]);
+    }
+    st_raw<T, PER>(K + crow, kv[u]);
+    if (lane == 0) {
+      m[(size_t)h * C + s] = m_new;
+      last_frame[(size_t)h * C + s] = f;
+    }
+    for (int t = lane; t < Tt; t += 32)
+      codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
   }
-  for (int t = lane; t < Tt; t += 32)
-    codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
   pdl_trigger();
 }
 
@@ -473,8 +529,12 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
                       int32_t* match_out, void* ws, int32_t* st, cudaStream_t s) {
   const int H = c->H, C = c->C, Tt = c->T;
   MergeWs w = carve(ws, H, n_f, C);
-  // the plan keeps one int per key of a frame in shared memory
-  const size_t plan_smem = (size_t)n_f * sizeof(int);
+  // the plan keeps one int per key of a frame and a hash table of the
+  // frame's groups (3 ints per entry, at least 4/3 n_f entries) in shared
+  // memory
+  int lg_tab = 6;
+  while ((1 << lg_tab) * 3 < n_f * 4) ++lg_tab;
+  const size_t plan_smem = (size_t)n_f * sizeof(int) + 3 * ((size_t)sizeof(int) << lg_tab);
   if (plan_smem > 48 * 1024 &&
       cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan_smem) != cudaSuccess) {
     (void)cudaGetLastError();
@@ -482,12 +542,12 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
   }
   const int Nrow = F * n_f;
   fastar::launch_pdl((cand_init_kernel), H, kPlanThreads, 0, s, c->last_frame, c->size, C, first_frame - 1,
-                                              w.cand[0], w.ncand[0], w.best, w.rep_j, w.gcnt, n_f, st);
+                                              w.cand[0], w.ncand[0], w.best, n_f, st);
   FASTAR_LAUNCHED(s, "cand_init");
   const dim3 wgrid((n_f + 7) / 8, H), wblock(256);
   const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
   if (tc_nn) {
-    fastar::launch_pdl((cand_norm_kernel), wgrid, wblock, 0, s, (const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
+    fastar::launch_pdl((cand_norm_kernel), dim3((n_f + 8 * kNormCands - 1) / (8 * kNormCands), H), wblock, 0, s, (const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
                                               w.stage, n_f, st);
     FASTAR_LAUNCHED(s, "cand_norm");
   }
@@ -509,12 +569,11 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     } else if (rc != FASTAR_OK) {
       return rc;
     }
-    fastar::launch_pdl((plan_kernel), H, kPlanThreads, (size_t)n_f * sizeof(int), s, 
-        n_f, C, f, tau, w.best, match_out, fi * n_f, Nrow, w.match, w.cand[nxt], w.ncand[nxt], w.rep_j,
-        w.gcnt, w.plan_slot, w.plan_kind, w.plan_cnt, w.evict, c->last_frame, c->m, c->size, c->inserted,
-        c->evicted, st);
+    fastar::launch_pdl((plan_kernel), H, kPlanThreads, plan_smem, s, n_f, C, f, tau, lg_tab, w.best, match_out,
+                       fi * n_f, Nrow, w.match, w.cand[nxt], w.ncand[nxt], w.plan_slot, w.plan_kind, w.plan_cnt,
+                       w.evict, c->last_frame, c->m, c->size, c->inserted, c->evicted, st);
     FASTAR_LAUNCHED(s, "plan");
-    fastar::launch_pdl((apply_kernel<T, D>), wgrid, wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
+    fastar::launch_pdl((apply_kernel<T, D>), dim3((n_f + 8 * kApplyKeys - 1) / (8 * kApplyKeys), H), wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
                                                 w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m,
                                                 c->codes, c->last_frame, C, st);
     FASTAR_LAUNCHED(s, "apply");
