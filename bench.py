@@ -226,6 +226,7 @@ def algorithmic(cfg, path, match, snap_size, snap_lf):
     size = path.cache.size.long()
     n_live = int(size.sum())
     kept = int(path.kept_cnt.long().sum())
+    kept_tiles = int(((path.kept_cnt.long() + 63) // 64).sum())
     rows = H * (2 * Nq + P)
     by = {}
     by["hash"] = rows * (D * e + T * 4) + H * T * Nq * (4 + 4 + 4) + T * cfg.B * D * e
@@ -276,6 +277,10 @@ def algorithmic(cfg, path, match, snap_size, snap_lf):
         "annsa_tc": {"flops": fl["annsa"],
                      "bytes": (T * (H * Nq * D * e + n_live * (2 * D * e + 4 + 2 * T * 4))
                                + (T * H * Nq * (D * 4 + 8) if T > 1 else H * Nq * (D * e + 4)))},
+        # the kept rows of each (head, frame), read once and written as
+        # 64-row tiles (zero rows up to the tile) that annca_tc then loads
+        "annca_compact": {"flops": 0, "bytes": 2 * kept * D * e + 2 * kept_tiles * 64 * D * e
+                          + (kept + H * F) * 4},
         "annsa_combine": {"flops": 0, "bytes": T * H * Nq * (D * 4 + 8) + H * Nq * (D * e + 4)},
         "hash_tc": {"flops": 2 * rows * T * cfg.B * D / 3, "bytes": (rows * (D * e + T * 4)) / 3},
         "apply": {"flops": 0, "bytes": by["merge"] / F * 0.5},
@@ -393,7 +398,7 @@ def run_ours(args, cfg):
                               path.kept_cnt, status=st)
         rec(3)
         fa.fastar_annca_attention(q, kp, vp, path.kept_idx, path.kept_cnt, cfg.F, cfg.n_f,
-                                  path.scale, path.o_ca, status=st)
+                                  path.scale, path.o_ca, ws=path.ws_annca, status=st)
         rec(4)
         fa.fastar_annsa_attention(q, path.q_codes, path.q_perm, path.q_offsets, path.cache,
                                   path.scale, path.o_sa, path.lse, ws=path.ws_annsa, status=st)

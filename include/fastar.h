@@ -91,8 +91,9 @@ const char* fastar_timing_name(int i);
 /*
  * Bytes of workspace a call needs.  Arguments that an op does not use are
  * ignored.  op: FASTAR_OP_*; H heads; N rows per head (hash: N; merge:
- * n_f, the tokens per frame; prune: P; annca: P; annsa: Nq); D head dim;
- * T tables; B bits; C cache capacity.
+ * n_f, the tokens per frame; prune: P; annca: F, the frames of the chunk;
+ * annsa: Nq); D head dim; T tables; B bits; C cache capacity (annca: P, the
+ * prompt tokens).
  */
 size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C);
 
@@ -248,7 +249,9 @@ int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes,
  *
  * q [H][F*n_f][D], k_p, v_p [H][P][D] dt; kept_idx/kept_cnt from
  * fastar_annca_prune (or any ascending id list); out [H][F*n_f][D] dt.
- * scale must be positive and finite (FASTAR_ERR_ARG otherwise).
+ * ws: fastar_workspace_size(FASTAR_OP_ANNCA, H, F, D, 0, 0, P) bytes (the
+ * kept rows of each frame are compacted there; FASTAR_ERR_WORKSPACE when
+ * smaller).  scale must be positive and finite (FASTAR_ERR_ARG otherwise).
  * fp32 accumulation.  Passing kept = 0..P-1 gives dense attention.
  */
 int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p,

@@ -219,13 +219,18 @@ def fastar_annca_prune(q_codes, p_codes, F, n_f, B, kept_idx, kept_cnt, status=N
            "fastar_annca_prune")
 
 
-def fastar_annca_attention(q, k_p, v_p, kept_idx, kept_cnt, F, n_f, scale, out, status=None,
-                           stream=None):
-    """out [H][F*n_f][D]: cross-attention of each frame over its kept tokens."""
+def fastar_annca_attention(q, k_p, v_p, kept_idx, kept_cnt, F, n_f, scale, out, ws=None,
+                           status=None, stream=None):
+    """out [H][F*n_f][D]: cross-attention of each frame over its kept tokens.
+
+    ws: a uint8 device tensor of at least
+    fastar_workspace_size(OP_ANNCA, H, F, D, 0, 0, P) bytes; one is allocated
+    for the call when it is None."""
     H, Nq, D = q.shape
     P = k_p.shape[1]
+    ws, nbytes = _ws(OP_ANNCA, H, F, D, 0, 0, P, ws, q.device)
     _check(lib().fastar_annca_attention(_dt(q), _p(q), _p(k_p), _p(v_p), _p(kept_idx),
-                                        _p(kept_cnt), H, F, n_f, P, D, scale, _p(out), None, 0,
+                                        _p(kept_cnt), H, F, n_f, P, D, scale, _p(out), _p(ws), nbytes,
                                         _p(status), _stream(stream)), "fastar_annca_attention")
 
 

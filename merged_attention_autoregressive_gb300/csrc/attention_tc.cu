@@ -2,18 +2,21 @@
 //
 // One CTA owns 128 queries (one per softmax thread) and walks their keys 64
 // at a time through a warp-specialised pipeline:
-//   warp 0     producer: AnnCA's queries (one TMA box pair), then for every
-//              key tile the key and value rows (cp.async gathers into the
-//              128-byte swizzled layout, 2-stage ring) and the tile's mask
-//              metadata, fetched one tile ahead;
+//   warp 0     producer: AnnCA's queries (one TMA box pair), then the key
+//              rows and, separately, the value rows and mask metadata of
+//              every tile (cp.async gathers into the 128-byte swizzled
+//              layout, 2-stage rings), each as soon as its stage is free: a
+//              key stage once its QK product is done, a value stage once its
+//              PV product is; row sources and metadata are fetched ahead;
 //   warp 1     MMA issuer: S_j = Q K_j^T (M 128, N 64, K 128) into one of two
-//              TMEM S buffers and O += P_j V_j (M 128, N 128, K 64; V read as
-//              an MN-major operand) into the TMEM accumulator, each as soon as
-//              its inputs are ready (QK at most one tile ahead of PV);
+//              TMEM buffers and O += P_j V_j (M 128, N 128, K 64; P_j read
+//              from TMEM, V as an MN-major operand) into the TMEM
+//              accumulator, each as soon as its inputs are ready (QK at most
+//              one tile ahead of PV);
 //   warps 2-5  softmax, one thread per query row (AnnSA: each also gathers
 //              its query row): read S_j from TMEM, apply the scale, the
 //              + ln m bias and the mask, keep a running max and sum in base 2,
-//              write P_j (bf16) over the spent key tile.  The running max is
+//              write P_j (bf16 pairs) over S_j in TMEM.  The running max is
 //              only raised (and O in TMEM rescaled) when a tile's maximum
 //              exceeds it by more than 2^8, so P stays <= 256 and rescaling
 //              is rare.
@@ -36,6 +39,7 @@
 // normalised output and the log-sum-exp; with more, each table writes an
 // unnormalised partial (o, running max, sum) and a combine kernel merges the
 // T partials of each query.
+#include <limits.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -54,13 +58,13 @@ constexpr uint32_t kIdlePolls = 1u << 22;  // MMA issuer: bound on polls that fi
 
 struct AttnSmem {
   uint8_t Q[kM * kD * 2];
-  uint8_t K[kStages][kN * kD * 2];  // key tile, then P_j (bf16, 128 rows x 64 keys)
+  uint8_t K[kStages][kN * kD * 2];
   uint8_t V[kStages][kN * kD * 2];
   float bias[kStages][kN];                      // AnnSA: log2 m of the tile's slots
   uint32_t kcodes[kStages][kMaxT - 1][kN];      // AnnSA: slot codes of the tables before t
   uint64_t bar_q;
-  uint64_t full[kStages], empty[kStages];
-  uint64_t sfull[2], sfree[2], pready[2], fin;
+  uint64_t kfull[kStages], vfull[kStages], kempty[kStages], vempty[kStages];
+  uint64_t sfull[2], pready[2], odone, fin;
   uint32_t tmem;
 };
 // At the end the output rows are staged through Q and K (free by then):
@@ -72,7 +76,7 @@ struct CaArgs {
   const __nv_bfloat16* v_p;
   const int32_t* kept_idx;
   const int32_t* kept_cnt;
-  int F, n_f, P;
+  int F, n_f, P, P64;  // P64: rows per (head, frame) of the compacted kept K / V
   __nv_bfloat16* out;
 };
 
@@ -95,15 +99,15 @@ struct SaArgs {
 };
 
 // Wait until the PV product of key tile j has landed in O (and, since one
-// thread issues every MMA in order, all products before it).  The commit
-// after PV_j arrives on empty[j % kStages].  A parity wait is only sound
-// while the barrier is at most one phase behind the awaited one: here the
-// previous phase on that barrier (PV_{j-2}) has completed, because the
-// producer waited for it before loading tile j, whose QK product the caller
-// has already seen; and the next phase (PV_{j+2}) cannot complete before the
-// caller has released P_{j+2}.
+// thread issues every MMA in order, all products before it); called by a
+// softmax thread that has seen S_{j+1}.  The commit after PV_j arrives on
+// vempty[j % kStages].  A parity wait is only sound while the barrier is at
+// most one phase behind the awaited one: the previous phase on that barrier
+// (PV_{j-2}) has completed, because QK_{j+1}, which the caller has seen
+// complete, was issued after PV_{j-1} (QK runs at most one tile ahead of PV) and the MMAs complete in issue order; and the next phase
+// (PV_{j+2}) cannot complete before the caller has written P_{j+2}.
 __device__ __forceinline__ bool wait_pv(AttnSmem& sm, int j) {
-  return tc::mbar_wait(&sm.empty[j % kStages], (uint32_t)(j / kStages) & 1u);
+  return tc::mbar_wait(&sm.vempty[j % kStages], (uint32_t)(j / kStages) & 1u);
 }
 
 // 2^x by the SFU instruction (relative error about 2^-22; results below
@@ -124,10 +128,51 @@ __device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
   return below_hi & ~below_lo;
 }
 
+// AnnCA: the kept prompt rows of each (head, frame), compacted in kept
+// order into Kc/Vc [(h * F + f) * P64 + k][D] (P64 = P rounded up to 64),
+// with zero rows up to the next multiple of 64, so that the attention kernel
+// loads whole key tiles with two TMA boxes.  One CTA per 64-row tile, a
+// warp per row at a time (8 bytes per lane).
+__global__ void __launch_bounds__(256) annca_compact_kernel(const __nv_bfloat16* __restrict__ k_p,
+                                                            const __nv_bfloat16* __restrict__ v_p,
+                                                            const int32_t* __restrict__ kept_idx,
+                                                            const int32_t* __restrict__ kept_cnt, int F, int P,
+                                                            int P64, __nv_bfloat16* __restrict__ kc,
+                                                            __nv_bfloat16* __restrict__ vc, int32_t* st) {
+  pdl_wait();
+  if (status_bad(st)) return;
+  const int t = blockIdx.x, f = blockIdx.y, h = blockIdx.z;
+  const int cnt = min(max(kept_cnt[(size_t)h * F + f], 0), P);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (t * kN < cnt) {
+    bool bad = false;
+    for (int r = warp; r < kN; r += 8) {
+      const int k = t * kN + r;
+      const size_t dst = (((size_t)h * F + f) * P64 + k) * kD + lane * 4;
+      uint2 ku = make_uint2(0u, 0u), vu = make_uint2(0u, 0u);
+      if (k < cnt) {
+        const int p = kept_idx[((size_t)h * F + f) * P + k];
+        if (p >= 0 && p < P) {
+          ku = *reinterpret_cast<const uint2*>(k_p + ((size_t)h * P + p) * kD + lane * 4);
+          vu = *reinterpret_cast<const uint2*>(v_p + ((size_t)h * P + p) * kD + lane * 4);
+        } else {
+          bad = true;
+        }
+      }
+      *reinterpret_cast<uint2*>(kc + dst) = ku;
+      *reinterpret_cast<uint2*>(vc + dst) = vu;
+    }
+    if (bad && lane == 0) status_set(st, FASTAR_ERR_DEVICE_ARG);
+  }
+  pdl_trigger();
+}
+
 // AnnCA: grid (query tiles, frames, heads); AnnSA: grid (query tiles,
 // tables, heads).
 template <bool kSA>
-__global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ, int H,
+__global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
+                                                             const __grid_constant__ CUtensorMap mapK,
+                                                             const __grid_constant__ CUtensorMap mapV, int H,
                                                              int Nq, float scale, CaArgs ca, SaArgs sa,
                                                              int32_t* st) {
   pdl_wait();
@@ -144,14 +189,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   if (tid == 0) {
     tc::mbar_init(&sm.bar_q, kSA ? 128 : 1);  // AnnSA: every softmax thread gathers its query row
     for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&sm.full[s], 32 + 1);  // 32 cp.async lanes + the metadata arrive
-      tc::mbar_init(&sm.empty[s], 1);      // PV commit (also: O holds this tile's product)
+      // AnnCA: one arrival with the TMA bytes; AnnSA: 32 cp.async lanes (+
+      // the metadata arrive for the values)
+      tc::mbar_init(&sm.kfull[s], kSA ? 32 : 1);
+      tc::mbar_init(&sm.vfull[s], kSA ? 32 + 1 : 1);
+      tc::mbar_init(&sm.kempty[s], 1);     // QK commit
+      tc::mbar_init(&sm.vempty[s], 1);     // PV commit (also: O holds this tile's product)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&sm.sfull[b], 1);      // QK commit
-      tc::mbar_init(&sm.sfree[b], 4);      // softmax warps
-      tc::mbar_init(&sm.pready[b], 4);     // softmax warps
+      tc::mbar_init(&sm.pready[b], 4);     // softmax warps (P written to TMEM)
     }
+    tc::mbar_init(&sm.odone, 1);           // commit after the last PV
     tc::mbar_init(&sm.fin, 1);             // last commit of the MMA issuer
     tc::fence_mbar_init();
   }
@@ -162,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = sm.tmem;  // S buffers at columns 0 and 64, O at 128
+  const uint32_t tmem = sm.tmem;  // S / P buffers at columns 0 and 64, O at 128
   bool ok = true;
   bool bad_index = false;
 
@@ -220,24 +269,34 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         tc::tma_load_2d(sm.Q + kM * 128, &mapQ, &sm.bar_q, 64, row0);
       }
     }
-    // row sources of tile j, rows lane and lane + 32 (AnnCA: prompt ids; AnnSA: slots)
+    // row sources of tile j, rows lane and lane + 32 (AnnCA: prompt ids;
+    // AnnSA: slots).  The loads are only issued here; the values are checked
+    // when the next tile becomes current, so the warp does not wait for them.
+    constexpr int kNoRow = INT_MIN;
+    const int lim = kSA ? sa.C : ca.P;
     auto fetch_src = [&](int j, int* out) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const int rr = lane + 32 * u, k = j * kN + rr;
-        out[u] = -1;
+        const int k = j * kN + lane + 32 * u;
+        out[u] = kNoRow;
         if (k < nkeys) {
-          int x;
-          if constexpr (!kSA) x = ca.kept_idx[((size_t)h * ca.F + g) * ca.P + k];
-          else x = sa.perm[((size_t)h * sa.T + kT) * sa.C + kbeg + k];
-          const int lim = kSA ? sa.C : ca.P;
-          if (x >= 0 && x < lim) out[u] = x; else bad_index = true;
+          if constexpr (!kSA) out[u] = ca.kept_idx[((size_t)h * ca.F + g) * ca.P + k];
+          else out[u] = sa.perm[((size_t)h * sa.T + kT) * sa.C + kbeg + k];
         }
       }
     };
-    // AnnSA metadata of those rows: codes of the earlier tables and log2 m
+    auto check_src = [&](int* v) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+        if (v[u] != kNoRow && (v[u] < 0 || v[u] >= lim)) {
+          bad_index = true;
+          v[u] = kNoRow;
+        }
+    };
+    // AnnSA metadata of those rows: codes of the earlier tables and the
+    // group counts m (log2 m is taken when the metadata is stored)
     uint32_t kc[kMaxT - 1][2];
-    float bs[2];
+    int mraw[2];
     auto fetch_meta = [&](const int* src) {
       if constexpr (kSA) {
 #pragma unroll
@@ -245,58 +304,130 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
           for (int w = 0; w < kMaxT - 1; ++w)
             kc[w][u] = (w < kT && src[u] >= 0) ? sa.codes[((size_t)h * sa.T + w) * sa.C + src[u]] : 0xfffffffeu;
-          bs[u] = src[u] >= 0 ? log2f((float)max(sa.m[(size_t)h * sa.C + src[u]], 1)) : 0.f;
+          mraw[u] = src[u] >= 0 ? sa.m[(size_t)h * sa.C + src[u]] : 0;
         }
       }
     };
-    int src[2];
-    fetch_src(0, src);
-    fetch_meta(src);
     const __nv_bfloat16* kb = kSA ? sa.K : ca.k_p;
     const __nv_bfloat16* vb = kSA ? sa.V : ca.v_p;
     const size_t rows_per_head = kSA ? (size_t)sa.C : (size_t)ca.P;
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int s = j % kStages;
-      int nsrc[2] = {-1, -1};
-      if (j + 1 < ntiles) fetch_src(j + 1, nsrc);  // in flight during the wait below
-      if (j >= kStages) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.empty[s], (uint32_t)((j / kStages) - 1) & 1u));
-      if (!ok) break;
-      if constexpr (kSA) {
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-#pragma unroll
-          for (int w = 0; w < kMaxT - 1; ++w)
-            if (w < kT) sm.kcodes[s][w][lane + 32 * u] = kc[w][u];
-          sm.bias[s][lane + 32 * u] = bs[u];
-        }
-      }
-      const uint32_t kt = tc::smem_u32(sm.K[s]), vt = tc::smem_u32(sm.V[s]);
+    // Key and value gathers advance independently: the key rows of tile j go
+    // into key stage j % kStages once QK_{j-2} has freed it, the value rows
+    // and metadata into value stage j % kStages once PV_{j-2} has.  Each side
+    // keeps its own row sources, fetched one tile ahead.
+    auto gather = [&](uint32_t tile, const __nv_bfloat16* base, const int* src) {
 #pragma unroll
       for (int i = 0; i < kN * 16 / 32; ++i) {
         const int rr = 2 * i + (lane >> 4), ch = lane & 15;
         const int sr = __shfl_sync(0xffffffffu, src[rr >> 5], rr & 31);
         const uint32_t off = tc::sw128_offset(rr, ch, kN);
-        if (sr >= 0) {
-          const size_t row = ((size_t)h * rows_per_head + sr) * kD;
-          tc::cp_async16(kt + off, (const char*)(kb + row) + ch * 16, 16u);
-          tc::cp_async16(vt + off, (const char*)(vb + row) + ch * 16, 16u);
-        } else {
-          tc::cp_async16(kt + off, kb, 0u);
-          tc::cp_async16(vt + off, vb, 0u);
+        if (sr >= 0) tc::cp_async16(tile + off, (const char*)(base + ((size_t)h * rows_per_head + sr) * kD) + ch * 16, 16u);
+        else tc::cp_async16(tile + off, base, 0u);
+      }
+    };
+    int ksrc[2] = {kNoRow, kNoRow}, knext[2] = {kNoRow, kNoRow}, vsrc[2] = {kNoRow, kNoRow},
+        vnext[2] = {kNoRow, kNoRow};
+    if constexpr (kSA) {
+      fetch_src(0, ksrc);
+      check_src(ksrc);
+      vsrc[0] = ksrc[0];
+      vsrc[1] = ksrc[1];
+      fetch_meta(vsrc);
+      if (ntiles > 1) {
+        fetch_src(1, knext);
+        fetch_src(1, vnext);
+      }
+    } else if (lane == 0) {
+      tc::prefetch_tensormap(&mapK);
+      tc::prefetch_tensormap(&mapV);
+    }
+    int jk = 0, jv = 0;
+    uint32_t idle = 0;
+    while (ok && jv < ntiles) {
+      bool did = false;
+      if (jk < ntiles) {
+        const int s = jk % kStages;
+        int ready = 1;
+        if (jk >= kStages)
+          ready = lane == 0 ? (int)tc::mbar_test_wait(&sm.kempty[s], (uint32_t)((jk / kStages) - 1) & 1u) : 0;
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          if constexpr (!kSA) {
+            if (lane == 0) {
+              const int row = (h * ca.F + g) * ca.P64 + jk * kN;
+              tc::mbar_arrive_expect_tx(&sm.kfull[s], kN * kD * 2);
+              tc::tma_load_2d(sm.K[s], &mapK, &sm.kfull[s], 0, row);
+              tc::tma_load_2d(sm.K[s] + kN * 128, &mapK, &sm.kfull[s], 64, row);
+            }
+          } else {
+            gather(tc::smem_u32(sm.K[s]), kb, ksrc);
+            tc::cp_async_arrive_noinc(&sm.kfull[s]);
+          }
+          ++jk;
+          if constexpr (kSA) {
+            ksrc[0] = knext[0];
+            ksrc[1] = knext[1];
+            check_src(ksrc);
+            knext[0] = knext[1] = kNoRow;
+            if (jk + 1 < ntiles) fetch_src(jk + 1, knext);
+          }
+          did = true;
         }
       }
-      tc::cp_async_arrive_noinc(&sm.full[s]);
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm.full[s]);  // the metadata written above
-      src[0] = nsrc[0];
-      src[1] = nsrc[1];
-      if (j + 1 < ntiles) fetch_meta(src);  // lands while tile j is consumed
+      if (jv < jk) {
+        const int s = jv % kStages;
+        int ready = 1;
+        if (jv >= kStages)
+          ready = lane == 0 ? (int)tc::mbar_test_wait(&sm.vempty[s], (uint32_t)((jv / kStages) - 1) & 1u) : 0;
+        if (__shfl_sync(0xffffffffu, ready, 0)) {
+          if constexpr (kSA) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+#pragma unroll
+              for (int w = 0; w < kMaxT - 1; ++w)
+                if (w < kT) sm.kcodes[s][w][lane + 32 * u] = kc[w][u];
+              sm.bias[s][lane + 32 * u] = vsrc[u] >= 0 ? log2f((float)max(mraw[u], 1)) : 0.f;
+            }
+          }
+          if constexpr (!kSA) {
+            if (lane == 0) {
+              const int row = (h * ca.F + g) * ca.P64 + jv * kN;
+              tc::mbar_arrive_expect_tx(&sm.vfull[s], kN * kD * 2);
+              tc::tma_load_2d(sm.V[s], &mapV, &sm.vfull[s], 0, row);
+              tc::tma_load_2d(sm.V[s] + kN * 128, &mapV, &sm.vfull[s], 64, row);
+            }
+          } else {
+            gather(tc::smem_u32(sm.V[s]), vb, vsrc);
+            tc::cp_async_arrive_noinc(&sm.vfull[s]);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&sm.vfull[s]);  // the metadata written above
+          }
+          ++jv;
+          if constexpr (kSA) {
+            vsrc[0] = vnext[0];
+            vsrc[1] = vnext[1];
+            check_src(vsrc);
+            if (jv < ntiles) fetch_meta(vsrc);  // lands while tile jv - 1 is consumed
+            vnext[0] = vnext[1] = kNoRow;
+            if (jv + 1 < ntiles) fetch_src(jv + 1, vnext);
+          }
+          did = true;
+        }
+      }
+      if (did) {
+        idle = 0;
+      } else if (++idle > kIdlePolls) {
+        ok = false;
+      } else {
+        __nanosleep(32);
+      }
     }
   } else if (warp == 1) {
     // ================================================= MMA issuer
-    // Issues QK_j (S_j = Q K_j^T into S buffer j & 1) and PV_j (O += P_j V_j)
-    // in whichever order their inputs become ready, with QK at most one tile
-    // ahead of PV.
+    // Issues QK_j (S_j = Q K_j^T into TMEM buffer j & 1) and PV_j (O += P_j
+    // V_j, P_j read from the same TMEM buffer, where the softmax wrote it
+    // over S_j) in whichever order their inputs become ready, with QK at
+    // most one tile ahead of PV: QK_{j+2} is issued after PV_j, and the MMAs
+    // of one thread run in issue order, so it cannot overwrite P_j early.
     constexpr uint32_t idesc_qk = tc::idesc_bf16_f32(kM, kN, 0, 0);
     constexpr uint32_t idesc_pv = tc::idesc_bf16_f32(kM, kD, 0, 1);
     if (ntiles > 0) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.bar_q, 0));
@@ -305,21 +436,24 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     while (ok && jp < ntiles) {
       bool did = false;
       if (jp < jq) {
-        const int b = jp & 1;
-        int ready = lane == 0 ? (int)tc::mbar_test_wait(&sm.pready[b], (uint32_t)(jp >> 1) & 1u) : 0;
+        const int s = jp % kStages, b = jp & 1;
+        int ready = 0;
+        if (lane == 0)
+          ready = tc::mbar_test_wait(&sm.pready[b], (uint32_t)(jp >> 1) & 1u) &&
+                  tc::mbar_test_wait(&sm.vfull[s], (uint32_t)(jp / kStages) & 1u);
         ready = __shfl_sync(0xffffffffu, ready, 0);
         if (ready) {
           tc::fence_proxy_async_smem();
           tc::tc_fence_after();
           if (lane == 0) {
-            const int s = jp % kStages;
-            const uint32_t p0 = tc::smem_u32(sm.K[s]), v0 = tc::smem_u32(sm.V[s]);
+            const uint32_t v0 = tc::smem_u32(sm.V[s]);
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk)
-              tc::mma_bf16(tmem + 128, tc::sdesc_kmajor_sw128(p0 + kk * 32),
-                           tc::sdesc_mnmajor_sw128(v0 + kk * 16 * 128, kN * 128), idesc_pv,
-                           (jp > 0 || kk > 0) ? 1u : 0u);
-            tc::mma_commit(&sm.empty[s]);
+              tc::mma_bf16_tmem_a(tmem + 128, tmem + b * kN + kk * 8,
+                                  tc::sdesc_mnmajor_sw128(v0 + kk * 16 * 128, kN * 128), idesc_pv,
+                                  (jp > 0 || kk > 0) ? 1u : 0u);
+            tc::mma_commit(&sm.vempty[s]);
+            if (jp == ntiles - 1) tc::mma_commit(&sm.odone);
           }
           __syncwarp();
           ++jp;
@@ -328,10 +462,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       }
       if (!did && jq < ntiles && jq <= jp + 1) {
         const int s = jq % kStages, b = jq & 1;
-        int ready = 0;
-        if (lane == 0)
-          ready = tc::mbar_test_wait(&sm.full[s], (uint32_t)(jq / kStages) & 1u) &&
-                  (jq < 2 || tc::mbar_test_wait(&sm.sfree[b], (uint32_t)((jq >> 1) - 1) & 1u));
+        int ready = lane == 0 ? (int)tc::mbar_test_wait(&sm.kfull[s], (uint32_t)(jq / kStages) & 1u) : 0;
         ready = __shfl_sync(0xffffffffu, ready, 0);
         if (ready) {
           tc::fence_proxy_async_smem();
@@ -346,6 +477,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
                            idesc_qk, kk > 0 ? 1u : 0u);
             }
             tc::mma_commit(&sm.sfull[b]);
+            tc::mma_commit(&sm.kempty[s]);
           }
           __syncwarp();
           ++jq;
@@ -393,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < ntiles && ok; ++j) {
       const int s = j % kStages, b = j & 1;
-      if constexpr (kSA) ok = tc::mbar_wait(&sm.full[s], (uint32_t)(j / kStages) & 1u);  // metadata
+      if constexpr (kSA) ok = tc::mbar_wait(&sm.vfull[s], (uint32_t)(j / kStages) & 1u);  // metadata
       ok = ok && tc::mbar_wait(&sm.sfull[b], (uint32_t)(j >> 1) & 1u);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -407,10 +539,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
       for (int q = 0; q < 2; ++q)
         if (live[q]) tc::tmem_ld32(tmem + lane_base + b * kN + q * 32, v[q]);
-      // S_j is in registers: release the S buffer
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&sm.sfree[b]);
       // scores in log2 units (masked: -inf) and their maximum; AnnCA keeps
       // the raw products and scales the maximum (scale > 0)
       float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -474,13 +602,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       }
       l_run *= alpha;
       m_run = m_new;
-      // P_j (bf16) over the spent key tile: 128 rows x 64 keys, one swizzle
-      // atom per row; masked scores are -inf and give 0 (scale > 0)
+      // P_j (bf16 pairs, 32 columns) over S_j in TMEM; masked scores are
+      // -inf and give 0 (scale > 0)
       const float m_sub = m_run == -INFINITY ? 0.f : m_run;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t packed_all[32];
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        uint32_t packed[16];
+        uint32_t* packed = packed_all + 16 * q;
         if (live[q]) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
@@ -501,14 +630,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 #pragma unroll
           for (int i = 0; i < 16; ++i) packed[i] = 0u;
         }
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<uint4*>(sm.K[s] + tc::sw128_offset(r, q * 4 + k, kM)) =
-              make_uint4(packed[4 * k], packed[4 * k + 1], packed[4 * k + 2], packed[4 * k + 3]);
       }
+      tc::tmem_st32u(tmem + lane_base + b * kN, packed_all);
       const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
       l_run += psum;
-      tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.pready[b]);
@@ -517,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     // are free once the last PV product has landed), then written one row
     // per warp instruction
     if (ok && ntiles > 0) {
-      ok = __all_sync(0xffffffffu, wait_pv(sm, ntiles - 1));
+      ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.odone, 0));  // the last PV product
       tc::tc_fence_after();
     }
     if constexpr (kSA) tc::cp_async_wait_all();  // the query rows (no key tile may have waited for them)
@@ -676,18 +801,20 @@ __global__ void __launch_bounds__(256) annsa_combine_kernel(const float* __restr
 }
 
 template <bool kSA>
-int launch_attn(const CUtensorMap& map, dim3 grid, int H, int Nq, float scale, const CaArgs& ca,
-                const SaArgs& sa, int32_t* st, cudaStream_t s) {
+int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid, int H, int Nq,
+                float scale, const CaArgs& ca, const SaArgs& sa, int32_t* st, cudaStream_t s) {
   const size_t smem = sizeof(AttnSmem) + 1024;
   if (cudaFuncSetAttribute(attn_tc_kernel<kSA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  fastar::launch_pdl((attn_tc_kernel<kSA>), grid, kThreads, smem, s, map, H, Nq, scale, ca, sa, st);
+  fastar::launch_pdl((attn_tc_kernel<kSA>), grid, kThreads, smem, s, mq, mk, mv, H, Nq, scale, ca, sa, st);
   FASTAR_LAUNCHED(s, kSA ? "annsa_tc" : "annca_tc");
   return FASTAR_OK;
 }
+
+int p64_of(int P) { return (P + kN - 1) / kN * kN; }
 
 }  // namespace
 
@@ -699,18 +826,43 @@ size_t annsa_tc_ws_bytes(int H, int Nq, int D, int T) {
   return ((o + 255) & ~(size_t)255) + ((ml + 255) & ~(size_t)255);
 }
 
+size_t annca_tc_ws_bytes(int H, int F, int P, int D) {
+  if (D != kD) return 0;
+  const size_t half = (size_t)H * F * p64_of(P) * kD * sizeof(__nv_bfloat16);
+  return 2 * ((half + 255) & ~(size_t)255);
+}
+
 int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
                     const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P, int D,
-                    float scale, void* out, int32_t* st, cudaStream_t s) {
+                    float scale, void* out, void* ws, size_t ws_bytes, int32_t* st, cudaStream_t s) {
   if (dt != FASTAR_BF16 || D != kD) return FASTAR_ERR_UNSUPPORTED;
   const int Nq = F * n_f;
   if (Nq == 0 || H == 0) return FASTAR_OK;
-  CUtensorMap mapQ;
-  if (make_tmap_bf16_2d(&mapQ, q, (uint64_t)H * Nq, kD, kM, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
-  CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P,
+  const int P64 = p64_of(P);
+  if (P64 == 0) {
+    // no prompt tokens: every kept set is empty
+    CUtensorMap mq;
+    if (make_tmap_bf16_2d(&mq, q, (uint64_t)H * Nq, kD, kM, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+    CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P, 0,
+              (__nv_bfloat16*)out};
+    SaArgs sa{};
+    return launch_attn<false>(mq, mq, mq, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
+  }
+  if (!ws || ws_bytes < annca_tc_ws_bytes(H, F, P, D)) return FASTAR_ERR_WORKSPACE;
+  const size_t half = (((size_t)H * F * P64 * kD * sizeof(__nv_bfloat16)) + 255) & ~(size_t)255;
+  __nv_bfloat16* kc = (__nv_bfloat16*)ws;
+  __nv_bfloat16* vc = (__nv_bfloat16*)((char*)ws + half);
+  fastar::launch_pdl((annca_compact_kernel), dim3(P64 / kN, F, H), 256, 0, s, (const __nv_bfloat16*)k_p,
+                     (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, P, P64, kc, vc, st);
+  FASTAR_LAUNCHED(s, "annca_compact");
+  CUtensorMap mq, mk, mv;
+  if (make_tmap_bf16_2d(&mq, q, (uint64_t)H * Nq, kD, kM, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(&mk, kc, (uint64_t)H * F * P64, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(&mv, vc, (uint64_t)H * F * P64, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P, P64,
             (__nv_bfloat16*)out};
   SaArgs sa{};
-  return launch_attn<false>(mapQ, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
+  return launch_attn<false>(mq, mk, mv, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
 }
 
 int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
@@ -728,7 +880,8 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
   // every table in one launch: the tables' CTAs fill each other's waves
-  const int rc = launch_attn<true>(dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa, st, s);
+  const int rc = launch_attn<true>(dummy, dummy, dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca,
+                                   sa, st, s);
   if (rc != FASTAR_OK || c->T == 1) return rc;
   fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);

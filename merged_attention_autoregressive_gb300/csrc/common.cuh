@@ -198,7 +198,7 @@ int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F,
                  cudaStream_t s);
 int launch_annca(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
                  const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f,
-                 int P, int D, float scale, void* out, int32_t* st, cudaStream_t s);
+                 int P, int D, float scale, void* out, void* ws, size_t ws_bytes, int32_t* st, cudaStream_t s);
 int launch_annsa(fastar_dtype dt, const void* q, const uint32_t* q_codes,
                  const int32_t* q_perm, const int32_t* q_offsets, int Nq,
                  const fastar_cache* c, float scale, void* out, float* lse, void* ws,

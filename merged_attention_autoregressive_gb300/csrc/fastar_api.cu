@@ -37,7 +37,8 @@ int launch_annca_simt(fastar_dtype dt, const void* q, const void* k_p, const voi
                       int D, float scale, void* out, int32_t* st, cudaStream_t s);
 int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
                     const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P,
-                    int D, float scale, void* out, int32_t* st, cudaStream_t s);
+                    int D, float scale, void* out, void* ws, size_t ws_bytes, int32_t* st, cudaStream_t s);
+size_t annca_tc_ws_bytes(int H, int F, int P, int D);
 int launch_annsa_simt(fastar_dtype dt, const void* q, const uint32_t* q_codes, int Nq,
                       const fastar_cache* c, float scale, void* out, float* lse, int32_t* st,
                       cudaStream_t s);
@@ -55,8 +56,9 @@ int launch_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void*
 
 int launch_annca(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
                  const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P,
-                 int D, float scale, void* out, int32_t* st, cudaStream_t s) {
-  int rc = launch_annca_tc(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, st, s);
+                 int D, float scale, void* out, void* ws, size_t ws_bytes, int32_t* st, cudaStream_t s) {
+  int rc = launch_annca_tc(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, ws, ws_bytes,
+                           st, s);
   if (rc != FASTAR_ERR_UNSUPPORTED) return rc;
   return launch_annca_simt(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, st, s);
 }
@@ -127,6 +129,7 @@ size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C) {
   if (H < 0 || N < 0 || C < 0) return 0;
   switch (op) {
     case FASTAR_OP_MERGE: return merge_ws_bytes(H, N, C);
+    case FASTAR_OP_ANNCA: return annca_tc_ws_bytes(H, N, C, D);  // N = frames F, C = prompt tokens P
     case FASTAR_OP_ANNSA: return annsa_ws_bytes(H, N, D, T);
     default: return 0;
   }
@@ -196,8 +199,6 @@ int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p, cons
                            const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f,
                            int P, int D, float scale, void* out, void* ws, size_t ws_bytes,
                            int32_t* dev_status, cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
   if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
   if (H < 0 || F < 0 || n_f < 0 || P < 0) return FASTAR_ERR_ARG;
   if (!(scale > 0.f && scale < INFINITY)) return FASTAR_ERR_ARG;
@@ -205,8 +206,12 @@ int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p, cons
   if ((size_t)H * F * n_f == 0) return FASTAR_OK;
   if (!q || !out || !kept_cnt || !aligned16(q) || !aligned16(out)) return FASTAR_ERR_ARG;
   if (P > 0 && (!k_p || !v_p || !kept_idx || !aligned16(k_p) || !aligned16(v_p))) return FASTAR_ERR_ARG;
-  return launch_annca(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, dev_status,
-                      stream);
+  if (dt == FASTAR_BF16 && D == 128 && P > 0) {
+    const size_t need = annca_tc_ws_bytes(H, F, P, D);
+    if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
+  }
+  return launch_annca(dt, q, k_p, v_p, kept_idx, kept_cnt, H, F, n_f, P, D, scale, out, ws, ws_bytes,
+                      dev_status, stream);
 }
 
 int fastar_annsa_attention(fastar_dtype dt, const void* q, const uint32_t* q_codes,

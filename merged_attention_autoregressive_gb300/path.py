@@ -11,7 +11,7 @@ from __future__ import annotations
 
 import torch
 
-from . import (Cache, OP_ANNSA, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
+from . import (Cache, OP_ANNCA, OP_ANNSA, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
                fastar_annsa_attention, fastar_hash, fastar_tempcache_merge,
                fastar_workspace_size)
 
@@ -44,6 +44,8 @@ class ChunkPath:
         self.ws_merge = torch.empty(max(1, fastar_workspace_size(OP_MERGE, H, n_f, D, T, B, C)),
                                     dtype=torch.uint8, device=dev)
         self.ws_annsa = torch.empty(max(1, fastar_workspace_size(OP_ANNSA, H, Nq, D, T, B, C)),
+                                    dtype=torch.uint8, device=dev)
+        self.ws_annca = torch.empty(max(1, fastar_workspace_size(OP_ANNCA, H, F, D, T, B, P)),
                                     dtype=torch.uint8, device=dev)
 
     # -- pieces -----------------------------------------------------------
@@ -79,7 +81,7 @@ class ChunkPath:
         fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
                            self.kept_idx, self.kept_cnt, status=st, stream=stream)
         fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
-                               self.scale, self.o_ca, status=st, stream=stream)
+                               self.scale, self.o_ca, ws=self.ws_annca, status=st, stream=stream)
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
                                stream=stream)

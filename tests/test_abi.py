@@ -86,6 +86,11 @@ def test_host_argument_errors_need_no_gpu(L):
     for bad in (0.0, -0.1, float("inf"), float("nan")):
         assert L.fastar_annca_attention(0, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
                                         ctypes.c_float(bad), fake, None, 0, None, None) == 1
+    # attention: the bf16 tensor-core path compacts the kept rows into ws
+    assert L.fastar_annca_attention(0, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
+                                    ctypes.c_float(0.1), fake, None, 0, None, None) == 4
+    need = L.fastar_workspace_size(3, 1, 1, 128, 0, 0, 4)
+    assert need >= 2 * 64 * 128 * 2
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
