@@ -160,6 +160,42 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t
   d |= (uint64_t)2 << 61;
   return d;
 }
+// A descriptor moved `bytes` further into shared memory: the start address
+// field holds the address / 16 in 14 bits, which cannot carry over for
+// addresses inside the CTA's shared memory window (< 256 KiB).
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) {
+  return desc + (uint64_t)(bytes >> 4);
+}
+// Two fp32 products in one instruction, each rounded to nearest as a
+// separate multiplication would be: (x0, x1) *= (m0, m1).
+__device__ __forceinline__ void mul2(float& x0, float& x1, float m0, float m1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "mul.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}\n"
+      : "+f"(x0), "+f"(x1)
+      : "f"(m0), "f"(m1));
+}
+// The largest of three floats; a NaN operand is ignored, as by fmaxf.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// One lane of the (fully active) warp is elected.  The MMA issuers compute
+// their descriptors on every lane, so the values are warp-uniform, and let the
+// elected lane issue: issuing from a lane picked by its index was measured to
+// take about twice as long per MMA instruction.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(e));
+  return e != 0u;
+}
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator,
 // M x N tile; a_mn / b_mn select MN-major (transposed) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, int b_mn) {

@@ -21,10 +21,13 @@
 //   match[H][n_f], plan_slot[H][n_f], plan_kind[H][n_f], plan_cnt[H][n_f],
 //   evict[H][n_f],
 //   best[H][n_f] (packed best candidate per key, see pack_best),
-//   cinv[H][C] (inverse norms of the first frame's candidates),
+//   cinv[H][ldc] (inverse norms of the first frame's candidates; NaN for an
+//   unusable one; ldc = C rounded up to 4),
 //   stage[H][n_f][128] bf16 (copies of the first n_f first-frame candidate
 //   rows, contiguous, so that the NN kernel can load them by TMA),
-//   invn[2][H][n_f] (inverse norms of the keys of the last two frames)
+//   invn[2][H][ldn] (inverse norms of the keys of the last two frames; the
+//   plan of a frame sets NaN for its keys that joined another key's group,
+//   which are no candidates of the next frame; ldn = n_f rounded up to 4)
 // best is zeroed when a call starts and again by each plan after it has
 // read it.
 #include <math.h>
@@ -50,7 +53,10 @@ struct MergeWs {
   float* cinv;
   float* invn[2];
   __nv_bfloat16* stage;
+  int ldc, ldn;  // row strides of cinv and invn (multiples of 4 floats)
 };
+
+static inline int round4(int x) { return (x + 3) & ~3; }
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -60,8 +66,8 @@ size_t merge_ws_bytes(int H, int n_f, int C) {
   b += 2 * align256((size_t)H * 4);       // ncand
   b += 5 * align256((size_t)H * n_f * 4); // match, plan_slot, plan_kind, plan_cnt, evict
   b += align256((size_t)H * n_f * 8);     // best
-  b += align256((size_t)H * C * 4);       // cinv
-  b += 2 * align256((size_t)H * n_f * 4); // invn
+  b += align256((size_t)H * round4(C) * 4);       // cinv
+  b += 2 * align256((size_t)H * round4(n_f) * 4); // invn
   b += align256((size_t)H * n_f * 128 * 2); // stage
   return b;
 }
@@ -80,9 +86,11 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
   w.plan_cnt = take((size_t)H * n_f * 4);
   w.evict = take((size_t)H * n_f * 4);
   w.best = (unsigned long long*)take((size_t)H * n_f * 8);
-  w.cinv = (float*)take((size_t)H * C * 4);
-  w.invn[0] = (float*)take((size_t)H * n_f * 4);
-  w.invn[1] = (float*)take((size_t)H * n_f * 4);
+  w.ldc = round4(C);
+  w.ldn = round4(n_f);
+  w.cinv = (float*)take((size_t)H * w.ldc * 4);
+  w.invn[0] = (float*)take((size_t)H * w.ldn * 4);
+  w.invn[1] = (float*)take((size_t)H * w.ldn * 4);
   w.stage = (__nv_bfloat16*)take((size_t)H * n_f * 128 * 2);
   return w;
 }
@@ -133,7 +141,7 @@ constexpr int kNormCands = 4;
 __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __restrict__ K, int C,
                                                         const int32_t* __restrict__ cand,
                                                         const int32_t* __restrict__ ncand, float* cinv,
-                                                        __nv_bfloat16* stage, int n_f, int32_t* st) {
+                                                        int ldc, __nv_bfloat16* stage, int n_f, int32_t* st) {
   pdl_wait();
   if (status_bad(st)) return;
   const int h = blockIdx.y, lane = threadIdx.x & 31;
@@ -149,13 +157,16 @@ __global__ void __launch_bounds__(256) cand_norm_kernel(const __nv_bfloat16* __r
       if (sl[u] >= 0) row[u] = *reinterpret_cast<const uint2*>(K + ((size_t)h * C + sl[u]) * 128 + lane * 4);
 #pragma unroll
     for (int u = 0; u < kNormCands; ++u) {
-      if (sl[u] < 0) continue;
       const int c = c0 + u;
+      if (sl[u] < 0) {
+        if (c < nc && lane == 0) cinv[(size_t)h * ldc + c] = __int_as_float(0x7fc00000);
+        continue;
+      }
       if (c < n_f) *reinterpret_cast<uint2*>(stage + ((size_t)h * n_f + c) * 128 + lane * 4) = row[u];
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&row[u].x));
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&row[u].y));
       const float n2 = warp_sum(a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y);
-      if (lane == 0) cinv[(size_t)h * C + c] = n2 > 0.f ? 1.f / sqrtf(n2) : __int_as_float(0x7fc00000);
+      if (lane == 0) cinv[(size_t)h * ldc + c] = n2 > 0.f ? 1.f / sqrtf(n2) : __int_as_float(0x7fc00000);
     }
   }
   pdl_trigger();
@@ -260,7 +271,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
                                                             const int32_t* __restrict__ last_frame,
                                                             const int32_t* __restrict__ m,
                                                             int32_t* size, int64_t* inserted,
-                                                            int64_t* evicted, int32_t* st) {
+                                                            int64_t* evicted, float* __restrict__ invn, int ldn,
+                                                            int32_t* st) {
   pdl_wait();
   extern __shared__ int plan_smem[];
   const int ntab = 1 << lg_tab;
@@ -413,6 +425,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
       plan_slot[(size_t)h * n_f + j] = slot;
       plan_kind[(size_t)h * n_f + j] = kind;
       plan_cnt[(size_t)h * n_f + j] = cnt;
+      // a key that joined another key's group is no candidate of the next
+      // frame: the tensor-core NN reads this as "not a group"
+      if (invn && kind == KIND_MEMBER) invn[(size_t)h * ldn + j] = __int_as_float(0x7fc00000);
       if (isc) cand_next[(size_t)h * C + cp] = slot;
     }
     urank_base += tot & 0xffff;
@@ -518,10 +533,9 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
 }
 
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
-                 int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv,
-                 const int32_t* prev_slot, const int32_t* prev_kind, const float* invn_prev,
-                 float* invn_out, unsigned long long* best_out, const void* stage, float tau, int32_t* st,
-                 cudaStream_t s);
+                 int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv, int ldc,
+                 const int32_t* prev_slot, const float* invn_prev, float* invn_out, int ldn,
+                 unsigned long long* best_out, const void* stage, float tau, int32_t* st, cudaStream_t s);
 
 template <typename T, int D>
 static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
@@ -548,7 +562,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
   const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
   if (tc_nn) {
     fastar::launch_pdl((cand_norm_kernel), dim3((n_f + 8 * kNormCands - 1) / (8 * kNormCands), H), wblock, 0, s, (const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
-                                              w.stage, n_f, st);
+                                              w.ldc, w.stage, n_f, st);
     FASTAR_LAUNCHED(s, "cand_norm");
   }
   for (int fi = 0; fi < F; ++fi) {
@@ -560,7 +574,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     int rc = FASTAR_ERR_UNSUPPORTED;
     if (tc_nn)
       rc = launch_nn_tc(FASTAR_BF16, k_new, n_f, Nrow, H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.cinv,
-                        w.plan_slot, w.plan_kind, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.best, w.stage,
+                        w.ldc, w.plan_slot, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.ldn, w.best, w.stage,
                         tau, st, s);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       fastar::launch_pdl((nn_simt_kernel<T, D>), wgrid, wblock, 0, s, kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
@@ -571,7 +585,8 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     }
     fastar::launch_pdl((plan_kernel), H, kPlanThreads, plan_smem, s, n_f, C, f, tau, lg_tab, w.best, match_out,
                        fi * n_f, Nrow, w.match, w.cand[nxt], w.ncand[nxt], w.plan_slot, w.plan_kind, w.plan_cnt,
-                       w.evict, c->last_frame, c->m, c->size, c->inserted, c->evicted, st);
+                       w.evict, c->last_frame, c->m, c->size, c->inserted, c->evicted,
+                       tc_nn ? w.invn[fi & 1] : nullptr, w.ldn, st);
     FASTAR_LAUNCHED(s, "plan");
     fastar::launch_pdl((apply_kernel<T, D>), dim3((n_f + 8 * kApplyKeys - 1) / (8 * kApplyKeys), H), wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
                                                 w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m,
