@@ -126,6 +126,34 @@ int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D,
                 int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * fastar_hash_many -- the same codes (and optional bucket CSR) for up to
+ * FASTAR_MAX_HASH_JOBS inputs that share H, D, the hyperplanes, T and B, in
+ * one pass: the result equals one fastar_hash call per job, in job order.
+ * The chunk path hashes its queries, new keys and prompt keys this way (the
+ * hash is computed once and serves all three modules; same passages as
+ * fastar_hash).
+ *
+ * jobs    host array of n_jobs entries (1 <= n_jobs <= FASTAR_MAX_HASH_JOBS),
+ *         read during the call only; job j: x [H][N][D] dt, codes
+ *         [H][T][N], optional perm / offsets as for fastar_hash.  A job with
+ *         N == 0 is skipped.
+ * Errors as for fastar_hash; FASTAR_ERR_ARG for a bad n_jobs or job.
+ */
+#define FASTAR_MAX_HASH_JOBS 4
+typedef struct fastar_hash_job {
+  const void* x;
+  int N;
+  uint32_t* codes;
+  int32_t* perm;
+  int32_t* offsets;
+} fastar_hash_job;
+
+int fastar_hash_many(fastar_dtype dt, int n_jobs, const fastar_hash_job* jobs,
+                     int H, int D, const void* planes, int T, int B,
+                     void* ws, size_t ws_bytes, int32_t* dev_status,
+                     cudaStream_t stream);
+
+/*
  * The merged cache of one layer: fixed capacity C per head, all buffers
  * caller-owned device memory, allocated once.  Initialise last_frame to -1
  * and every other buffer to 0.  Checkpointing the cache means copying

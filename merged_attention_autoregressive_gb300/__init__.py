@@ -24,7 +24,7 @@ STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "
           18: "FASTAR_ERR_DEVICE_ARG"}
 EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
-           "fastar_workspace_size", "fastar_hash",
+           "fastar_workspace_size", "fastar_hash", "fastar_hash_many",
            "fastar_tempcache_merge", "fastar_annca_prune", "fastar_annca_attention",
            "fastar_annsa_attention"]
 
@@ -47,6 +47,12 @@ class CacheStruct(ctypes.Structure):
 
 _lib = None
 _VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+MAX_HASH_JOBS = 4
+
+
+class HashJob(ctypes.Structure):
+    """fastar_hash_job: one input of fastar_hash_many."""
+    _fields_ = [("x", _VP), ("N", _I), ("codes", _VP), ("perm", _VP), ("offsets", _VP)]
 
 
 def lib() -> ctypes.CDLL:
@@ -69,6 +75,8 @@ def lib() -> ctypes.CDLL:
         L.fastar_workspace_size.restype = _SZ
         L.fastar_workspace_size.argtypes = [_I] * 7
         L.fastar_hash.argtypes = [_I, _VP, _I, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_hash_many.argtypes = [_I, _I, ctypes.POINTER(HashJob), _I, _I, _VP, _I, _I, _VP, _SZ,
+                                       _VP, _VP]
         L.fastar_tempcache_merge.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
                                              ctypes.c_int32, _F, _VP, _VP, _SZ, _VP, _VP]
         L.fastar_annca_prune.argtypes = [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP, _VP]
@@ -163,6 +171,23 @@ def fastar_hash(x, planes, T, B, codes, perm=None, offsets=None, status=None, st
     H, N, D = x.shape
     _check(lib().fastar_hash(_dt(x), _p(x), H, N, D, _p(planes), T, B, _p(codes), _p(perm),
                              _p(offsets), None, 0, _p(status), _stream(stream)), "fastar_hash")
+
+
+def fastar_hash_many(jobs, planes, T, B, status=None, stream=None):
+    """One pass over up to MAX_HASH_JOBS inputs that share H and D.
+
+    jobs: list of (x [H][N][D], codes [H][T][N], perm or None, offsets or
+    None); the result equals one fastar_hash call per job."""
+    if not 1 <= len(jobs) <= MAX_HASH_JOBS:
+        raise ValueError(f"1 to {MAX_HASH_JOBS} jobs")
+    arr = (HashJob * len(jobs))()
+    H, _, D = jobs[0][0].shape
+    for j, (x, codes, perm, offsets) in enumerate(jobs):
+        if x.shape[0] != H or x.shape[2] != D or x.dtype != jobs[0][0].dtype:
+            raise ValueError("jobs must share H, D and the dtype")
+        arr[j] = HashJob(_p(x), x.shape[1], _p(codes), _p(perm), _p(offsets))
+    _check(lib().fastar_hash_many(_dt(jobs[0][0]), len(jobs), arr, H, D, _p(planes), T, B, None, 0,
+                                  _p(status), _stream(stream)), "fastar_hash_many")
 
 
 class Cache:

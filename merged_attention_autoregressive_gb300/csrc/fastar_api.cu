@@ -32,6 +32,8 @@ int launch_hash_simt(fastar_dtype dt, const void* x, int H, int N, int D, const 
                      int T, int B, uint32_t* codes, int32_t* st, cudaStream_t s);
 int launch_hash_tc(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes,
                    int T, int B, uint32_t* codes, int32_t* st, cudaStream_t s);
+int launch_hash_tc_many(fastar_dtype dt, int n, const void* const* xs, const int* Ns, uint32_t* const* codes,
+                        int H, int D, const void* planes, int T, int B, int32_t* st, cudaStream_t s);
 int launch_annca_simt(fastar_dtype dt, const void* q, const void* k_p, const void* v_p,
                       const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f, int P,
                       int D, float scale, void* out, int32_t* st, cudaStream_t s);
@@ -150,6 +152,46 @@ int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void*
   int rc = launch_hash(dt, x, H, N, D, planes, T, B, codes, dev_status, stream);
   if (rc != FASTAR_OK || !perm) return rc;
   return launch_csr(codes, H * T, N, nullptr, 1, 1 << B, perm, offsets, dev_status, stream);
+}
+
+int fastar_hash_many(fastar_dtype dt, int n_jobs, const fastar_hash_job* jobs, int H, int D,
+                     const void* planes, int T, int B, void* ws, size_t ws_bytes, int32_t* dev_status,
+                     cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
+  if (n_jobs < 1 || n_jobs > FASTAR_MAX_HASH_JOBS || !jobs) return FASTAR_ERR_ARG;
+  if (H < 0 || T < 1 || B < 1 || T > 8) return FASTAR_ERR_ARG;
+  if (!dim_ok(D) || T * B > kMaxTB) return FASTAR_ERR_UNSUPPORTED;
+  const void* xs[FASTAR_MAX_HASH_JOBS];
+  int Ns[FASTAR_MAX_HASH_JOBS];
+  uint32_t* cs[FASTAR_MAX_HASH_JOBS];
+  int n = 0;
+  for (int j = 0; j < n_jobs; ++j) {
+    const fastar_hash_job& q = jobs[j];
+    if (q.N < 0 || (q.perm == nullptr) != (q.offsets == nullptr)) return FASTAR_ERR_ARG;
+    if (q.perm && B > kMaxCsrBits) return FASTAR_ERR_UNSUPPORTED;
+    if ((size_t)H * q.N == 0) continue;
+    if (!q.x || !q.codes || !aligned16(q.x)) return FASTAR_ERR_ARG;
+    xs[n] = q.x;
+    Ns[n] = q.N;
+    cs[n] = q.codes;
+    ++n;
+  }
+  if (n == 0) return FASTAR_OK;
+  if (!planes || !aligned16(planes)) return FASTAR_ERR_ARG;
+  int rc = launch_hash_tc_many(dt, n, xs, Ns, cs, H, D, planes, T, B, dev_status, stream);
+  if (rc == FASTAR_ERR_UNSUPPORTED) {
+    rc = FASTAR_OK;
+    for (int j = 0; j < n && rc == FASTAR_OK; ++j)
+      rc = launch_hash(dt, xs[j], H, Ns[j], D, planes, T, B, cs[j], dev_status, stream);
+  }
+  for (int j = 0; j < n_jobs && rc == FASTAR_OK; ++j) {
+    const fastar_hash_job& q = jobs[j];
+    if (q.perm && (size_t)H * q.N > 0)
+      rc = launch_csr(q.codes, H * T, q.N, nullptr, 1, 1 << B, q.perm, q.offsets, dev_status, stream);
+  }
+  return rc;
 }
 
 static int check_cache(const fastar_cache* c) {

@@ -370,29 +370,33 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
       int best_slot = 0x7fffffff;
       for (int t = 0; t < s.tiles; ++t, ++g) {
         const int b = g % kAcc;
+        const int c = (s.ct0 + t) * kN + half * 32;  // this warp's first column
+        // the candidates' inverse norms are loaded before the wait, so that
+        // their latency overlaps it (NaN past the last candidate)
+        float mi[32];
+        if (c + 32 <= s.nc) {
+          const float4* m4 = reinterpret_cast<const float4*>(mrow + c);  // 16-byte aligned: ld % 4 == 0
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 ib = __ldg(m4 + i);
+            mi[4 * i] = ib.x;
+            mi[4 * i + 1] = ib.y;
+            mi[4 * i + 2] = ib.z;
+            mi[4 * i + 3] = ib.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mi[i] = c + i < s.nc ? __ldg(mrow + c + i) : __int_as_float(0x7fc00000);
+        }
         if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.tfull[b], (uint32_t)(g / kAcc) & 1u));
         if (!ok) continue;
         tc::tc_fence_after();
-        const int c = (s.ct0 + t) * kN + half * 32;  // this warp's first column
         if (c < s.nc) {
           float cs[32];
           tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + b * kN + half * 32, cs);
           // cs = dot * inverse candidate norm, in place (NaN: not a group)
-          if (c + 32 <= s.nc) {
-            const float4* m4 = reinterpret_cast<const float4*>(mrow + c);  // 16-byte aligned: ld % 4 == 0
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 ib = __ldg(m4 + i);
-              cs[4 * i] *= ib.x;
-              cs[4 * i + 1] *= ib.y;
-              cs[4 * i + 2] *= ib.z;
-              cs[4 * i + 3] *= ib.w;
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              cs[i] = c + i < s.nc ? cs[i] * __ldg(mrow + c + i) : __int_as_float(0x7fc00000);
-          }
+          for (int i = 0; i < 32; ++i) cs[i] *= mi[i];
           // phase 1: the tile's largest cosine (NaN columns are ignored);
           // four independent chains keep the dependency depth short
           float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};

@@ -12,7 +12,7 @@ from __future__ import annotations
 import torch
 
 from . import (Cache, OP_ANNCA, OP_ANNSA, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
-               fastar_annsa_attention, fastar_hash, fastar_tempcache_merge,
+               fastar_annsa_attention, fastar_hash, fastar_hash_many, fastar_tempcache_merge,
                fastar_workspace_size)
 
 
@@ -47,6 +47,11 @@ class ChunkPath:
                                     dtype=torch.uint8, device=dev)
         self.ws_annca = torch.empty(max(1, fastar_workspace_size(OP_ANNCA, H, F, D, T, B, P)),
                                     dtype=torch.uint8, device=dev)
+        # the cross-attention branch's stream and the two events that fork
+        # and join it
+        self._side = torch.cuda.Stream(device=dev)
+        self._hashed = torch.cuda.Event()
+        self._cross_done = torch.cuda.Event()
 
     # -- pieces -----------------------------------------------------------
     def merge(self, k, v, first_frame, F=None, stream=None):
@@ -68,20 +73,30 @@ class ChunkPath:
         return codes, match
 
     def step(self, q, k, v, kp, vp, first_frame, stream=None):
-        """The whole path for one chunk: q, k, v [H][F*n_f][D]; kp, vp [H][P][D]."""
+        """The whole path for one chunk: q, k, v [H][F*n_f][D]; kp, vp [H][P][D].
+
+        The cross-attention branch (prune, AnnCA) needs only the codes, not
+        the merged cache, so it runs on a second stream while the merge runs;
+        `stream` (default: the current stream) waits for both branches before
+        this returns, so later work on it sees every output."""
         st = self.status
-        fastar_hash(q, self.planes, self.T, self.B, self.q_codes, self.q_perm, self.q_offsets,
-                    status=st, stream=stream)
-        fastar_hash(k, self.planes, self.T, self.B, self.k_codes, status=st, stream=stream)
+        main = torch.cuda.current_stream() if stream is None else (
+            stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream)))
+        jobs = [(q, self.q_codes, self.q_perm, self.q_offsets), (k, self.k_codes, None, None)]
         if self.P:
-            fastar_hash(kp, self.planes, self.T, self.B, self.p_codes, status=st, stream=stream)
+            jobs.append((kp, self.p_codes, None, None))
+        fastar_hash_many(jobs, self.planes, self.T, self.B, status=st, stream=main)
+        self._hashed.record(main)
+        self._side.wait_event(self._hashed)
+        fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
+                           self.kept_idx, self.kept_cnt, status=st, stream=self._side)
+        fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
+                               self.scale, self.o_ca, ws=self.ws_annca, status=st, stream=self._side)
+        self._cross_done.record(self._side)
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
-                               stream=stream)
-        fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
-                           self.kept_idx, self.kept_cnt, status=st, stream=stream)
-        fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
-                               self.scale, self.o_ca, ws=self.ws_annca, status=st, stream=stream)
+                               stream=main)
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
-                               stream=stream)
+                               stream=main)
+        main.wait_event(self._cross_done)

@@ -86,6 +86,25 @@ def test_host_argument_errors_need_no_gpu(L):
     for bad in (0.0, -0.1, float("inf"), float("nan")):
         assert L.fastar_annca_attention(0, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
                                         ctypes.c_float(bad), fake, None, 0, None, None) == 1
+    # batched hash: job count, job arguments, head dim
+    import merged_attention_autoregressive_gb300 as m
+    jobs = (m.HashJob * 5)()
+    for j in range(5):
+        jobs[j] = m.HashJob(fake, 8, fake, None, None)
+    L.fastar_hash_many.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(m.HashJob)] + \
+        [ctypes.c_int] * 2 + [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                              ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.fastar_hash_many(0, 0, jobs, 1, 128, fake, 1, 4, None, 0, None, None) == 1
+    assert L.fastar_hash_many(0, 5, jobs, 1, 128, fake, 1, 4, None, 0, None, None) == 1
+    assert L.fastar_hash_many(0, 2, None, 1, 128, fake, 1, 4, None, 0, None, None) == 1
+    assert L.fastar_hash_many(0, 2, jobs, 1, 96, fake, 1, 4, None, 0, None, None) == 2
+    jobs[1] = m.HashJob(fake, 8, fake, fake, None)  # perm without offsets
+    assert L.fastar_hash_many(0, 2, jobs, 1, 128, fake, 1, 4, None, 0, None, None) == 1
+    jobs[1] = m.HashJob(vp(0x1004), 8, fake, None, None)  # misaligned rows
+    assert L.fastar_hash_many(0, 2, jobs, 1, 128, fake, 1, 4, None, 0, None, None) == 1
+    for j in range(2):
+        jobs[j] = m.HashJob(None, 0, None, None, None)  # nothing to hash: OK, no device work
+    assert L.fastar_hash_many(0, 2, jobs, 1, 128, None, 1, 4, None, 0, None, None) == 0
     # attention: the bf16 tensor-core path compacts the kept rows into ws
     assert L.fastar_annca_attention(0, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
                                     ctypes.c_float(0.1), fake, None, 0, None, None) == 4

@@ -193,3 +193,35 @@ def test_empty_sets_give_zero_output():
     assert (host(path.o_sa)[:, ::2] == 0).all()
     assert np.isneginf(host(path.lse)[:, ::2]).all()
     check_att(path.o_sa, o_sa, "AnnSA crafted", rep)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_hash_many_equals_single_calls(dtype):
+    """One batched hash pass gives exactly the codes and bucket CSR of one
+    fastar_hash call per input (ragged row counts, an empty input, several
+    128-row tiles and a partial last tile; bf16 uses the tensor-core kernel,
+    fp32 the per-input fallback)."""
+    from merged_attention_autoregressive_gb300 import fastar_hash, fastar_hash_many
+    g = torch.Generator().manual_seed(7)
+    H, D, T, B = 3, 128, 2, 8
+    planes = torch.randn(T * B, D, generator=g).to(dtype).cuda()
+    Ns = [517, 100, 0, 64]
+    xs = [torch.randn(H, n, D, generator=g).to(dtype).cuda() for n in Ns]
+    i32 = dict(dtype=torch.int32, device="cuda")
+    many = [torch.full((H, T, max(n, 1)), -1, **i32) for n in Ns]
+    perm = torch.full((H, T, Ns[0]), -1, **i32)
+    offs = torch.full((H, T, (1 << B) + 1), -1, **i32)
+    jobs = [(xs[0], many[0], perm, offs)] + [(xs[j], many[j][:, :, :Ns[j]], None, None)
+                                             for j in range(1, len(Ns))]
+    fastar_hash_many(jobs, planes, T, B)
+    for j, n in enumerate(Ns):
+        if n == 0:
+            continue
+        one = torch.full((H, T, n), -1, **i32)
+        p1 = torch.full((H, T, n), -1, **i32) if j == 0 else None
+        o1 = torch.full((H, T, (1 << B) + 1), -1, **i32) if j == 0 else None
+        fastar_hash(xs[j], planes, T, B, one, p1, o1)
+        torch.cuda.synchronize()
+        assert torch.equal(many[j][:, :, :n].cpu(), one.cpu()), f"job {j} codes"
+        if j == 0:
+            assert torch.equal(perm.cpu(), p1.cpu()) and torch.equal(offs.cpu(), o1.cpu())
