@@ -126,6 +126,20 @@ int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D,
                 int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * fastar_bucket_csr -- the bucket CSR of fastar_hash (perm / offsets) for
+ * codes that are already there: per group g (a head and table), a stable
+ * counting sort of the ids 0..N-1 by code.  Same passage as fastar_hash (the
+ * buckets of each LSH table).
+ *
+ * codes   [G][N] uint32, every value < 2^B (FASTAR_ERR_DEVICE_ARG otherwise)
+ * perm    [G][N] int32   ids grouped by code, ascending id inside a bucket
+ * offsets [G][2^B+1] int32 offsets[c] = number of ids whose code is < c
+ * Limits: B <= 12.
+ */
+int fastar_bucket_csr(const uint32_t* codes, int G, int N, int B, int32_t* perm,
+                      int32_t* offsets, int32_t* dev_status, cudaStream_t stream);
+
+/*
  * fastar_hash_many -- the same codes (and optional bucket CSR) for up to
  * FASTAR_MAX_HASH_JOBS inputs that share H, D, the hyperplanes, T and B, in
  * one pass: the result equals one fastar_hash call per job, in job order.

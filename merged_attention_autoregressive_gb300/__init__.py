@@ -24,7 +24,7 @@ STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "
           18: "FASTAR_ERR_DEVICE_ARG"}
 EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
-           "fastar_workspace_size", "fastar_hash", "fastar_hash_many",
+           "fastar_workspace_size", "fastar_hash", "fastar_hash_many", "fastar_bucket_csr",
            "fastar_tempcache_merge", "fastar_annca_prune", "fastar_annca_attention",
            "fastar_annsa_attention"]
 
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
         L.fastar_workspace_size.restype = _SZ
         L.fastar_workspace_size.argtypes = [_I] * 7
         L.fastar_hash.argtypes = [_I, _VP, _I, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_bucket_csr.argtypes = [_VP, _I, _I, _I, _VP, _VP, _VP, _VP]
         L.fastar_hash_many.argtypes = [_I, _I, ctypes.POINTER(HashJob), _I, _I, _VP, _I, _I, _VP, _SZ,
                                        _VP, _VP]
         L.fastar_tempcache_merge.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
@@ -171,6 +172,14 @@ def fastar_hash(x, planes, T, B, codes, perm=None, offsets=None, status=None, st
     H, N, D = x.shape
     _check(lib().fastar_hash(_dt(x), _p(x), H, N, D, _p(planes), T, B, _p(codes), _p(perm),
                              _p(offsets), None, 0, _p(status), _stream(stream)), "fastar_hash")
+
+
+def fastar_bucket_csr(codes, B, perm, offsets, status=None, stream=None):
+    """perm / offsets of codes [..., N] (leading dims flattened into groups)."""
+    N = codes.shape[-1]
+    G = codes.numel() // max(N, 1)
+    _check(lib().fastar_bucket_csr(_p(codes), G, N, B, _p(perm), _p(offsets), _p(status),
+                                   _stream(stream)), "fastar_bucket_csr")
 
 
 def fastar_hash_many(jobs, planes, T, B, status=None, stream=None):

@@ -20,6 +20,11 @@ constexpr int kCsrThreads = 1024;
 // cnt holds the (warp, bucket) counts bucket-major with a padded row of W+1
 // entries per bucket: warp w's lanes, which hit different buckets, land in
 // different banks, and the (bucket, warp) scan order is contiguous.
+// Codes a warp holds in registers for passes 1 and 3: up to kCsrRegs per
+// lane (segments of up to 32 * kCsrRegs ids); longer segments are read
+// again from global memory in pass 3.
+constexpr int kCsrRegs = 8;
+
 __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __restrict__ keys, int N,
                                                           const int32_t* __restrict__ n_dev, int n_div,
                                                           int nb, int lgW, int32_t* __restrict__ perm,
@@ -38,12 +43,27 @@ __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __rest
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   for (int i = threadIdx.x; i < nb * SW; i += blockDim.x) cnt[i] = 0;
-  __syncthreads();
   const int seg = (n + W - 1) >> lgW;
   const int beg = min(n, warp * seg), end = min(n, beg + seg);
+  // the warp's first 32 * kCsrRegs codes, all loads in flight together
+  uint32_t reg[kCsrRegs];
+#pragma unroll
+  for (int r = 0; r < kCsrRegs; ++r) {
+    const int i = beg + r * 32 + lane;
+    reg[r] = (warp < W && i < end) ? __ldg(kg + i) : 0xffffffffu;
+  }
+  __syncthreads();
   bool bad = false;
   if (warp < W) {
-    for (int i = beg + lane; i < end; i += 32) {
+#pragma unroll
+    for (int r = 0; r < kCsrRegs; ++r) {
+      const int i = beg + r * 32 + lane;
+      if (i >= end) continue;
+      const uint32_t c = reg[r];
+      if (c >= (uint32_t)nb) { bad = true; continue; }
+      atomicAdd(&cnt[c * SW + warp], 1);
+    }
+    for (int i = beg + 32 * kCsrRegs + lane; i < end; i += 32) {
       const uint32_t c = __ldg(kg + i);
       if (c >= (uint32_t)nb) { bad = true; continue; }
       atomicAdd(&cnt[c * SW + warp], 1);
@@ -69,12 +89,11 @@ __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __rest
   __syncthreads();
   for (int c = threadIdx.x; c < nb; c += blockDim.x) og[c] = cnt[c * SW];  // warp 0 base of bucket c
   if (threadIdx.x == 0) og[nb] = n;
-  // stable scatter
+  // stable scatter, 32 ids of the segment at a time in id order
   if (warp < W) {
-    for (int base = beg; base < end; base += 32) {
-      const int i = base + lane;
+    auto place = [&](int i, uint32_t c) {
       const bool valid = i < end;
-      const uint32_t c = valid ? __ldg(kg + i) : 0xffffffffu;
+      if (!valid) c = 0xffffffffu;
       const unsigned peers = __match_any_sync(0xffffffffu, c);
       const int rank = __popc(peers & lanemask_lt());
       int pos = 0;
@@ -85,6 +104,13 @@ __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __rest
         if (rank == 0) cnt[c * SW + warp] += __popc(peers);
       }
       __syncwarp();
+    };
+#pragma unroll
+    for (int r = 0; r < kCsrRegs; ++r)
+      if (beg + r * 32 < end) place(beg + r * 32 + lane, reg[r]);
+    for (int base = beg + 32 * kCsrRegs; base < end; base += 32) {
+      const int i = base + lane;
+      place(i, i < end ? __ldg(kg + i) : 0xffffffffu);
     }
   }
   pdl_trigger();

@@ -154,6 +154,15 @@ int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void*
   return launch_csr(codes, H * T, N, nullptr, 1, 1 << B, perm, offsets, dev_status, stream);
 }
 
+int fastar_bucket_csr(const uint32_t* codes, int G, int N, int B, int32_t* perm, int32_t* offsets,
+                      int32_t* dev_status, cudaStream_t stream) {
+  if (G < 0 || N < 0 || B < 1) return FASTAR_ERR_ARG;
+  if (B > kMaxCsrBits) return FASTAR_ERR_UNSUPPORTED;
+  if ((size_t)G * N == 0) return FASTAR_OK;
+  if (!codes || !perm || !offsets) return FASTAR_ERR_ARG;
+  return launch_csr(codes, G, N, nullptr, 1, 1 << B, perm, offsets, dev_status, stream);
+}
+
 int fastar_hash_many(fastar_dtype dt, int n_jobs, const fastar_hash_job* jobs, int H, int D,
                      const void* planes, int T, int B, void* ws, size_t ws_bytes, int32_t* dev_status,
                      cudaStream_t stream) {

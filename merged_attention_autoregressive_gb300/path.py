@@ -12,7 +12,7 @@ from __future__ import annotations
 import torch
 
 from . import (Cache, OP_ANNCA, OP_ANNSA, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
-               fastar_annsa_attention, fastar_hash, fastar_hash_many, fastar_tempcache_merge,
+               fastar_annsa_attention, fastar_bucket_csr, fastar_hash, fastar_hash_many, fastar_tempcache_merge,
                fastar_workspace_size)
 
 
@@ -47,10 +47,11 @@ class ChunkPath:
                                     dtype=torch.uint8, device=dev)
         self.ws_annca = torch.empty(max(1, fastar_workspace_size(OP_ANNCA, H, F, D, T, B, P)),
                                     dtype=torch.uint8, device=dev)
-        # the cross-attention branch's stream and the two events that fork
-        # and join it
+        # the second stream (query CSR, cross-attention branch) and the
+        # events that fork and join it
         self._side = torch.cuda.Stream(device=dev)
         self._hashed = torch.cuda.Event()
+        self._csr_done = torch.cuda.Event()
         self._cross_done = torch.cuda.Event()
 
     # -- pieces -----------------------------------------------------------
@@ -75,19 +76,23 @@ class ChunkPath:
     def step(self, q, k, v, kp, vp, first_frame, stream=None):
         """The whole path for one chunk: q, k, v [H][F*n_f][D]; kp, vp [H][P][D].
 
-        The cross-attention branch (prune, AnnCA) needs only the codes, not
-        the merged cache, so it runs on a second stream while the merge runs;
-        `stream` (default: the current stream) waits for both branches before
-        this returns, so later work on it sees every output."""
+        The query buckets' CSR and the cross-attention branch (prune, AnnCA)
+        need only the codes, not the merged cache, so they run on a second
+        stream while the merge runs; AnnSA waits for the CSR, and `stream`
+        (default: the current stream) waits for both branches before this
+        returns, so later work on it sees every output."""
         st = self.status
         main = torch.cuda.current_stream() if stream is None else (
             stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream)))
-        jobs = [(q, self.q_codes, self.q_perm, self.q_offsets), (k, self.k_codes, None, None)]
+        jobs = [(q, self.q_codes, None, None), (k, self.k_codes, None, None)]
         if self.P:
             jobs.append((kp, self.p_codes, None, None))
         fastar_hash_many(jobs, self.planes, self.T, self.B, status=st, stream=main)
         self._hashed.record(main)
         self._side.wait_event(self._hashed)
+        fastar_bucket_csr(self.q_codes, self.B, self.q_perm, self.q_offsets, status=st,
+                          stream=self._side)
+        self._csr_done.record(self._side)
         fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
                            self.kept_idx, self.kept_cnt, status=st, stream=self._side)
         fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
@@ -96,6 +101,7 @@ class ChunkPath:
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
                                stream=main)
+        main.wait_event(self._csr_done)
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
                                stream=main)

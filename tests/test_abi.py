@@ -105,6 +105,14 @@ def test_host_argument_errors_need_no_gpu(L):
     for j in range(2):
         jobs[j] = m.HashJob(None, 0, None, None, None)  # nothing to hash: OK, no device work
     assert L.fastar_hash_many(0, 2, jobs, 1, 128, None, 1, 4, None, 0, None, None) == 0
+    # bucket CSR: sizes, bits, pointers
+    L.fastar_bucket_csr.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.fastar_bucket_csr(fake, -1, 8, 4, fake, fake, None, None) == 1
+    assert L.fastar_bucket_csr(fake, 2, 8, 13, fake, fake, None, None) == 2
+    assert L.fastar_bucket_csr(None, 2, 8, 4, fake, fake, None, None) == 1
+    assert L.fastar_bucket_csr(fake, 2, 8, 4, fake, None, None, None) == 1
+    assert L.fastar_bucket_csr(None, 0, 8, 4, None, None, None, None) == 0
     # attention: the bf16 tensor-core path compacts the kept rows into ws
     assert L.fastar_annca_attention(0, fake, fake, fake, fake, fake, 1, 1, 4, 4, 128,
                                     ctypes.c_float(0.1), fake, None, 0, None, None) == 4
