@@ -488,11 +488,9 @@ def run_ours(args, cfg):
         prep()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
-        for dst, src in ((q, hq), (k, hk), (v, hv), (kp, hkp), (vp, hvp)):
-            dst.copy_(src, non_blocking=True)
-        chunk()
-        ho_ca.copy_(path.o_ca, non_blocking=True)
-        ho_sa.copy_(path.o_sa, non_blocking=True)
+        # the public host-to-host chunk: copies in per branch, outputs copied
+        # out as soon as they are final, all inside the timed region
+        path.step_host(hq, hk, hv, hkp, hvp, ho_ca, ho_sa, first)
         s1.record(stream)
         torch.cuda.synchronize()
         if i >= 3:

@@ -52,6 +52,15 @@ class ChunkPath:
         self._side = torch.cuda.Stream(device=dev)
         self._hashed = torch.cuda.Event()
         self._csr_done = torch.cuda.Event()
+        # host-to-host chunks: device copies of the inputs, their copy stream
+        # and the events that release each branch
+        self._dev_in = None
+        self._copy_in = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+        self._in_free = torch.cuda.Event()
+        self._in_k = torch.cuda.Event()
+        self._in_v = torch.cuda.Event()
+        self._in_qp = torch.cuda.Event()
+        self._in_vp = torch.cuda.Event()
         self._cross_done = torch.cuda.Event()
 
     # -- pieces -----------------------------------------------------------
@@ -81,23 +90,84 @@ class ChunkPath:
         stream while the merge runs; AnnSA waits for the CSR, and `stream`
         (default: the current stream) waits for both branches before this
         returns, so later work on it sees every output."""
+        self._run(q, k, v, kp, vp, first_frame, self._main(stream))
+
+    def step_host(self, hq, hk, hv, hkp, hvp, ho_ca, ho_sa, first_frame, stream=None):
+        """The chunk from host memory to host memory (pinned tensors, same
+        shapes as step's; ho_ca, ho_sa receive o_ca and o_sa).
+
+        The inputs are copied in on two copy streams in the order the
+        branches need them (k then v for the merge branch; q, the prompt
+        keys and the prompt values for the cross-attention branch, which
+        also builds the query CSR that AnnSA needs), each branch hashes and
+        starts as soon as its inputs have landed, and each output is copied
+        out as soon as it is final.  `stream` (default: the current stream)
+        waits for all of it, so the host buffers are complete once it has
+        synchronised."""
+        main = self._main(stream)
+        dev = self.q_codes.device
+        if self._dev_in is None or self._dev_in[0].shape != hq.shape or self._dev_in[3].shape != hkp.shape:
+            self._dev_in = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq, hk, hv, hkp, hvp)]
+        dq, dk, dv, dkp, dvp = self._dev_in
+        # the staging buffers are free once the previous work on `main` is
+        self._in_free.record(main)
+        cm, cx = self._copy_in
+        for c in (cm, cx):
+            c.wait_event(self._in_free)
+        with torch.cuda.stream(cm):
+            dk.copy_(hk, non_blocking=True)
+            self._in_k.record(cm)
+            dv.copy_(hv, non_blocking=True)
+            self._in_v.record(cm)
+        with torch.cuda.stream(cx):
+            dq.copy_(hq, non_blocking=True)
+            dkp.copy_(hkp, non_blocking=True)
+            self._in_qp.record(cx)
+            dvp.copy_(hvp, non_blocking=True)
+            self._in_vp.record(cx)
+        self._run(dq, dk, dv, dkp, dvp, first_frame, main, host_out=(ho_ca, ho_sa))
+
+    # -- internals ----------------------------------------------------------
+    @staticmethod
+    def _main(stream):
+        if stream is None:
+            return torch.cuda.current_stream()
+        return stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream))
+
+    def _run(self, q, k, v, kp, vp, first_frame, main, host_out=None):
         st = self.status
-        main = torch.cuda.current_stream() if stream is None else (
-            stream if isinstance(stream, torch.cuda.Stream) else torch.cuda.ExternalStream(int(stream)))
-        jobs = [(q, self.q_codes, None, None), (k, self.k_codes, None, None)]
+        staged = host_out is not None
+        side = self._side
+        cross = [(q, self.q_codes, None, None)]
         if self.P:
-            jobs.append((kp, self.p_codes, None, None))
-        fastar_hash_many(jobs, self.planes, self.T, self.B, status=st, stream=main)
-        self._hashed.record(main)
-        self._side.wait_event(self._hashed)
-        fastar_bucket_csr(self.q_codes, self.B, self.q_perm, self.q_offsets, status=st,
-                          stream=self._side)
-        self._csr_done.record(self._side)
+            cross.append((kp, self.p_codes, None, None))
+        if staged:
+            # each branch hashes its own inputs once they have landed
+            main.wait_event(self._in_k)
+            fastar_hash_many([(k, self.k_codes, None, None)], self.planes, self.T, self.B, status=st,
+                             stream=main)
+            side.wait_event(self._in_qp)
+            fastar_hash_many(cross, self.planes, self.T, self.B, status=st, stream=side)
+        else:
+            # one pass over every input
+            fastar_hash_many([(k, self.k_codes, None, None)] + cross, self.planes, self.T, self.B,
+                             status=st, stream=main)
+            self._hashed.record(main)
+            side.wait_event(self._hashed)
+        fastar_bucket_csr(self.q_codes, self.B, self.q_perm, self.q_offsets, status=st, stream=side)
+        self._csr_done.record(side)
         fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
-                           self.kept_idx, self.kept_cnt, status=st, stream=self._side)
+                           self.kept_idx, self.kept_cnt, status=st, stream=side)
+        if staged:
+            side.wait_event(self._in_vp)
         fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
-                               self.scale, self.o_ca, ws=self.ws_annca, status=st, stream=self._side)
-        self._cross_done.record(self._side)
+                               self.scale, self.o_ca, ws=self.ws_annca, status=st, stream=side)
+        if staged:
+            with torch.cuda.stream(side):
+                host_out[0].copy_(self.o_ca, non_blocking=True)
+        self._cross_done.record(side)
+        if staged:
+            main.wait_event(self._in_v)
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
                                stream=main)
@@ -105,4 +175,7 @@ class ChunkPath:
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
                                stream=main)
+        if staged:
+            with torch.cuda.stream(main):
+                host_out[1].copy_(self.o_sa, non_blocking=True)
         main.wait_event(self._cross_done)

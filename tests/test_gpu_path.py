@@ -225,3 +225,28 @@ def test_hash_many_equals_single_calls(dtype):
         assert torch.equal(many[j][:, :, :n].cpu(), one.cpu()), f"job {j} codes"
         if j == 0:
             assert torch.equal(perm.cpu(), p1.cpu()) and torch.equal(offs.cpu(), o1.cpu())
+
+
+def test_step_host_matches_step():
+    """The host-to-host chunk (inputs copied in per branch, outputs copied
+    out as soon as they are final) gives exactly what the device chunk
+    gives: same kernels, only the copies and the stream order differ."""
+    cfg = CONFIGS[0].replace(dtype="bf16", n_f=197, F=2, past_frames=5, P=77, T=3, B=7, C=700,
+                             D=128, H=3, redraw=0.3)
+    d = layer_data(cfg)
+    paths = [_path(cfg), _path(cfg)]
+    for p in paths:
+        p.planes.copy_(dev(d.planes, cfg.dtype))
+        build_cache(cfg, d, p, Report(), check=False)
+    a, b = paths
+    ins = [dev(x, cfg.dtype) for x in (d.chunk_q[0], d.chunk_k[0], d.chunk_v[0], d.prompt_k, d.prompt_v)]
+    first = cfg.past_frames
+    a.step(*ins, first)
+    hs = [x.cpu().pin_memory() for x in ins]
+    ho_ca = torch.empty(b.o_ca.shape, dtype=b.o_ca.dtype).pin_memory()
+    ho_sa = torch.empty(b.o_sa.shape, dtype=b.o_sa.dtype).pin_memory()
+    b.step_host(*hs, ho_ca, ho_sa, first)
+    torch.cuda.synchronize()
+    assert int(a.status.item()) == 0 and int(b.status.item()) == 0
+    assert torch.equal(ho_ca, a.o_ca.cpu()) and torch.equal(ho_sa, a.o_sa.cpu())
+    assert torch.equal(a.cache.K.cpu(), b.cache.K.cpu()) and torch.equal(a.match.cpu(), b.match.cpu())
