@@ -286,7 +286,8 @@ def algorithmic(cfg, path, match, snap_size, snap_lf):
         "annca_compact": {"flops": 0, "bytes": 2 * kept * D * e + 2 * kept_tiles * 64 * D * e
                           + (kept + H * F) * 4},
         "annsa_combine": {"flops": 0, "bytes": T * H * Nq * (D * 4 + 8) + H * Nq * (D * e + 4)},
-        "hash_tc": {"flops": 2 * rows * T * cfg.B * D / 3, "bytes": (rows * (D * e + T * 4)) / 3},
+        # one launch for the queries, the new keys and the prompt keys
+        "hash_tc": {"flops": 2 * rows * T * cfg.B * D, "bytes": rows * (D * e + T * 4)},
         "apply": {"flops": 0, "bytes": by["merge"] / F * 0.5},
     }
     return by, fl, kern, {"n_live": n_live, "kept": kept, "allowed_pairs": pairs,
