@@ -233,6 +233,24 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
                            int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * fastar_tempcache_merge_ev -- fastar_tempcache_merge whose codes_new (and
+ * v_new) may still be in the making when the call is issued: codes_ready
+ * (an event recorded after the work that writes them, typically on another
+ * stream; NULL: none) is waited on by `stream` right before the first
+ * kernel that reads codes_new or v_new.  The candidate setup, the first
+ * frame's nearest-neighbour search and its plan, which read only k_new and
+ * the cache, run before that wait, so a caller can hash the chunk on
+ * another stream meanwhile.  k_new must be ready on `stream` as usual.
+ * Same arguments, results and errors otherwise.
+ */
+int fastar_tempcache_merge_ev(const fastar_cache* cache, const void* k_new,
+                              const void* v_new, const uint32_t* codes_new,
+                              int F, int n_f, int32_t first_frame, float tau,
+                              int32_t* match_out, void* ws, size_t ws_bytes,
+                              int32_t* dev_status, cudaStream_t stream,
+                              cudaEvent_t codes_ready);
+
+/*
  * fastar_tempcache_merge_noalloc -- fastar_tempcache_merge without a
  * caller workspace.  The paper has no counterpart: this is a convenience of
  * this library for callers that cannot allocate device memory, such as a

@@ -25,7 +25,7 @@ STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "
 EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
            "fastar_workspace_size", "fastar_hash", "fastar_hash_many", "fastar_bucket_csr",
-           "fastar_tempcache_merge", "fastar_annca_prune", "fastar_annca_attention",
+           "fastar_tempcache_merge", "fastar_tempcache_merge_ev", "fastar_annca_prune", "fastar_annca_attention",
            "fastar_annsa_attention"]
 
 
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
                                        _VP, _VP]
         L.fastar_tempcache_merge.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
                                              ctypes.c_int32, _F, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_tempcache_merge_ev.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
+                                                ctypes.c_int32, _F, _VP, _VP, _SZ, _VP, _VP, _VP]
         L.fastar_annca_prune.argtypes = [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _SZ, _VP, _VP]
         L.fastar_annca_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F,
                                              _VP, _VP, _SZ, _VP, _VP]
@@ -235,13 +237,20 @@ class Cache:
 
 
 def fastar_tempcache_merge(cache: Cache, k_new, v_new, codes_new, F, n_f, first_frame, tau,
-                           match_out=None, ws=None, status=None, stream=None):
-    """Merge the F frames of a chunk (k_new/v_new [H][F*n_f][D]) into `cache`."""
+                           match_out=None, ws=None, status=None, stream=None, codes_ready=None):
+    """Merge the F frames of a chunk (k_new/v_new [H][F*n_f][D]) into `cache`.
+
+    codes_ready: a torch.cuda.Event after which codes_new and v_new are
+    final (fastar_tempcache_merge_ev); None: they are ready on `stream`."""
     ws, nbytes = _ws(OP_MERGE, cache.H, n_f, cache.D, cache.T, cache.B, cache.C, ws, k_new.device)
     cs = cache.struct()
-    _check(lib().fastar_tempcache_merge(ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F,
-                                        n_f, first_frame, tau, _p(match_out), _p(ws), nbytes,
-                                        _p(status), _stream(stream)), "fastar_tempcache_merge")
+    args = (ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F, n_f, first_frame, tau,
+            _p(match_out), _p(ws), nbytes, _p(status), _stream(stream))
+    if codes_ready is None:
+        _check(lib().fastar_tempcache_merge(*args), "fastar_tempcache_merge")
+    else:
+        _check(lib().fastar_tempcache_merge_ev(*args, codes_ready.cuda_event),
+               "fastar_tempcache_merge_ev")
 
 
 def fastar_annca_prune(q_codes, p_codes, F, n_f, B, kept_idx, kept_cnt, status=None, stream=None):

@@ -215,22 +215,45 @@ static int check_cache(const fastar_cache* c) {
   return FASTAR_OK;
 }
 
-int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const void* v_new,
-                           const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
-                           int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
-                           cudaStream_t stream) {
+static int merge_checked(const fastar_cache* cache, const void* k_new, const void* v_new,
+                         const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                         int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                         cudaStream_t stream, cudaEvent_t codes_ready) {
   int rc = check_cache(cache);
   if (rc != FASTAR_OK) return rc;
   if (F < 0 || n_f < 0 || n_f > cache->C) return FASTAR_ERR_ARG;
   if (n_f > FASTAR_MAX_FRAME_KEYS) return FASTAR_ERR_UNSUPPORTED;
-  if (F == 0 || n_f == 0 || cache->H == 0) return FASTAR_OK;
+  if (F == 0 || n_f == 0 || cache->H == 0) {
+    // nothing to merge; the caller's stream still follows the event
+    if (codes_ready && cudaStreamWaitEvent(stream, codes_ready, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FASTAR_ERR_CUDA;
+    }
+    return FASTAR_OK;
+  }
   if (!k_new || !v_new || !codes_new || !aligned16(k_new) || !aligned16(v_new)) return FASTAR_ERR_ARG;
   if (first_frame < 0 || (int64_t)first_frame + F > 0x7fffff00) return FASTAR_ERR_ARG;
   if (tau != tau) return FASTAR_ERR_ARG;
   const size_t need = merge_ws_bytes(cache->H, n_f, cache->C);
   if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
   return launch_merge(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws,
-                      dev_status, stream);
+                      dev_status, stream, codes_ready);
+}
+
+int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const void* v_new,
+                           const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                           int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                           cudaStream_t stream) {
+  return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
+                       dev_status, stream, nullptr);
+}
+
+int fastar_tempcache_merge_ev(const fastar_cache* cache, const void* k_new, const void* v_new,
+                              const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                              int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
+                              cudaStream_t stream, cudaEvent_t codes_ready) {
+  return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
+                       dev_status, stream, codes_ready);
 }
 
 int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,

@@ -540,7 +540,7 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
 template <typename T, int D>
 static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
                       const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
-                      int32_t* match_out, void* ws, int32_t* st, cudaStream_t s) {
+                      int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready) {
   const int H = c->H, C = c->C, Tt = c->T;
   MergeWs w = carve(ws, H, n_f, C);
   // the plan keeps one int per key of a frame and a hash table of the
@@ -588,6 +588,11 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
                        w.evict, c->last_frame, c->m, c->size, c->inserted, c->evicted,
                        tc_nn ? w.invn[fi & 1] : nullptr, w.ldn, st);
     FASTAR_LAUNCHED(s, "plan");
+    // the first kernel that reads codes_new (or v_new): wait for them here
+    if (fi == 0 && codes_ready && cudaStreamWaitEvent(s, codes_ready, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FASTAR_ERR_CUDA;
+    }
     fastar::launch_pdl((apply_kernel<T, D>), dim3((n_f + 8 * kApplyKeys - 1) / (8 * kApplyKeys), H), wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
                                                 w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m,
                                                 c->codes, c->last_frame, C, st);
@@ -598,15 +603,15 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
 
 int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
                  const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
-                 int32_t* match_out, void* ws, int32_t* st, cudaStream_t s) {
+                 int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready) {
   if (c->dt == FASTAR_F32 && c->D == 64)
-    return merge_impl<float, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+    return merge_impl<float, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
   if (c->dt == FASTAR_F32 && c->D == 128)
-    return merge_impl<float, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+    return merge_impl<float, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
   if (c->dt == FASTAR_BF16 && c->D == 64)
-    return merge_impl<__nv_bfloat16, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+    return merge_impl<__nv_bfloat16, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
   if (c->dt == FASTAR_BF16 && c->D == 128)
-    return merge_impl<__nv_bfloat16, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s);
+    return merge_impl<__nv_bfloat16, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
   return FASTAR_ERR_UNSUPPORTED;
 }
 

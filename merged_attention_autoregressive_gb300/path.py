@@ -50,7 +50,8 @@ class ChunkPath:
         # the second stream (query CSR, cross-attention branch) and the
         # events that fork and join it
         self._side = torch.cuda.Stream(device=dev)
-        self._hashed = torch.cuda.Event()
+        self._fork = torch.cuda.Event()
+        self._codes_ready = torch.cuda.Event()
         self._csr_done = torch.cuda.Event()
         # host-to-host chunks: device copies of the inputs, their copy stream
         # and the events that release each branch
@@ -85,9 +86,11 @@ class ChunkPath:
     def step(self, q, k, v, kp, vp, first_frame, stream=None):
         """The whole path for one chunk: q, k, v [H][F*n_f][D]; kp, vp [H][P][D].
 
-        The query buckets' CSR and the cross-attention branch (prune, AnnCA)
-        need only the codes, not the merged cache, so they run on a second
-        stream while the merge runs; AnnSA waits for the CSR, and `stream`
+        The second stream hashes the chunk while the merge starts (its first
+        NN search and plan need only the keys and the cache; it waits for
+        the key codes before its first apply), then builds the query CSR and
+        runs the cross-attention branch (prune, AnnCA), which needs the codes
+        but not the merged cache; AnnSA waits for the CSR, and `stream`
         (default: the current stream) waits for both branches before this
         returns, so later work on it sees every output."""
         self._run(q, k, v, kp, vp, first_frame, self._main(stream))
@@ -141,19 +144,25 @@ class ChunkPath:
         cross = [(q, self.q_codes, None, None)]
         if self.P:
             cross.append((kp, self.p_codes, None, None))
+        # The second stream hashes the chunk while the merge starts on `main`
+        # (candidate setup, the first frame's NN search and plan need only k
+        # and the cache); the merge waits for the key codes (and v) right
+        # before its first apply.
         if staged:
-            # each branch hashes its own inputs once they have landed
             main.wait_event(self._in_k)
+            side.wait_event(self._in_k)
             fastar_hash_many([(k, self.k_codes, None, None)], self.planes, self.T, self.B, status=st,
-                             stream=main)
+                             stream=side)
+            side.wait_event(self._in_v)
+            self._codes_ready.record(side)
             side.wait_event(self._in_qp)
             fastar_hash_many(cross, self.planes, self.T, self.B, status=st, stream=side)
         else:
-            # one pass over every input
+            self._fork.record(main)
+            side.wait_event(self._fork)
             fastar_hash_many([(k, self.k_codes, None, None)] + cross, self.planes, self.T, self.B,
-                             status=st, stream=main)
-            self._hashed.record(main)
-            side.wait_event(self._hashed)
+                             status=st, stream=side)
+            self._codes_ready.record(side)
         fastar_bucket_csr(self.q_codes, self.B, self.q_perm, self.q_offsets, status=st, stream=side)
         self._csr_done.record(side)
         fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
@@ -166,11 +175,9 @@ class ChunkPath:
             with torch.cuda.stream(side):
                 host_out[0].copy_(self.o_ca, non_blocking=True)
         self._cross_done.record(side)
-        if staged:
-            main.wait_event(self._in_v)
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
-                               stream=main)
+                               stream=main, codes_ready=self._codes_ready)
         main.wait_event(self._csr_done)
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,

@@ -118,6 +118,9 @@ def test_host_argument_errors_need_no_gpu(L):
                                     ctypes.c_float(0.1), fake, None, 0, None, None) == 4
     need = L.fastar_workspace_size(3, 1, 1, 128, 0, 0, 4)
     assert need >= 2 * 64 * 128 * 2
+    # merge with a codes-ready event: same argument checks
+    assert L.fastar_tempcache_merge_ev(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
+                                       None, 0, None, None, None) == 1
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
