@@ -367,7 +367,10 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
       // plan still decides.  The slot search below then only runs for tiles
       // holding such a candidate.
       float best = na2 > 0.f ? (a.tau - 1e-5f) * sqrtf(na2) : INFINITY;
-      int best_slot = 0x7fffffff;
+      // The best candidate's slot: best_slot, or (best_c >= 0) srow[best_c],
+      // read only when an exact tie needs it and once at the item's end, so
+      // that a new maximum costs no dependent load.
+      int best_slot = 0x7fffffff, best_c = -1;
       for (int t = 0; t < s.tiles; ++t, ++g) {
         const int b = g % kAcc;
         const int c = (s.ct0 + t) * kN + half * 32;  // this warp's first column
@@ -411,15 +414,24 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
 #pragma unroll
             for (int i = 0; i < 32; ++i) e4[i & 3] |= (cs[i] == tmax ? 1u : 0u) << i;
             uint32_t eq = (e4[0] | e4[1]) | (e4[2] | e4[3]);
-            int smin = 0x7fffffff;
-            const bool any = eq != 0u;
-            while (eq) {
-              smin = min(smin, __ldg(srow + c + __ffs(eq) - 1));
-              eq &= eq - 1u;
-            }
-            if (any && (tmax > best || smin < best_slot)) {
-              best = tmax;
-              best_slot = smin;
+            if (eq != 0u) {
+              if (tmax > best && (eq & (eq - 1u)) == 0u) {
+                // one column reaches a new maximum
+                best = tmax;
+                best_c = c + __ffs(eq) - 1;
+              } else {
+                // several equal columns, or equal to the current best: the
+                // lowest slot wins
+                int smin = 0x7fffffff;
+                while (eq) {
+                  smin = min(smin, __ldg(srow + c + __ffs(eq) - 1));
+                  eq &= eq - 1u;
+                }
+                const int cur = tmax > best ? 0x7fffffff : (best_c >= 0 ? __ldg(srow + best_c) : best_slot);
+                best = tmax;
+                best_slot = min(smin, cur);
+                best_c = -1;
+              }
             }
           }
         }
@@ -427,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.tempty[b]);
       }
+      if (best_c >= 0) best_slot = __ldg(srow + best_c);
       // merge the two column halves of each row, then publish the item's
       // best (the barrier after the reads keeps the next item's writes out)
       if (half == 1) {
