@@ -503,15 +503,21 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
 #pragma unroll
       for (int i = 0; i < PER; ++i) acc[i] = (float)m_old[u] * acc[i] + x[i];
       if (cnt[u] > 1) {
-        // the other members of the group, in ascending key order
+        // the other members of the group, in ascending key order: the warp
+        // tests 32 keys per step and adds the members it finds in order
         const int32_t* mt = match + (size_t)h * n_f;
         int left = cnt[u] - 1;
-        for (int jj = j + 1; jj < n_f && left > 0; ++jj) {
-          if (mt[jj] != s) continue;
-          ld_vec<T, PER>(v_frame + ((size_t)h * row_stride_keys + jj) * D + lane * PER, x);
+        for (int base = j + 1; base < n_f && left > 0; base += 32) {
+          const int jj = base + lane;
+          unsigned bits = __ballot_sync(0xffffffffu, jj < n_f && mt[jj] == s);
+          while (bits != 0u && left > 0) {
+            const int k = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            ld_vec<T, PER>(v_frame + ((size_t)h * row_stride_keys + base + k) * D + lane * PER, x);
 #pragma unroll
-          for (int i = 0; i < PER; ++i) acc[i] += x[i];
-          --left;
+            for (int i = 0; i < PER; ++i) acc[i] += x[i];
+            --left;
+          }
         }
       }
       const float mf = (float)m_new;
