@@ -15,7 +15,7 @@
 
 namespace fastar {
 
-constexpr int kCsrThreads = 1024;
+constexpr int kCsrThreads = 256;  // 8 warps
 
 // cnt holds the (warp, bucket) counts bucket-major with a padded row of W+1
 // entries per bucket: warp w's lanes, which hit different buckets, land in
@@ -23,7 +23,7 @@ constexpr int kCsrThreads = 1024;
 // Codes a warp holds in registers for passes 1 and 3: up to kCsrRegs per
 // lane (segments of up to 32 * kCsrRegs ids); longer segments are read
 // again from global memory in pass 3.
-constexpr int kCsrRegs = 8;
+constexpr int kCsrRegs = 24;
 
 __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __restrict__ keys, int N,
                                                           const int32_t* __restrict__ n_dev, int n_div,
@@ -120,7 +120,9 @@ int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_d
                int32_t* perm, int32_t* offsets, int32_t* st, cudaStream_t s) {
   if (G == 0) return FASTAR_OK;
   if (nb > (1 << kMaxCsrBits)) return FASTAR_ERR_UNSUPPORTED;
-  int lgW = 5;
+  // 8 warps per histogram: a (bucket, warp) scan of 8 nb entries; more warps
+  // would add scan work faster than they take counting and placing work
+  int lgW = 3;
   while (lgW > 0 && (size_t)((1 << lgW) + 1) * nb * sizeof(int) > 128 * 1024) --lgW;
   const size_t smem = (size_t)((1 << lgW) + 1) * nb * sizeof(int);
   if (smem > 48 * 1024 &&

@@ -456,12 +456,23 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
                                                     const int32_t* __restrict__ plan_cnt, T* K, T* V,
                                                     int32_t* m, uint32_t* codes, int32_t* last_frame,
                                                     int C, int32_t* st) {
-  pdl_wait();
   constexpr int PER = D / 32;
-  if (status_bad(st)) return;
   const int h = blockIdx.y;
   const int j0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kApplyKeys;
   const int lane = threadIdx.x & 31;
+  // the keys' k and v rows are inputs of the call (an earlier kernel of the
+  // call has already waited for their producers): load them before the wait
+  using Raw = typename VecOf<T, PER>::type;
+  Raw kv[kApplyKeys], vv[kApplyKeys], vo[kApplyKeys];
+#pragma unroll
+  for (int u = 0; u < kApplyKeys; ++u) {
+    if (j0 + u >= n_f) continue;
+    const size_t krow = ((size_t)h * row_stride_keys + j0 + u) * D + lane * PER;
+    kv[u] = ld_raw<T, PER>(k_frame + krow);
+    vv[u] = ld_raw<T, PER>(v_frame + krow);
+  }
+  pdl_wait();
+  if (status_bad(st)) return;
   int kind[kApplyKeys], slot[kApplyKeys], cnt[kApplyKeys], m_old[kApplyKeys];
 #pragma unroll
   for (int u = 0; u < kApplyKeys; ++u) {
@@ -475,15 +486,9 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
       cnt[u] = plan_cnt[(size_t)h * n_f + j];
     }
   }
-  using Raw = typename VecOf<T, PER>::type;
-  Raw kv[kApplyKeys], vv[kApplyKeys], vo[kApplyKeys];
 #pragma unroll
   for (int u = 0; u < kApplyKeys; ++u) {
     m_old[u] = 0;
-    if (kind[u] == KIND_MEMBER) continue;
-    const size_t krow = ((size_t)h * row_stride_keys + j0 + u) * D + lane * PER;
-    kv[u] = ld_raw<T, PER>(k_frame + krow);
-    vv[u] = ld_raw<T, PER>(v_frame + krow);
     if (kind[u] == KIND_LEADER) {
       m_old[u] = m[(size_t)h * C + slot[u]];
       vo[u] = ld_raw<T, PER>(V + ((size_t)h * C + slot[u]) * D + lane * PER);
