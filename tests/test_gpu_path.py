@@ -250,3 +250,45 @@ def test_step_host_matches_step():
     assert int(a.status.item()) == 0 and int(b.status.item()) == 0
     assert torch.equal(ho_ca, a.o_ca.cpu()) and torch.equal(ho_sa, a.o_sa.cpu())
     assert torch.equal(a.cache.K.cpu(), b.cache.K.cpu()) and torch.equal(a.match.cpu(), b.match.cpu())
+
+
+def _sample_rows(nq, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(nq, size=min(k, nq), replace=False))
+
+
+def test_14b_shapes_head_sample():
+    """configs[4] shapes (n_f 3600, Nq 10,800, 21 merged past frames, C 32,768,
+    T 2 x B 10) on a seeded sample of layers and heads: heads are independent,
+    so each sampled head's results equal its results inside the 40-head layer.
+    Every index output is checked in full; attention on sampled query rows."""
+    base = CONFIGS[4]
+    for layer, heads in ((0, [0, 29]), (1, [13])):
+        cfg = base.replace(H=len(heads))
+        d = layer_data(cfg, layer=layer, chunks=1, heads=heads)
+        path = _path(cfg)
+        path.planes.copy_(dev(d.planes, cfg.dtype))
+        rep = Report()
+        st = build_cache(cfg, d, path, rep)
+        run_chunk(cfg, d, path, st, rep, rows=_sample_rows(cfg.Nq, 192, layer))
+        print("layer", layer, "heads", heads, "report", rep)
+
+
+def test_rollout_head_sample():
+    """configs[2] shapes from an empty cache (5 % of keys redrawn per frame),
+    24 chunks on a seeded sample of heads, with the capacity cut to 4096 so
+    that the cache fills (about chunk 12) and eviction runs from then on.
+    Every chunk's indices and merge are checked against the oracle chain;
+    attention on sampled rows of every chunk."""
+    chunks = 24
+    cfg = CONFIGS[2].replace(H=2, C=4096, chunks=chunks)
+    d = layer_data(cfg, chunks=chunks, heads=[0, 11])
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    for c in range(chunks):
+        st = run_chunk(cfg, d, path, st, rep, chunk=c,
+                       rows=_sample_rows(cfg.Nq, 128 if c % 8 == 7 else 16, c))
+    assert int(host(path.cache.size).min()) == cfg.C  # the cache filled up
+    assert int(host(path.cache.evicted).sum()) > 0    # and evicted groups
+    print("report", rep)
