@@ -539,8 +539,41 @@ def run_ours(args, cfg):
             "wall_s_timed": t_wall,
             "e2e": {"value": e2e_ms, "unit": "ms/chunk", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h}}
+    if cfg.P:
+        # AnnCA pruning of this chunk: kept prompt tokens per (head, frame)
+        # and, where the prompt has a relevance label, the share of the
+        # relevant tokens that survive
+        kc = path.kept_cnt.cpu().numpy()
+        ki = path.kept_idx.cpu().numpy()
+        rel = np.asarray(d.prompt_rel)
+        pr = {"kept_per_head_frame": {"min": int(kc.min()), "mean": float(kc.mean()),
+                                      "max": int(kc.max()), "of": cfg.P}}
+        if not rel.all():
+            hit = tot = 0
+            for h in range(cfg.H):
+                for f in range(cfg.F):
+                    kept = ki[h, f, :kc[h, f]]
+                    hit += int(rel[h][kept].sum())
+                    tot += int(rel[h].sum())
+            pr["recall_relevant"] = hit / max(tot, 1)
+            pr["relevant_share_of_prompt"] = float(rel.mean())
+        line["prune"] = pr
+    if cfg.layers > 1:
+        # layers are independent and identical in shape: one layer is timed
+        # and the per-chunk figures are scaled to all of them
+        L = cfg.layers
+        line["value"] *= L
+        line["ms_per_step"] *= L
+        line["e2e"]["value"] *= L
+        line["e2e"]["h2d_bytes_per_step"] *= L
+        line["e2e"]["d2h_bytes_per_step"] *= L
+        line["config"]["layers"] = L
+        line["config"]["timed_layers"] = 1
+        line["config"]["scaled"] = f"one layer timed, x{L}"
     if not args.no_dense and rank == 0:
         line["dense"] = dense_reference_ms(cfg, d)
+        if cfg.layers > 1:
+            line["dense"]["ms_all_layers"] = line["dense"]["ms"] * cfg.layers
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         h = 0
         st_h = oracle_cache_one_head(cfg, d, h)
@@ -554,11 +587,90 @@ def run_ours(args, cfg):
         dist.destroy_process_group()
 
 
+def run_rollout(args, cfg):
+    """A rollout of cfg.chunks chunks from an empty cache (the long-rollout
+    workload): per chunk the latency of the public chunk call, the live
+    groups and the device memory held, and whether they stay flat."""
+    import torch
+
+    import merged_attention_autoregressive_gb300 as fa
+    from merged_attention_autoregressive_gb300 import build as fbuild
+    from merged_attention_autoregressive_gb300.path import ChunkPath
+    from workloads.gen import HeadStream, planes as gen_planes, prompt as gen_prompt
+
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    fbuild.build()
+    fa.lib()
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", tdt)  # noqa: E731
+    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt)
+    path.planes.copy_(todev(gen_planes(cfg, 0)))
+    streams = [HeadStream(cfg, 0, h) for h in range(cfg.H)]
+    pk, pv, _ = zip(*[gen_prompt(cfg, 0, h, s.centroids) for h, s in enumerate(streams)])
+    kp, vp = todev(np.stack(pk)), todev(np.stack(pv))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def next_chunk():
+        fr = [[s.frame() for _ in range(cfg.F)] for s in streams]
+        cat = lambda i: todev(np.stack([np.concatenate([f[i] for f in hf], axis=0) for hf in fr]))  # noqa: E731
+        return cat(2), cat(0), cat(1)  # q, k, v
+
+    ms, n_live, resident = [], [], []
+    n0 = fa.fastar_launch_count()
+    clocks = Clocks(local)
+    clocks.start()
+    t0 = time.time()
+    for c in range(cfg.chunks):
+        q, k, v = next_chunk()
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        path.step(q, k, v, kp, vp, cfg.past_frames + c * cfg.F)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+        n_live.append(float(path.cache.size.float().mean().item()))
+        resident.append(torch.cuda.memory_allocated())
+    clocks.window(t0, time.time())
+    clk = clocks.stop()
+    assert int(path.status.item()) == 0, fa.STATUS.get(int(path.status.item()))
+    launches = fa.fastar_launch_count() - n0
+    tail = np.array(ms[-100:]) if len(ms) >= 100 else np.array(ms)
+    slope = float(np.polyfit(np.arange(len(tail)), tail, 1)[0]) * 100 / float(tail.mean())
+    last50 = np.array(ms[-50:])
+    row = cfg.D * 2 * (2 if cfg.dtype == "bf16" else 4)  # K and V bytes per key
+    line = {"metric": METRIC, "value": float(np.mean(ms)), "unit": "ms/chunk", "n_gpus": 1,
+            "steps": cfg.chunks, "warmup": 0, "ms_per_step": float(np.mean(ms)),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq, "P": cfg.P,
+                       "T": cfg.T, "B": cfg.B, "C": cfg.C, "chunks": cfg.chunks,
+                       "l2": "flushed before every chunk (256 MiB write)",
+                       "parallelism": "single GPU"},
+            "rollout": {
+                "ms_first_chunk": ms[0], "ms_median": float(np.median(ms)),
+                "ms_median_last50": float(np.median(last50)),
+                "slope_last100_pct_of_mean_per_100_chunks": slope,
+                "max_over_median_last50": float(last50.max() / np.median(last50)),
+                "ms_every_10th_chunk": ms[::10],
+                "n_live_every_10th_chunk": n_live[::10], "n_live_final": n_live[-1],
+                "device_bytes_allocated": {"min": min(resident), "max": max(resident)},
+                "cache_live_kv_bytes_final": int(n_live[-1] * cfg.H * row),
+                "dense_cache_keys_equiv": cfg.chunks * cfg.F * cfg.n_f,
+                "dense_cache_kv_bytes_equiv": cfg.chunks * cfg.F * cfg.n_f * cfg.H * row},
+            "gpu_launches": launches, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif cfg.chunks > 1:
+        run_rollout(args, cfg)
     else:
         run_ours(args, cfg)
 
