@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--recall", action="store_true",
+                    help="sweep tau, T and B: recall and density of AnnSA and AnnCA (one JSON line)")
     return ap.parse_args()
 
 
@@ -602,6 +604,103 @@ def run_ours(args, cfg):
         dist.destroy_process_group()
 
 
+def recall_metrics(cfg, path, d, chunk_q, history_k=None, history_v=None):
+    """Synthetic recall and density of one chunk's sparse selections, from
+    the path's outputs: per head the share of the dense softmax mass that
+    AnnSA's allowed slots carry (exp(lse of the kernel - dense lse), same
+    logits: scale q.K + ln m over the live cache), the allowed density, the
+    same share for AnnCA's kept prompt tokens, and, given the unmerged
+    history, the relative error of the AnnSA output against dense attention
+    over it.  Dense references are plain torch fp32 / SDPA (measurement)."""
+    import torch
+    import torch.nn.functional as Fn
+    H, T = cfg.H, cfg.T
+    q = torch.as_tensor(chunk_q).cuda().float()
+    kp = torch.as_tensor(d.prompt_k).cuda().float()
+    out = {"annsa_retained": [], "annsa_density": [], "annca_retained": [], "annca_kept_share": [],
+           "annsa_rel_err_vs_dense_history": [], "annca_rel_err_vs_dense_prompt": []}
+    size = path.cache.size.tolist()
+    lse = path.lse.float()
+    for h in range(H):
+        n = size[h]
+        K = path.cache.K[h, :n].float()
+        logits = cfg.scale * q[h] @ K.T + torch.log(path.cache.m[h, :n].float())[None, :]
+        dense_lse = torch.logsumexp(logits, dim=1)
+        out["annsa_retained"].append(float(torch.exp(lse[h] - dense_lse).mean()))
+        allowed = torch.zeros_like(logits, dtype=torch.bool)
+        for t in range(T):
+            allowed |= path.q_codes[h, t][:, None] == path.cache.codes[h, t, :n][None, :]
+        out["annsa_density"].append(float(allowed.float().mean()))
+        if cfg.P:
+            sp = torch.softmax(cfg.scale * q[h] @ kp[h].T, dim=1)
+            ret, share = [], []
+            for f in range(cfg.F):
+                keep = torch.zeros(cfg.P, dtype=torch.bool, device="cuda")
+                keep[path.kept_idx[h, f, :int(path.kept_cnt[h, f])].long()] = True
+                ret.append(sp[f * cfg.n_f:(f + 1) * cfg.n_f][:, keep].sum(dim=1).mean())
+                share.append(keep.float().mean())
+            out["annca_retained"].append(float(torch.stack(ret).mean()))
+            out["annca_kept_share"].append(float(torch.stack(share).mean()))
+            o_ca_dense = Fn.scaled_dot_product_attention(q[h][None], kp[h][None],
+                                                         torch.as_tensor(d.prompt_v[h]).cuda().float()[None])[0]
+            out["annca_rel_err_vs_dense_prompt"].append(
+                float((path.o_ca[h].float() - o_ca_dense).norm() / o_ca_dense.norm()))
+        if history_k is not None:
+            Kh = torch.as_tensor(history_k[h]).cuda().float()
+            Vh = torch.as_tensor(history_v[h]).cuda().float()
+            o_dense = Fn.scaled_dot_product_attention(q[h][None], Kh[None], Vh[None])[0]
+            out["annsa_rel_err_vs_dense_history"].append(
+                float((path.o_sa[h].float() - o_dense).norm() / o_dense.norm()))
+    return {k: (float(np.mean(v)) if v else None) for k, v in out.items()}
+
+
+def run_recall(args, cfg):
+    """Sweep of the LSH and merge parameters on cfg's shapes (a seeded
+    sample of heads): recall and density of AnnSA and AnnCA, and the output
+    error against dense attention, per (tau, T, B)."""
+    import torch
+
+    import merged_attention_autoregressive_gb300 as fa
+    from merged_attention_autoregressive_gb300 import build as fbuild
+    from merged_attention_autoregressive_gb300.path import ChunkPath
+
+    fbuild.build()
+    fa.lib()
+    heads = [0, 5]
+    settings = [(0.95, 2, 8), (0.90, 2, 8), (0.99, 2, 8), (0.95, 1, 8), (0.95, 4, 8), (0.95, 2, 6),
+                (0.95, 2, 10)]
+    rows = []
+    for tau, T, B in settings:
+        c = cfg.replace(H=len(heads), tau=tau, T=T, B=B)
+        d = layer_data(c, chunks=1, heads=heads)
+        todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", torch.bfloat16)  # noqa: E731
+        path = ChunkPath(c.H, c.D, c.n_f, c.F, c.P, c.T, c.B, c.C, c.tau, torch.bfloat16)
+        path.planes.copy_(todev(d.planes))
+        f = 0
+        while f < c.past_frames:
+            nF = min(c.F, c.past_frames - f)
+            path.merge(todev(np.concatenate(d.past_k[f:f + nF], 1)),
+                       todev(np.concatenate(d.past_v[f:f + nF], 1)), f, F=nF)
+            f += nF
+        path.step(todev(d.chunk_q[0]), todev(d.chunk_k[0]), todev(d.chunk_v[0]), todev(d.prompt_k),
+                  todev(d.prompt_v), c.past_frames)
+        torch.cuda.synchronize()
+        assert int(path.status.item()) == 0
+        hk = np.concatenate(d.past_k + [d.chunk_k[0]], axis=1)
+        hv = np.concatenate(d.past_v + [d.chunk_v[0]], axis=1)
+        m = recall_metrics(c, path, d, d.chunk_q[0], hk, hv)
+        m.update({"tau": tau, "T": T, "B": B,
+                  "n_live_per_head": float(path.cache.size.float().mean()),
+                  "keys_before_merge_per_head": (c.past_frames + c.F) * c.n_f})
+        rows.append(m)
+    line = {"metric": "synthetic recall / density of the sparse selections", "unit": "share",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "heads_sampled": heads, "D": cfg.D, "Nq": cfg.Nq,
+                       "P": cfg.P, "past_frames": cfg.past_frames},
+            "sweep": rows}
+    print(json.dumps(line), flush=True)
+
+
 def run_rollout(args, cfg):
     """A rollout of cfg.chunks chunks from an empty cache (the long-rollout
     workload): per chunk the latency of the public chunk call, the live
@@ -684,6 +783,8 @@ def main():
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.recall:
+        run_recall(args, cfg)
     elif cfg.chunks > 1:
         run_rollout(args, cfg)
     else:

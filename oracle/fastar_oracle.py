@@ -31,6 +31,10 @@ Readings taken where the pages are silent:
   attend  -- a chunk's frames are merged first, then its queries attend the
              whole live cache; logit = q.k / sqrt(D) + ln m; a query with no
              allowed key gets a zero output and lse = -inf.
+  recall  -- the pages report recall and density of the sparse selections
+             without a formula; here a query's retained share is the dense
+             softmax weight (same logits) on its allowed keys, and density is
+             the allowed share of the (query, key) pairs.
 
 Parity pins of every function live in tests/test_oracle_pins.py; there is
 no worked numeric example on the pages, so the pins are closed forms
@@ -405,3 +409,63 @@ def annsa_attention(q, q_codes, state: CacheState, scale: float, rows=None):
         o[h], lse[h] = masked_attention(q[h, rows], state.K[h, :size], state.V[h, :size],
                                         allowed, bias, scale)
     return o, lse
+
+
+# ---------------------------------------------------------------- recall / density
+# The pages measure how much of the dense attention the sparse selections
+# keep (recall and density: FAST-AR summary, paperlayer.ai section 7 and
+# appendix tables; gist.science technical summary, results).  Our synthetic
+# counterpart, per query i:
+#   retained_i = sum_{j allowed} w_ij / sum_j w_ij,  w_ij = exp(logit_ij),
+# with the same logits as the attention (AnnSA: scale q.K[s] + ln m[s] over
+# the live cache; AnnCA: scale q.k_p over the prompt), i.e. the share of the
+# dense softmax mass that the allowed keys carry.  Density is the allowed
+# share of the (query, key) pairs.
+
+def retained_mass(q, k, allowed, bias, scale: float):
+    """Per query: the share of the dense softmax weight on its allowed keys.
+
+    q: [n][D], k: [M][D], allowed: [n][M] bool, bias: [M].  fp64 weights
+    relative to each row's dense maximum; a row of M = 0 keys gives 0.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    if k.shape[0] == 0:
+        return np.zeros(q.shape[0])
+    s = scale * (q @ k.T) + np.asarray(bias, dtype=np.float64)[None, :]
+    w = np.exp(s - np.max(s, axis=1, keepdims=True))
+    return np.sum(np.where(allowed, w, 0.0), axis=1) / np.sum(w, axis=1)
+
+
+def annsa_retained(q, q_codes, state: "CacheState", scale: float, rows=None):
+    """AnnSA: (retained [H][n], density [H]) over the live cache."""
+    q = np.asarray(q, dtype=np.float64)
+    H, Nq, _ = q.shape
+    rows = np.arange(Nq) if rows is None else np.asarray(rows)
+    ret = np.zeros((H, rows.size))
+    dens = np.zeros(H)
+    for h in range(H):
+        size = int(state.size[h])
+        allowed = annsa_allowed(np.asarray(q_codes)[h][:, rows], state.codes[h, :, :size])
+        bias = np.log(state.m[h, :size].astype(np.float64))
+        ret[h] = retained_mass(q[h, rows], state.K[h, :size], allowed, bias, scale)
+        dens[h] = allowed.mean() if allowed.size else 0.0
+    return ret, dens
+
+
+def annca_retained(q, k_p, kept_idx, kept_cnt, F: int, n_f: int, scale: float):
+    """AnnCA: (retained [H][F*n_f], kept share [H][F]) over the prompt."""
+    q = np.asarray(q, dtype=np.float64)
+    H, Nq, _ = q.shape
+    P = np.asarray(k_p).shape[1]
+    ret = np.zeros((H, Nq))
+    share = np.zeros((H, F))
+    for h in range(H):
+        for f in range(F):
+            keep = np.zeros(P, dtype=bool)
+            keep[np.asarray(kept_idx[h, f, :kept_cnt[h, f]], dtype=np.int64)] = True
+            sl = slice(f * n_f, (f + 1) * n_f)
+            allowed = np.broadcast_to(keep[None, :], (n_f, P))
+            ret[h, sl] = retained_mass(q[h, sl], np.asarray(k_p)[h], allowed, np.zeros(P), scale)
+            share[h, f] = keep.mean() if P else 0.0
+    return ret, share

@@ -292,3 +292,29 @@ def test_rollout_head_sample():
     assert int(host(path.cache.size).min()) == cfg.C  # the cache filled up
     assert int(host(path.cache.evicted).sum()) > 0    # and evicted groups
     print("report", rep)
+
+
+def test_recall_metrics_match_oracle():
+    """The recall / density measurement of bench.py (the kernels' lse and
+    kept lists against dense torch references) agrees with the oracle's
+    definitions (retained softmax share, allowed density) on one chunk."""
+    import bench
+    cfg = CONFIGS[0].replace(dtype="bf16", n_f=197, F=2, past_frames=5, P=77, T=3, B=7, C=700,
+                             D=128, H=3, redraw=0.3)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    build_cache(cfg, d, path, Report(), check=False)
+    ins = [dev(x, cfg.dtype) for x in (d.chunk_q[0], d.chunk_k[0], d.chunk_v[0], d.prompt_k, d.prompt_v)]
+    path.step(*ins, cfg.past_frames)
+    torch.cuda.synchronize()
+    assert int(path.status.item()) == 0
+    got = bench.recall_metrics(cfg, path, d, d.chunk_q[0])
+    st = cache_to_oracle(path.cache, cfg.dtype)
+    ret, dens = O.annsa_retained(d.chunk_q[0], host(path.q_codes), st, cfg.scale)
+    assert abs(got["annsa_retained"] - ret.mean()) <= 2e-3 * ret.mean()
+    assert abs(got["annsa_density"] - dens.mean()) <= 1e-6
+    rca, share = O.annca_retained(d.chunk_q[0], d.prompt_k, host(path.kept_idx), host(path.kept_cnt),
+                                  cfg.F, cfg.n_f, cfg.scale)
+    assert abs(got["annca_retained"] - rca.mean()) <= 1e-4
+    assert abs(got["annca_kept_share"] - share.mean()) <= 1e-6

@@ -411,3 +411,52 @@ def test_annsa_allowed_fixture_and_single_bucket_dense():
     s = 0.35 * q[0] @ st.K[0, :10].T + np.log(st.m[0, :10])
     np.testing.assert_allclose(o[0], softmax(s, axis=1) @ st.V[0, :10], atol=1e-13)
     np.testing.assert_allclose(lse[0], logsumexp(s, axis=1), atol=1e-13)
+
+
+def test_retained_mass_is_the_allowed_softmax_share():
+    """retained = exp(lse over the allowed keys - lse over all keys), an
+    identity between two different computations (weights summed here,
+    log-sum-exp in masked_attention), plus its end points."""
+    rng = np.random.default_rng(11)
+    n, M, D = 7, 19, 16
+    q, k, v = rng.standard_normal((n, D)), rng.standard_normal((M, D)), rng.standard_normal((M, D))
+    bias = np.log(rng.integers(1, 5, size=M).astype(np.float64))
+    allowed = rng.random((n, M)) < 0.4
+    allowed[:, 0] = True
+    scale = 0.25
+    r = O.retained_mass(q, k, allowed, bias, scale)
+    _, lse_a = O.masked_attention(q, k, v, allowed, bias, scale)
+    _, lse_all = O.masked_attention(q, k, v, np.ones((n, M), bool), bias, scale)
+    np.testing.assert_allclose(r, np.exp(lse_a - lse_all), rtol=1e-12)
+    np.testing.assert_allclose(r, [softmax(scale * q[i] @ k.T + bias)[allowed[i]].sum() for i in range(n)],
+                               rtol=1e-12)
+    np.testing.assert_array_equal(O.retained_mass(q, k, np.ones((n, M), bool), bias, scale), 1.0)
+    np.testing.assert_array_equal(O.retained_mass(q, k, np.zeros((n, M), bool), bias, scale), 0.0)
+
+
+def test_annsa_and_annca_retained_end_points():
+    """One shared code everywhere: AnnSA keeps everything (retained 1,
+    density 1); disjoint codes: nothing.  AnnCA with everything kept: 1."""
+    rng = np.random.default_rng(12)
+    H, T, D, Nq, C, size = 2, 2, 8, 5, 16, 9
+    st = O.CacheState.empty(H, C, D, T, "f32")
+    st.K[:, :size] = rng.standard_normal((H, size, D))
+    st.m[:, :size] = rng.integers(1, 4, size=(H, size))
+    st.size[:] = size
+    q = rng.standard_normal((H, Nq, D))
+    qc = np.zeros((H, T, Nq), np.uint32)
+    st.codes[:] = 0
+    r, dens = O.annsa_retained(q, qc, st, 0.3)
+    np.testing.assert_allclose(r, 1.0, rtol=1e-12)
+    np.testing.assert_array_equal(dens, 1.0)
+    st.codes[:] = 1
+    r, dens = O.annsa_retained(q, qc, st, 0.3)
+    np.testing.assert_array_equal(r, 0.0)
+    np.testing.assert_array_equal(dens, 0.0)
+    P, F, n_f = 6, 1, Nq
+    kp = rng.standard_normal((H, P, D))
+    idx = np.tile(np.arange(P, dtype=np.int32), (H, F, 1))
+    cnt = np.full((H, F), P, np.int32)
+    r, share = O.annca_retained(q, kp, idx, cnt, F, n_f, 0.3)
+    np.testing.assert_allclose(r, 1.0, rtol=1e-12)
+    np.testing.assert_array_equal(share, 1.0)
