@@ -88,6 +88,21 @@ int fastar_timing_begin(cudaEvent_t* events, int capacity);
 int fastar_timing_end(void);
 const char* fastar_timing_name(int i);
 
+/* Self-check of the device error path (a diagnostic; the paper has no
+ * counterpart).  Every mbarrier wait in this library's tensor-core kernels
+ * is bounded: when it runs out the kernel writes FASTAR_ERR_TIMEOUT into
+ * the caller's sticky status word, frees the TMEM it holds and returns, so
+ * that the context stays usable and every later kernel of the library that
+ * is given the same word exits without writing its outputs.  This call
+ * launches one small kernel that allocates TMEM and waits, with that same
+ * bounded wait but `polls` polls (1..FASTAR_CHECK_WAIT_MAX_POLLS, each at
+ * most about 2 us), on a barrier that nothing arrives on; afterwards
+ * *dev_status holds FASTAR_ERR_TIMEOUT (or the error already there).
+ * Asynchronous on `stream`; FASTAR_ERR_ARG for a null word or polls out of
+ * range. */
+#define FASTAR_CHECK_WAIT_MAX_POLLS 65536
+int fastar_check_bounded_wait(int polls, int32_t* dev_status, cudaStream_t stream);
+
 /*
  * Bytes of workspace a call needs.  Arguments that an op does not use are
  * ignored.  op: FASTAR_OP_*; H heads; N rows per head (hash: N; merge:

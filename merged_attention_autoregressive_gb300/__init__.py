@@ -26,7 +26,7 @@ EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
            "fastar_workspace_size", "fastar_hash", "fastar_hash_many", "fastar_bucket_csr",
            "fastar_tempcache_merge", "fastar_tempcache_merge_ev", "fastar_annca_prune", "fastar_annca_attention",
-           "fastar_annsa_attention"]
+           "fastar_annsa_attention", "fastar_check_bounded_wait"]
 
 
 class FastarError(RuntimeError):
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
                                              _VP, _VP, _SZ, _VP, _VP]
         L.fastar_annsa_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _I, ctypes.POINTER(CacheStruct),
                                              _F, _VP, _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_check_bounded_wait.argtypes = [_I, _VP, _VP]
         for name in EXPORTS[7:]:
             getattr(L, name).restype = _I
         _lib = L
@@ -118,6 +119,14 @@ def _stream(stream):
 def _check(rc: int, where: str):
     if rc != 0:
         raise FastarError(rc, where)
+
+
+def fastar_check_bounded_wait(polls, status, stream=None):
+    """Run the library's bounded-wait error path once (see the C header):
+    afterwards `status` holds FASTAR_ERR_TIMEOUT (17) unless it already held
+    an error."""
+    _check(lib().fastar_check_bounded_wait(int(polls), _p(status), _stream(stream)),
+           "fastar_check_bounded_wait")
 
 
 def fastar_launch_count() -> int:

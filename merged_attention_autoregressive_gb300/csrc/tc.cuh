@@ -65,11 +65,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
 // try_wait suspends the thread in hardware until the phase completes or the
 // suspend hint passes, so waiting warps leave the issue slots to the warps
 // that compute instead of spinning; the loop bounds the total wait.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_polls(bar, parity, kWaitPolls);
 }
 
 // ------------------------------------------------------------- TMA

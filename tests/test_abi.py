@@ -121,6 +121,11 @@ def test_host_argument_errors_need_no_gpu(L):
     # merge with a codes-ready event: same argument checks
     assert L.fastar_tempcache_merge_ev(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                        None, 0, None, None, None) == 1
+    # bounded-wait self-check: null status word, polls out of range
+    L.fastar_check_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    assert L.fastar_check_bounded_wait(8, None, None) == 1
+    assert L.fastar_check_bounded_wait(0, fake, None) == 1
+    assert L.fastar_check_bounded_wait(65537, fake, None) == 1
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
