@@ -372,6 +372,99 @@ def dense_reference_ms(cfg, d, reps=10):
     return {"ms": ms, "keys": n_keys, "tflops": flops / ms / 1e9, "impl": "torch SDPA (bf16)"}
 
 
+def dense_ours(cfg, d, reps=10):
+    """Dense attention of the same chunk through this library's own kernels.
+
+    A cache in which every key of the unmerged history is its own group
+    (m = 1) and every code is 0 (one table of one bit, one bucket) makes
+    AnnSA dense attention over the history; a kept list holding every
+    prompt token makes AnnCA dense cross-attention.  The cache buffers are
+    caller-owned, so they are written directly here (set-up, untimed).  This
+    measures the attention kernels on dense work: their tensor-core
+    throughput against the measured bf16 peak, beside torch SDPA."""
+    import torch
+    import torch.nn.functional as Fn
+
+    import merged_attention_autoregressive_gb300 as fa
+    dt = torch.bfloat16
+    H, D, Nq, P, F = cfg.H, cfg.D, cfg.Nq, cfg.P, cfg.F
+    K = torch.from_numpy(np.concatenate(d.past_k + [d.chunk_k[0]], axis=1)).to("cuda", dt)
+    V = torch.from_numpy(np.concatenate(d.past_v + [d.chunk_v[0]], axis=1)).to("cuda", dt)
+    n = K.shape[1]
+    q = torch.from_numpy(d.chunk_q[0]).to("cuda", dt)
+    kp = torch.from_numpy(d.prompt_k).to("cuda", dt)
+    vp = torch.from_numpy(d.prompt_v).to("cuda", dt)
+    c = fa.Cache(H, n, D, 1, 1, dt)
+    c.K.copy_(K)
+    c.V.copy_(V)
+    c.m.fill_(1)
+    c.last_frame.zero_()
+    c.size.fill_(n)
+    c.inserted.fill_(n)
+    c.perm[:, 0].copy_(torch.arange(n, dtype=torch.int32, device="cuda"))
+    c.offsets[:, 0] = torch.tensor([0, n, n], dtype=torch.int32, device="cuda")
+    i32 = dict(dtype=torch.int32, device="cuda")
+    q_codes = torch.zeros(H, 1, Nq, **i32)
+    q_perm = torch.arange(Nq, **i32).repeat(H, 1, 1).contiguous()
+    q_off = torch.tensor([0, Nq, Nq], **i32).repeat(H, 1, 1).contiguous()
+    kept_idx = torch.arange(max(P, 1), **i32).repeat(H, F, 1).contiguous()
+    kept_cnt = torch.full((H, F), P, **i32)
+    o_sa = torch.empty(H, Nq, D, dtype=dt, device="cuda")
+    o_ca = torch.empty(H, Nq, D, dtype=dt, device="cuda")
+    lse = torch.empty(H, Nq, dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, **i32)
+    ws_sa = torch.empty(max(1, fa.fastar_workspace_size(fa.OP_ANNSA, H, Nq, D, 1, 1, n)), dtype=torch.uint8,
+                        device="cuda")
+    ws_ca = torch.empty(max(1, fa.fastar_workspace_size(fa.OP_ANNCA, H, F, D, 1, 1, P)), dtype=torch.uint8,
+                        device="cuda")
+    scale = D ** -0.5
+    stream = torch.cuda.current_stream()
+
+    def sa():
+        fa.fastar_annsa_attention(q, q_codes, q_perm, q_off, c, scale, o_sa, lse, ws=ws_sa, status=st)
+
+    def ca():
+        if P:
+            fa.fastar_annca_attention(q, kp, vp, kept_idx, kept_cnt, F, cfg.n_f, scale, o_ca, ws=ws_ca,
+                                      status=st)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(reps):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        return s.elapsed_time(e) / reps
+
+    ms_sa, ms_ca = timed(sa), timed(ca)
+    assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))
+    # agreement with SDPA on a few heads (bf16 outputs of both)
+    err = 0.0
+    for h in range(min(H, 2)):
+        ref = Fn.scaled_dot_product_attention(q[h][None], K[h][None], V[h][None])[0]
+        err = max(err, float((o_sa[h].float() - ref.float()).abs().max()))
+        if P:
+            ref = Fn.scaled_dot_product_attention(q[h][None], kp[h][None], vp[h][None])[0]
+            err = max(err, float((o_ca[h].float() - ref.float()).abs().max()))
+    pk = peaks()
+    fl_sa, fl_ca = 4 * D * H * Nq * n, 4 * D * H * Nq * P
+    out = {"impl": "this library's AnnSA / AnnCA kernels, one bucket (dense)", "keys": n,
+           "ms": ms_sa + ms_ca, "ms_self": ms_sa, "ms_cross": ms_ca,
+           "tflops_self": fl_sa / ms_sa / 1e9,
+           "frac_self": fl_sa / ms_sa / 1e9 / pk["bf16_tflops"],
+           "tflops_cross": fl_ca / ms_ca / 1e9 if P else None,
+           "frac_cross": fl_ca / ms_ca / 1e9 / pk["bf16_tflops"] if P else None,
+           "peak_tflops": pk["bf16_tflops"], "peak_of": "measured bf16 burst",
+           "max_abs_err_vs_sdpa": err}
+    del c, K, V
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, cfg):
     import torch
     import torch.distributed as dist
@@ -591,6 +684,8 @@ def run_ours(args, cfg):
         line["dense"] = dense_reference_ms(cfg, d)
         if cfg.layers > 1:
             line["dense"]["ms_all_layers"] = line["dense"]["ms"] * cfg.layers
+        if cfg.dtype == "bf16" and cfg.D == 128:
+            line["dense_ours"] = dense_ours(cfg, d)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         h = 0
         st_h = oracle_cache_one_head(cfg, d, h)

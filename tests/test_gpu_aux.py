@@ -99,3 +99,48 @@ def test_checkpoint_resume_is_bit_identical():
     # unused slots hold m = 0, so this holds whether or not the cache is full
     assert int(a.cache.m.long().sum()) + int(a.cache.evicted.sum()) == inserted
     assert np.isfinite(ref[-1][2].float().cpu().numpy()).any()
+
+
+def test_one_bucket_cache_gives_dense_attention():
+    """With every code 0 (one table, one bit) and m = 1 everywhere, AnnSA is
+    plain softmax attention over every cached key, and AnnCA with every
+    prompt token kept is plain cross-attention: both against the oracle's
+    fp64 attention with everything allowed (the bench's dense run)."""
+    import merged_attention_autoregressive_gb300 as fa
+    import oracle as O
+    rng = np.random.default_rng(7)
+    H, n, Nq, P, F, D = 2, 700, 300, 90, 2, 128
+    n_f = Nq // F
+    bf = lambda a: torch.from_numpy(a.astype(np.float32)).to("cuda", torch.bfloat16)  # noqa: E731
+    K, V, q = bf(rng.normal(size=(H, n, D))), bf(rng.normal(size=(H, n, D))), bf(rng.normal(size=(H, Nq, D)))
+    kp, vp = bf(rng.normal(size=(H, P, D))), bf(rng.normal(size=(H, P, D)))
+    i32 = dict(dtype=torch.int32, device="cuda")
+    c = fa.Cache(H, n, D, 1, 1)
+    c.K.copy_(K)
+    c.V.copy_(V)
+    c.m.fill_(1)
+    c.last_frame.zero_()
+    c.size.fill_(n)
+    c.perm[:, 0].copy_(torch.arange(n, **i32))
+    c.offsets[:, 0] = torch.tensor([0, n, n], **i32)
+    q_codes = torch.zeros(H, 1, Nq, **i32)
+    q_perm = torch.arange(Nq, **i32).repeat(H, 1, 1).contiguous()
+    q_off = torch.tensor([0, Nq, Nq], **i32).repeat(H, 1, 1).contiguous()
+    o_sa = torch.empty(H, Nq, D, dtype=torch.bfloat16, device="cuda")
+    o_ca = torch.empty_like(o_sa)
+    st = torch.zeros(1, **i32)
+    scale = D ** -0.5
+    fa.fastar_annsa_attention(q, q_codes, q_perm, q_off, c, scale, o_sa, status=st)
+    kept_idx = torch.arange(P, **i32).repeat(H, F, 1).contiguous()
+    kept_cnt = torch.full((H, F), P, **i32)
+    fa.fastar_annca_attention(q, kp, vp, kept_idx, kept_cnt, F, n_f, scale, o_ca, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    h64 = lambda t: t.float().cpu().numpy().astype(np.float64)  # noqa: E731
+    for h in range(H):
+        for out, kk, vv in ((o_sa, K, V), (o_ca, kp, vp)):
+            ref = O.masked_attention(h64(q[h]), h64(kk[h]), h64(vv[h]),
+                                     np.ones((Nq, kk.shape[1]), bool), np.zeros(kk.shape[1]), scale)
+            ref = ref[0] if isinstance(ref, tuple) else ref
+            err = np.abs(h64(out[h]) - ref)
+            assert err.max() <= 1e-2 and err.mean() <= 1e-3, (h, err.max(), err.mean())
