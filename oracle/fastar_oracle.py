@@ -25,6 +25,12 @@ Readings taken where the pages are silent:
              becomes the matching key with the lowest token index; the
              stored value is the count-weighted mean rounded to the storage
              type after each update.
+  mean-key -- the representative ablation ([PL] appendix C, representative
+             selection: last-key, mean-key, medoid-key): in "mean" mode the
+             stored key is the count-weighted mean of every key that joined
+             the group, updated and rounded like the value, and the group's
+             codes are the hash of that stored key (its bucket).  The
+             medoid-key variant needs every past member and is not built.
   insert  -- unmatched keys fill free slots in ascending order, then the
              slots with the smallest (last_frame, slot) among those not
              refreshed in this frame are evicted (least recently refreshed).
@@ -212,7 +218,8 @@ def tempcache_nn(state: CacheState, k: np.ndarray, f: int, tau: float):
     return match, listed
 
 
-def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match) -> CacheState:
+def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match, rep: str = "last",
+                          planes=None, B: int | None = None) -> CacheState:
     """Merge one frame's keys into the cache given its NN matches (in place).
 
     k, v: [H][n][D]; codes: [H][T][n]; match: [H][n] slot or -1.
@@ -221,6 +228,9 @@ def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match) -> Cach
     matching index.  Unmatched keys become groups of count 1, placed in free
     slots first, then in evicted slots (smallest (last_frame, slot) among
     slots with last_frame < f), both in ascending order.
+    rep="mean" ([PL] appendix C, mean-key representative): the matched
+    group's key is K' = round((m K + sum k)/m') instead, and its codes are
+    hash(K') with `planes` [T*B][D] and B bits per table.
     """
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -236,8 +246,16 @@ def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match) -> Cach
             for j in S:
                 total = total + v[h, j]
             state.V[h, s] = round_storage(total / m_new, state.dtype)
-            state.K[h, s] = k[h, S[0]]
-            state.codes[h, :, s] = codes[h, :, S[0]]
+            if rep == "mean":
+                ktot = m_old * state.K[h, s]
+                for j in S:
+                    ktot = ktot + k[h, j]
+                state.K[h, s] = round_storage(ktot / m_new, state.dtype)
+                T = state.codes.shape[1]
+                state.codes[h, :, s] = hash_codes(state.K[h, s][None, None], planes, T, B)[0][0, :, 0]
+            else:
+                state.K[h, s] = k[h, S[0]]
+                state.codes[h, :, s] = codes[h, :, S[0]]
             state.last_frame[h, s] = f
             state.m[h, s] = m_new
         U = np.nonzero(mh < 0)[0]
@@ -269,12 +287,14 @@ def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match) -> Cach
 
 
 def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int,
-                    first_frame: int, tau: float, match_override=None):
+                    first_frame: int, tau: float, match_override=None, rep: str = "last",
+                    planes=None, B: int | None = None):
     """Merge a chunk of F frames, frame by frame, into a copy of `state`.
 
     k_new, v_new: [H][F*n_f][D]; codes_new: [H][T][F*n_f].
     match_override: optional [H][F*n_f] matches to use instead of the
     oracle's own (to continue from another implementation's decisions).
+    rep, planes, B: the representative mode (tempcache_apply_frame).
     Returns (new_state, match [H][F*n_f], listed [H][F*n_f]).
     """
     st = state.copy()
@@ -289,7 +309,7 @@ def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int
             mt = np.asarray(match_override)[:, sl].astype(np.int64)
         match[:, sl], listed[:, sl] = mt, ls
         tempcache_apply_frame(st, np.asarray(k_new)[:, sl], np.asarray(v_new)[:, sl],
-                              np.asarray(codes_new)[:, :, sl], f, mt)
+                              np.asarray(codes_new)[:, :, sl], f, mt, rep=rep, planes=planes, B=B)
     return st, match, listed
 
 

@@ -291,6 +291,93 @@ def test_tempcache_invariants_on_synthetic_layer():
     np.testing.assert_array_equal(codes, st.codes[:, :, :st.size[0]])
 
 
+def _frames(g, nframes):
+    out = []
+    for f in range(nframes):
+        k = np.stack([g[f"f{f}_k0"], g[f"f{f}_k1"]])[None]
+        v = np.stack([g[f"f{f}_v0"], g[f"f{f}_v1"]])[None]
+        codes = np.asarray(g[f"f{f}_codes"], dtype=np.uint32).reshape(1, 1, 2)
+        out.append((k, v, codes, g[f"f{f}_match"]))
+    return out
+
+
+def test_tempcache_meankey_fixture():
+    """Mean-key representative (paperlayer.ai appendix C) on a hand-derived
+    history: the group key is the running count-weighted mean, its code the
+    hash of that mean, and the next frame matches against it (a key that
+    the mean accepts and the last key would not)."""
+    g = load("tempcache_meankey_small.txt")
+    D, C, tau = int(g["D"]), int(g["C"]), float(g["tau"])
+    planes = np.asarray(g["planes"], dtype=np.float64).reshape(2, D)
+    st = O.CacheState.empty(1, C, D, 1, "f64")
+    for f, (k, v, codes, want) in enumerate(_frames(g, 3)):
+        st, match, listed = O.tempcache_merge(st, k, v, codes, 1, 2, f, tau, rep="mean", planes=planes, B=2)
+        np.testing.assert_array_equal(match[0], want)
+        assert not listed.any()
+    for s in range(3):
+        np.testing.assert_array_equal(st.K[0, s], g[f"K{s}"])
+        np.testing.assert_array_equal(st.V[0, s], g[f"V{s}"])
+    np.testing.assert_array_equal(st.m[0], g["m"])
+    np.testing.assert_array_equal(st.codes[0, 0], g["codes"])
+    np.testing.assert_array_equal(st.last_frame[0], g["last_frame"])
+    assert st.size[0] == g["size"] and st.inserted[0] == g["inserted"] and st.evicted[0] == g["evicted"]
+    # the last-key mode keeps (1, 1/4) as the key of slot 0, which frame 2's
+    # first key does not reach (cosine 0.8824): it opens a new group instead
+    st = O.CacheState.empty(1, C, D, 1, "f64")
+    for f, (k, v, codes, _) in enumerate(_frames(g, 3)):
+        st, match, _ = O.tempcache_merge(st, k, v, codes, 1, 2, f, tau)
+    np.testing.assert_array_equal(match[0], [-1, -1])
+    np.testing.assert_array_equal(st.K[0, 0], [1, 0.25, 0, 0])
+    assert st.size[0] == 4
+
+
+def test_tempcache_meankey_equals_lastkey_on_exact_duplicates():
+    """Closed form: the mean of identical keys is that key, so on frames that
+    are exact permutations of each other the two representative modes give
+    the same cache, bit for bit."""
+    rng = np.random.default_rng(11)
+    n, D, T, B = 10, 8, 2, 3
+    planes = rng.standard_normal((T * B, D))
+    base = rng.standard_normal((n, D))
+    a = O.CacheState.empty(1, 32, D, T, "f64")
+    b = O.CacheState.empty(1, 32, D, T, "f64")
+    k = base
+    for f in range(4):
+        if f:
+            k = k[rng.permutation(n)]
+        v = rng.standard_normal((1, n, D))
+        codes, _ = O.hash_codes(k[None], planes, T, B)
+        a, ma, _ = O.tempcache_merge(a, k[None], v, codes, 1, n, f, 0.95)
+        b, mb, _ = O.tempcache_merge(b, k[None], v, codes, 1, n, f, 0.95, rep="mean", planes=planes, B=B)
+        np.testing.assert_array_equal(ma, mb)
+    for name in ("K", "V", "m", "codes", "last_frame", "size", "inserted", "evicted"):
+        np.testing.assert_array_equal(getattr(a, name), getattr(b, name), err_msg=name)
+    assert (a.m[0, :n] == 4).all()
+
+
+def test_tempcache_meankey_invariants_on_synthetic_layer():
+    """Mean-key mode on the tiny synthetic layer: every live group's codes
+    are the hash of its stored key (outside margin bits), counts add up,
+    and merged keys are means (not copies of an inserted key)."""
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(C=300, redraw=0.3)
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    pool = set()
+    for f, (k, v) in enumerate(zip(d.past_k + [d.chunk_k[0]], d.past_v + [d.chunk_v[0]])):
+        codes, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
+        st, match, listed = O.tempcache_merge(st, k, v, codes, 1, cfg.n_f, f, cfg.tau, rep="mean",
+                                              planes=d.planes, B=cfg.B)
+        pool |= {row.tobytes() for row in np.asarray(k[0], dtype=np.float64)}
+        assert st.m[0, :st.size[0]].sum() + st.evicted[0] == st.inserted[0]
+    n = st.size[0]
+    codes, margin = O.hash_codes(st.K[:, :n], d.planes, cfg.T, cfg.B)
+    assert not ((codes ^ st.codes[:, :, :n]) & ~margin).any()
+    merged = st.m[0, :n] > 1
+    assert merged.any()
+    assert sum(st.K[0, s].tobytes() not in pool for s in np.nonzero(merged)[0]) > 0
+
+
 def test_tempcache_capacity_error():
     st = O.CacheState.empty(1, 2, 2, 1, "f64")
     k = np.array([[[1.0, 0.0], [0.0, 1.0], [1.0, 1.0]]])
