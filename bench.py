@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--rep", default="last", choices=["last", "mean"],
+                    help="TempCache representative: last key (the method) or mean key (ablation)")
     ap.add_argument("--recall", action="store_true",
                     help="sweep tau, T and B: recall and density of AnnSA and AnnCA (one JSON line)")
     return ap.parse_args()
@@ -482,7 +484,7 @@ def run_ours(args, cfg):
     d = layer_data(cfg, layer=rank_layer(rank), chunks=1)
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", tdt)  # noqa: E731
-    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt)
+    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt, rep=args.rep)
     path.planes.copy_(todev(d.planes))
     f = 0
     while f < cfg.past_frames:
@@ -508,7 +510,8 @@ def run_ours(args, cfg):
                             path.planes, cfg.T, cfg.B, status=st)
         rec(1)
         fa.fastar_tempcache_merge(path.cache, k, v, path.k_codes, cfg.F, cfg.n_f, first, cfg.tau,
-                                  match_out=path.match, ws=path.ws_merge, status=st)
+                                  match_out=path.match, ws=path.ws_merge, status=st, rep=args.rep,
+                                  planes=path.planes)
         rec(2)
         fa.fastar_annca_prune(path.q_codes, path.p_codes, cfg.F, cfg.n_f, cfg.B, path.kept_idx,
                               path.kept_cnt, status=st)
@@ -628,7 +631,7 @@ def run_ours(args, cfg):
             "dtype": cfg.dtype, "data": "synthetic",
             "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq, "P": cfg.P,
                        "T": cfg.T, "B": cfg.B, "C": cfg.C, "past_frames": cfg.past_frames,
-                       "l2": "flushed before every step (256 MiB write)",
+                       "l2": "flushed before every step (256 MiB write)", "representative": args.rep,
                        "parallelism": (f"layer-parallel x{world}: rank r runs layer r, no collective"
                                        if world > 1 else "single GPU")},
             "effective_tflops": eff_tflops,
@@ -713,7 +716,8 @@ def recall_metrics(cfg, path, d, chunk_q, history_k=None, history_v=None):
     q = torch.as_tensor(chunk_q).cuda().float()
     kp = torch.as_tensor(d.prompt_k).cuda().float()
     out = {"annsa_retained": [], "annsa_density": [], "annca_retained": [], "annca_kept_share": [],
-           "annsa_rel_err_vs_dense_history": [], "annca_rel_err_vs_dense_prompt": []}
+           "annsa_rel_err_vs_dense_history": [], "annca_rel_err_vs_dense_prompt": [],
+           "tempcache_rel_err_vs_dense_history": [], "tempcache_lse_gap": []}
     size = path.cache.size.tolist()
     lse = path.lse.float()
     for h in range(H):
@@ -746,6 +750,13 @@ def recall_metrics(cfg, path, d, chunk_q, history_k=None, history_v=None):
             o_dense = Fn.scaled_dot_product_attention(q[h][None], Kh[None], Vh[None])[0]
             out["annsa_rel_err_vs_dense_history"].append(
                 float((path.o_sa[h].float() - o_dense).norm() / o_dense.norm()))
+            # TempCache alone: dense attention over the merged groups (+ ln m)
+            # against dense attention over the unmerged history
+            o_merged = torch.softmax(logits, dim=1) @ path.cache.V[h, :n].float()
+            out["tempcache_rel_err_vs_dense_history"].append(
+                float((o_merged - o_dense).norm() / o_dense.norm()))
+            lse_hist = torch.logsumexp(cfg.scale * q[h] @ Kh.T, dim=1)
+            out["tempcache_lse_gap"].append(float((dense_lse - lse_hist).abs().mean()))
     return {k: (float(np.mean(v)) if v else None) for k, v in out.items()}
 
 
@@ -762,14 +773,17 @@ def run_recall(args, cfg):
     fbuild.build()
     fa.lib()
     heads = [0, 5]
-    settings = [(0.95, 2, 8), (0.90, 2, 8), (0.99, 2, 8), (0.95, 1, 8), (0.95, 4, 8), (0.95, 2, 6),
-                (0.95, 2, 10)]
+    # (tau, T, B, representative): the LSH / merge sweep with the method's
+    # last-key groups, then the mean-key ablation (paperlayer.ai appendix C)
+    settings = [(0.95, 2, 8, "last"), (0.90, 2, 8, "last"), (0.99, 2, 8, "last"), (0.95, 1, 8, "last"),
+                (0.95, 4, 8, "last"), (0.95, 2, 6, "last"), (0.95, 2, 10, "last"),
+                (0.95, 2, 8, "mean"), (0.90, 2, 8, "mean"), (0.99, 2, 8, "mean")]
     rows = []
-    for tau, T, B in settings:
+    for tau, T, B, rep in settings:
         c = cfg.replace(H=len(heads), tau=tau, T=T, B=B)
         d = layer_data(c, chunks=1, heads=heads)
         todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", torch.bfloat16)  # noqa: E731
-        path = ChunkPath(c.H, c.D, c.n_f, c.F, c.P, c.T, c.B, c.C, c.tau, torch.bfloat16)
+        path = ChunkPath(c.H, c.D, c.n_f, c.F, c.P, c.T, c.B, c.C, c.tau, torch.bfloat16, rep=rep)
         path.planes.copy_(todev(d.planes))
         f = 0
         while f < c.past_frames:
@@ -777,14 +791,25 @@ def run_recall(args, cfg):
             path.merge(todev(np.concatenate(d.past_k[f:f + nF], 1)),
                        todev(np.concatenate(d.past_v[f:f + nF], 1)), f, F=nF)
             f += nF
-        path.step(todev(d.chunk_q[0]), todev(d.chunk_k[0]), todev(d.chunk_v[0]), todev(d.prompt_k),
-                  todev(d.prompt_v), c.past_frames)
+        ins = [todev(x) for x in (d.chunk_q[0], d.chunk_k[0], d.chunk_v[0], d.prompt_k, d.prompt_v)]
         torch.cuda.synchronize()
+        snap = path.cache.snapshot()
+        # chunk latency on these heads (cache restored before each call, L2 warm)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ms = []
+        for r in range(12):
+            path.cache.restore(snap)
+            ev[0].record()
+            path.step(*ins, c.past_frames)
+            ev[1].record()
+            torch.cuda.synchronize()
+            if r >= 2:
+                ms.append(ev[0].elapsed_time(ev[1]))
         assert int(path.status.item()) == 0
         hk = np.concatenate(d.past_k + [d.chunk_k[0]], axis=1)
         hv = np.concatenate(d.past_v + [d.chunk_v[0]], axis=1)
         m = recall_metrics(c, path, d, d.chunk_q[0], hk, hv)
-        m.update({"tau": tau, "T": T, "B": B,
+        m.update({"tau": tau, "T": T, "B": B, "rep": rep, "chunk_ms_2_heads_l2_warm": float(np.median(ms)),
                   "n_live_per_head": float(path.cache.size.float().mean()),
                   "keys_before_merge_per_head": (c.past_frames + c.F) * c.n_f})
         rows.append(m)

@@ -266,6 +266,38 @@ int fastar_tempcache_merge_ev(const fastar_cache* cache, const void* k_new,
                               cudaEvent_t codes_ready);
 
 /*
+ * fastar_tempcache_merge_rep -- fastar_tempcache_merge_ev with a choice of
+ * the group representative.
+ *
+ * Passage: FAST-AR summary (paperlayer.ai) appendix C, representative
+ * selection in KV merging (last-key, mean-key and medoid-key
+ * representatives of a group of corresponding keys; the method keeps the
+ * last key).
+ *
+ * rep = FASTAR_REP_LAST: exactly fastar_tempcache_merge_ev (planes may be
+ * NULL).  rep = FASTAR_REP_MEAN: step 2 keeps the count-weighted mean key
+ * instead of the lowest j's key, K' = (m K + sum_{j in S} k_j) / m' (fp32,
+ * rounded to dt like V), and the group's codes become the hash of the stored
+ * K' with `planes` [T*B][D] dt (the hyperplanes codes_new came from; bits as
+ * in fastar_hash, a zero projection gives 0).  Unmatched keys are inserted
+ * as in the last-key mode.  The next frame is matched against the stored
+ * (mean) keys.  codes_ready as in fastar_tempcache_merge_ev (NULL: none).
+ * Errors as fastar_tempcache_merge, plus FASTAR_ERR_ARG for an unknown rep,
+ * or a NULL or misaligned planes with FASTAR_REP_MEAN; FASTAR_ERR_UNSUPPORTED
+ * when T*B > 64 with FASTAR_REP_MEAN.  The medoid-key representative needs
+ * every past member of a group and is not offered.
+ */
+#define FASTAR_REP_LAST 0
+#define FASTAR_REP_MEAN 1
+int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new,
+                               const void* v_new, const uint32_t* codes_new,
+                               int F, int n_f, int32_t first_frame, float tau,
+                               int rep, const void* planes,
+                               int32_t* match_out, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, cudaStream_t stream,
+                               cudaEvent_t codes_ready);
+
+/*
  * fastar_tempcache_merge_noalloc -- fastar_tempcache_merge without a
  * caller workspace.  The paper has no counterpart: this is a convenience of
  * this library for callers that cannot allocate device memory, such as a

@@ -19,6 +19,8 @@ LIB_PATH = os.path.join(_PKG, "libfastar.so")
 
 BF16, F32 = 0, 1
 OP_HASH, OP_MERGE, OP_PRUNE, OP_ANNCA, OP_ANNSA = 0, 1, 2, 3, 4
+REP_LAST, REP_MEAN = 0, 1
+REPS = {"last": REP_LAST, "mean": REP_MEAN}
 STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "FASTAR_ERR_CUDA",
           4: "FASTAR_ERR_WORKSPACE", 16: "FASTAR_ERR_CAPACITY", 17: "FASTAR_ERR_TIMEOUT",
           18: "FASTAR_ERR_DEVICE_ARG"}
@@ -26,7 +28,7 @@ EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
            "fastar_workspace_size", "fastar_hash", "fastar_hash_many", "fastar_bucket_csr",
            "fastar_tempcache_merge", "fastar_tempcache_merge_ev", "fastar_annca_prune", "fastar_annca_attention",
-           "fastar_annsa_attention", "fastar_check_bounded_wait"]
+           "fastar_annsa_attention", "fastar_check_bounded_wait", "fastar_tempcache_merge_rep"]
 
 
 class FastarError(RuntimeError):
@@ -88,6 +90,8 @@ def lib() -> ctypes.CDLL:
         L.fastar_annsa_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _I, ctypes.POINTER(CacheStruct),
                                              _F, _VP, _VP, _VP, _SZ, _VP, _VP]
         L.fastar_check_bounded_wait.argtypes = [_I, _VP, _VP]
+        L.fastar_tempcache_merge_rep.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
+                                                 ctypes.c_int32, _F, _I, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]
         for name in EXPORTS[7:]:
             getattr(L, name).restype = _I
         _lib = L
@@ -246,13 +250,22 @@ class Cache:
 
 
 def fastar_tempcache_merge(cache: Cache, k_new, v_new, codes_new, F, n_f, first_frame, tau,
-                           match_out=None, ws=None, status=None, stream=None, codes_ready=None):
+                           match_out=None, ws=None, status=None, stream=None, codes_ready=None,
+                           rep="last", planes=None):
     """Merge the F frames of a chunk (k_new/v_new [H][F*n_f][D]) into `cache`.
 
     codes_ready: a torch.cuda.Event after which codes_new and v_new are
-    final (fastar_tempcache_merge_ev); None: they are ready on `stream`."""
+    final (fastar_tempcache_merge_ev); None: they are ready on `stream`.
+    rep: "last" (the method's representative) or "mean" (the mean-key
+    ablation, fastar_tempcache_merge_rep; needs the hash `planes`)."""
     ws, nbytes = _ws(OP_MERGE, cache.H, n_f, cache.D, cache.T, cache.B, cache.C, ws, k_new.device)
     cs = cache.struct()
+    if rep != "last":
+        _check(lib().fastar_tempcache_merge_rep(
+            ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F, n_f, first_frame, tau, REPS[rep],
+            _p(planes), _p(match_out), _p(ws), nbytes, _p(status), _stream(stream),
+            None if codes_ready is None else codes_ready.cuda_event), "fastar_tempcache_merge_rep")
+        return
     args = (ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F, n_f, first_frame, tau,
             _p(match_out), _p(ws), nbytes, _p(status), _stream(stream))
     if codes_ready is None:

@@ -192,7 +192,7 @@ int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_d
 int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
                  const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                  int32_t* match_out, void* ws, int32_t* st, cudaStream_t s,
-                 cudaEvent_t codes_ready = nullptr);
+                 cudaEvent_t codes_ready = nullptr, int rep = 0, const void* planes = nullptr);
 size_t merge_ws_bytes(int H, int n_f, int C);
 int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,
                  int P, int T, int B, int32_t* kept_idx, int32_t* kept_cnt, int32_t* st,

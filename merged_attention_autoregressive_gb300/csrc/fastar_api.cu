@@ -218,9 +218,15 @@ static int check_cache(const fastar_cache* c) {
 static int merge_checked(const fastar_cache* cache, const void* k_new, const void* v_new,
                          const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                          int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
-                         cudaStream_t stream, cudaEvent_t codes_ready) {
+                         cudaStream_t stream, cudaEvent_t codes_ready, int rep = FASTAR_REP_LAST,
+                         const void* planes = nullptr) {
   int rc = check_cache(cache);
   if (rc != FASTAR_OK) return rc;
+  if (rep != FASTAR_REP_LAST && rep != FASTAR_REP_MEAN) return FASTAR_ERR_ARG;
+  if (rep == FASTAR_REP_MEAN) {
+    if (!planes || !aligned16(planes)) return FASTAR_ERR_ARG;
+    if (cache->T * cache->B > 64) return FASTAR_ERR_UNSUPPORTED;
+  }
   if (F < 0 || n_f < 0 || n_f > cache->C) return FASTAR_ERR_ARG;
   if (n_f > FASTAR_MAX_FRAME_KEYS) return FASTAR_ERR_UNSUPPORTED;
   if (F == 0 || n_f == 0 || cache->H == 0) {
@@ -237,7 +243,7 @@ static int merge_checked(const fastar_cache* cache, const void* k_new, const voi
   const size_t need = merge_ws_bytes(cache->H, n_f, cache->C);
   if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
   return launch_merge(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws,
-                      dev_status, stream, codes_ready);
+                      dev_status, stream, codes_ready, rep, planes);
 }
 
 int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const void* v_new,
@@ -254,6 +260,14 @@ int fastar_tempcache_merge_ev(const fastar_cache* cache, const void* k_new, cons
                               cudaStream_t stream, cudaEvent_t codes_ready) {
   return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
                        dev_status, stream, codes_ready);
+}
+
+int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new, const void* v_new,
+                               const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                               int rep, const void* planes, int32_t* match_out, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, cudaStream_t stream, cudaEvent_t codes_ready) {
+  return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
+                       dev_status, stream, codes_ready, rep, planes);
 }
 
 int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,

@@ -86,6 +86,7 @@ struct NnArgs {
   float* invn_out;                 // inverse norms of this frame's keys [H][ldn]
   unsigned long long* best_out;    // packed best candidate [H][n_f]
   float tau;                       // join threshold on the cosine
+  int from_cache;                  // candidates of every frame are staged cache rows (mean-key groups)
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -120,8 +121,9 @@ struct Seg {
   int h, qt, ct0, ct1, tiles, nc;
 };
 
+__device__ __forceinline__ bool later_frame(const NnArgs& a) { return a.fi > 0 && !a.from_cache; }
 __device__ __forceinline__ int head_cands(const NnArgs& a, int h) {
-  return a.fi > 0 ? a.n_f : min(max(a.ncand[h], 0), a.C);
+  return later_frame(a) ? a.n_f : min(max(a.ncand[h], 0), a.C);
 }
 __device__ __forceinline__ void walk_head(const NnArgs& a, Walk& w, int h) {
   w.h = h;
@@ -165,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
   NnSmem& sm = *reinterpret_cast<NnSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int atiles = (a.n_f + kM - 1) / kM;
-  const bool later = a.fi > 0;
+  const bool later = later_frame(a);
   // After the first frame every head has n_f candidates, so the unit range
   // and the first segment are known before the wait.
   int u0 = 0, u1 = 0, npre = 0;
@@ -474,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
                  int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv, int ldc,
                  const int32_t* prev_slot, const float* invn_prev, float* invn_out, int ldn,
-                 unsigned long long* best_out, const void* stage, float tau, int32_t* st, cudaStream_t s) {
+                 unsigned long long* best_out, const void* stage, float tau, int32_t* st, cudaStream_t s,
+                 int from_cache) {
   if (dt != FASTAR_BF16 || D != kD) return FASTAR_ERR_UNSUPPORTED;
   if (n_f == 0 || H == 0) return FASTAR_OK;
   if ((ldc & 3) || (ldn & 3) || ldc < C || ldn < n_f) return FASTAR_ERR_ARG;
@@ -497,7 +500,7 @@ int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, i
   const long long units = (long long)((n_f + kM - 1) / kM) * H * max(1, (n_f + kN - 1) / kN);
   const int grid = (int)std::min<long long>(2LL * sms, units);
   NnArgs a{(const __nv_bfloat16*)k_new, (const __nv_bfloat16*)K, H, n_f, Nrow, fi, C, ldn, ldc, cand, ncand, cinv,
-           prev_slot, invn_prev, invn_out, best_out, tau};
+           prev_slot, invn_prev, invn_out, best_out, tau, from_cache};
   fastar::launch_pdl((nn_tc_kernel), dim3(grid), kThreads, smem, s, mapA, mapB, mapS, a, st);
   FASTAR_LAUNCHED(s, "nn_tc");
   return FASTAR_OK;

@@ -445,8 +445,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
 // One warp per kApplyKeys consecutive keys (their plan records, then all of
 // their rows, are loaded before any is used); lane l handles the D/32
 // consecutive dimensions starting at l * D/32 (one vector access per row).
+// With the mean-key representative (planes != nullptr; FAST-AR summary,
+// paperlayer.ai, appendix C) a joined group's key becomes the count-weighted
+// mean of its keys, summed like the value, and its codes the hash of the
+// stored mean: one warp-reduced dot product per hyperplane, a zero
+// projection giving bit 0.
 constexpr int kApplyKeys = 4;
-template <typename T, int D>
+
+template <typename T>
+__device__ __forceinline__ float stored(float x) {
+  T y;
+  Elem<T>::st(&y, x);
+  return Elem<T>::ld(&y);
+}
+template <typename T, int D, bool kMean>
 __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
                                                     const uint32_t* __restrict__ codes_frame, int n_f,
                                                     int row_stride_keys, int Tt, int32_t f,
@@ -455,7 +467,8 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
                                                     const int32_t* __restrict__ plan_kind,
                                                     const int32_t* __restrict__ plan_cnt, T* K, T* V,
                                                     int32_t* m, uint32_t* codes, int32_t* last_frame,
-                                                    int C, int32_t* st) {
+                                                    int C, const T* __restrict__ planes, int Bb,
+                                                    int32_t* st) {
   constexpr int PER = D / 32;
   const int h = blockIdx.y;
   const int j0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kApplyKeys;
@@ -463,7 +476,8 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
   // the keys' k and v rows are inputs of the call (an earlier kernel of the
   // call has already waited for their producers): load them before the wait
   using Raw = typename VecOf<T, PER>::type;
-  Raw kv[kApplyKeys], vv[kApplyKeys], vo[kApplyKeys];
+  Raw kv[kApplyKeys], vv[kApplyKeys], vo[kApplyKeys], ko[kApplyKeys];
+  constexpr bool mean_key = kMean;
 #pragma unroll
   for (int u = 0; u < kApplyKeys; ++u) {
     if (j0 + u >= n_f) continue;
@@ -492,6 +506,7 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
     if (kind[u] == KIND_LEADER) {
       m_old[u] = m[(size_t)h * C + slot[u]];
       vo[u] = ld_raw<T, PER>(V + ((size_t)h * C + slot[u]) * D + lane * PER);
+      if constexpr (kMean) ko[u] = ld_raw<T, PER>(K + ((size_t)h * C + slot[u]) * D + lane * PER);
     }
   }
 #pragma unroll
@@ -502,11 +517,17 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
     int m_new = 1;
     if (kind[u] == KIND_LEADER) {
       m_new = m_old[u] + cnt[u];
-      float acc[PER], x[PER];
+      float acc[PER], x[PER], kacc[PER];
       raw_to_float<T, PER>(vo[u], acc);
       raw_to_float<T, PER>(vv[u], x);
 #pragma unroll
       for (int i = 0; i < PER; ++i) acc[i] = (float)m_old[u] * acc[i] + x[i];
+      if constexpr (kMean) {
+        raw_to_float<T, PER>(ko[u], kacc);
+        raw_to_float<T, PER>(kv[u], x);
+#pragma unroll
+        for (int i = 0; i < PER; ++i) kacc[i] = (float)m_old[u] * kacc[i] + x[i];
+      }
       if (cnt[u] > 1) {
         // the other members of the group, in ascending key order: the warp
         // tests 32 keys per step and adds the members it finds in order
@@ -521,6 +542,11 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
             ld_vec<T, PER>(v_frame + ((size_t)h * row_stride_keys + base + k) * D + lane * PER, x);
 #pragma unroll
             for (int i = 0; i < PER; ++i) acc[i] += x[i];
+            if constexpr (kMean) {
+              ld_vec<T, PER>(k_frame + ((size_t)h * row_stride_keys + base + k) * D + lane * PER, x);
+#pragma unroll
+              for (int i = 0; i < PER; ++i) kacc[i] += x[i];
+            }
             --left;
           }
         }
@@ -529,16 +555,43 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
 #pragma unroll
       for (int i = 0; i < PER; ++i) acc[i] = acc[i] / mf;
       st_vec<T, PER>(V + crow, acc);
+      if constexpr (kMean) {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) kacc[i] = kacc[i] / mf;
+        st_vec<T, PER>(K + crow, kacc);
+        // codes of the stored (rounded) mean key
+#pragma unroll
+        for (int i = 0; i < PER; ++i) kacc[i] = stored<T>(kacc[i]);
+        uint32_t code = 0u;
+        for (int r = 0; r < Tt * Bb; ++r) {
+          float pr[PER];
+          ld_vec<T, PER>(planes + (size_t)r * D + lane * PER, pr);
+          float dot = 0.f;
+#pragma unroll
+          for (int i = 0; i < PER; ++i) dot = fmaf(pr[i], kacc[i], dot);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+          const int t = r / Bb, b = r - t * Bb;
+          code |= (dot > 0.f ? 1u : 0u) << b;
+          if (b == Bb - 1) {
+            if (lane == 0) codes[((size_t)h * Tt + t) * C + s] = code;
+            code = 0u;
+          }
+        }
+      }
     } else {
       st_raw<T, PER>(V + crow, vv[u]);
     }
-    st_raw<T, PER>(K + crow, kv[u]);
+    // K and codes of key j (a mean-key group's were written above)
+    const bool own_key = !kMean || kind[u] != KIND_LEADER;
+    if (own_key) st_raw<T, PER>(K + crow, kv[u]);
     if (lane == 0) {
       m[(size_t)h * C + s] = m_new;
       last_frame[(size_t)h * C + s] = f;
     }
-    for (int t = lane; t < Tt; t += 32)
-      codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
+    if (own_key)
+      for (int t = lane; t < Tt; t += 32)
+        codes[((size_t)h * Tt + t) * C + s] = codes_frame[((size_t)h * Tt + t) * row_stride_keys + j];
   }
   pdl_trigger();
 }
@@ -546,13 +599,18 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
 int launch_nn_tc(fastar_dtype dt, const void* k_new, int n_f, int Nrow, int H, int fi, const void* K,
                  int C, int D, const int32_t* cand, const int32_t* ncand, const float* cinv, int ldc,
                  const int32_t* prev_slot, const float* invn_prev, float* invn_out, int ldn,
-                 unsigned long long* best_out, const void* stage, float tau, int32_t* st, cudaStream_t s);
+                 unsigned long long* best_out, const void* stage, float tau, int32_t* st, cudaStream_t s,
+                 int from_cache);
 
 template <typename T, int D>
 static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
                       const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
-                      int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready) {
+                      int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready,
+                      int rep, const void* planes) {
   const int H = c->H, C = c->C, Tt = c->T;
+  // mean-key groups: every frame's candidates are cache rows (their stored
+  // means), staged like the first frame's; the apply re-hashes merged keys
+  const bool mean_key = rep == FASTAR_REP_MEAN;
   MergeWs w = carve(ws, H, n_f, C);
   // the plan keeps one int per key of a frame and a hash table of the
   // frame's groups (3 ints per entry, at least 4/3 n_f entries) in shared
@@ -583,10 +641,16 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     const T* vf = (const T*)v_new + (size_t)fi * n_f * D;
     const uint32_t* cf = codes_new + (size_t)fi * n_f;
     int rc = FASTAR_ERR_UNSUPPORTED;
+    if (tc_nn && mean_key && fi > 0) {
+      // the candidates the previous plan listed, with the keys its apply wrote
+      fastar::launch_pdl((cand_norm_kernel), dim3((n_f + 8 * kNormCands - 1) / (8 * kNormCands), H), wblock, 0, s,
+                         (const __nv_bfloat16*)c->K, C, w.cand[cur], w.ncand[cur], w.cinv, w.ldc, w.stage, n_f, st);
+      FASTAR_LAUNCHED(s, "cand_norm");
+    }
     if (tc_nn)
       rc = launch_nn_tc(FASTAR_BF16, k_new, n_f, Nrow, H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.cinv,
                         w.ldc, w.plan_slot, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.ldn, w.best, w.stage,
-                        tau, st, s);
+                        tau, st, s, mean_key ? 1 : 0);
     if (rc == FASTAR_ERR_UNSUPPORTED) {
       fastar::launch_pdl((nn_simt_kernel<T, D>), wgrid, wblock, 0, s, kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], w.best, st);
@@ -604,9 +668,15 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
       (void)cudaGetLastError();
       return FASTAR_ERR_CUDA;
     }
-    fastar::launch_pdl((apply_kernel<T, D>), dim3((n_f + 8 * kApplyKeys - 1) / (8 * kApplyKeys), H), wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match, w.plan_slot,
-                                                w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m,
-                                                c->codes, c->last_frame, C, st);
+    const dim3 agrid((n_f + 8 * kApplyKeys - 1) / (8 * kApplyKeys), H);
+    if (mean_key)
+      fastar::launch_pdl((apply_kernel<T, D, true>), agrid, wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match,
+                         w.plan_slot, w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m, c->codes, c->last_frame,
+                         C, (const T*)planes, c->B, st);
+    else
+      fastar::launch_pdl((apply_kernel<T, D, false>), agrid, wblock, 0, s, kf, vf, cf, n_f, Nrow, Tt, f, w.match,
+                         w.plan_slot, w.plan_kind, w.plan_cnt, (T*)c->K, (T*)c->V, c->m, c->codes, c->last_frame,
+                         C, (const T*)nullptr, c->B, st);
     FASTAR_LAUNCHED(s, "apply");
   }
   return launch_csr(c->codes, H * Tt, C, c->size, Tt, 1 << c->B, c->perm, c->offsets, st, s);
@@ -614,15 +684,16 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
 
 int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
                  const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
-                 int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready) {
+                 int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready,
+                 int rep, const void* planes) {
   if (c->dt == FASTAR_F32 && c->D == 64)
-    return merge_impl<float, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
+    return merge_impl<float, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
   if (c->dt == FASTAR_F32 && c->D == 128)
-    return merge_impl<float, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
+    return merge_impl<float, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
   if (c->dt == FASTAR_BF16 && c->D == 64)
-    return merge_impl<__nv_bfloat16, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
+    return merge_impl<__nv_bfloat16, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
   if (c->dt == FASTAR_BF16 && c->D == 128)
-    return merge_impl<__nv_bfloat16, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready);
+    return merge_impl<__nv_bfloat16, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
   return FASTAR_ERR_UNSUPPORTED;
 }
 

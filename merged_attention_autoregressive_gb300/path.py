@@ -19,8 +19,9 @@ from . import (Cache, OP_ANNCA, OP_ANNSA, OP_MERGE, fastar_annca_attention, fast
 class ChunkPath:
     """Buffers and calls of one layer's per-chunk path."""
 
-    def __init__(self, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda"):
+    def __init__(self, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last"):
         self.H, self.D, self.n_f, self.F, self.P = H, D, n_f, F, P
+        self.rep = rep  # TempCache representative: "last" (the method) or "mean" (ablation)
         self.T, self.B, self.C, self.tau, self.dtype = T, B, C, tau, dtype
         self.Nq = F * n_f
         self.scale = D ** -0.5
@@ -80,7 +81,7 @@ class ChunkPath:
         fastar_hash(k, self.planes, self.T, self.B, codes, status=self.status, stream=stream)
         fastar_tempcache_merge(self.cache, k, v, codes, F, self.n_f, first_frame, self.tau,
                                match_out=match, ws=self.ws_merge, status=self.status,
-                               stream=stream)
+                               stream=stream, rep=self.rep, planes=self.planes)
         return codes, match
 
     def step(self, q, k, v, kp, vp, first_frame, stream=None):
@@ -177,7 +178,7 @@ class ChunkPath:
         self._cross_done.record(side)
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
-                               stream=main, codes_ready=self._codes_ready)
+                               stream=main, codes_ready=self._codes_ready, rep=self.rep, planes=self.planes)
         main.wait_event(self._csr_done)
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,

@@ -126,6 +126,12 @@ def test_host_argument_errors_need_no_gpu(L):
     assert L.fastar_check_bounded_wait(8, None, None) == 1
     assert L.fastar_check_bounded_wait(0, fake, None) == 1
     assert L.fastar_check_bounded_wait(65537, fake, None) == 1
+    # merge with a representative mode: unknown mode, mean-key without planes
+    import merged_attention_autoregressive_gb300 as m2
+    cs = m2.CacheStruct(1, 128, 64, 1, 4, 0, *([0x1000] * 10))
+    for rep, planes in ((2, fake), (1, None), (1, vp(0x1004))):
+        assert L.fastar_tempcache_merge_rep(ctypes.byref(cs), fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9),
+                                            rep, planes, None, None, 0, None, None, None) == 1
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
