@@ -431,6 +431,85 @@ def annsa_attention(q, q_codes, state: CacheState, scale: float, rows=None):
     return o, lse
 
 
+# ---------------------------------------------------------------- denoising steps
+# One chunk is denoised over S steps, each with its own queries, keys and
+# values; generation is conditioned on the history in the cache ([PL]
+# related work: chunked autoregressive denoising conditioned on previously
+# generated history).  Sparse attention is off for the first 30 % of the
+# denoising steps ([RB] limitations, fifth point).  Readings: step s is dense
+# iff s < 0.3 S; a step before the last attends the cache's groups (+ ln m)
+# together with its own keys (count 1) and writes nothing to the cache;
+# the last step merges its keys into the cache (TempCache) and attends the
+# merged cache, as the single-step chunk does.  A sparse step restricts
+# self-attention to pairs that share a bucket in some table (on the cache
+# and on its own keys alike) and cross-attention to each frame's kept prompt
+# tokens; a dense step allows every live pair and every prompt token.
+DENSE_FRAC = 0.3
+
+
+def denoise_schedule(S: int, dense_frac: float = DENSE_FRAC):
+    """dense[s] for the S denoising steps of a chunk: s < dense_frac * S."""
+    return [s < dense_frac * S for s in range(S)]
+
+
+def denoise_step_attention(q, q_codes, state: CacheState, k, v, k_codes, dense: bool, scale: float):
+    """Self-attention of a non-final denoising step over the cache and the
+    step's own keys (not merged).  q, k, v: [H][Nq][D]; q_codes, k_codes:
+    [H][T][Nq].  Returns (o [H][Nq][D], lse [H][Nq])."""
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    H, Nq, D = q.shape
+    o = np.zeros((H, Nq, D))
+    lse = np.zeros((H, Nq))
+    for h in range(H):
+        size = int(state.size[h])
+        K = np.concatenate([state.K[h, :size], k[h]])
+        V = np.concatenate([state.V[h, :size], v[h]])
+        bias = np.concatenate([np.log(state.m[h, :size].astype(np.float64)), np.zeros(k.shape[1])])
+        if dense:
+            allowed = np.ones((Nq, K.shape[0]), dtype=bool)
+        else:
+            allowed = np.concatenate([annsa_allowed(np.asarray(q_codes)[h], state.codes[h, :, :size]),
+                                      annsa_allowed(np.asarray(q_codes)[h], np.asarray(k_codes)[h])], axis=1)
+        o[h], lse[h] = masked_attention(q[h], K, V, allowed, bias, scale)
+    return o, lse
+
+
+def denoise_chunk(state: CacheState, steps, k_p, v_p, planes, T: int, B: int, F: int, n_f: int,
+                  first_frame: int, tau: float, scale: float, dense_frac: float = DENSE_FRAC):
+    """The S denoising steps of one chunk.  steps: list of (q, k, v), each
+    [H][F*n_f][D].  Returns (outs, final_state, match) where outs[s] =
+    (o_sa, lse_sa, o_ca) and match is the final merge's."""
+    dense = denoise_schedule(len(steps), dense_frac)
+    pc, _ = hash_codes(k_p, planes, T, B)
+    H, P = np.asarray(k_p).shape[:2]
+    st = state
+    outs = []
+    match = None
+    for s, (q, k, v) in enumerate(steps):
+        qc, _ = hash_codes(q, planes, T, B)
+        kc, _ = hash_codes(k, planes, T, B)
+        if dense[s]:
+            idx = np.tile(np.arange(P), (H, F, 1))
+            cnt = np.full((H, F), P)
+        else:
+            idx, cnt = annca_prune(qc, pc, F, n_f)
+        o_ca = annca_attention(q, k_p, v_p, idx, cnt, F, n_f, scale)
+        if s + 1 < len(steps):
+            o_sa, lse = denoise_step_attention(q, qc, st, k, v, kc, dense[s], scale)
+        else:
+            st, match, _ = tempcache_merge(st, k, v, kc, F, n_f, first_frame, tau)
+            if dense[s]:
+                qc = np.zeros((H, 1, np.asarray(q).shape[1]), np.uint32)
+                view = dataclasses.replace(st, codes=np.zeros((H, 1, st.C), np.uint32))
+                o_sa, lse = annsa_attention(q, qc, view, scale)
+            else:
+                o_sa, lse = annsa_attention(q, qc, st, scale)
+        outs.append((o_sa, lse, o_ca))
+    return outs, st, match
+
+
 # ---------------------------------------------------------------- recall / density
 # The pages measure how much of the dense attention the sparse selections
 # keep (recall and density: FAST-AR summary, paperlayer.ai section 7 and

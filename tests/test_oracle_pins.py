@@ -547,3 +547,109 @@ def test_annsa_and_annca_retained_end_points():
     r, share = O.annca_retained(q, kp, idx, cnt, F, n_f, 0.3)
     np.testing.assert_allclose(r, 1.0, rtol=1e-12)
     np.testing.assert_array_equal(share, 1.0)
+
+
+# ------------------------------------------------------- denoising steps
+def test_denoise_schedule_hand_values():
+    """Sparse attention is off for the first 30 % of the denoising steps
+    (paper.rainbus.top, limitations): step s is dense iff s < 0.3 S."""
+    want = {1: [1], 2: [1, 0], 3: [1, 0, 0], 4: [1, 1, 0, 0], 5: [1, 1, 0, 0, 0],
+            10: [1, 1, 1, 0, 0, 0, 0, 0, 0, 0]}
+    for S, w in want.items():
+        assert O.denoise_schedule(S) == [bool(x) for x in w], S
+
+
+def _perm_history(rng, n, D, frames):
+    st = O.CacheState.empty(1, 64, D, 1, "f64")
+    allk, allv = [], []
+    k = rng.standard_normal((n, D))
+    for f in range(frames):
+        if f:
+            k = k[rng.permutation(n)]
+        v = rng.standard_normal((n, D))
+        allk.append(k)
+        allv.append(v)
+        st, _, _ = O.tempcache_merge(st, k[None], v[None], np.zeros((1, 1, n), np.uint32), 1, n, f, 0.95)
+    return st, np.concatenate(allk), np.concatenate(allv)
+
+
+def test_denoise_dense_step_equals_dense_attention_over_history_and_chunk():
+    """A dense step over a cache of exact-duplicate groups equals dense
+    softmax attention over the full unmerged history plus the step's own
+    keys (Lemma 5.1 for the cache part; the step's keys count once)."""
+    rng = np.random.default_rng(21)
+    n, D = 10, 16
+    st, Kh, Vh = _perm_history(rng, n, D, 4)
+    q, k, v = (rng.standard_normal((1, 7, D)) for _ in range(3))
+    codes = np.zeros((1, 1, 7), np.uint32)
+    o, lse = O.denoise_step_attention(q, codes, st, k, v, codes, True, 1 / math.sqrt(D))
+    K = np.concatenate([Kh, k[0]])
+    V = np.concatenate([Vh, v[0]])
+    s = (q[0] @ K.T) / math.sqrt(D)
+    np.testing.assert_allclose(o[0], softmax(s, axis=1) @ V, atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse[0], logsumexp(s, axis=1), atol=1e-12, rtol=0)
+
+
+def test_denoise_sparse_step_mask_by_brute_force():
+    """A sparse step allows (query, key) iff some table's codes agree, on the
+    cache's groups and on the step's own keys alike: checked against a mask
+    built pair by pair and scipy's softmax over the allowed logits."""
+    rng = np.random.default_rng(22)
+    H, D, T, B, nq, nk, C = 1, 8, 2, 2, 6, 5, 16
+    st = O.CacheState.empty(H, C, D, T, "f64")
+    planes = rng.standard_normal((T * B, D))
+    k0 = rng.standard_normal((1, 9, D))
+    c0, _ = O.hash_codes(k0, planes, T, B)
+    st, _, _ = O.tempcache_merge(st, k0, rng.standard_normal((1, 9, D)), c0, 1, 9, 0, 2.0)
+    q, k, v = rng.standard_normal((1, nq, D)), rng.standard_normal((1, nk, D)), rng.standard_normal((1, nk, D))
+    qc, _ = O.hash_codes(q, planes, T, B)
+    kc, _ = O.hash_codes(k, planes, T, B)
+    o, _ = O.denoise_step_attention(q, qc, st, k, v, kc, False, 0.5)
+    size = int(st.size[0])
+    keys = [st.K[0, s] for s in range(size)] + [k[0, j] for j in range(nk)]
+    vals = [st.V[0, s] for s in range(size)] + [v[0, j] for j in range(nk)]
+    kcodes = [[int(st.codes[0, t, s]) for t in range(T)] for s in range(size)] + \
+        [[int(kc[0, t, j]) for t in range(T)] for j in range(nk)]
+    for i in range(nq):
+        ok = [any(int(qc[0, t, i]) == kcodes[j][t] for t in range(T)) for j in range(len(keys))]
+        if not any(ok):
+            np.testing.assert_array_equal(o[0, i], 0)
+            continue
+        logits = np.array([0.5 * q[0, i] @ keys[j] for j in range(len(keys)) if ok[j]])
+        ref = softmax(logits) @ np.array([vals[j] for j in range(len(keys)) if ok[j]])
+        np.testing.assert_allclose(o[0, i], ref, atol=1e-12, rtol=0)
+
+
+def test_denoise_chunk_writes_the_cache_only_at_the_last_step():
+    """Non-final steps leave the cache as it was; the final state is the
+    TempCache merge of the last step's keys, and the last step attends the
+    merged cache (dense when the schedule says so)."""
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(redraw=0.3)
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    for f in range(cfg.past_frames):
+        c, _ = O.hash_codes(d.past_k[f], d.planes, cfg.T, cfg.B)
+        st, _, _ = O.tempcache_merge(st, d.past_k[f], d.past_v[f], c, 1, cfg.n_f, f, cfg.tau)
+    rng = np.random.default_rng(5)
+    steps = [tuple(x + rng.normal(0, 0.05 * (3 - s), x.shape) for x in (d.chunk_q[0], d.chunk_k[0], d.chunk_v[0]))
+             for s in range(4)]
+    before = st.copy()
+    outs, fin, match = O.denoise_chunk(st, steps, d.prompt_k, d.prompt_v, d.planes, cfg.T, cfg.B, cfg.F,
+                                       cfg.n_f, cfg.past_frames, cfg.tau, cfg.scale)
+    for name in ("K", "V", "m", "codes", "size"):
+        np.testing.assert_array_equal(getattr(st, name), getattr(before, name))
+    kc, _ = O.hash_codes(steps[-1][1], d.planes, cfg.T, cfg.B)
+    want, want_match, _ = O.tempcache_merge(before, steps[-1][1], steps[-1][2], kc, cfg.F, cfg.n_f,
+                                            cfg.past_frames, cfg.tau)
+    np.testing.assert_array_equal(fin.K, want.K)
+    np.testing.assert_array_equal(match, want_match)
+    qc, _ = O.hash_codes(steps[-1][0], d.planes, cfg.T, cfg.B)
+    o_last, _ = O.annsa_attention(steps[-1][0], qc, fin, cfg.scale)   # step 3 of 4 is sparse
+    np.testing.assert_array_equal(outs[-1][0], o_last)
+    # a dense first step differs from its sparse counterpart (the schedule matters)
+    q0, k0, v0 = steps[0]
+    q0c, _ = O.hash_codes(q0, d.planes, cfg.T, cfg.B)
+    k0c, _ = O.hash_codes(k0, d.planes, cfg.T, cfg.B)
+    o_sparse, _ = O.denoise_step_attention(q0, q0c, before, k0, v0, k0c, False, cfg.scale)
+    assert np.abs(outs[0][0] - o_sparse).max() > 1e-3
