@@ -393,6 +393,45 @@ int fastar_annsa_attention(fastar_dtype dt, const void* q,
                            float* lse, void* ws, size_t ws_bytes,
                            int32_t* dev_status, cudaStream_t stream);
 
+/*
+ * fastar_annsa_attention_part / fastar_annsa_combine -- AnnSA over several
+ * key sets whose results are merged exactly, for the denoising steps of a
+ * chunk.
+ *
+ * Passage: FAST-AR analysis (paper.rainbus.top), limitations (sparse
+ * attention is off for the first 30 % of the denoising steps) and method
+ * steps, AnnSA; FAST-AR summary (paperlayer.ai) related work (each chunk is
+ * denoised conditioned on the history).  A denoising step before the last
+ * attends the cache together with its own keys, which are not merged into
+ * it: the caller describes those keys as a second fastar_cache (K, V = the
+ * step's keys and values, m = 1, codes and CSR of their hash, size = Nq)
+ * and, for a dense step, both key sets with one table of one bit whose codes
+ * are all 0 (every pair allowed).
+ *
+ * fastar_annsa_attention_part computes what fastar_annsa_attention does
+ * for `cache`, but leaves each table's unnormalised partial (fp32 o, max,
+ * sum) in slots part_base .. part_base + T - 1 of a workspace of part_total
+ * slots (sized by fastar_workspace_size(FASTAR_OP_ANNSA_PARTS, H, Nq, D,
+ * part_total, ...)); nothing else is written.  fastar_annsa_combine then
+ * merges the part_total partials of every query (the softmax over the union
+ * of the key sets, which must be disjoint) into out [H][Nq][D] dt and the
+ * optional lse [H][Nq].  1 <= part_total <= 4 and part_base + T <=
+ * part_total (FASTAR_ERR_ARG otherwise); bf16 with D = 128 only
+ * (FASTAR_ERR_UNSUPPORTED otherwise).  Every slot must be written by a part
+ * call on the same stream before the combine.
+ */
+#define FASTAR_OP_ANNSA_PARTS 5
+int fastar_annsa_attention_part(fastar_dtype dt, const void* q,
+                                const uint32_t* q_codes, const int32_t* q_perm,
+                                const int32_t* q_offsets, int Nq,
+                                const fastar_cache* cache, float scale,
+                                int part_base, int part_total, void* ws,
+                                size_t ws_bytes, int32_t* dev_status,
+                                cudaStream_t stream);
+int fastar_annsa_combine(int H, int Nq, int D, int part_total, const void* ws,
+                         size_t ws_bytes, void* out, float* lse,
+                         int32_t* dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libfastar.so")
 
 BF16, F32 = 0, 1
-OP_HASH, OP_MERGE, OP_PRUNE, OP_ANNCA, OP_ANNSA = 0, 1, 2, 3, 4
+OP_HASH, OP_MERGE, OP_PRUNE, OP_ANNCA, OP_ANNSA, OP_ANNSA_PARTS = 0, 1, 2, 3, 4, 5
 REP_LAST, REP_MEAN = 0, 1
 REPS = {"last": REP_LAST, "mean": REP_MEAN}
 STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "FASTAR_ERR_CUDA",
@@ -28,7 +28,8 @@ EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_timing_begin", "fastar_timing_end", "fastar_timing_name",
            "fastar_workspace_size", "fastar_hash", "fastar_hash_many", "fastar_bucket_csr",
            "fastar_tempcache_merge", "fastar_tempcache_merge_ev", "fastar_annca_prune", "fastar_annca_attention",
-           "fastar_annsa_attention", "fastar_check_bounded_wait", "fastar_tempcache_merge_rep"]
+           "fastar_annsa_attention", "fastar_check_bounded_wait", "fastar_tempcache_merge_rep",
+           "fastar_annsa_attention_part", "fastar_annsa_combine"]
 
 
 class FastarError(RuntimeError):
@@ -90,6 +91,9 @@ def lib() -> ctypes.CDLL:
         L.fastar_annsa_attention.argtypes = [_I, _VP, _VP, _VP, _VP, _I, ctypes.POINTER(CacheStruct),
                                              _F, _VP, _VP, _VP, _SZ, _VP, _VP]
         L.fastar_check_bounded_wait.argtypes = [_I, _VP, _VP]
+        L.fastar_annsa_attention_part.argtypes = [_I, _VP, _VP, _VP, _VP, _I, ctypes.POINTER(CacheStruct),
+                                                  _F, _I, _I, _VP, _SZ, _VP, _VP]
+        L.fastar_annsa_combine.argtypes = [_I, _I, _I, _I, _VP, _SZ, _VP, _VP, _VP, _VP]
         L.fastar_tempcache_merge_rep.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
                                                  ctypes.c_int32, _F, _I, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]
         for name in EXPORTS[7:]:
@@ -233,6 +237,18 @@ class Cache:
 
     BUFFERS = ("K", "V", "m", "codes", "last_frame", "size", "inserted", "evicted", "perm", "offsets")
 
+    @classmethod
+    def view(cls, T, B, **buffers):
+        """A cache description over existing tensors (nothing is allocated):
+        K, V [H][C][D], m, last_frame [H][C], codes, perm [H][T][C], size [H],
+        inserted, evicted [H] and offsets [H][T][2^B+1], all given."""
+        c = cls.__new__(cls)
+        c.H, c.C, c.D = buffers["K"].shape
+        c.T, c.B, c.dtype = T, B, buffers["K"].dtype
+        for n in cls.BUFFERS:
+            setattr(c, n, buffers[n])
+        return c
+
     def struct(self) -> CacheStruct:
         return CacheStruct(self.H, self.D, self.C, self.T, self.B,
                            BF16 if self.dtype == torch.bfloat16 else F32,
@@ -297,6 +313,24 @@ def fastar_annca_attention(q, k_p, v_p, kept_idx, kept_cnt, F, n_f, scale, out, 
     _check(lib().fastar_annca_attention(_dt(q), _p(q), _p(k_p), _p(v_p), _p(kept_idx),
                                         _p(kept_cnt), H, F, n_f, P, D, scale, _p(out), _p(ws), nbytes,
                                         _p(status), _stream(stream)), "fastar_annca_attention")
+
+
+def fastar_annsa_attention_part(q, q_codes, q_perm, q_offsets, cache: Cache, scale, part_base, part_total, ws,
+                                status=None, stream=None):
+    """Per-table partials of AnnSA over `cache` into slots part_base.. of ws."""
+    H, Nq, D = q.shape
+    nbytes = ws.numel() * ws.element_size()
+    cs = cache.struct()
+    _check(lib().fastar_annsa_attention_part(_dt(q), _p(q), _p(q_codes), _p(q_perm), _p(q_offsets), Nq,
+                                             ctypes.byref(cs), scale, part_base, part_total, _p(ws), nbytes,
+                                             _p(status), _stream(stream)), "fastar_annsa_attention_part")
+
+
+def fastar_annsa_combine(part_total, ws, out, lse=None, status=None, stream=None):
+    """out [H][Nq][D] (and lse) from the part_total partials in ws."""
+    H, Nq, D = out.shape
+    _check(lib().fastar_annsa_combine(H, Nq, D, part_total, _p(ws), ws.numel() * ws.element_size(), _p(out),
+                                      _p(lse), _p(status), _stream(stream)), "fastar_annsa_combine")
 
 
 def fastar_annsa_attention(q, q_codes, q_perm, q_offsets, cache: Cache, scale, out, lse=None,

@@ -96,6 +96,8 @@ struct SaArgs {
   float2* ws_ml; // [T][H][Nq] their (max in log2 units, sum)
   __nv_bfloat16* out;
   float* lse;
+  int slot0;       // first partial slot of this call (table t writes slot0 + t)
+  int parts_only;  // write partials even for one table (no output)
 };
 
 // Wait until the PV product of key tile j has landed in O (and, since one
@@ -666,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         }
         __syncwarp();
         const size_t ri = (size_t)h * Nq + my_row;
-        if (sa.T == 1) {
+        if (sa.T == 1 && !sa.parts_only) {
           // a single table: the partial is the result
           const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
           if (my_row >= 0 && sa.lse) sa.lse[ri] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
@@ -688,10 +690,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
             const int row = __shfl_sync(0xffffffffu, my_row, rr);
             if (row < 0) continue;
             const float4 x = *reinterpret_cast<const float4*>(wbase + rr * 512 + ((lane + rr) & 31) * 16);
-            *reinterpret_cast<float4*>(sa.ws_o + (((size_t)kT * H + h) * Nq + row) * kD + lane * 4) = x;
+            *reinterpret_cast<float4*>(sa.ws_o + (((size_t)(sa.slot0 + kT) * H + h) * Nq + row) * kD + lane * 4) = x;
           }
           if (my_row >= 0)
-            sa.ws_ml[((size_t)kT * H + h) * Nq + my_row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
+            sa.ws_ml[((size_t)(sa.slot0 + kT) * H + h) * Nq + my_row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
         }
       } else {
         // normalised bf16 rows of 256 bytes; chunk i of row `lane` at position (i + lane) % 16
@@ -875,7 +877,7 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   const size_t o_bytes = ((size_t)c->T * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
   SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
-            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse};
+            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0};
   CaArgs ca{};
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
@@ -885,6 +887,43 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   if (rc != FASTAR_OK || c->T == 1) return rc;
   fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);
+  FASTAR_LAUNCHED(s, "annsa_combine");
+  return FASTAR_OK;
+}
+
+
+size_t annsa_parts_ws_bytes(int H, int Nq, int D, int parts) {
+  if (D != kD || parts < 1 || parts > kMaxT) return 0;
+  const size_t o = (size_t)parts * H * Nq * kD * sizeof(float);
+  const size_t ml = (size_t)parts * H * Nq * sizeof(float2);
+  return ((o + 255) & ~(size_t)255) + ((ml + 255) & ~(size_t)255);
+}
+
+// The partials of one AnnSA call for slots base .. base + T - 1 of a
+// workspace of `parts` slots (no output), and the merge of all slots.
+int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_perm, int Nq,
+                       const fastar_cache* c, float scale, int base, int parts, void* ws, int32_t* st,
+                       cudaStream_t s) {
+  if (c->dt != FASTAR_BF16 || c->D != kD) return FASTAR_ERR_UNSUPPORTED;
+  if (Nq == 0 || c->H == 0) return FASTAR_OK;
+  const size_t o_bytes = ((size_t)parts * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
+  SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
+            (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
+            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1};
+  CaArgs ca{};
+  CUtensorMap dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  return launch_attn<true>(dummy, dummy, dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa,
+                           st, s);
+}
+
+int launch_annsa_combine(int H, int Nq, int parts, const void* ws, void* out, float* lse, int32_t* st,
+                         cudaStream_t s) {
+  if (Nq == 0 || H == 0) return FASTAR_OK;
+  const size_t o_bytes = ((size_t)parts * H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
+  fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), H), 256, 0, s,
+                     (const float*)ws, (const float2*)((const char*)ws + o_bytes), parts, H, Nq,
+                     (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");
   return FASTAR_OK;
 }

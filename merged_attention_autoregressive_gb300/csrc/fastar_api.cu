@@ -48,6 +48,12 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
                     const int32_t* q_offsets, int Nq, const fastar_cache* c, float scale, void* out,
                     float* lse, void* ws, int32_t* st, cudaStream_t s);
 size_t annsa_tc_ws_bytes(int H, int Nq, int D, int T);
+size_t annsa_parts_ws_bytes(int H, int Nq, int D, int parts);
+int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_perm, int Nq,
+                       const fastar_cache* c, float scale, int base, int parts, void* ws, int32_t* st,
+                       cudaStream_t s);
+int launch_annsa_combine(int H, int Nq, int parts, const void* ws, void* out, float* lse, int32_t* st,
+                         cudaStream_t s);
 
 int launch_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes, int T,
                 int B, uint32_t* codes, int32_t* st, cudaStream_t s) {
@@ -133,6 +139,7 @@ size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C) {
     case FASTAR_OP_MERGE: return merge_ws_bytes(H, N, C);
     case FASTAR_OP_ANNCA: return annca_tc_ws_bytes(H, N, C, D);  // N = frames F, C = prompt tokens P
     case FASTAR_OP_ANNSA: return annsa_ws_bytes(H, N, D, T);
+    case FASTAR_OP_ANNSA_PARTS: return annsa_parts_ws_bytes(H, N, D, T);  // T = part_total
     default: return 0;
   }
 }
@@ -318,6 +325,37 @@ int fastar_annsa_attention(fastar_dtype dt, const void* q, const uint32_t* q_cod
   if (need && (!ws || ws_bytes < need || ((uintptr_t)ws & 255))) return FASTAR_ERR_WORKSPACE;
   return launch_annsa(dt, q, q_codes, q_perm, q_offsets, Nq, cache, scale, out, lse, ws,
                       dev_status, stream);
+}
+
+int fastar_annsa_attention_part(fastar_dtype dt, const void* q, const uint32_t* q_codes,
+                                const int32_t* q_perm, const int32_t* q_offsets, int Nq,
+                                const fastar_cache* cache, float scale, int part_base, int part_total,
+                                void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  (void)q_offsets;
+  int rc = check_cache(cache);
+  if (rc != FASTAR_OK) return rc;
+  if (dt != cache->dt || Nq < 0) return FASTAR_ERR_ARG;
+  if (!(scale > 0.f && scale < INFINITY)) return FASTAR_ERR_ARG;
+  if (part_total < 1 || part_total > 4 || part_base < 0 || part_base + cache->T > part_total)
+    return FASTAR_ERR_ARG;
+  if (dt != FASTAR_BF16 || cache->D != 128) return FASTAR_ERR_UNSUPPORTED;
+  if (Nq == 0 || cache->H == 0) return FASTAR_OK;
+  if (!q || !q_codes || !q_perm || !aligned16(q)) return FASTAR_ERR_ARG;
+  const size_t need = annsa_parts_ws_bytes(cache->H, Nq, cache->D, part_total);
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
+  return launch_annsa_parts(q, q_codes, q_perm, Nq, cache, scale, part_base, part_total, ws, dev_status,
+                            stream);
+}
+
+int fastar_annsa_combine(int H, int Nq, int D, int part_total, const void* ws, size_t ws_bytes, void* out,
+                         float* lse, int32_t* dev_status, cudaStream_t stream) {
+  if (H < 0 || Nq < 0 || part_total < 1 || part_total > 4) return FASTAR_ERR_ARG;
+  if (D != 128) return FASTAR_ERR_UNSUPPORTED;
+  if (H == 0 || Nq == 0) return FASTAR_OK;
+  if (!out || !aligned16(out)) return FASTAR_ERR_ARG;
+  const size_t need = annsa_parts_ws_bytes(H, Nq, D, part_total);
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
+  return launch_annsa_combine(H, Nq, part_total, ws, out, lse, dev_status, stream);
 }
 
 }  // extern "C"

@@ -9,11 +9,15 @@ Every step is one C-ABI call; this class only owns the buffers.
 """
 from __future__ import annotations
 
+from types import SimpleNamespace
+
 import torch
 
-from . import (Cache, OP_ANNCA, OP_ANNSA, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
-               fastar_annsa_attention, fastar_bucket_csr, fastar_hash, fastar_hash_many, fastar_tempcache_merge,
-               fastar_workspace_size)
+from . import (Cache, OP_ANNCA, OP_ANNSA, OP_ANNSA_PARTS, OP_MERGE, fastar_annca_attention, fastar_annca_prune,
+               fastar_annsa_attention, fastar_annsa_attention_part, fastar_annsa_combine, fastar_bucket_csr,
+               fastar_hash, fastar_hash_many, fastar_tempcache_merge, fastar_workspace_size)
+
+DENSE_FRAC = 0.3  # sparse attention is off for this share of a chunk's denoising steps
 
 
 class ChunkPath:
@@ -130,6 +134,111 @@ class ChunkPath:
             dvp.copy_(hvp, non_blocking=True)
             self._in_vp.record(cx)
         self._run(dq, dk, dv, dkp, dvp, first_frame, main, host_out=(ho_ca, ho_sa))
+
+    # -- denoising steps -----------------------------------------------------
+    def denoise_step(self, s, S, q, k, v, kp, vp, first_frame, dense_frac=DENSE_FRAC):
+        """Step s of the S denoising steps of a chunk (FAST-AR analysis,
+        paper.rainbus.top: sparse attention is off for the first 30 % of the
+        steps; each chunk is denoised conditioned on the history).
+
+        Step s is dense iff s < dense_frac * S.  A step before the last
+        attends the cache together with its own keys (count 1; the cache is
+        not written): two partial AnnSA calls, one over the cache and one
+        over a cache description of the step's keys, merged exactly by
+        fastar_annsa_combine; dense steps give both key sets one table of one
+        bit with every code 0, and keep every prompt token.  The last step
+        merges its keys into the cache and attends the merged cache, as
+        `step` does (dense per the schedule).  Outputs: o_sa, lse, o_ca."""
+        dense = s < dense_frac * S
+        dn = self._denoise_views()
+        st = self.status
+        if s + 1 == S and not dense:
+            self.step(q, k, v, kp, vp, first_frame)
+            return
+        if s + 1 == S:
+            fastar_hash(k, self.planes, self.T, self.B, self.k_codes, status=st)
+            fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame, self.tau,
+                                   match_out=self.match, ws=self.ws_merge, status=st, rep=self.rep,
+                                   planes=self.planes)
+            fastar_annsa_attention_part(q, dn.qc0, dn.qp0, dn.qo0, dn.cache_dense, self.scale, 0, 1, dn.ws,
+                                        status=st)
+            fastar_annsa_combine(1, dn.ws, self.o_sa, self.lse, status=st)
+        elif dense:
+            chunk = self._chunk_view(k, v, dense=True)
+            fastar_annsa_attention_part(q, dn.qc0, dn.qp0, dn.qo0, dn.cache_dense, self.scale, 0, 2, dn.ws,
+                                        status=st)
+            fastar_annsa_attention_part(q, dn.qc0, dn.qp0, dn.qo0, chunk, self.scale, 1, 2, dn.ws, status=st)
+            fastar_annsa_combine(2, dn.ws, self.o_sa, self.lse, status=st)
+        else:
+            T = self.T
+            jobs = [(q, self.q_codes, self.q_perm, self.q_offsets), (k, self.k_codes, dn.k_perm, dn.k_off)]
+            if self.P:
+                jobs.append((kp, self.p_codes, None, None))
+            fastar_hash_many(jobs, self.planes, T, self.B, status=st)
+            chunk = self._chunk_view(k, v, dense=False)
+            fastar_annsa_attention_part(q, self.q_codes, self.q_perm, self.q_offsets, self.cache, self.scale, 0,
+                                        2 * T, dn.ws, status=st)
+            fastar_annsa_attention_part(q, self.q_codes, self.q_perm, self.q_offsets, chunk, self.scale, T,
+                                        2 * T, dn.ws, status=st)
+            fastar_annsa_combine(2 * T, dn.ws, self.o_sa, self.lse, status=st)
+        if dense:
+            kept, cnt = dn.kept_all, dn.cnt_all
+        else:
+            fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
+                               self.kept_idx, self.kept_cnt, status=st)
+            kept, cnt = self.kept_idx, self.kept_cnt
+        fastar_annca_attention(q, kp, vp, kept, cnt, self.F, self.n_f, self.scale, self.o_ca, ws=self.ws_annca,
+                               status=st)
+
+    def _chunk_view(self, k, v, dense):
+        dn = self._denoise_views()
+        if dense:
+            return Cache.view(1, 1, K=k, V=v, m=dn.ones, codes=dn.qc0, last_frame=dn.lf, size=dn.nq,
+                              inserted=dn.cnt64, evicted=dn.cnt64, perm=dn.qp0, offsets=dn.qo0)
+        return Cache.view(self.T, self.B, K=k, V=v, m=dn.ones, codes=self.k_codes, last_frame=dn.lf,
+                          size=dn.nq, inserted=dn.cnt64, evicted=dn.cnt64, perm=dn.k_perm, offsets=dn.k_off)
+
+    def _denoise_views(self):
+        """Buffers of the denoising steps, built once: one-bucket (dense)
+        views of the queries, of the cache and of a step's keys (codes 0; the
+        CSR kernel turns them into an identity order and offsets (0, N, N)),
+        every prompt token kept (the prune of all-zero codes), and a step's
+        keys described as a cache (m = 1, size = Nq, their own CSR)."""
+        if getattr(self, "_dn", None) is not None:
+            return self._dn
+        if 2 * self.T > 4:
+            raise ValueError("denoising steps need T <= 2 (2 T partial results per query)")
+        H, C, Nq, F, P, D = self.H, self.C, self.Nq, self.F, self.P, self.D
+        dev = self.q_codes.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        dn = SimpleNamespace()
+
+        def one_bucket(n):
+            codes = torch.zeros(H, 1, n, **i32)
+            perm = torch.empty(H, 1, n, **i32)
+            off = torch.empty(H, 1, 3, **i32)
+            fastar_bucket_csr(codes, 1, perm, off, status=self.status)
+            return codes, perm, off
+
+        dn.qc0, dn.qp0, dn.qo0 = one_bucket(Nq)
+        cc0, cp0, co0 = one_bucket(C)
+        c = self.cache
+        dn.cache_dense = Cache.view(1, 1, K=c.K, V=c.V, m=c.m, codes=cc0, last_frame=c.last_frame, size=c.size,
+                                    inserted=c.inserted, evicted=c.evicted, perm=cp0, offsets=co0)
+        dn.kept_all = torch.empty(H, F, max(P, 1), **i32)
+        dn.cnt_all = torch.empty(H, F, **i32)
+        fastar_annca_prune(dn.qc0, torch.zeros(H, 1, P, **i32), F, self.n_f, 1, dn.kept_all, dn.cnt_all,
+                           status=self.status)
+        dn.ones = torch.ones(H, Nq, **i32)
+        dn.lf = torch.zeros(H, Nq, **i32)
+        dn.nq = torch.full((H,), Nq, **i32)
+        dn.cnt64 = torch.zeros(H, dtype=torch.int64, device=dev)
+        dn.k_perm = torch.empty(H, self.T, Nq, **i32)
+        dn.k_off = torch.empty(H, self.T, (1 << self.B) + 1, **i32)
+        dn.ws = torch.empty(fastar_workspace_size(OP_ANNSA_PARTS, H, Nq, D, 2 * self.T, self.B, C),
+                            dtype=torch.uint8, device=dev)
+        self._dn = dn
+        return dn
 
     # -- internals ----------------------------------------------------------
     @staticmethod

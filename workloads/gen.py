@@ -263,3 +263,25 @@ def layer_data(cfg: Config, layer: int = 0, chunks: int | None = None,
     pk, pv, pr = zip(*[prompt(cfg, layer, h, s.centroids) for h, s in zip(heads, streams)])
     return LayerData(cfg, layer, planes(cfg, layer), past_k, past_v, ck, cv, cq,
                      np.stack(pk), np.stack(pv), np.stack(pr))
+
+
+_P_DENOISE = 6
+
+
+def denoise_steps(cfg: Config, d: LayerData, S: int, chunk: int = 0, layer: int = 0):
+    """Inputs of the S denoising steps of chunk `chunk`: step s sees the
+    chunk's queries, keys and values plus N(0, sigma_s^2) per coordinate,
+    sigma_s = 0.05 (S - 1 - s) (the last step sees the clean chunk), each
+    drawn from its own stream and rounded once to the storage type.  A
+    stand-in for the activations of successive denoising steps, which change
+    less as the latent gets cleaner."""
+    out = []
+    for s in range(S):
+        sigma = 0.05 * (S - 1 - s)
+        rng = _rng(cfg, layer, 0, _P_DENOISE, extra=chunk * 1000 + s)
+        step = []
+        for x in (d.chunk_q[chunk], d.chunk_k[chunk], d.chunk_v[chunk]):
+            noise = rng.standard_normal(x.shape, dtype=np.float32) * np.float32(sigma)
+            step.append(to_storage(x + noise, cfg.dtype))
+        out.append(tuple(step))
+    return out
