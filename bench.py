@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--rep", default="last", choices=["last", "mean"],
                     help="TempCache representative: last key (the method) or mean key (ablation)")
+    ap.add_argument("--denoise", type=int, default=0,
+                    help="time the S denoising steps of one chunk (dense for the first 30%%) against "
+                         "all-dense and all-sparse schedules (one JSON line)")
     ap.add_argument("--recall", action="store_true",
                     help="sweep tau, T and B: recall and density of AnnSA and AnnCA (one JSON line)")
     return ap.parse_args()
@@ -898,11 +901,81 @@ def run_rollout(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def run_denoise(args, cfg):
+    """The S denoising steps of one chunk on cfg's shapes (cache of the past
+    frames built first): per chunk and per step device time with the
+    pages' schedule (sparse attention off for the first 30 % of the steps),
+    and with every step dense or every step sparse for comparison.  The
+    cache is restored and L2 flushed before every chunk (untimed)."""
+    import torch
+
+    import merged_attention_autoregressive_gb300 as fa
+    from merged_attention_autoregressive_gb300 import build as fbuild
+    from merged_attention_autoregressive_gb300.path import ChunkPath
+    from workloads import denoise_steps
+
+    fbuild.build()
+    fa.lib()
+    S = args.denoise
+    d = layer_data(cfg, chunks=1)
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", torch.bfloat16)  # noqa: E731
+    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, torch.bfloat16)
+    path.planes.copy_(todev(d.planes))
+    f = 0
+    while f < cfg.past_frames:
+        nF = min(cfg.F, cfg.past_frames - f)
+        path.merge(todev(np.concatenate(d.past_k[f:f + nF], 1)), todev(np.concatenate(d.past_v[f:f + nF], 1)),
+                   f, F=nF)
+        f += nF
+    steps = [tuple(todev(x) for x in st) for st in denoise_steps(cfg, d, S)]
+    kp, vp = todev(d.prompt_k), todev(d.prompt_v)
+    torch.cuda.synchronize()
+    snap = path.cache.snapshot()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def chunk(frac, ev=None):
+        for s, (q, k, v) in enumerate(steps):
+            path.denoise_step(s, S, q, k, v, kp, vp, cfg.past_frames, dense_frac=frac)
+            if ev is not None:
+                ev[s + 1].record(stream)
+
+    out = {}
+    for name, frac in (("schedule_0.3", 0.3), ("all_dense", 1.01), ("all_sparse", 0.0)):
+        for _ in range(3):
+            path.cache.restore(snap)
+            chunk(frac)
+        reps = max(3, min(args.steps, 20))
+        per_chunk, per_step = [], []
+        for _ in range(reps):
+            path.cache.restore(snap)
+            flush.fill_(1)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(S + 1)]
+            ev[0].record(stream)
+            chunk(frac, ev)
+            torch.cuda.synchronize()
+            per_chunk.append(ev[0].elapsed_time(ev[S]))
+            per_step.append([ev[s].elapsed_time(ev[s + 1]) for s in range(S)])
+        assert int(path.status.item()) == 0, fa.STATUS.get(int(path.status.item()))
+        out[name] = {"ms_per_chunk": float(np.median(per_chunk)),
+                     "ms_per_step": np.median(np.array(per_step), axis=0).round(4).tolist(),
+                     "dense_steps": [s < frac * S for s in range(S)]}
+    line = {"metric": "per-chunk FAST-AR attention ms over the denoising steps of a chunk", "unit": "ms/chunk",
+            "value": out["schedule_0.3"]["ms_per_chunk"], "higher_is_better": False, "data": "synthetic",
+            "config": {"workload": cfg.name, "H": cfg.H, "Nq": cfg.Nq, "P": cfg.P, "T": cfg.T, "B": cfg.B,
+                       "past_frames": cfg.past_frames, "denoise_steps": S,
+                       "l2": "flushed before every chunk (256 MiB write)"},
+            "schedules": out}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.denoise:
+        run_denoise(args, cfg)
     elif args.recall:
         run_recall(args, cfg)
     elif cfg.chunks > 1:
