@@ -6,9 +6,19 @@
 #include <atomic>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 
 namespace fastar {
+// Every compute call is an NVTX range named after it, so that a profiler's
+// timeline shows which call launched which kernels (a no-op without one).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 static std::atomic<uint64_t> g_launches{0};
 
 // launch timing: caller-created events, recorded after each launch
@@ -147,6 +157,7 @@ size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C) {
 int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void* planes, int T,
                 int B, uint32_t* codes, int32_t* perm, int32_t* offsets, void* ws, size_t ws_bytes,
                 int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_hash");
   (void)ws;
   (void)ws_bytes;
   if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
@@ -163,6 +174,7 @@ int fastar_hash(fastar_dtype dt, const void* x, int H, int N, int D, const void*
 
 int fastar_bucket_csr(const uint32_t* codes, int G, int N, int B, int32_t* perm, int32_t* offsets,
                       int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_bucket_csr");
   if (G < 0 || N < 0 || B < 1) return FASTAR_ERR_ARG;
   if (B > kMaxCsrBits) return FASTAR_ERR_UNSUPPORTED;
   if ((size_t)G * N == 0) return FASTAR_OK;
@@ -173,6 +185,7 @@ int fastar_bucket_csr(const uint32_t* codes, int G, int N, int B, int32_t* perm,
 int fastar_hash_many(fastar_dtype dt, int n_jobs, const fastar_hash_job* jobs, int H, int D,
                      const void* planes, int T, int B, void* ws, size_t ws_bytes, int32_t* dev_status,
                      cudaStream_t stream) {
+  CallRange range("fastar_hash_many");
   (void)ws;
   (void)ws_bytes;
   if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
@@ -257,6 +270,7 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const v
                            const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                            int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
                            cudaStream_t stream) {
+  CallRange range("fastar_tempcache_merge");
   return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
                        dev_status, stream, nullptr);
 }
@@ -265,6 +279,7 @@ int fastar_tempcache_merge_ev(const fastar_cache* cache, const void* k_new, cons
                               const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                               int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
                               cudaStream_t stream, cudaEvent_t codes_ready) {
+  CallRange range("fastar_tempcache_merge_ev");
   return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
                        dev_status, stream, codes_ready);
 }
@@ -273,6 +288,7 @@ int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new, con
                                const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                                int rep, const void* planes, int32_t* match_out, void* ws, size_t ws_bytes,
                                int32_t* dev_status, cudaStream_t stream, cudaEvent_t codes_ready) {
+  CallRange range("fastar_tempcache_merge_rep");
   return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
                        dev_status, stream, codes_ready, rep, planes);
 }
@@ -280,6 +296,7 @@ int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new, con
 int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,
                        int P, int T, int B, int32_t* kept_idx, int32_t* kept_cnt, void* ws,
                        size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annca_prune");
   (void)ws;
   (void)ws_bytes;
   if (H < 0 || F < 0 || n_f < 0 || P < 0 || T < 1 || T > 8 || B < 1) return FASTAR_ERR_ARG;
@@ -294,6 +311,7 @@ int fastar_annca_attention(fastar_dtype dt, const void* q, const void* k_p, cons
                            const int32_t* kept_idx, const int32_t* kept_cnt, int H, int F, int n_f,
                            int P, int D, float scale, void* out, void* ws, size_t ws_bytes,
                            int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annca_attention");
   if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
   if (H < 0 || F < 0 || n_f < 0 || P < 0) return FASTAR_ERR_ARG;
   if (!(scale > 0.f && scale < INFINITY)) return FASTAR_ERR_ARG;
@@ -313,6 +331,7 @@ int fastar_annsa_attention(fastar_dtype dt, const void* q, const uint32_t* q_cod
                            const int32_t* q_perm, const int32_t* q_offsets, int Nq,
                            const fastar_cache* cache, float scale, void* out, float* lse, void* ws,
                            size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annsa_attention");
   int rc = check_cache(cache);
   if (rc != FASTAR_OK) return rc;
   if (dt != cache->dt) return FASTAR_ERR_ARG;
@@ -331,6 +350,7 @@ int fastar_annsa_attention_part(fastar_dtype dt, const void* q, const uint32_t* 
                                 const int32_t* q_perm, const int32_t* q_offsets, int Nq,
                                 const fastar_cache* cache, float scale, int part_base, int part_total,
                                 void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annsa_attention_part");
   (void)q_offsets;
   int rc = check_cache(cache);
   if (rc != FASTAR_OK) return rc;
@@ -349,6 +369,7 @@ int fastar_annsa_attention_part(fastar_dtype dt, const void* q, const uint32_t* 
 
 int fastar_annsa_combine(int H, int Nq, int D, int part_total, const void* ws, size_t ws_bytes, void* out,
                          float* lse, int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annsa_combine");
   if (H < 0 || Nq < 0 || part_total < 1 || part_total > 4) return FASTAR_ERR_ARG;
   if (D != 128) return FASTAR_ERR_UNSUPPORTED;
   if (H == 0 || Nq == 0) return FASTAR_OK;
