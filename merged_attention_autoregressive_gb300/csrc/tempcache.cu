@@ -452,6 +452,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
 // projection giving bit 0.
 constexpr int kApplyKeys = 4;
 
+// Sign bits of 16 warp-wide dot products: p[r] is this lane's share of
+// product r.  A reduce-scatter over the warp (lanes exchange half of their
+// values at each of four steps) leaves lane l with the sum over 16 lanes of
+// product (l >> 1) & 15, one more exchange completes it over all 32 lanes,
+// and a ballot over the even lanes collects the 16 signs (bit r = [sum_r > 0]).
+__device__ __forceinline__ uint32_t warp_sign_bits16(float (&p)[16], int lane) {
+  float a[8], b4[4], c2[2];
+  const bool h16 = lane & 16, h8 = lane & 8, h4 = lane & 4, h2 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float keep = h16 ? p[i + 8] : p[i], send = h16 ? p[i] : p[i + 8];
+    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = h8 ? a[i + 4] : a[i], send = h8 ? a[i] : a[i + 4];
+    b4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = h4 ? b4[i + 2] : b4[i], send = h4 ? b4[i] : b4[i + 2];
+    c2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const float keep = h2 ? c2[1] : c2[0], send = h2 ? c2[0] : c2[1];
+  float sum = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  const uint32_t even = __ballot_sync(0xffffffffu, sum > 0.f) & 0x55555555u;
+  // lane 2r holds product r: compact the even bits
+  uint32_t bits = 0u;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) bits |= ((even >> (2 * r)) & 1u) << r;
+  return bits;
+}
+
 template <typename T>
 __device__ __forceinline__ float stored(float x) {
   T y;
@@ -562,22 +596,25 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
         // codes of the stored (rounded) mean key
 #pragma unroll
         for (int i = 0; i < PER; ++i) kacc[i] = stored<T>(kacc[i]);
-        uint32_t code = 0u;
-        for (int r = 0; r < Tt * Bb; ++r) {
-          float pr[PER];
-          ld_vec<T, PER>(planes + (size_t)r * D + lane * PER, pr);
-          float dot = 0.f;
+        // one bit per hyperplane, 16 hyperplanes per warp reduction
+        const int R = Tt * Bb;  // <= 64
+        uint64_t signs = 0ull;
+        for (int r0 = 0; r0 < R; r0 += 16) {
+          float p[16];
 #pragma unroll
-          for (int i = 0; i < PER; ++i) dot = fmaf(pr[i], kacc[i], dot);
+          for (int i = 0; i < 16; ++i) {
+            p[i] = 0.f;
+            if (r0 + i < R) {
+              float pr[PER];
+              ld_vec<T, PER>(planes + (size_t)(r0 + i) * D + lane * PER, pr);
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-          const int t = r / Bb, b = r - t * Bb;
-          code |= (dot > 0.f ? 1u : 0u) << b;
-          if (b == Bb - 1) {
-            if (lane == 0) codes[((size_t)h * Tt + t) * C + s] = code;
-            code = 0u;
+              for (int e = 0; e < PER; ++e) p[i] = fmaf(pr[e], kacc[e], p[i]);
+            }
           }
+          signs |= (uint64_t)warp_sign_bits16(p, lane) << r0;
         }
+        if (lane < Tt)
+          codes[((size_t)h * Tt + lane) * C + s] = (uint32_t)(signs >> (lane * Bb)) & ((1u << Bb) - 1u);
       }
     } else {
       st_raw<T, PER>(V + crow, vv[u]);
