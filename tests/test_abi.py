@@ -132,9 +132,55 @@ def test_host_argument_errors_need_no_gpu(L):
     for rep, planes in ((2, fake), (1, None), (1, vp(0x1004))):
         assert L.fastar_tempcache_merge_rep(ctypes.byref(cs), fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9),
                                             rep, planes, None, None, 0, None, None, None) == 1
+    # AnnSA partials / combine: slot range, head dim, workspace
+    L.fastar_annsa_attention_part.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(m2.CacheStruct),
+                                              ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]
+    cs2 = m2.CacheStruct(1, 128, 64, 2, 4, 0, *([0x1000] * 10))
+    for base, total in ((0, 5), (0, 0), (3, 4), (-1, 2)):   # T = 2 slots from base must fit in total <= 4
+        assert L.fastar_annsa_attention_part(0, fake, fake, fake, fake, 8, ctypes.byref(cs2), ctypes.c_float(0.1),
+                                             base, total, fake, 1 << 20, None, None) == 1
+    assert L.fastar_annsa_attention_part(0, fake, fake, fake, fake, 8, ctypes.byref(cs2), ctypes.c_float(0.1),
+                                         0, 2, fake, 16, None, None) == 4       # workspace too small
+    L.fastar_annsa_combine.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_size_t] + [ctypes.c_void_p] * 4
+    assert L.fastar_annsa_combine(1, 8, 128, 5, fake, 1 << 20, fake, None, None, None) == 1
+    assert L.fastar_annsa_combine(1, 8, 64, 2, fake, 1 << 20, fake, None, None, None) == 2
+    assert L.fastar_annsa_combine(1, 8, 128, 2, fake, 16, fake, None, None, None) == 4
+    assert L.fastar_annsa_combine(0, 8, 128, 2, None, 0, None, None, None, None) == 0
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
+
+
+def test_annsa_parts_workspace_grows_with_slots(L):
+    from merged_attention_autoregressive_gb300 import OP_ANNSA, OP_ANNSA_PARTS
+    w1 = L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 1, 8, 32768)
+    w4 = L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 4, 8, 32768)
+    assert w1 >= 12 * 4680 * (128 * 4 + 8) and w4 >= 4 * 12 * 4680 * (128 * 4 + 8)
+    # two slots hold what the two-table call keeps; a single table keeps nothing
+    assert L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 2, 8, 32768) == \
+        L.fastar_workspace_size(OP_ANNSA, 12, 4680, 128, 2, 8, 32768)
+    assert L.fastar_workspace_size(OP_ANNSA, 12, 4680, 128, 1, 8, 32768) == 0
+    assert L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 5, 8, 32768) == 0
+
+
+def test_cache_view_describes_given_tensors():
+    """Cache.view wraps existing tensors (here on the CPU: no device call)."""
+    import torch
+    import merged_attention_autoregressive_gb300 as m
+    H, C, D, T, B = 2, 10, 128, 2, 3
+    bufs = dict(K=torch.zeros(H, C, D, dtype=torch.bfloat16), V=torch.zeros(H, C, D, dtype=torch.bfloat16),
+                m=torch.ones(H, C, dtype=torch.int32), codes=torch.zeros(H, T, C, dtype=torch.int32),
+                last_frame=torch.zeros(H, C, dtype=torch.int32), size=torch.full((H,), C, dtype=torch.int32),
+                inserted=torch.zeros(H, dtype=torch.int64), evicted=torch.zeros(H, dtype=torch.int64),
+                perm=torch.zeros(H, T, C, dtype=torch.int32),
+                offsets=torch.zeros(H, T, (1 << B) + 1, dtype=torch.int32))
+    c = m.Cache.view(T, B, **bufs)
+    assert (c.H, c.C, c.D, c.T, c.B) == (H, C, D, T, B)
+    cs = c.struct()
+    assert cs.K == bufs["K"].data_ptr() and cs.offsets == bufs["offsets"].data_ptr()
+    assert (cs.H, cs.D, cs.C, cs.T, cs.B, cs.dt) == (H, D, C, T, B, m.BF16)
 
 
 def test_merge_rejects_small_workspace(L):
