@@ -31,6 +31,14 @@ Readings taken where the pages are silent:
              the group, updated and rounded like the value, and the group's
              codes are the hash of that stored key (its bucket).  The
              medoid-key variant needs every past member and is not built.
+  denoise  -- step s of S is dense iff s < 0.3 S; a step before the last
+             attends the cache plus its own keys and writes nothing; the
+             last step merges and attends the merged cache.
+  quant    -- the quantised matcher: per-dimension uniform b-bit codes over
+             the searched vectors' own range; approximate scores on the
+             decoded vectors; top-k per query (ties: lower index), attended
+             exactly; TempCache takes the approximate top-1 and merges iff
+             its exact cosine reaches tau.
   insert  -- unmatched keys fill free slots in ascending order, then the
              slots with the smallest (last_frame, slot) among those not
              refreshed in this frame are evicted (least recently refreshed).
@@ -508,6 +516,116 @@ def denoise_chunk(state: CacheState, steps, k_p, v_p, planes, T: int, B: int, F:
                 o_sa, lse = annsa_attention(q, qc, st, scale)
         outs.append((o_sa, lse, o_ca))
     return outs, st, match
+
+
+# ---------------------------------------------------------------- quantised ANN
+# The pages' other matcher ([PL] section 5 "ANN Attention": keep the keys
+# with the largest query-key products, found by LSH or by quantised
+# similarity search without offline preprocessing; [RB] reproduction: FAISS,
+# 8-bit quantisation by default; [PL] appendix C: 2-bit to 32-bit).
+# Readings: uniform scalar quantisation per dimension with `bits` bits, its
+# range the minimum and maximum of the vectors being searched (nothing is
+# trained offline); approximate scores use the decoded vectors; a query
+# keeps the k keys of largest approximate score (ties: lower index) and
+# attends them exactly (stored keys and values, + ln m); the TempCache
+# matcher takes the candidate of largest approximate cosine and merges iff
+# its exact cosine reaches tau.
+
+def sq_range(x):
+    """Per-dimension (lo, hi) of the rows of x [N][D]."""
+    x = np.asarray(x, dtype=np.float64)
+    return x.min(axis=0), x.max(axis=0)
+
+
+def sq_encode(x, lo, hi, bits: int):
+    """Codes in [0, 2^bits - 1]: round((x - lo) / (hi - lo) * (2^bits - 1)),
+    half away from zero; a dimension with hi == lo codes to 0."""
+    L = float((1 << bits) - 1)
+    x = np.asarray(x, dtype=np.float64)
+    span = np.asarray(hi, dtype=np.float64) - np.asarray(lo, dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        u = np.where(span > 0, (x - lo) / np.where(span > 0, span, 1.0), 0.0)
+    return np.clip(np.floor(u * L + 0.5), 0, L).astype(np.int64)
+
+
+def sq_decode(c, lo, hi, bits: int):
+    """The decoded vector lo + c (hi - lo) / (2^bits - 1)."""
+    L = float((1 << bits) - 1)
+    return np.asarray(lo, dtype=np.float64) + np.asarray(c, dtype=np.float64) * \
+        (np.asarray(hi, dtype=np.float64) - np.asarray(lo, dtype=np.float64)) / L
+
+
+def quant_topk(q, keys, bias, k: int, bits: int, scale: float):
+    """allowed [n][M]: per query the k keys of largest approximate score
+    scale q . decode(encode(key)) + bias (ties: lower index)."""
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    n, M = q.shape[0], keys.shape[0]
+    allowed = np.zeros((n, M), dtype=bool)
+    if M == 0 or k <= 0:
+        return allowed
+    lo, hi = sq_range(keys)
+    xt = sq_decode(sq_encode(keys, lo, hi, bits), lo, hi, bits)
+    s = scale * (q @ xt.T) + np.asarray(bias, dtype=np.float64)[None, :]
+    order = np.lexsort((np.broadcast_to(np.arange(M), s.shape), -s), axis=1)[:, :min(k, M)]
+    np.put_along_axis(allowed, order, True, axis=1)
+    return allowed
+
+
+def annsa_quant_attention(q, state: CacheState, k: int, bits: int, scale: float):
+    """AnnSA with the quantised matcher: per query the k live slots of largest
+    approximate logit, attended exactly.  Returns (o, lse)."""
+    q = np.asarray(q, dtype=np.float64)
+    H, Nq, D = q.shape
+    o = np.zeros((H, Nq, D))
+    lse = np.zeros((H, Nq))
+    for h in range(H):
+        size = int(state.size[h])
+        bias = np.log(np.maximum(state.m[h, :size], 1).astype(np.float64))
+        allowed = quant_topk(q[h], state.K[h, :size], bias, k, bits, scale)
+        o[h], lse[h] = masked_attention(q[h], state.K[h, :size], state.V[h, :size], allowed, bias, scale)
+    return o, lse
+
+
+def annca_quant_attention(q, k_p, v_p, k: int, bits: int, scale: float):
+    """AnnCA with the quantised matcher: per query the k prompt tokens of
+    largest approximate score, attended exactly.  Returns o."""
+    q = np.asarray(q, dtype=np.float64)
+    H, Nq, D = q.shape
+    o = np.zeros((H, Nq, np.asarray(v_p).shape[2]))
+    for h in range(H):
+        P = np.asarray(k_p).shape[1]
+        allowed = quant_topk(q[h], k_p[h], np.zeros(P), k, bits, scale)
+        o[h], _ = masked_attention(q[h], k_p[h], v_p[h], allowed, np.zeros(P), scale)
+    return o
+
+
+def tempcache_nn_quant(state: CacheState, k: np.ndarray, f: int, tau: float, bits: int):
+    """TempCache's top-1 correspondence with the quantised matcher: the
+    candidate (slot refreshed in frame f-1) of largest cosine between the new
+    key and the candidate's decoded key (ties: lowest slot), merged iff the
+    exact cosine reaches tau.  Returns match [H][n] (slot or -1)."""
+    k = np.asarray(k, dtype=np.float64)
+    H, n, D = k.shape
+    match = np.full((H, n), -1, dtype=np.int64)
+    for h in range(H):
+        size = int(state.size[h])
+        cand = np.nonzero(state.last_frame[h, :size] == f - 1)[0]
+        if cand.size == 0:
+            continue
+        Kc = state.K[h, cand]
+        lo, hi = sq_range(Kc)
+        Kt = sq_decode(sq_encode(Kc, lo, hi, bits), lo, hi, bits)
+        kn = np.linalg.norm(k[h], axis=1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            approx = (k[h] @ Kt.T) / (kn[:, None] * np.linalg.norm(Kt, axis=1)[None, :])
+            exact = (k[h] @ Kc.T) / (kn[:, None] * np.linalg.norm(Kc, axis=1)[None, :])
+        approx[~np.isfinite(approx)] = -np.inf
+        best = np.argmax(approx, axis=1)
+        ex = exact[np.arange(n), best]
+        ok = np.isfinite(approx[np.arange(n), best]) & (ex >= tau)
+        match[h, ok] = cand[best[ok]]
+    return match
 
 
 # ---------------------------------------------------------------- recall / density

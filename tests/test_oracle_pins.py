@@ -653,3 +653,84 @@ def test_denoise_chunk_writes_the_cache_only_at_the_last_step():
     k0c, _ = O.hash_codes(k0, d.planes, cfg.T, cfg.B)
     o_sparse, _ = O.denoise_step_attention(q0, q0c, before, k0, v0, k0c, False, cfg.scale)
     assert np.abs(outs[0][0] - o_sparse).max() > 1e-3
+
+
+# ----------------------------------------------------- quantised ANN matcher
+def test_quant_fixture_codes_and_top1():
+    g = load("quant_small.txt")
+    keys = np.asarray(g["keys"], dtype=np.float64).reshape(3, 2)
+    lo, hi = O.sq_range(keys)
+    np.testing.assert_array_equal(lo, g["lo"])
+    np.testing.assert_array_equal(hi, g["hi"])
+    np.testing.assert_array_equal(O.sq_encode(keys, lo, hi, 2).ravel(), g["codes_b2"])
+    c1 = O.sq_encode(keys, lo, hi, 1)
+    np.testing.assert_array_equal(c1.ravel(), g["codes_b1"])
+    np.testing.assert_array_equal(O.sq_decode(c1, lo, hi, 1).ravel(), g["decoded_b1"])
+    q = np.asarray(g["queries"], dtype=np.float64).reshape(3, 2)
+    allowed = O.quant_topk(q, keys, np.zeros(3), 1, 1, 1.0)
+    np.testing.assert_array_equal(np.argmax(allowed, axis=1), g["top1_b1"])
+    assert (allowed.sum(axis=1) == 1).all()
+
+
+def test_quant_error_bound_and_many_bits_equal_exact_topk():
+    """|x - decode(encode(x))| <= step / 2 per coordinate; with 24 bits the
+    quantised top-k is the exact top-k (random data, no near ties)."""
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal((200, 16))
+    lo, hi = O.sq_range(x)
+    for bits in (2, 4, 8, 12):
+        step = (hi - lo) / ((1 << bits) - 1)
+        err = np.abs(O.sq_decode(O.sq_encode(x, lo, hi, bits), lo, hi, bits) - x)
+        assert (err <= step / 2 + 1e-12).all(), bits
+    q = rng.standard_normal((30, 16))
+    bias = rng.standard_normal(200) * 0.1
+    allowed = O.quant_topk(q, x, bias, 7, 24, 0.25)
+    s = 0.25 * q @ x.T + bias
+    srt = np.sort(s, axis=1)
+    assert (srt[:, -7] - srt[:, -8] > 1e-6).all()
+    exact = np.zeros_like(allowed)
+    np.put_along_axis(exact, np.argsort(-s, axis=1)[:, :7], True, axis=1)
+    np.testing.assert_array_equal(allowed, exact)
+
+
+def test_quant_annsa_with_every_key_is_dense_attention():
+    """k >= the live slots: the quantised matcher keeps everything and the
+    output is the softmax over all logits scale q.K + ln m (scipy)."""
+    rng = np.random.default_rng(32)
+    H, D, n = 1, 8, 12
+    st = O.CacheState.empty(H, 16, D, 1, "f64")
+    st.K[0, :n] = rng.standard_normal((n, D))
+    st.V[0, :n] = rng.standard_normal((n, D))
+    st.m[0, :n] = rng.integers(1, 5, n)
+    st.size[0] = n
+    q = rng.standard_normal((1, 5, D))
+    o, lse = O.annsa_quant_attention(q, st, 100, 4, 0.3)
+    logits = 0.3 * q[0] @ st.K[0, :n].T + np.log(st.m[0, :n])
+    np.testing.assert_allclose(o[0], softmax(logits, axis=1) @ st.V[0, :n], atol=1e-12, rtol=0)
+    np.testing.assert_allclose(lse[0], logsumexp(logits, axis=1), atol=1e-12, rtol=0)
+    # AnnCA likewise over every prompt token
+    kp, vp = rng.standard_normal((1, 9, D)), rng.standard_normal((1, 9, D))
+    oc = O.annca_quant_attention(q, kp, vp, 9, 2, 0.3)
+    np.testing.assert_allclose(oc[0], softmax(0.3 * q[0] @ kp[0].T, axis=1) @ vp[0], atol=1e-12, rtol=0)
+
+
+def test_quant_tempcache_matches_exact_at_many_bits_and_never_below_tau():
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(redraw=0.3)
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    for f in range(cfg.past_frames):
+        c, _ = O.hash_codes(d.past_k[f], d.planes, cfg.T, cfg.B)
+        st, _, _ = O.tempcache_merge(st, d.past_k[f], d.past_v[f], c, 1, cfg.n_f, f, cfg.tau)
+    k = d.chunk_k[0]
+    f = cfg.past_frames
+    exact, listed = O.tempcache_nn(st, k, f, cfg.tau)
+    q24 = O.tempcache_nn_quant(st, k, f, cfg.tau, 24)
+    np.testing.assert_array_equal(q24[~listed], exact[~listed])
+    q1 = O.tempcache_nn_quant(st, k, f, cfg.tau, 1)
+    kk = np.asarray(k[0], dtype=np.float64)
+    for j in np.nonzero(q1[0] >= 0)[0]:
+        s = q1[0, j]
+        cos = kk[j] @ st.K[0, s] / (np.linalg.norm(kk[j]) * np.linalg.norm(st.K[0, s]))
+        assert cos >= cfg.tau
+    assert (q1[0] >= 0).sum() <= (exact[0] >= 0).sum() + listed.sum()
