@@ -511,7 +511,6 @@ __global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_f
   // call has already waited for their producers): load them before the wait
   using Raw = typename VecOf<T, PER>::type;
   Raw kv[kApplyKeys], vv[kApplyKeys], vo[kApplyKeys], ko[kApplyKeys];
-  constexpr bool mean_key = kMean;
 #pragma unroll
   for (int u = 0; u < kApplyKeys; ++u) {
     if (j0 + u >= n_f) continue;
