@@ -261,6 +261,22 @@ class Cache:
         for n in self.BUFFERS:
             getattr(self, n).copy_(snap[n], non_blocking=True)
 
+    def save(self, path: str):
+        """Write a checkpoint of the cache (every buffer and its shape
+        parameters) to `path` with torch.save; a rollout resumed from it
+        continues bit for bit as if it had not stopped."""
+        torch.save({"shape": (self.H, self.C, self.D, self.T, self.B, str(self.dtype)),
+                    "buffers": {n: getattr(self, n).detach().cpu() for n in self.BUFFERS}}, path)
+
+    def load(self, path: str):
+        """Restore a checkpoint written by `save` into this cache's buffers
+        (same H, C, D, T, B and dtype, or ValueError)."""
+        ck = torch.load(path, map_location="cpu")
+        if tuple(ck["shape"]) != (self.H, self.C, self.D, self.T, self.B, str(self.dtype)):
+            raise ValueError(f"checkpoint of shape {ck['shape']} does not fit this cache")
+        for n in self.BUFFERS:
+            getattr(self, n).copy_(ck["buffers"][n])
+
     def nbytes(self) -> int:
         return sum(getattr(self, n).numel() * getattr(self, n).element_size() for n in self.BUFFERS)
 

@@ -196,3 +196,27 @@ def test_merge_rejects_small_workspace(L):
                                   ctypes.c_void_p(fake), 1, 65, 0, ctypes.c_float(0.9), None,
                                   ctypes.c_void_p(4096), 1 << 30, None, None)
     assert rc == 1
+
+
+def test_cache_checkpoint_round_trip(tmp_path):
+    """Cache.save / Cache.load restore every buffer exactly (CPU tensors);
+    a checkpoint of another shape is refused."""
+    import torch
+    import merged_attention_autoregressive_gb300 as m
+    g = torch.Generator().manual_seed(3)
+    a = m.Cache(2, 16, 64, 2, 3, torch.bfloat16, device="cpu")
+    for n in a.BUFFERS:
+        t = getattr(a, n)
+        if t.is_floating_point():
+            t.copy_(torch.randn(t.shape, generator=g).to(t.dtype))
+        else:
+            t.copy_(torch.randint(-5, 100, t.shape, generator=g).to(t.dtype))
+    path = str(tmp_path / "cache.pt")
+    a.save(path)
+    b = m.Cache(2, 16, 64, 2, 3, torch.bfloat16, device="cpu")
+    b.load(path)
+    for n in a.BUFFERS:
+        assert torch.equal(getattr(a, n), getattr(b, n)), n
+    c = m.Cache(2, 32, 64, 2, 3, torch.bfloat16, device="cpu")
+    with pytest.raises(ValueError):
+        c.load(path)
