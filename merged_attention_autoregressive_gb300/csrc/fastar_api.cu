@@ -115,7 +115,7 @@ const char* fastar_status_string(int status) {
   }
 }
 
-int fastar_version(void) { return 100; }
+int fastar_version(void) { return 200; }
 
 uint64_t fastar_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
