@@ -23,16 +23,22 @@ import oracle as O
 
 ATT_MAX, ATT_MEAN = 1e-2, 1e-3
 TDT = {"bf16": torch.bfloat16, "f32": torch.float32}
+ALL_REPORTS = []  # every Report of the session, summed up at the end of the run (conftest)
 
 
 @dataclass
 class Report:
+    """Listed (near-boundary) decisions and value differences of one test:
+    they are counted, not failed."""
     listed_hash_bits: int = 0
     differing_listed_bits: int = 0
     listed_nn: int = 0
     differing_listed_nn: int = 0
     v_ulp_diffs: int = 0
     att: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        ALL_REPORTS.append(self)
 
 
 def dev(x: np.ndarray, dtype: str, device="cuda"):
