@@ -226,6 +226,42 @@ def tempcache_nn(state: CacheState, k: np.ndarray, f: int, tau: float):
     return match, listed
 
 
+def tempcache_nn_lsh(state: CacheState, k: np.ndarray, k_codes: np.ndarray, f: int, tau: float):
+    """The search variant that matches against every previous frame ([GS]
+    2.A: "the most similar key in previous frames"; the method's default
+    takes only the previous frame, [RB] method steps): the candidates of key
+    j are the live groups refreshed before frame f that share an LSH bucket
+    with it in some table; top-1 cosine among them (ties: lowest slot),
+    merged iff the cosine reaches tau.  k_codes: [H][T][n].  Returns
+    (match [H][n], listed [H][n]) with the listing rule of tempcache_nn."""
+    k = np.asarray(k, dtype=np.float64)
+    H, n, D = k.shape
+    match = np.full((H, n), -1, dtype=np.int64)
+    listed = np.zeros((H, n), dtype=bool)
+    for h in range(H):
+        size = int(state.size[h])
+        live = np.nonzero((state.last_frame[h, :size] >= 0) & (state.last_frame[h, :size] < f))[0]
+        if live.size == 0:
+            continue
+        share = annsa_allowed(np.asarray(k_codes)[h], state.codes[h][:, live])   # [n][live]
+        Kc = state.K[h, live]
+        kn = np.linalg.norm(k[h], axis=1)
+        cn = np.linalg.norm(Kc, axis=1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            cos = (k[h] @ Kc.T) / (kn[:, None] * cn[None, :])
+        cos[~np.isfinite(cos) | ~share] = -np.inf
+        best = np.argmax(cos, axis=1)
+        top1 = cos[np.arange(n), best]
+        ok = top1 >= tau
+        match[h, ok] = live[best[ok]]
+        near_tau = np.abs(top1 - tau) < NN_MARGIN
+        srt = np.sort(cos, axis=1)
+        with np.errstate(invalid="ignore"):   # rows with fewer than two candidates: no tie
+            near_tie = (srt[:, -1] - srt[:, -2]) < NN_MARGIN if live.size > 1 else np.zeros(n, dtype=bool)
+        listed[h] = np.isfinite(top1) & (near_tau | (near_tie & (top1 >= tau - NN_MARGIN)))
+    return match, listed
+
+
 def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match, rep: str = "last",
                           planes=None, B: int | None = None) -> CacheState:
     """Merge one frame's keys into the cache given its NN matches (in place).

@@ -734,3 +734,46 @@ def test_quant_tempcache_matches_exact_at_many_bits_and_never_below_tau():
         cos = kk[j] @ st.K[0, s] / (np.linalg.norm(kk[j]) * np.linalg.norm(st.K[0, s]))
         assert cos >= cfg.tau
     assert (q1[0] >= 0).sum() <= (exact[0] >= 0).sum() + listed.sum()
+
+
+# ------------------------------------------ TempCache search over all previous frames
+def test_tempcache_lsh_search_single_bucket_is_exact_search_over_all_groups():
+    """With every code equal (one bucket) the LSH-candidate search is the
+    exact top-1 cosine over every live group of earlier frames, checked by
+    brute force; with the real codes a match always shares a bucket."""
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(redraw=0.3)
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    for f in range(cfg.past_frames):
+        c, _ = O.hash_codes(d.past_k[f], d.planes, cfg.T, cfg.B)
+        st, _, _ = O.tempcache_merge(st, d.past_k[f], d.past_v[f], c, 1, cfg.n_f, f, cfg.tau)
+    k = d.chunk_k[0]
+    f = cfg.past_frames
+    one = st.copy()
+    one.codes[:] = 0
+    match, listed = O.tempcache_nn_lsh(one, k, np.zeros((1, cfg.T, cfg.n_f), np.uint32), f, cfg.tau)
+    kk = np.asarray(k[0], dtype=np.float64)
+    size = int(st.size[0])
+    for j in range(cfg.n_f):
+        best, arg = -np.inf, -1
+        for s in range(size):
+            c = kk[j] @ st.K[0, s] / (np.linalg.norm(kk[j]) * np.linalg.norm(st.K[0, s]))
+            if c > best:
+                best, arg = c, s
+        if listed[0, j]:
+            continue
+        assert match[0, j] == (arg if best >= cfg.tau else -1), j
+    # the method's previous-frame search is a special case: every match it
+    # makes among groups that share a bucket is found by the wider search too
+    codes, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
+    wide, wl = O.tempcache_nn_lsh(st, k, codes, f, cfg.tau)
+    for j in np.nonzero(wide[0] >= 0)[0]:
+        s = wide[0, j]
+        assert any(codes[0, t, j] == st.codes[0, t, s] for t in range(cfg.T))
+    narrow, nl = O.tempcache_nn(st, k, f, cfg.tau)
+    for j in np.nonzero(narrow[0] >= 0)[0]:
+        s = narrow[0, j]
+        shares = any(codes[0, t, j] == st.codes[0, t, s] for t in range(cfg.T))
+        if shares and not (wl[0, j] or nl[0, j]):
+            assert wide[0, j] >= 0, j   # that group is a candidate of the wider search too
