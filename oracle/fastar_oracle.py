@@ -228,8 +228,9 @@ def tempcache_nn(state: CacheState, k: np.ndarray, f: int, tau: float):
 
 def tempcache_nn_lsh(state: CacheState, k: np.ndarray, k_codes: np.ndarray, f: int, tau: float):
     """The search variant that matches against every previous frame ([GS]
-    2.A: "the most similar key in previous frames"; the method's default
-    takes only the previous frame, [RB] method steps): the candidates of key
+    2.A looks for the nearest key over the earlier frames with LSH or
+    quantisation; the method's default takes only the previous frame, [RB]
+    method steps): the candidates of key
     j are the live groups refreshed before frame f that share an LSH bucket
     with it in some table; top-1 cosine among them (ties: lowest slot),
     merged iff the cosine reaches tau.  k_codes: [H][T][n].  Returns
