@@ -90,7 +90,8 @@ def round_storage(x: np.ndarray, dtype: str) -> np.ndarray:
 # --------------------------------------------------------------------------
 # step 1: random-hyperplane LSH  ([PL] section 2 "ANN search", section 5
 # "ANN Attention"; [GS] 2.B mechanism: queries and prompt keys projected
-# into one shared LSH space; [RB] "hash once, serves all three modules")
+# into one shared LSH space; [RB] technical novelty: the encoding is
+# computed once and used by all three modules)
 # --------------------------------------------------------------------------
 def hash_codes(x: np.ndarray, planes: np.ndarray, T: int, B: int):
     """codes[h][t][i] = sum_b [planes[t*B+b] . x[h][i] > 0] << b.

@@ -11,7 +11,7 @@ What the pages describe, and what the synthetic data imitates
   "Motivation", self-attention redundancy bullet; FAST-AR analysis
   (paper.rainbus.top), figure 3 description.
 * Cached keys repeat across frames (near-duplicates) -- same passages, and
-  the abstract ("near-duplicate cached keys across frames").
+  the abstract, which names cached keys that nearly repeat frame to frame.
 * Each prompt only matters for a few tokens per frame -- paperlayer.ai,
   section 4, cross-attention overhead bullet; rainbus figure 4.
 
