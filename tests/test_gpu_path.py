@@ -257,8 +257,8 @@ def _sample_rows(nq, k, seed):
 
 
 def test_14b_shapes_head_sample():
-    """configs[4] shapes (n_f 3600, Nq 10,800, 21 merged past frames, C 32,768,
-    T 2 x B 10) on a seeded sample of layers and heads: heads are independent,
+    """The 14B-like 720p layer's shapes (n_f 3600, Nq 10,800, 21 merged past
+    frames, C 32,768, T 2 x B 10) on a seeded sample of layers and heads: heads are independent,
     so each sampled head's results equal its results inside the 40-head layer.
     Every index output is checked in full; attention on sampled query rows."""
     base = CONFIGS[4]
@@ -274,7 +274,8 @@ def test_14b_shapes_head_sample():
 
 
 def test_rollout_head_sample():
-    """configs[2] shapes from an empty cache (5 % of keys redrawn per frame),
+    """The long-rollout workload's shapes (the one-layer Wan-1.3B-like chunk,
+    5 % of keys redrawn per frame) from an empty cache,
     24 chunks on a seeded sample of heads, with the capacity cut to 4096 so
     that the cache fills (about chunk 12) and eviction runs from then on.
     Every chunk's indices and merge are checked against the oracle chain;
