@@ -784,8 +784,9 @@ def test_quant_topk_overlap_rises_with_precision():
     the quantised matcher rises with the bits per value) on one synthetic
     head of the Wan-1.3B-like layer: the quantised top-k (k = 28 % of the
     live groups) shares more of the exact top-k as the bits grow, and all of
-    it at 16 bits.  Measured here (400 queries): 1 bit 0.876, 2 bits 0.898,
-    4 bits 0.977, 8 bits 0.9985, 16 bits 1.0."""
+    it at 16 bits but for near-ties at the k-th score.  Measured here (400
+    queries): 1 bit 0.876, 2 bits 0.898, 4 bits 0.977, 8 bits 0.9985,
+    16 bits 0.999996."""
     from workloads import CONFIGS, layer_data
     cfg = CONFIGS[1].replace(H=1, past_frames=6)
     d = layer_data(cfg, chunks=1, heads=[0])
@@ -803,4 +804,5 @@ def test_quant_topk_overlap_rises_with_precision():
     overlap = [float((O.quant_topk(q, K, bias, k, b, cfg.scale) & exact).sum() / exact.sum())
                for b in (1, 2, 4, 8, 16)]
     assert all(a <= b + 1e-12 for a, b in zip(overlap, overlap[1:])), overlap
-    assert overlap[0] < 0.95 and overlap[-1] == 1.0, overlap
+    # at 16 bits only near-ties at the k-th score can swap a key
+    assert overlap[0] < 0.95 and overlap[-1] >= 0.9999, overlap
