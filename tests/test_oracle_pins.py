@@ -806,3 +806,89 @@ def test_quant_topk_overlap_rises_with_precision():
     assert all(a <= b + 1e-12 for a, b in zip(overlap, overlap[1:])), overlap
     # at 16 bits only near-ties at the k-th score can swap a key
     assert overlap[0] < 0.95 and overlap[-1] >= 0.9999, overlap
+
+
+# ------------------------------------------------ TempCache listing rule (hand cases)
+# The near-boundary rule of the NN decision (an NN choice whose margin is
+# below 1e-4 is listed and may go either way on the GPU): with tau = 0.95, a
+# decision is listed iff its top-1 cosine lies within 1e-4 of tau, or its
+# top-2 gap is below 1e-4 while the top-1 can still reach tau (top-1 >=
+# tau - 1e-4).  Each case below puts unit key (1, 0) against candidates at
+# hand-chosen cosines c, placed at (c, +-sqrt(1 - c^2)) (alternating sides)
+# so that their cosine with the key is c to fp64 rounding; the expected
+# match and listed flag follow from the rule by hand.
+_TAU = 0.95
+_NN_CASES = [
+    # (candidate cosines in slot order, expected match slot, expected listed)
+    ((1.0, 1.0), 0, True),                       # exact tie at cosine 1 -> lowest slot, listed
+    ((_TAU + 5e-5,), 0, True),                   # top-1 just above tau: matched, listed
+    ((_TAU - 5e-5,), -1, True),                  # top-1 just below tau: unmatched, listed
+    ((_TAU - 0.01, _TAU - 0.01 + 5e-5), -1, False),   # near tie far below tau: not listed
+    ((_TAU - 1.5e-4, _TAU - 2.0e-4), -1, False),  # near tie just beyond tau - 1e-4: not listed
+    ((_TAU + 0.02, _TAU + 0.02 - 5e-5), 0, True),  # near tie above tau: listed, larger wins
+    ((_TAU + 0.02 - 5e-5, _TAU + 0.02), 1, True),  # same, larger one in the higher slot
+    ((_TAU + 0.02, _TAU + 0.02 - 2e-4), 0, False),  # gap 2e-4: a clear winner
+    ((_TAU + 1.5e-4,), 0, False),                # 1.5e-4 above tau: outside the margin
+    ((_TAU - 0.3, _TAU + 0.04, _TAU - 0.2), 1, False),  # clear winner in the middle slot
+]
+
+
+def _nn_state(cosines, frame=4, T=1):
+    """Candidates at the given cosines to (1, 0), refreshed in frame-1, plus
+    one live group of an older frame that is exactly aligned with the key
+    (cosine 1) and must never be a candidate of the previous-frame search."""
+    n = len(cosines)
+    st = O.CacheState.empty(1, n + 4, 2, T, "f64")
+    for s, c in enumerate(cosines):
+        side = 1.0 if s % 2 == 0 else -1.0
+        st.K[0, s] = (c, side * math.sqrt(max(0.0, 1.0 - c * c)))
+        st.last_frame[0, s] = frame - 1
+        st.m[0, s] = 1
+    st.K[0, n] = (1.0, 0.0)
+    st.last_frame[0, n] = frame - 2
+    st.m[0, n] = 1
+    st.size[0] = n + 1
+    st.inserted[0] = n + 1
+    return st
+
+
+@pytest.mark.parametrize("cosines,want_match,want_listed", _NN_CASES)
+def test_tempcache_nn_listing_rule_hand_cases(cosines, want_match, want_listed):
+    st = _nn_state(cosines)
+    k = np.array([[[1.0, 0.0]]])
+    match, listed = O.tempcache_nn(st, k, 4, _TAU)
+    assert match[0, 0] == want_match
+    assert bool(listed[0, 0]) == want_listed
+
+
+@pytest.mark.parametrize("cosines,want_match,want_listed", _NN_CASES)
+def test_tempcache_nn_lsh_listing_rule_hand_cases(cosines, want_match, want_listed):
+    """The search over every earlier frame lists by the same rule.  Every
+    candidate shares the key's bucket here; the aligned older group is a
+    candidate too, but it sits in another bucket, so it must be skipped:
+    with it counted every case would match it at cosine 1."""
+    st = _nn_state(cosines)
+    n = len(cosines)
+    st.codes[0, 0, :n] = 3
+    st.codes[0, 0, n] = 5                      # the aligned older group: other bucket
+    k = np.array([[[1.0, 0.0]]])
+    match, listed = O.tempcache_nn_lsh(st, k, np.array([[[3]]], dtype=np.uint32), 4, _TAU)
+    assert match[0, 0] == want_match
+    assert bool(listed[0, 0]) == want_listed
+
+
+def test_tempcache_nn_lsh_searches_older_frames_in_the_bucket():
+    """An older group in the key's bucket is a candidate of the search over
+    every earlier frame (not of the previous-frame search): put in the key's
+    bucket, the aligned older group of the fixture wins at cosine 1, and an
+    exact tie with it at cosine 1 is listed."""
+    st = _nn_state((_TAU + 0.02,))
+    st.codes[0, 0, :2] = 3
+    k = np.array([[[1.0, 0.0]]])
+    match, listed = O.tempcache_nn_lsh(st, k, np.array([[[3]]], dtype=np.uint32), 4, _TAU)
+    assert match[0, 0] == 1 and not listed[0, 0]
+    prev, _ = O.tempcache_nn(st, k, 4, _TAU)
+    assert prev[0, 0] == 0
+    st.K[0, 0] = (2.0, 0.0)                     # previous-frame group now aligned too
+    match, listed = O.tempcache_nn_lsh(st, k, np.array([[[3]]], dtype=np.uint32), 4, _TAU)
+    assert match[0, 0] == 0 and listed[0, 0]
