@@ -247,6 +247,10 @@ int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new,
                            int32_t* match_out, void* ws, size_t ws_bytes,
                            int32_t* dev_status, cudaStream_t stream);
 
+/* Largest frame (keys per frame) the merge accepts: the per-frame plan keeps
+ * each key's match and a hash table of the frame's groups in shared memory. */
+#define FASTAR_MAX_FRAME_KEYS 6144
+
 /*
  * fastar_tempcache_merge_ev -- fastar_tempcache_merge whose codes_new (and
  * v_new) may still be in the making when the call is issued: codes_ready
@@ -316,10 +320,6 @@ int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new,
  * it zeroed).  The first call on a device looks up the array's address with
  * that device current; make it before any stream capture.
  */
-/* Largest frame (keys per frame) the merge accepts: the per-frame plan keeps
- * each key's match and a hash table of the frame's groups in shared memory. */
-#define FASTAR_MAX_FRAME_KEYS 6144
-
 #define FASTAR_NOALLOC_SCRATCH_BYTES (16u << 20)
 int fastar_tempcache_merge_noalloc(const fastar_cache* cache, const void* k_new,
                                    const void* v_new, const uint32_t* codes_new,

@@ -66,14 +66,24 @@ extern "C" int fastar_tempcache_merge_noalloc(const fastar_cache* cache, const v
                                               int n_f, int32_t first_frame, float tau,
                                               int32_t* match_out, int32_t* dev_status,
                                               cudaStream_t stream) {
-  if (!cache || n_f < 0) return FASTAR_ERR_ARG;
-  const size_t need = fastar_workspace_size(FASTAR_OP_MERGE, cache->H, n_f, cache->D, cache->T,
-                                            cache->B, cache->C);
-  if (need > (size_t)FASTAR_NOALLOC_SCRATCH_BYTES) return FASTAR_ERR_WORKSPACE;
+  // Argument checks, the no-op cases and the workspace check are the
+  // workspace merge's own: the array is handed over only when the call will
+  // launch work and the array is large enough; otherwise the merge is given
+  // no workspace and answers exactly as fastar_tempcache_merge would (OK for
+  // an empty call, ERR_ARG / ERR_UNSUPPORTED for bad arguments, and
+  // FASTAR_ERR_WORKSPACE when the problem needs more than the array).
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
-  if (rc != FASTAR_OK) return rc;
+  size_t scratch_bytes = 0;
+  if (cache && F > 0 && n_f > 0 && cache->H > 0 && n_f <= cache->C && n_f <= FASTAR_MAX_FRAME_KEYS) {
+    const size_t need = fastar_workspace_size(FASTAR_OP_MERGE, cache->H, n_f, cache->D, cache->T,
+                                              cache->B, cache->C);
+    if (need <= (size_t)FASTAR_NOALLOC_SCRATCH_BYTES) {
+      const int rc = scratch_address(&scratch);
+      if (rc != FASTAR_OK) return rc;
+      scratch_bytes = (size_t)FASTAR_NOALLOC_SCRATCH_BYTES;
+    }
+  }
   return fastar_tempcache_merge(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau,
-                                match_out, scratch, (size_t)FASTAR_NOALLOC_SCRATCH_BYTES,
+                                match_out, scratch, scratch_bytes,
                                 dev_status, stream);
 }
