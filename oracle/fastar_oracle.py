@@ -218,8 +218,8 @@ def tempcache_nn(state: CacheState, k: np.ndarray, f: int, tau: float):
         match[h, ok] = cand[best[ok]]
         near_tau = np.abs(top1 - tau) < NN_MARGIN
         if cand.size > 1:
-            srt = np.sort(cos, axis=1)
-            near_tie = (srt[:, -1] - srt[:, -2]) < NN_MARGIN
+            top2 = np.partition(cos, cand.size - 2, axis=1)    # [..., second, first]
+            near_tie = (top2[:, -1] - top2[:, -2]) < NN_MARGIN
         else:
             near_tie = np.zeros(n, dtype=bool)
         # a near tie only matters when the best cosine can reach tau
@@ -257,9 +257,12 @@ def tempcache_nn_lsh(state: CacheState, k: np.ndarray, k_codes: np.ndarray, f: i
         ok = top1 >= tau
         match[h, ok] = live[best[ok]]
         near_tau = np.abs(top1 - tau) < NN_MARGIN
-        srt = np.sort(cos, axis=1)
         with np.errstate(invalid="ignore"):   # rows with fewer than two candidates: no tie
-            near_tie = (srt[:, -1] - srt[:, -2]) < NN_MARGIN if live.size > 1 else np.zeros(n, dtype=bool)
+            if live.size > 1:
+                top2 = np.partition(cos, live.size - 2, axis=1)    # [..., second, first]
+                near_tie = (top2[:, -1] - top2[:, -2]) < NN_MARGIN
+            else:
+                near_tie = np.zeros(n, dtype=bool)
         listed[h] = np.isfinite(top1) & (near_tau | (near_tie & (top1 >= tau - NN_MARGIN)))
     return match, listed
 
