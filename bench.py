@@ -2,23 +2,28 @@
 """Per-chunk FAST-AR attention path on one GB300: latency, TFLOP/s, roofline.
 
 A step is one pass of the whole per-chunk path over one chunk of the
-configured workload (default: one attention layer at Wan-1.3B-like width,
-12 heads x D 128, 3 latent frames of 1560 tokens, 21 merged past frames,
-512 prompt tokens, 2 LSH tables x 8 bits):
+configured workload.  Default: the 14B-like 720p chunk -- 40 independent
+attention layers, each with 40 heads x D 128, 3 latent frames of 3600 tokens
+(10,800 queries), a cache of 21 merged past frames (capacity 32,768 groups
+per head), 512 prompt tokens, 2 LSH tables x 10 bits.  Per layer:
     hash(queries, new keys, prompt keys) -> TempCache merge (3 frames)
-    -> AnnCA prune -> AnnCA attention -> AnnSA attention.
-The timed step is the public per-chunk call (ChunkPath.step): the
-cross-attention branch (prune, AnnCA) runs on a second stream beside the
-merge and is joined before the call returns; CUDA events on the calling
-stream bracket it.  The merge mutates the cache, so the pre-chunk cache
-snapshot is restored before every step and L2 is flushed (a 256 MiB write)
-outside the timed window.  Per-stage and per-kernel times come from
-separate passes that run the stages one after the other on one stream.
+    -> AnnCA prune -> AnnCA attention -> AnnSA attention,
+and the 40 layers run one after the other inside the timed region
+(ChunkStack.step: each layer's ChunkPath.step, whose cross-attention branch
+runs on a second stream beside the merge).  CUDA events on the calling
+stream bracket the step.  The merge mutates the caches, so the pre-chunk
+snapshot of every layer's cache is restored before every step and L2 is
+flushed (a 256 MiB write), both outside the timed window; the inputs of a
+step (about 14 GB) are far larger than L2 anyway.  Per-stage and per-kernel
+times come from separate passes that run the stages one after the other.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config I] [--shard heads|layers]
 
-Prints one JSON line.  `--impl reference` times the fp64 oracle on the
-host cores instead (one head of the chunk per step, scaled to the chunk).
+Prints one JSON line.  `--impl reference` times the fp64 oracle on the host
+cores instead (see oracle_baseline).  Under torchrun each rank runs its
+share of the chunk (by default heads [r H / N, (r+1) H / N) of every layer,
+no collective on the data path) and the job's time is the slowest rank's.
 """
 from __future__ import annotations
 
@@ -39,17 +44,25 @@ sys.path.insert(0, ROOT)
 from workloads import CONFIGS, layer_data  # noqa: E402
 
 METRIC = "per-chunk FAST-AR attention ms, effective TFLOP/s, % of GB300 roofline"
+# the whole chunk is fixed and split over the ranks, so scaling is strong
+SCALING = {"heads": "strong", "layers": "strong"}
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=None,
+                    help="workload index (default: the 40-layer 14B-like chunk; --recall and --denoise "
+                         "default to the one-layer Wan-1.3B-like chunk)")
+    ap.add_argument("--shard", default="heads", choices=["heads", "layers"],
+                    help="multi-GPU split of the chunk: heads of every layer (default) or whole layers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-rollout", action="store_true",
+                    help="skip the 200-chunk rollout measurement appended to the default line")
     ap.add_argument("--rep", default="last", choices=["last", "mean"],
                     help="TempCache representative: last key (the method) or mean key (ablation)")
     ap.add_argument("--denoise", type=int, default=0,
@@ -57,7 +70,7 @@ def parse():
                          "all-dense and all-sparse schedules (one JSON line)")
     ap.add_argument("--recall", action="store_true",
                     help="sweep tau, T and B: recall and density of AnnSA and AnnCA (one JSON line)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def rank_info():
@@ -65,10 +78,32 @@ def rank_info():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def rank_layer(rank: int) -> int:
-    """The layer a rank runs: N GPUs run N independent layers of the same
-    shape (weak scaling; heads and layers share nothing on the path)."""
-    return rank
+def shard(cfg, rank: int, world: int, mode: str = "heads"):
+    """The (layers, heads) of the chunk that rank `rank` of `world` runs.
+
+    heads:  every layer, heads [r H / N, (r+1) H / N) (each GPU owns its
+            heads' cache slices; heads share nothing on the path);
+    layers: layers r, r + N, r + 2N, ... with every head.
+    Over all ranks every (layer, head) of the chunk is run exactly once."""
+    if mode == "heads":
+        if world > cfg.H:
+            raise ValueError(f"{world} ranks for {cfg.H} heads")
+        return list(range(cfg.layers)), list(range(rank * cfg.H // world, (rank + 1) * cfg.H // world))
+    if mode == "layers":
+        if world > cfg.layers:
+            raise ValueError(f"{world} ranks for {cfg.layers} layers")
+        return list(range(rank, cfg.layers, world)), list(range(cfg.H))
+    raise ValueError(mode)
+
+
+def config_dict(cfg, args, world):
+    """The workload description printed by both arms (identical keys)."""
+    return {"workload": cfg.name, "layers": cfg.layers, "H": cfg.H, "D": cfg.D, "n_f": cfg.n_f, "F": cfg.F,
+            "Nq": cfg.Nq, "P": cfg.P, "T": cfg.T, "B": cfg.B, "C": cfg.C, "tau": cfg.tau,
+            "past_frames": cfg.past_frames, "representative": args.rep,
+            "l2": "flushed before every step (256 MiB write); inputs larger than L2",
+            "parallelism": (f"{args.shard}-sharded x{world}, no collective on the data path" if world > 1
+                            else "single GPU")}
 
 
 def job_max(x: float, world: int, device) -> float:
@@ -164,37 +199,118 @@ class Clocks:
 
 
 # ----------------------------------------------------------------- oracle leg
-def oracle_chunk_one_head(cfg, d, head: int, st_head):
-    """The oracle's whole per-chunk path for one head; returns seconds."""
-    import oracle as O
-    sl = slice(head, head + 1)
-    q, k, v = d.chunk_q[0][sl], d.chunk_k[0][sl], d.chunk_v[0][sl]
-    t0 = time.perf_counter()
-    qc, _ = O.hash_codes(q, d.planes, cfg.T, cfg.B)
-    O.bucket_csr(qc, 1 << cfg.B)
-    kc, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
-    pc, _ = O.hash_codes(d.prompt_k[sl], d.planes, cfg.T, cfg.B)
-    st, _, _ = O.tempcache_merge(st_head, k, v, kc, cfg.F, cfg.n_f, cfg.past_frames, cfg.tau)
-    O.bucket_csr(st.codes, 1 << cfg.B)
-    idx, cnt = O.annca_prune(qc, pc, cfg.F, cfg.n_f)
-    O.annca_attention(q, d.prompt_k[sl], d.prompt_v[sl], idx, cnt, cfg.F, cfg.n_f, cfg.scale)
-    O.annsa_attention(q, qc, st, cfg.scale)
-    return time.perf_counter() - t0
+# The oracle (numpy fp64) is timed on the host cores, one process per core
+# (spawned, each with one BLAS thread), each process owning one (layer, head)
+# unit of the chunk: it draws that head's frames with the seeded generator,
+# merges the past frames (set-up, untimed), then times the whole per-chunk
+# path of its unit -- hash of queries, new keys and prompt keys, query CSR,
+# TempCache merge of the chunk's frames, cache CSR, AnnCA prune, AnnCA,
+# AnnSA -- once per step from the same pre-chunk state.  A step is one unit
+# on every process at once; the chunk's time is extrapolated from the
+# throughput (units per second) to all its (layer, head) units.
 
-
-def oracle_cache_one_head(cfg, d, head: int):
+def _oracle_unit_setup(cfg, layer: int, head: int):
     import oracle as O
-    sl = slice(head, head + 1)
+    cfg = cfg.replace(H=1)
+    d = layer_data(cfg, layer=layer, chunks=1, heads=[head])
     st = O.CacheState.empty(1, cfg.C, cfg.D, cfg.T, cfg.dtype)
     f = 0
     while f < cfg.past_frames:
         nF = min(cfg.F, cfg.past_frames - f)
-        k = np.concatenate(d.past_k[f:f + nF], axis=1)[sl]
-        v = np.concatenate(d.past_v[f:f + nF], axis=1)[sl]
+        k = np.concatenate(d.past_k[f:f + nF], axis=1)
+        v = np.concatenate(d.past_v[f:f + nF], axis=1)
         kc, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
         st, _, _ = O.tempcache_merge(st, k, v, kc, nF, cfg.n_f, f, cfg.tau)
         f += nF
-    return st
+    return cfg, d, st
+
+
+def _oracle_unit_chunk(cfg, d, st) -> float:
+    """The oracle's whole per-chunk path for one (layer, head); seconds."""
+    import oracle as O
+    q, k, v = d.chunk_q[0], d.chunk_k[0], d.chunk_v[0]
+    t0 = time.perf_counter()
+    qc, _ = O.hash_codes(q, d.planes, cfg.T, cfg.B)
+    O.bucket_csr(qc, 1 << cfg.B)
+    kc, _ = O.hash_codes(k, d.planes, cfg.T, cfg.B)
+    pc, _ = O.hash_codes(d.prompt_k, d.planes, cfg.T, cfg.B)
+    st2, _, _ = O.tempcache_merge(st, k, v, kc, cfg.F, cfg.n_f, cfg.past_frames, cfg.tau)
+    O.bucket_csr(st2.codes, 1 << cfg.B)
+    idx, cnt = O.annca_prune(qc, pc, cfg.F, cfg.n_f)
+    O.annca_attention(q, d.prompt_k, d.prompt_v, idx, cnt, cfg.F, cfg.n_f, cfg.scale)
+    O.annsa_attention(q, qc, st2, cfg.scale)
+    return time.perf_counter() - t0
+
+
+def _oracle_worker(conn, cfg, layer, head):
+    """Process body: set up one unit, then time it once per 'go'."""
+    try:
+        cfg, d, st = _oracle_unit_setup(cfg, layer, head)
+        conn.send(("ready", None))
+        while True:
+            msg = conn.recv()
+            if msg != "go":
+                break
+            conn.send(("done", _oracle_unit_chunk(cfg, d, st)))
+    except Exception as e:  # reported to the parent, which raises
+        conn.send(("error", repr(e)))
+    finally:
+        conn.close()
+
+
+class OracleTeam:
+    """One spawned process per host core, each owning a (layer, head) unit."""
+
+    def __init__(self, cfg, workers: int):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+        for k in saved:
+            os.environ[k] = "1"
+        self.units = [(w // cfg.H % cfg.layers, w % cfg.H) for w in range(workers)]
+        self.conns, self.procs = [], []
+        try:
+            for layer, head in self.units:
+                a, b = ctx.Pipe()
+                p = ctx.Process(target=_oracle_worker, args=(b, cfg, layer, head), daemon=True)
+                p.start()
+                self.conns.append(a)
+                self.procs.append(p)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        t0 = time.perf_counter()
+        self._collect("ready")
+        self.setup_s = time.perf_counter() - t0
+
+    def _collect(self, want):
+        out = []
+        for c in self.conns:
+            kind, val = c.recv()
+            if kind != want:
+                raise RuntimeError(f"oracle worker: {kind} {val}")
+            out.append(val)
+        return out
+
+    def step(self):
+        """One unit on every process at once: (wall seconds, per-unit seconds)."""
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send("go")
+        per = self._collect("done")
+        return time.perf_counter() - t0, per
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send("stop")
+            except (BrokenPipeError, OSError):
+                pass
+        for p in self.procs:
+            p.join(timeout=10)
 
 
 def host_cores():
@@ -204,131 +320,208 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def oracle_baseline(cfg, timed_steps: int, warm_steps: int):
+    """Time the oracle on the host cores (see above).  Returns the JSON
+    object of the measurement: per-chunk ms extrapolated from the measured
+    unit throughput, the measured step times and what the sample was."""
+    workers = min(host_cores(), cfg.layers * cfg.H)
+    team = OracleTeam(cfg, workers)
+    try:
+        for _ in range(warm_steps):
+            team.step()
+        walls, units = [], []
+        for _ in range(timed_steps):
+            w, per = team.step()
+            walls.append(w)
+            units.extend(per)
+    finally:
+        team.close()
+    step_s = statistics.mean(walls)
+    units_per_chunk = cfg.layers * cfg.H
+    chunk_ms = step_s * units_per_chunk / workers * 1e3
+    return {"value": chunk_ms, "unit": "ms/chunk", "cores": workers, "kind": "oracle",
+            "ms_per_step": step_s * 1e3, "steps": timed_steps, "warmup": warm_steps,
+            "unit_ms_mean": statistics.mean(units) * 1e3, "setup_s": team.setup_s,
+            "sample": (f"{workers} (layer, head) units of the {cfg.layers}-layer x {cfg.H}-head chunk, one per "
+                       f"process (one BLAS thread each, {workers} processes on {host_cores()} host cores); a step "
+                       f"times every process's unit once (hash, query CSR, merge of the chunk's {cfg.F} frames, "
+                       f"cache CSR, prune, AnnCA, AnnSA; past frames merged untimed); per chunk = step time x "
+                       f"{units_per_chunk} units / {workers}")}
+
+
 def run_reference(args, cfg):
     rank, world, _ = rank_info()
     if rank != 0:
         return
-    d = layer_data(cfg, chunks=1)
-    # one head of the chunk per step; the sample is capped at 24 heads so the
-    # CPU run stays within a few minutes whatever --steps says
-    n_meas = min(args.steps, 24)
-    n_warm = min(args.warmup, 2)
-    heads = [h % cfg.H for h in range(n_warm + n_meas)]
-    states = {h: oracle_cache_one_head(cfg, d, h) for h in sorted(set(heads))}
-    times = []
-    for i, h in enumerate(heads):
-        t = oracle_chunk_one_head(cfg, d, h, states[h])
-        if i >= n_warm:
-            times.append(t)
-    per_chunk_ms = statistics.mean(times) * cfg.H * 1e3
-    cores = host_cores()
-    line = {"impl": "reference", "metric": METRIC, "value": per_chunk_ms, "unit": "ms/chunk",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per_chunk_ms, "higher_is_better": False, "scaling": "weak",
+    timed, warm = min(args.steps, 8), min(args.warmup, 1)
+    t_run = time.perf_counter()
+    ob = oracle_baseline(cfg, timed, warm)
+    t_run = time.perf_counter() - t_run
+    line = {"impl": "reference", "metric": METRIC, "value": ob["value"], "unit": "ms/chunk",
+            "n_gpus": args.gpus, "steps": timed, "warmup": warm,
+            "ms_per_step": ob["ms_per_step"], "higher_is_better": False, "scaling": SCALING[args.shard],
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq,
-                       "P": cfg.P, "T": cfg.T, "B": cfg.B, "C": cfg.C},
-            "cpu_baseline": {"value": per_chunk_ms, "unit": "ms/chunk", "cores": cores,
-                             "kind": "oracle",
-                             "sample": f"{n_meas} single-head samples of the {cfg.H}-head chunk "
-                                       f"(heads in turn, after {n_warm} warm-up samples), mean x H; "
-                                       "past frames merged untimed"},
-            "e2e": {"value": per_chunk_ms, "unit": "ms/chunk", "h2d_bytes_per_step": 0,
+            "config": config_dict(cfg, args, world),
+            "extrapolated_to_chunk": {"value": ob["value"], "unit": "ms/chunk",
+                                      "from": "unit throughput of the timed steps (see cpu_baseline.sample)"},
+            "cpu_baseline": {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean",
+                                                "setup_s")},
+            "wall_s": t_run,
+            "e2e": {"value": ob["value"], "unit": "ms/chunk", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ----------------------------------------------------------------- GPU leg
-def algorithmic(cfg, path, match, snap_size, snap_lf):
-    """Algorithmic bytes and flops of one step, per stage and per kernel.
+def _pairs_union(q_codes, c_codes, sizes, B):
+    """Allowed (query, slot) pairs of one layer, by inclusion-exclusion over
+    the tables: a pair is allowed iff its codes agree in some table, so
+    |union| = sum over non-empty table subsets S of (-1)^(|S|+1) times the
+    number of pairs whose codes agree in every table of S, counted from
+    joint code histograms.  q_codes [H][T][Nq], c_codes [H][T][C] (int32,
+    device), sizes [H] live slots.  Returns (total, per-table pairs not
+    already allowed by an earlier table)."""
+    import itertools
 
-    Bytes count each input read once and each output written once; flops
-    are 2*M*N*K for a GEMM and 4*D per (query, key) pair of attention.
-    Returns (bytes per stage, flops per stage, per-kernel models, stats);
-    a per-kernel model gives the bytes and flops of one launch (averaged over
-    the launches of that kernel in a step).
-    """
     import torch
-    H, D, T, Nq, P, n_f, F = cfg.H, cfg.D, cfg.T, cfg.Nq, cfg.P, cfg.n_f, cfg.F
+    H, T, Nq = q_codes.shape
+    C = c_codes.shape[2]
+    live = torch.arange(C, device=c_codes.device)[None, :] < sizes[:, None].long()
+    hq = torch.arange(H, device=q_codes.device)[:, None].expand(H, Nq)
+    hc = torch.arange(H, device=c_codes.device)[:, None].expand(H, C)
+
+    def agree(S):
+        kq, kc = hq.long(), hc.long()
+        for t in S:
+            kq = (kq << B) | q_codes[:, t].long()
+            kc = (kc << B) | c_codes[:, t].long()
+        kc = kc[live]
+        uq, cq = torch.unique(kq.reshape(-1), return_counts=True)
+        uc, cc = torch.unique(kc, return_counts=True)
+        idx = torch.searchsorted(uc, uq).clamp_max(max(uc.numel() - 1, 0))
+        hit = uc[idx] == uq if uc.numel() else torch.zeros_like(uq, dtype=torch.bool)
+        return int((cq[hit] * cc[idx[hit]]).sum())
+
+    cache = {}
+
+    def count(S):
+        if S not in cache:
+            cache[S] = agree(S)
+        return cache[S]
+
+    def union(tables):
+        tot = 0
+        for r in range(1, len(tables) + 1):
+            for S in itertools.combinations(tables, r):
+                tot += (-1) ** (r + 1) * count(S)
+        return tot
+
+    by_table = [union(tuple(range(t + 1))) - union(tuple(range(t))) if t else count((0,)) for t in range(T)]
+    return sum(by_table), by_table
+
+
+def annsa_tiles(path, n_live):
+    """Key tiles the AnnSA kernel walks for this layer (its work performed):
+    per table t, the queries in table-t bucket order are cut into tiles of
+    128; a tile walks the cache slots of every table-t bucket from its first
+    query's to its last query's, 64 at a time.  Returns the number of
+    (128-query x 64-key) tiles."""
+    import torch
+    H, T, Nq = path.q_codes.shape
+    nb = 1 << path.B
+    tiles = 0
+    idx = torch.arange(0, Nq, 128, device=path.q_codes.device)
+    last = torch.clamp(idx + 127, max=Nq - 1)
+    for t in range(T):
+        perm = path.q_perm[:, t].long()
+        codes = path.q_codes[:, t].long()
+        c_lo = torch.gather(codes, 1, perm[:, idx])
+        c_hi = torch.gather(codes, 1, perm[:, last])
+        off = path.cache.offsets[:, t].long()
+        kb = torch.gather(off, 1, c_lo).clamp(max=n_live[:, None])
+        ke = torch.gather(off, 1, (c_hi + 1).clamp(max=nb)).clamp(max=n_live[:, None])
+        tiles += int(((ke - kb).clamp(min=0) + 63).div(64, rounding_mode="floor").sum())
+    return tiles
+
+
+def layer_work(cfg, path, snap):
+    """Algorithmic work of one layer's chunk (from its outputs after a step).
+
+    Bytes count each input read once and each output written once
+    (element size e); flops are 2 M N K for a GEMM and 4 D per allowed
+    (query, key) pair of attention.  Returns a dict of stage bytes / flops,
+    per-kernel models (bytes and flops of all launches of the layer) and
+    counts."""
+    import torch
+    H, D, T, Nq, P, n_f, F = path.H, cfg.D, cfg.T, cfg.Nq, cfg.P, cfg.n_f, cfg.F
     e = 2 if cfg.dtype == "bf16" else 4
     size = path.cache.size.long()
     n_live = int(size.sum())
     kept = int(path.kept_cnt.long().sum())
     kept_tiles = int(((path.kept_cnt.long() + 63) // 64).sum())
     rows = H * (2 * Nq + P)
-    by = {}
-    by["hash"] = rows * (D * e + T * 4) + H * T * Nq * (4 + 4 + 4) + T * cfg.B * D * e
-    # merge: new k, v read; candidate K read; matched V read; K, V written for
-    # touched slots; per-slot metadata; cache CSR (codes read, perm written)
-    mt = match.view(H, F, n_f)
-    cand = []
-    prev_cnt = int(((snap_lf == cfg.past_frames - 1) & (torch.arange(cfg.C, device=snap_lf.device)[None]
-                                                         < snap_size[:, None])).sum())
-    by["merge"] = 0
+    C = path.C
+    lf0 = snap["last_frame"]
+    ar = torch.arange(C, device=lf0.device)[None]
+    cand = [int(((lf0 == cfg.past_frames - 1) & (ar < snap["size"][:, None])).sum())]
+    mt = path.match.view(H, F, n_f).long()
+    hh = torch.arange(H, device=mt.device)[:, None].expand(H, n_f)
+    merge_b, apply_b, nn_fl, nn_b = 0, 0, 0, 0
     for fi in range(F):
-        cand.append(prev_cnt)
         m = mt[:, fi]
-        n_matched = int((m >= 0).sum())
-        n_groups = sum(int(torch.unique(m[h][m[h] >= 0]).numel()) for h in range(H))
-        t_f = n_groups + int((m < 0).sum())
-        prev_cnt = t_f
-        by["merge"] += (2 * H * n_f * D * e + cand[-1] * D * e + n_matched * D * e
-                        + 2 * t_f * D * e + t_f * (4 * 2 + T * 4) + H * n_f * 4 * 4)
-    by["merge"] += n_live * T * (4 + 4) + H * T * ((1 << cfg.B) + 1) * 4
-    by["prune"] = H * T * (Nq + P) * 4 + H * F * P * 4
-    by["annca"] = H * Nq * D * e * 2 + kept * 2 * D * e + H * F * P * 4
-    by["annsa"] = (H * Nq * D * e * 2 + H * T * Nq * 4 + n_live * (2 * D * e + 4 + 2 * T * 4)
-                   + H * Nq * 4)
-    # allowed pairs, split by the first table in which they collide
-    pairs_t = [0] * T
-    qc = path.q_codes.long()
-    for h in range(H):
-        n = int(size[h])
-        cc = path.cache.codes[h, :, :n].long()
-        for q0 in range(0, Nq, 1024):
-            seen = torch.zeros(min(1024, Nq - q0), n, dtype=torch.bool, device=qc.device)
-            for t in range(T):
-                hit = (qc[h, t, q0:q0 + 1024, None] == cc[t][None]) & ~seen
-                pairs_t[t] += int(hit.sum())
-                seen |= hit
-    pairs = sum(pairs_t)
-    nn_flops = [2 * D * n_f * c for c in cand]
-    fl = {"hash": 2 * rows * T * cfg.B * D, "merge": sum(nn_flops), "prune": 0,
+        matched = m >= 0
+        n_matched = int(matched.sum())
+        groups = int(torch.unique((hh * C + m)[matched]).numel())
+        new = H * n_f - n_matched
+        touched = groups + new
+        nn_fl += 2 * D * n_f * cand[-1]
+        nn_b += (H * n_f + cand[-1]) * D * e
+        # apply: new k, v read; matched groups' V read; K, V, m, last_frame
+        # and codes of every touched slot written
+        apply_b += 2 * H * n_f * D * e + groups * D * e + touched * (2 * D * e + 8 + T * 4)
+        if fi + 1 < F:
+            cand.append(touched)
+    csr_b = n_live * T * (4 + 4) + H * T * ((1 << cfg.B) + 1) * 4
+    merge_b = nn_b + apply_b + csr_b
+    pairs, pairs_t = _pairs_union(path.q_codes, path.cache.codes, size, cfg.B)
+    sa_tiles = annsa_tiles(path, size)
+    by = {"hash": rows * (D * e + T * 4) + T * cfg.B * D * e,
+          "merge": merge_b,
+          "prune": H * T * (Nq + P) * 4 + H * F * P * 4,
+          "annca": 2 * H * Nq * D * e + kept * 2 * D * e + H * F * P * 4,
+          "annsa": (2 * H * Nq * D * e + H * T * Nq * 4 + n_live * (2 * D * e + 4 + T * 4)
+                    + H * Nq * 4)}
+    fl = {"hash": 2 * rows * T * cfg.B * D, "merge": nn_fl, "prune": 0,
           "annca": 4 * D * n_f * kept, "annsa": 4 * D * pairs}
     kern = {
-        "nn_tc": {"flops": sum(nn_flops) / F,
-                  "bytes": sum((H * n_f + c) * D * e for c in cand) / F},
-        "annca_tc": {"flops": fl["annca"], "bytes": by["annca"]},
-        # one launch for all tables; per table the queries and the live
-        # slots (K, V, m, codes); with T > 1 each table writes an fp32
-        # partial (o, max, sum) that the combine kernel reads back
-        "annsa_tc": {"flops": fl["annsa"],
-                     "bytes": (T * (H * Nq * D * e + n_live * (2 * D * e + 4 + 2 * T * 4))
-                               + (T * H * Nq * (D * 4 + 8) if T > 1 else H * Nq * (D * e + 4)))},
-        # the kept rows of each (head, frame), read once and written as
-        # 64-row tiles (zero rows up to the tile) that annca_tc then loads
-        "annca_compact": {"flops": 0, "bytes": 2 * kept * D * e + 2 * kept_tiles * 64 * D * e
-                          + (kept + H * F) * 4},
-        "annsa_combine": {"flops": 0, "bytes": T * H * Nq * (D * 4 + 8) + H * Nq * (D * e + 4)},
-        # one launch for the queries, the new keys and the prompt keys
-        "hash_tc": {"flops": 2 * rows * T * cfg.B * D, "bytes": rows * (D * e + T * 4)},
-        "apply": {"flops": 0, "bytes": by["merge"] / F * 0.5},
+        "nn_tc": {"flops": nn_fl, "bytes": nn_b},
+        "apply": {"flops": 0, "bytes": apply_b},
+        "annca_tc": {"flops": fl["annca"], "bytes": by["annca"],
+                     "work_flops": 4 * 128 * 64 * D * sum(int(x) for x in
+                                                          ((path.kept_cnt.long() + 63) // 64).view(-1).tolist())
+                     * ((n_f + 127) // 128)},
+        # the stage's algorithmic bytes (Q, live K/V/m/codes, O, lse, q codes
+        # each once) and its allowed-pair flops
+        "annsa_tc": {"flops": fl["annsa"], "bytes": by["annsa"],
+                     "work_flops": 4 * 128 * 64 * D * sa_tiles},
+        "annca_compact": {"flops": 0, "bytes": 2 * kept * D * e + 2 * kept_tiles * 64 * D * e + (kept + H * F) * 4},
+        "hash_tc": {"flops": fl["hash"], "bytes": rows * (D * e + T * 4)},
     }
-    return by, fl, kern, {"n_live": n_live, "kept": kept, "allowed_pairs": pairs,
-                          "allowed_pairs_by_table": pairs_t,
-                          "density": pairs / max(1, Nq * n_live)}
+    return {"bytes": by, "flops": fl, "kern": kern,
+            "stats": {"n_live": n_live, "kept": kept, "allowed_pairs": pairs, "allowed_pairs_by_table": pairs_t,
+                      "annsa_key_tiles": sa_tiles, "density_den": Nq * n_live}}
 
 
 KERNEL_SOURCES = {"nn_tc": "nn_tc.cu", "annca_tc": "attention_tc.cu", "annsa_tc": "attention_tc.cu",
-                  "hash_tc": "hash_tc.cu"}
+                  "hash_tc": "hash_tc.cu", "apply": "tempcache.cu"}
 
 
-def profiled_traffic(kernel):
+def profiled_traffic(kernel, workload):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
-    (profiles/traffic_<kernel>.txt), or None when there is none or the
-    kernel's source has changed since the counters were taken."""
+    (profiles/traffic_<kernel>_<workload>.txt), or None when there is none
+    or the kernel's source has changed since the counters were taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}.txt")
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
     src = KERNEL_SOURCES.get(kernel)
     if not src or not os.path.exists(path):
         return None
@@ -348,21 +541,17 @@ def profiled_traffic(kernel):
         return None
 
 
-def dense_reference_ms(cfg, d, reps=10):
-    """Dense attention of the same chunk: torch SDPA over the unmerged history."""
+def dense_sdpa(q, K, V, kp, vp, reps=5):
+    """Dense attention of one layer's chunk: torch SDPA over the unmerged
+    history and over the whole prompt (bf16).  Returns ms per layer."""
     import torch
     import torch.nn.functional as Fn
-    dt = torch.bfloat16
-    K = torch.from_numpy(np.concatenate(d.past_k + [d.chunk_k[0]], axis=1)).to("cuda", dt)
-    V = torch.from_numpy(np.concatenate(d.past_v + [d.chunk_v[0]], axis=1)).to("cuda", dt)
-    q = torch.from_numpy(d.chunk_q[0]).to("cuda", dt)
-    kp = torch.from_numpy(d.prompt_k).to("cuda", dt)
-    vp = torch.from_numpy(d.prompt_v).to("cuda", dt)
 
     def run():
         Fn.scaled_dot_product_attention(q[None], K[None], V[None])
-        Fn.scaled_dot_product_attention(q[None], kp[None], vp[None])
-    for _ in range(3):
+        if kp.shape[1]:
+            Fn.scaled_dot_product_attention(q[None], kp[None], vp[None])
+    for _ in range(2):
         run()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -371,14 +560,11 @@ def dense_reference_ms(cfg, d, reps=10):
         run()
     e.record()
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e) / reps
-    n_keys = K.shape[1]
-    flops = 4 * cfg.D * cfg.H * cfg.Nq * (n_keys + cfg.P)
-    return {"ms": ms, "keys": n_keys, "tflops": flops / ms / 1e9, "impl": "torch SDPA (bf16)"}
+    return s.elapsed_time(e) / reps
 
 
-def dense_ours(cfg, d, reps=10):
-    """Dense attention of the same chunk through this library's own kernels.
+def dense_ours(q, K, V, kp, vp, n_f, F, reps=5):
+    """Dense attention of one layer's chunk through this library's own kernels.
 
     A cache in which every key of the unmerged history is its own group
     (m = 1) and every code is 0 (one table of one bit, one bucket) makes
@@ -391,15 +577,10 @@ def dense_ours(cfg, d, reps=10):
     import torch.nn.functional as Fn
 
     import merged_attention_autoregressive_gb300 as fa
-    dt = torch.bfloat16
-    H, D, Nq, P, F = cfg.H, cfg.D, cfg.Nq, cfg.P, cfg.F
-    K = torch.from_numpy(np.concatenate(d.past_k + [d.chunk_k[0]], axis=1)).to("cuda", dt)
-    V = torch.from_numpy(np.concatenate(d.past_v + [d.chunk_v[0]], axis=1)).to("cuda", dt)
+    H, Nq, D = q.shape
+    P = kp.shape[1]
     n = K.shape[1]
-    q = torch.from_numpy(d.chunk_q[0]).to("cuda", dt)
-    kp = torch.from_numpy(d.prompt_k).to("cuda", dt)
-    vp = torch.from_numpy(d.prompt_v).to("cuda", dt)
-    c = fa.Cache(H, n, D, 1, 1, dt)
+    c = fa.Cache(H, n, D, 1, 1, q.dtype)
     c.K.copy_(K)
     c.V.copy_(V)
     c.m.fill_(1)
@@ -414,8 +595,8 @@ def dense_ours(cfg, d, reps=10):
     q_off = torch.tensor([0, Nq, Nq], **i32).repeat(H, 1, 1).contiguous()
     kept_idx = torch.arange(max(P, 1), **i32).repeat(H, F, 1).contiguous()
     kept_cnt = torch.full((H, F), P, **i32)
-    o_sa = torch.empty(H, Nq, D, dtype=dt, device="cuda")
-    o_ca = torch.empty(H, Nq, D, dtype=dt, device="cuda")
+    o_sa = torch.empty(H, Nq, D, dtype=q.dtype, device="cuda")
+    o_ca = torch.empty(H, Nq, D, dtype=q.dtype, device="cuda")
     lse = torch.empty(H, Nq, dtype=torch.float32, device="cuda")
     st = torch.zeros(1, **i32)
     ws_sa = torch.empty(max(1, fa.fastar_workspace_size(fa.OP_ANNSA, H, Nq, D, 1, 1, n)), dtype=torch.uint8,
@@ -430,11 +611,10 @@ def dense_ours(cfg, d, reps=10):
 
     def ca():
         if P:
-            fa.fastar_annca_attention(q, kp, vp, kept_idx, kept_cnt, F, cfg.n_f, scale, o_ca, ws=ws_ca,
-                                      status=st)
+            fa.fastar_annca_attention(q, kp, vp, kept_idx, kept_cnt, F, n_f, scale, o_ca, ws=ws_ca, status=st)
 
     def timed(fn):
-        for _ in range(3):
+        for _ in range(2):
             fn()
         torch.cuda.synchronize()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -465,9 +645,126 @@ def dense_ours(cfg, d, reps=10):
            "frac_cross": fl_ca / ms_ca / 1e9 / pk["bf16_tflops"] if P else None,
            "peak_tflops": pk["bf16_tflops"], "peak_of": "measured bf16 burst",
            "max_abs_err_vs_sdpa": err}
-    del c, K, V
+    del c
     torch.cuda.empty_cache()
     return out
+
+
+class LayerSource:
+    """The frames, prompt and hyperplanes of one layer, as device tensors of
+    the heads `heads`: drawn on the device (workloads.gen_device) unless the
+    workload's prompt has its own clusters (the long-prompt workload, whose
+    relevance labels come from the host generator)."""
+
+    def __init__(self, cfg, layer, heads, device="cuda"):
+        import torch
+        self.cfg, self.hs, self.dev = cfg, slice(heads[0], heads[-1] + 1), device
+        self.tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+        self.rel = None
+        if cfg.prompt_clusters:
+            self.np = layer_data(cfg, layer=layer, chunks=1)
+            self.next = 0
+            self.rel = self.np.prompt_rel[self.hs]
+        else:
+            from workloads.gen_device import DeviceLayerStream
+            self.np = None
+            self.ds = DeviceLayerStream(cfg, layer, device)
+
+    def _dev(self, a):
+        import torch
+        return torch.from_numpy(np.ascontiguousarray(a[self.hs])).to(self.dev, self.tdt)
+
+    def planes(self):
+        import torch
+        if self.np is not None:
+            return torch.from_numpy(self.np.planes).to(self.dev, self.tdt)
+        return self.ds.planes()
+
+    def frames(self, n):
+        """(k, v, q) of the next n frames, concatenated over frames: [H][n n_f][D]."""
+        import torch
+        if self.np is not None:
+            cfg = self.cfg
+            f0 = self.next
+            self.next += n
+            if f0 >= cfg.past_frames:
+                c = (f0 - cfg.past_frames) // cfg.F
+                return self._dev(self.np.chunk_k[c]), self._dev(self.np.chunk_v[c]), self._dev(self.np.chunk_q[c])
+            cat = lambda xs: self._dev(np.concatenate(xs, axis=1))  # noqa: E731
+            return cat(self.np.past_k[f0:f0 + n]), cat(self.np.past_v[f0:f0 + n]), None
+        fr = [self.ds.frame() for _ in range(n)]
+        return tuple(torch.cat([f[i][self.hs] for f in fr], dim=1).contiguous() for i in range(3))
+
+    def prompt(self):
+        if self.np is not None:
+            return self._dev(self.np.prompt_k), self._dev(self.np.prompt_v)
+        kp, vp = self.ds.prompt()
+        return kp[self.hs].contiguous(), vp[self.hs].contiguous()
+
+
+def prepare_stack(cfg, args, layers, heads, keep_history=False):
+    """Caches of the rank's layers with their past frames merged, and the
+    chunk inputs.  Returns (stack, inputs, sources, history of the first
+    layer (K, V of every unmerged key) or None)."""
+    import torch
+
+    from merged_attention_autoregressive_gb300.path import ChunkStack
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    stack = ChunkStack(len(layers), len(heads), cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt,
+                       rep=args.rep)
+    inputs, sources, hist = [], [], None
+    for i, layer in enumerate(layers):
+        src = LayerSource(cfg, layer, heads)
+        path = stack.paths[i]
+        path.planes.copy_(src.planes())
+        hk, hv = [], []
+        f = 0
+        while f < cfg.past_frames:
+            nF = min(cfg.F, cfg.past_frames - f)
+            k, v, _ = src.frames(nF)
+            path.merge(k, v, f, F=nF)
+            if keep_history and i == 0:
+                hk.append(k)
+                hv.append(v)
+            f += nF
+        k, v, q = src.frames(cfg.F)
+        kp, vp = src.prompt()
+        inputs.append((q, k, v, kp, vp))
+        sources.append(src)
+        if keep_history and i == 0:
+            hist = (torch.cat(hk + [k], dim=1), torch.cat(hv + [v], dim=1))
+        torch.cuda.synchronize()
+        assert int(path.status.item()) == 0, f"layer {layer}: device status {int(path.status.item())}"
+    return stack, inputs, sources, hist
+
+
+def run_stages(path, x, first, cfg, args, ev):
+    """The five stages of one layer one after the other on the current
+    stream, recording ev[0..5] around them (per-stage times)."""
+    import torch
+
+    import merged_attention_autoregressive_gb300 as fa
+    q, k, v, kp, vp = x
+    stream = torch.cuda.current_stream()
+    st = path.status
+    ev[0].record(stream)
+    jobs = [(q, path.q_codes, path.q_perm, path.q_offsets), (k, path.k_codes, None, None)]
+    if cfg.P:
+        jobs.append((kp, path.p_codes, None, None))
+    fa.fastar_hash_many(jobs, path.planes, cfg.T, cfg.B, status=st)
+    ev[1].record(stream)
+    fa.fastar_tempcache_merge(path.cache, k, v, path.k_codes, cfg.F, cfg.n_f, first, cfg.tau,
+                              match_out=path.match, ws=path.ws_merge, status=st, rep=args.rep, planes=path.planes)
+    ev[2].record(stream)
+    fa.fastar_annca_prune(path.q_codes, path.p_codes[:, :, :cfg.P], cfg.F, cfg.n_f, cfg.B, path.kept_idx,
+                          path.kept_cnt, status=st)
+    ev[3].record(stream)
+    fa.fastar_annca_attention(q, kp, vp, path.kept_idx, path.kept_cnt, cfg.F, cfg.n_f, path.scale, path.o_ca,
+                              ws=path.ws_annca, status=st)
+    ev[4].record(stream)
+    fa.fastar_annsa_attention(q, path.q_codes, path.q_perm, path.q_offsets, path.cache, path.scale, path.o_sa,
+                              path.lse, ws=path.ws_annsa, status=st)
+    ev[5].record(stream)
 
 
 def run_ours(args, cfg):
@@ -476,7 +773,6 @@ def run_ours(args, cfg):
 
     import merged_attention_autoregressive_gb300 as fa
     from merged_attention_autoregressive_gb300 import build as fbuild
-    from merged_attention_autoregressive_gb300.path import ChunkPath
 
     rank, world, local = rank_info()
     torch.cuda.set_device(local)
@@ -484,64 +780,31 @@ def run_ours(args, cfg):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     fbuild.build()
     fa.lib()
-    d = layer_data(cfg, layer=rank_layer(rank), chunks=1)
-    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
-    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", tdt)  # noqa: E731
-    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt, rep=args.rep)
-    path.planes.copy_(todev(d.planes))
-    f = 0
-    while f < cfg.past_frames:
-        nF = min(cfg.F, cfg.past_frames - f)
-        path.merge(todev(np.concatenate(d.past_k[f:f + nF], 1)),
-                   todev(np.concatenate(d.past_v[f:f + nF], 1)), f, F=nF)
-        f += nF
-    torch.cuda.synchronize()
-    snap = path.cache.snapshot()
-    q, k, v = todev(d.chunk_q[0]), todev(d.chunk_k[0]), todev(d.chunk_v[0])
-    kp, vp = todev(d.prompt_k), todev(d.prompt_v)
+    layers, heads = shard(cfg, rank, world, args.shard)
+    want_dense = not args.no_dense and rank == 0 and cfg.dtype == "bf16"
+    t_prep = time.perf_counter()
+    stack, inputs, sources, hist = prepare_stack(cfg, args, layers, heads, keep_history=want_dense)
+    snaps = [p.cache.snapshot() for p in stack.paths]
+    t_prep = time.perf_counter() - t_prep
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
     first = cfg.past_frames
-    st = path.status
     stages = ["hash", "merge", "prune", "annca", "annsa"]
 
-    def step(ev=None):
-        rec = (lambda i: ev[i].record(stream)) if ev else (lambda i: None)
-        rec(0)
-        fa.fastar_hash_many([(q, path.q_codes, path.q_perm, path.q_offsets),
-                             (k, path.k_codes, None, None), (kp, path.p_codes, None, None)],
-                            path.planes, cfg.T, cfg.B, status=st)
-        rec(1)
-        fa.fastar_tempcache_merge(path.cache, k, v, path.k_codes, cfg.F, cfg.n_f, first, cfg.tau,
-                                  match_out=path.match, ws=path.ws_merge, status=st, rep=args.rep,
-                                  planes=path.planes)
-        rec(2)
-        fa.fastar_annca_prune(path.q_codes, path.p_codes, cfg.F, cfg.n_f, cfg.B, path.kept_idx,
-                              path.kept_cnt, status=st)
-        rec(3)
-        fa.fastar_annca_attention(q, kp, vp, path.kept_idx, path.kept_cnt, cfg.F, cfg.n_f,
-                                  path.scale, path.o_ca, ws=path.ws_annca, status=st)
-        rec(4)
-        fa.fastar_annsa_attention(q, path.q_codes, path.q_perm, path.q_offsets, path.cache,
-                                  path.scale, path.o_sa, path.lse, ws=path.ws_annsa, status=st)
-        rec(5)
-
-    def chunk():
-        # the public per-chunk call: the cross-attention branch runs on a
-        # second stream and is joined before it returns
-        path.step(q, k, v, kp, vp, first)
-
     def prep():
-        path.cache.restore(snap)
+        for p, sn in zip(stack.paths, snaps):
+            p.cache.restore(sn)
         flush.fill_(1)
+
+    def check():
+        for p in stack.paths:
+            assert int(p.status.item()) == 0, fa.STATUS.get(int(p.status.item()))
 
     for _ in range(max(3, args.warmup)):
         prep()
-        chunk()
-        prep()
-        step()
+        stack.step(inputs, first)
     torch.cuda.synchronize()
-    assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))
+    check()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = Clocks(local)
     n0 = fa.fastar_launch_count()
@@ -554,151 +817,195 @@ def run_ours(args, cfg):
     for i in range(args.steps):
         prep()
         evs[i][0].record(stream)
-        chunk()
+        stack.step(inputs, first)
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     clocks.window(t0, time.time())
     clk = clocks.stop()
     launches = fa.fastar_launch_count() - n0
-    assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))
+    check()
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
     ms = statistics.mean(step_ms)
-    # per-stage times: a separate pass that runs the stages one after the
-    # other on one stream, with events between them
-    n_ssteps = min(args.steps, 50)
-    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_ssteps)]
-    for i in range(n_ssteps):
-        prep()
-        step(sevs[i])
-    torch.cuda.synchronize()
-    stage_ms = {s: statistics.mean(e[j].elapsed_time(e[j + 1]) for e in sevs)
-                for j, s in enumerate(stages)}
-    # the job's time is its slowest rank's; every rank ran args.steps chunks
-    total_ms = job_max(sum(step_ms), world, "cuda")
-    value = total_ms / (args.steps * world)
+    # the job's time per chunk is its slowest rank's; the ranks together ran
+    # every (layer, head) of the chunk once per step
+    value = job_max(ms, world, "cuda")
 
-    # per-kernel durations: a separate pass with the library's launch timer
-    # (same restore + L2 flush protocol), events on the launch stream
-    timer = fa.LaunchTimer(64)
-    per_kernel = {}
-    n_tsteps = min(args.steps, 50)
-    for i in range(n_tsteps):
+    # per-stage times: the stages of every layer one after the other
+    n_ss = min(args.steps, 3)
+    stage_ms = {s_: 0.0 for s_ in stages}
+    for _ in range(n_ss):
         prep()
+        sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in stack.paths]
+        for p, x, ev in zip(stack.paths, inputs, sevs):
+            run_stages(p, x, first, cfg, args, ev)
+        torch.cuda.synchronize()
+        for j, s_ in enumerate(stages):
+            stage_ms[s_] += sum(ev[j].elapsed_time(ev[j + 1]) for ev in sevs) / n_ss
+    check()
+
+    # per-kernel durations: the library's launch timer (events on the launch
+    # stream after every kernel) over the same sequential stages
+    timer = fa.LaunchTimer(48 * len(stack.paths) + 16)
+    per_kernel = {}
+    n_ts = min(args.steps, 2)
+    for _ in range(n_ts):
+        prep()
+        sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in stack.paths]
         timer.begin()
-        step()
+        for p, x, ev in zip(stack.paths, inputs, sevs):
+            run_stages(p, x, first, cfg, args, ev)
         for name, ms_k in timer.end():
             per_kernel.setdefault(name, []).append(ms_k)
-    kernels = {k: {"launches_per_step": len(v) / n_tsteps, "avg_ms": statistics.mean(v),
-                   "ms_per_step": sum(v) / n_tsteps} for k, v in per_kernel.items()}
+    kernels = {k: {"launches_per_step": len(v) / n_ts, "avg_ms": statistics.mean(v),
+                   "ms_per_step": sum(v) / n_ts} for k, v in per_kernel.items()}
+    check()
 
-    # end to end through the C ABI with host buffers (pinned), copies timed
-    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
-    hkp, hvp = kp.cpu().pin_memory(), vp.cpu().pin_memory()
-    ho_ca, ho_sa = torch.empty_like(path.o_ca, device="cpu").pin_memory(), \
-        torch.empty_like(path.o_sa, device="cpu").pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hkp, hvp))
-    d2h = ho_ca.numel() * ho_ca.element_size() + ho_sa.numel() * ho_sa.element_size()
+    # end to end through the public call with host buffers (pinned): every
+    # layer's inputs copied in and both outputs copied out inside the window
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+    hin = [tuple(pinned_copy(t) for t in x) for x in inputs]
+    hout = [(torch.empty(p.o_ca.shape, dtype=p.o_ca.dtype, pin_memory=True),
+             torch.empty(p.o_sa.shape, dtype=p.o_sa.dtype, pin_memory=True)) for p in stack.paths]
+    h2d = sum(t.numel() * t.element_size() for x in hin for t in x)
+    d2h = sum(t.numel() * t.element_size() for x in hout for t in x)
     e2e = []
-    for i in range(args.steps + 3):
+    for i in range(args.steps + 2):
         prep()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
         s0.record(stream)
-        # the public host-to-host chunk: copies in per branch, outputs copied
-        # out as soon as they are final, all inside the timed region
-        path.step_host(hq, hk, hv, hkp, hvp, ho_ca, ho_sa, first)
+        stack.step_host(hin, hout, first, dev_in=inputs)
         s1.record(stream)
         torch.cuda.synchronize()
-        if i >= 3:
+        if i >= 2:
             e2e.append(s0.elapsed_time(s1))
-    e2e_ms = statistics.mean(e2e)
+    check()
+    e2e_ms = job_max(statistics.mean(e2e), world, "cuda")
+    del hin, hout
 
-    # algorithmic work of the step (from the last step's outputs)
-    by, fl, kern, stats = algorithmic(cfg, path, path.match.clone(), snap["size"], snap["last_frame"])
+    # algorithmic work of the step (from the last step's outputs), summed
+    # over this rank's layers
+    by = {s_: 0 for s_ in stages}
+    fl = {s_: 0 for s_ in stages}
+    kern, stats = {}, {}
+    for p, sn in zip(stack.paths, snaps):
+        w = layer_work(cfg, p, sn)
+        for s_ in stages:
+            by[s_] += w["bytes"][s_]
+            fl[s_] += w["flops"][s_]
+        for k_, m_ in w["kern"].items():
+            d_ = kern.setdefault(k_, {})
+            for kk, vv in m_.items():
+                d_[kk] = d_.get(kk, 0) + vv
+        for k_, v_ in w["stats"].items():
+            if isinstance(v_, list):
+                stats[k_] = [a + b for a, b in zip(stats.get(k_, [0] * len(v_)), v_)]
+            else:
+                stats[k_] = stats.get(k_, 0) + v_
+    stats["density"] = stats.pop("allowed_pairs") / max(1, stats.pop("density_den"))
     pk = peaks()
     # roofline of the kernel with the largest device time per step
     dom = max(kernels, key=lambda k: kernels[k]["ms_per_step"])
-    km = kern.get(dom, {"flops": 0, "bytes": 0})
+    nl = kernels[dom]["launches_per_step"]
+    km = {k: v / nl for k, v in kern.get(dom, {"flops": 0, "bytes": 0}).items()}
     kms = kernels[dom]["avg_ms"]
-    t_tc = km["flops"] / (pk["bf16_tflops"] * 1e12)
-    t_bw = km["bytes"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = km.get("flops", 0) / (pk["bf16_tflops"] * 1e12)
+    t_bw = km.get("bytes", 0) / (pk["hbm_gbs"] * 1e9)
     if t_tc >= t_bw:
         bound, achieved, peak, unit = "tensor", km["flops"] / kms / 1e9, pk["bf16_tflops"], "TFLOP/s"
     else:
         bound, achieved, peak, unit = "hbm", km["bytes"] / kms / 1e6, pk["hbm_gbs"], "GB/s"
-    traffic = profiled_traffic(dom)
+    roof = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": profiled_traffic(dom, cfg.name),
+            "peak_source": pk["source"] + " (burst)", "avg_launch_ms": kms, "launches_per_step": nl,
+            "algorithmic_bytes_per_launch": km.get("bytes", 0),
+            "algorithmic_flops_per_launch": km.get("flops", 0)}
+    work = {}
+    for k_ in ("annsa_tc", "annca_tc"):
+        if k_ in kern and k_ in kernels and kern[k_].get("work_flops"):
+            t_k = kernels[k_]["ms_per_step"]
+            work[k_] = {"mma_flops_issued": kern[k_]["work_flops"], "algorithmic_flops": kern[k_]["flops"],
+                        "TFLOP/s_issued": kern[k_]["work_flops"] / t_k / 1e9,
+                        "frac_of_peak_issued": kern[k_]["work_flops"] / t_k / 1e9 / pk["bf16_tflops"],
+                        "TFLOP/s_algorithmic": kern[k_]["flops"] / t_k / 1e9,
+                        "GB/s_algorithmic": kern[k_]["bytes"] / t_k / 1e6,
+                        "hbm_frac_algorithmic": kern[k_]["bytes"] / t_k / 1e6 / pk["hbm_gbs"]}
+    kernel_roofs = {}
+    for k_, m_ in kern.items():
+        if k_ in kernels:
+            t_k = kernels[k_]["ms_per_step"]
+            kernel_roofs[k_] = {"GB/s": m_["bytes"] / t_k / 1e6, "hbm_frac": m_["bytes"] / t_k / 1e6 / pk["hbm_gbs"],
+                                "TFLOP/s": m_["flops"] / t_k / 1e9,
+                                "tensor_frac": m_["flops"] / t_k / 1e9 / pk["bf16_tflops"]}
     eff_tflops = sum(fl.values()) / ms / 1e9
     line = {"metric": METRIC, "value": value, "unit": "ms/chunk", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": cfg.dtype, "data": "synthetic",
-            "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq, "P": cfg.P,
-                       "T": cfg.T, "B": cfg.B, "C": cfg.C, "past_frames": cfg.past_frames,
-                       "l2": "flushed before every step (256 MiB write)", "representative": args.rep,
-                       "parallelism": (f"layer-parallel x{world}: rank r runs layer r, no collective"
-                                       if world > 1 else "single GPU")},
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": value,
+            "higher_is_better": False, "scaling": SCALING[args.shard], "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic (seeded; drawn on the GPU, see workloads/gen_device.py)"
+            if cfg.prompt_clusters == 0 else "synthetic (seeded; host generator)",
+            "config": config_dict(cfg, args, world),
+            "rank0_share": {"layers": len(layers), "heads": len(heads)},
             "effective_tflops": eff_tflops,
             "stages_ms": stage_ms,
-            "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
-                         "unit": unit, "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": pk["source"] + " (burst)",
-                         "avg_launch_ms": kms, "launches_per_step": kernels[dom]["launches_per_step"],
-                         "algorithmic_bytes_per_launch": km["bytes"],
-                         "algorithmic_flops_per_launch": km["flops"]},
+            "roofline": roof,
+            "attention_work_performed": work,
             "kernels": kernels,
-            "stage_rooflines": {s: {"GB/s": by[s] / stage_ms[s] / 1e6,
-                                    "hbm_frac": by[s] / stage_ms[s] / 1e6 / pk["hbm_gbs"],
-                                    "TFLOP/s": fl[s] / stage_ms[s] / 1e9} for s in stages},
+            "kernel_rooflines": kernel_roofs,
+            "stage_rooflines": {s_: {"GB/s": by[s_] / stage_ms[s_] / 1e6,
+                                     "hbm_frac": by[s_] / stage_ms[s_] / 1e6 / pk["hbm_gbs"],
+                                     "TFLOP/s": fl[s_] / stage_ms[s_] / 1e9} for s_ in stages},
             "work": stats,
+            # the merge's kernels per layer: candidate set-up, per frame NN,
+            # plan and apply, and the cache CSR (the other CSR is the query's)
+            "merge_launches_per_layer": sum(kernels[k]["launches_per_step"] for k in
+                                            ("cand_init", "cand_norm", "nn_tc", "plan", "apply")
+                                            if k in kernels) / len(stack.paths) + 1,
             "gpu_launches": launches,
             "clocks": clk,
             "wall_s_timed": t_wall,
-            "e2e": {"value": e2e_ms, "unit": "ms/chunk", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h}}
-    if cfg.P:
+            "prep_s": t_prep,
+            "e2e": {"value": e2e_ms, "unit": "ms/chunk", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}}
+    if cfg.P and sources[0].rel is not None:
         # AnnCA pruning of this chunk: kept prompt tokens per (head, frame)
-        # and, where the prompt has a relevance label, the share of the
-        # relevant tokens that survive
-        kc = path.kept_cnt.cpu().numpy()
-        ki = path.kept_idx.cpu().numpy()
-        rel = np.asarray(d.prompt_rel)
-        pr = {"kept_per_head_frame": {"min": int(kc.min()), "mean": float(kc.mean()),
-                                      "max": int(kc.max()), "of": cfg.P}}
-        if not rel.all():
-            hit = tot = 0
-            for h in range(cfg.H):
-                for f in range(cfg.F):
-                    kept = ki[h, f, :kc[h, f]]
-                    hit += int(rel[h][kept].sum())
-                    tot += int(rel[h].sum())
-            pr["recall_relevant"] = hit / max(tot, 1)
-            pr["relevant_share_of_prompt"] = float(rel.mean())
-        line["prune"] = pr
-    if cfg.layers > 1:
-        # layers are independent and identical in shape: one layer is timed
-        # and the per-chunk figures are scaled to all of them
-        L = cfg.layers
-        line["value"] *= L
-        line["ms_per_step"] *= L
-        line["e2e"]["value"] *= L
-        line["e2e"]["h2d_bytes_per_step"] *= L
-        line["e2e"]["d2h_bytes_per_step"] *= L
-        line["config"]["layers"] = L
-        line["config"]["timed_layers"] = 1
-        line["config"]["scaled"] = f"one layer timed, x{L}"
-    if not args.no_dense and rank == 0:
-        line["dense"] = dense_reference_ms(cfg, d)
-        if cfg.layers > 1:
-            line["dense"]["ms_all_layers"] = line["dense"]["ms"] * cfg.layers
-        if cfg.dtype == "bf16" and cfg.D == 128:
-            line["dense_ours"] = dense_ours(cfg, d)
+        # and the share of the relevant tokens that survive
+        p0 = stack.paths[0]
+        kc = p0.kept_cnt.cpu().numpy()
+        ki = p0.kept_idx.cpu().numpy()
+        rel = np.asarray(sources[0].rel)
+        hit = tot = 0
+        for h in range(kc.shape[0]):
+            for f in range(cfg.F):
+                hit += int(rel[h][ki[h, f, :kc[h, f]]].sum())
+                tot += int(rel[h].sum())
+        line["prune"] = {"kept_per_head_frame": {"min": int(kc.min()), "mean": float(kc.mean()),
+                                                 "max": int(kc.max()), "of": cfg.P},
+                         "recall_relevant": hit / max(tot, 1), "relevant_share_of_prompt": float(rel.mean())}
+    if want_dense:
+        q, k, v, kp, vp = inputs[0]
+        K, V = hist
+        sd = dense_sdpa(q, K, V, kp, vp)
+        line["dense"] = {"impl": "torch SDPA (bf16)", "keys": K.shape[1], "ms_per_layer": sd,
+                         "ms": sd * cfg.layers, "timed": f"one layer of {len(heads)} heads, x {cfg.layers} layers",
+                         "tflops": 4 * cfg.D * len(heads) * cfg.Nq * (K.shape[1] + cfg.P) / sd / 1e9}
+        if cfg.D == 128:
+            do = dense_ours(q, K, V, kp, vp, cfg.n_f, cfg.F)
+            do["ms_per_layer"] = do["ms"]
+            do["ms"] = do["ms"] * cfg.layers
+            do["timed"] = f"one layer of {len(heads)} heads, x {cfg.layers} layers"
+            line["dense_ours"] = do
+        del K, V, hist
+    del stack, inputs, snaps
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_rollout and cfg.idx == 4:
+        line["rollout"] = rollout_measure(CONFIGS[2], args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        h = 0
-        st_h = oracle_cache_one_head(cfg, d, h)
-        secs = [oracle_chunk_one_head(cfg, d, h, st_h) for _ in range(2)]
-        line["cpu_baseline"] = {"value": min(secs) * cfg.H * 1e3, "unit": "ms/chunk",
-                                "cores": host_cores(), "kind": "oracle",
-                                "sample": "head 0 of the chunk (best of 2), x H heads"}
+        ob = oracle_baseline(cfg, 1, 0)
+        line["cpu_baseline"] = {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean",
+                                                   "setup_s")}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -824,43 +1131,31 @@ def run_recall(args, cfg):
     print(json.dumps(line), flush=True)
 
 
-def run_rollout(args, cfg):
+def rollout_measure(cfg, args):
     """A rollout of cfg.chunks chunks from an empty cache (the long-rollout
-    workload): per chunk the latency of the public chunk call, the live
-    groups and the device memory held, and whether they stay flat."""
+    workload, inputs drawn on the device): per chunk the latency of the
+    public chunk call (L2 flushed before each), the live groups and the
+    device memory held, and whether they stay flat.  Returns a dict."""
     import torch
 
     import merged_attention_autoregressive_gb300 as fa
-    from merged_attention_autoregressive_gb300 import build as fbuild
     from merged_attention_autoregressive_gb300.path import ChunkPath
-    from workloads.gen import HeadStream, planes as gen_planes, prompt as gen_prompt
+    from workloads.gen_device import DeviceLayerStream
 
-    rank, world, local = rank_info()
-    torch.cuda.set_device(local)
-    fbuild.build()
-    fa.lib()
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
-    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", tdt)  # noqa: E731
-    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt)
-    path.planes.copy_(todev(gen_planes(cfg, 0)))
-    streams = [HeadStream(cfg, 0, h) for h in range(cfg.H)]
-    pk, pv, _ = zip(*[gen_prompt(cfg, 0, h, s.centroids) for h, s in enumerate(streams)])
-    kp, vp = todev(np.stack(pk)), todev(np.stack(pv))
+    path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt, rep=args.rep)
+    ds = DeviceLayerStream(cfg, 0)
+    path.planes.copy_(ds.planes())
+    kp, vp = ds.prompt()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-
-    def next_chunk():
-        fr = [[s.frame() for _ in range(cfg.F)] for s in streams]
-        cat = lambda i: todev(np.stack([np.concatenate([f[i] for f in hf], axis=0) for hf in fr]))  # noqa: E731
-        return cat(2), cat(0), cat(1)  # q, k, v
-
     ms, n_live, resident = [], [], []
     n0 = fa.fastar_launch_count()
-    clocks = Clocks(local)
-    clocks.start()
-    t0 = time.time()
+    t_wall = time.perf_counter()
     for c in range(cfg.chunks):
-        q, k, v = next_chunk()
+        fr = [ds.frame() for _ in range(cfg.F)]
+        k, v, q = (torch.cat([f[i] for f in fr], dim=1).contiguous() for i in range(3))
+        del fr
         flush.fill_(1)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -869,35 +1164,63 @@ def run_rollout(args, cfg):
         torch.cuda.synchronize()
         ms.append(e0.elapsed_time(e1))
         n_live.append(float(path.cache.size.float().mean().item()))
+        del q, k, v
         resident.append(torch.cuda.memory_allocated())
-    clocks.window(t0, time.time())
-    clk = clocks.stop()
+    t_wall = time.perf_counter() - t_wall
     assert int(path.status.item()) == 0, fa.STATUS.get(int(path.status.item()))
     launches = fa.fastar_launch_count() - n0
     tail = np.array(ms[-100:]) if len(ms) >= 100 else np.array(ms)
     slope = float(np.polyfit(np.arange(len(tail)), tail, 1)[0]) * 100 / float(tail.mean())
     last50 = np.array(ms[-50:])
     row = cfg.D * 2 * (2 if cfg.dtype == "bf16" else 4)  # K and V bytes per key
-    line = {"metric": METRIC, "value": float(np.mean(ms)), "unit": "ms/chunk", "n_gpus": 1,
-            "steps": cfg.chunks, "warmup": 0, "ms_per_step": float(np.mean(ms)),
-            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-            "dtype": cfg.dtype, "data": "synthetic",
+    out = {"workload": cfg.name, "chunks": cfg.chunks, "H": cfg.H, "C": cfg.C,
+           "ms_mean": float(np.mean(ms)), "ms_first_chunk": ms[0], "ms_median": float(np.median(ms)),
+           "ms_median_last50": float(np.median(last50)),
+           "slope_last100_pct_of_mean_per_100_chunks": slope,
+           "max_over_median_last50": float(last50.max() / np.median(last50)),
+           "flat": bool(abs(slope) < 1.0 and last50.max() <= 1.1 * np.median(last50)
+                        and min(resident) == max(resident)),
+           "ms_every_10th_chunk": ms[::10],
+           "n_live_every_10th_chunk": n_live[::10], "n_live_final": n_live[-1],
+           "first_chunk_at_capacity": next((i for i, x in enumerate(n_live) if x >= cfg.C), None),
+           "device_bytes_allocated": {"min": min(resident), "max": max(resident)},
+           "cache_bytes": path.cache.nbytes(),
+           "cache_live_kv_bytes_final": int(n_live[-1] * cfg.H * row),
+           "dense_cache_keys_equiv": cfg.chunks * cfg.F * cfg.n_f,
+           "dense_cache_kv_bytes_equiv": cfg.chunks * cfg.F * cfg.n_f * cfg.H * row,
+           "gpu_launches": launches, "wall_s": t_wall,
+           "l2": "flushed before every chunk (256 MiB write)",
+           "data": "synthetic (seeded; drawn on the GPU)"}
+    del path
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_rollout(args, cfg):
+    """The long-rollout workload on its own (one JSON line)."""
+    import torch
+
+    import merged_attention_autoregressive_gb300 as fa
+    from merged_attention_autoregressive_gb300 import build as fbuild
+
+    rank, world, local = rank_info()
+    torch.cuda.set_device(local)
+    fbuild.build()
+    fa.lib()
+    clocks = Clocks(local)
+    clocks.start()
+    t0 = time.time()
+    ro = rollout_measure(cfg, args)
+    clocks.window(t0, time.time())
+    clk = clocks.stop()
+    line = {"metric": METRIC, "value": ro["ms_mean"], "unit": "ms/chunk", "n_gpus": 1,
+            "steps": cfg.chunks, "warmup": 0, "ms_per_step": ro["ms_mean"],
+            "higher_is_better": False, "scaling": "strong", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": ro["data"],
             "config": {"workload": cfg.name, "H": cfg.H, "D": cfg.D, "Nq": cfg.Nq, "P": cfg.P,
-                       "T": cfg.T, "B": cfg.B, "C": cfg.C, "chunks": cfg.chunks,
-                       "l2": "flushed before every chunk (256 MiB write)",
+                       "T": cfg.T, "B": cfg.B, "C": cfg.C, "chunks": cfg.chunks, "l2": ro["l2"],
                        "parallelism": "single GPU"},
-            "rollout": {
-                "ms_first_chunk": ms[0], "ms_median": float(np.median(ms)),
-                "ms_median_last50": float(np.median(last50)),
-                "slope_last100_pct_of_mean_per_100_chunks": slope,
-                "max_over_median_last50": float(last50.max() / np.median(last50)),
-                "ms_every_10th_chunk": ms[::10],
-                "n_live_every_10th_chunk": n_live[::10], "n_live_final": n_live[-1],
-                "device_bytes_allocated": {"min": min(resident), "max": max(resident)},
-                "cache_live_kv_bytes_final": int(n_live[-1] * cfg.H * row),
-                "dense_cache_keys_equiv": cfg.chunks * cfg.F * cfg.n_f,
-                "dense_cache_kv_bytes_equiv": cfg.chunks * cfg.F * cfg.n_f * cfg.H * row},
-            "gpu_launches": launches, "clocks": clk}
+            "rollout": ro, "gpu_launches": ro["gpu_launches"], "clocks": clk}
     print(json.dumps(line), flush=True)
 
 
@@ -971,6 +1294,8 @@ def run_denoise(args, cfg):
 
 def main():
     args = parse()
+    if args.config is None:
+        args.config = 1 if (args.denoise or args.recall) else 4
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)

@@ -23,7 +23,12 @@ DENSE_FRAC = 0.3  # sparse attention is off for this share of a chunk's denoisin
 class ChunkPath:
     """Buffers and calls of one layer's per-chunk path."""
 
-    def __init__(self, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last"):
+    def __init__(self, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last",
+                 share=None):
+        """share: another ChunkPath of the same shapes whose workspaces and
+        streams this one reuses (layers run one after the other on the same
+        streams, so their scratch never overlaps in time); caches, codes,
+        outputs and events stay per layer."""
         self.H, self.D, self.n_f, self.F, self.P = H, D, n_f, F, P
         self.rep = rep  # TempCache representative: "last" (the method) or "mean" (ablation)
         self.T, self.B, self.C, self.tau, self.dtype = T, B, C, tau, dtype
@@ -46,28 +51,39 @@ class ChunkPath:
         self.o_sa = torch.zeros(H, Nq, D, dtype=dtype, device=dev)
         self.lse = torch.zeros(H, Nq, dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, **i32)
-        self.ws_merge = torch.empty(max(1, fastar_workspace_size(OP_MERGE, H, n_f, D, T, B, C)),
-                                    dtype=torch.uint8, device=dev)
-        self.ws_annsa = torch.empty(max(1, fastar_workspace_size(OP_ANNSA, H, Nq, D, T, B, C)),
-                                    dtype=torch.uint8, device=dev)
-        self.ws_annca = torch.empty(max(1, fastar_workspace_size(OP_ANNCA, H, F, D, T, B, P)),
-                                    dtype=torch.uint8, device=dev)
-        # the second stream (query CSR, cross-attention branch) and the
-        # events that fork and join it
-        self._side = torch.cuda.Stream(device=dev)
+        if share is not None:
+            if (share.H, share.D, share.n_f, share.F, share.P, share.T, share.B, share.C) != \
+                    (H, D, n_f, F, P, T, B, C):
+                raise ValueError("a shared path must have the same shapes")
+            self.ws_merge, self.ws_annsa, self.ws_annca = share.ws_merge, share.ws_annsa, share.ws_annca
+            self._side, self._copy_in, self._copy_out = share._side, share._copy_in, share._copy_out
+        else:
+            self.ws_merge = torch.empty(max(1, fastar_workspace_size(OP_MERGE, H, n_f, D, T, B, C)),
+                                        dtype=torch.uint8, device=dev)
+            self.ws_annsa = torch.empty(max(1, fastar_workspace_size(OP_ANNSA, H, Nq, D, T, B, C)),
+                                        dtype=torch.uint8, device=dev)
+            self.ws_annca = torch.empty(max(1, fastar_workspace_size(OP_ANNCA, H, F, D, T, B, P)),
+                                        dtype=torch.uint8, device=dev)
+            # the second stream (query CSR, cross-attention branch)
+            self._side = torch.cuda.Stream(device=dev)
+            # host-to-host chunks: the streams that copy inputs in and outputs out
+            self._copy_in = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+            self._copy_out = torch.cuda.Stream(device=dev)
+        # the events that fork and join the second stream
         self._fork = torch.cuda.Event()
         self._codes_ready = torch.cuda.Event()
         self._csr_done = torch.cuda.Event()
-        # host-to-host chunks: device copies of the inputs, their copy stream
-        # and the events that release each branch
+        # host-to-host chunks: device copies of the inputs and the events
+        # that release each branch and each output
         self._dev_in = None
-        self._copy_in = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
-        self._in_free = torch.cuda.Event()
         self._in_k = torch.cuda.Event()
         self._in_v = torch.cuda.Event()
         self._in_qp = torch.cuda.Event()
         self._in_vp = torch.cuda.Event()
         self._cross_done = torch.cuda.Event()
+        self._ca_done = torch.cuda.Event()
+        self._sa_done = torch.cuda.Event()
+        self._out_done = torch.cuda.Event()
 
     # -- pieces -----------------------------------------------------------
     def merge(self, k, v, first_frame, F=None, stream=None):
@@ -100,7 +116,8 @@ class ChunkPath:
         returns, so later work on it sees every output."""
         self._run(q, k, v, kp, vp, first_frame, self._main(stream))
 
-    def step_host(self, hq, hk, hv, hkp, hvp, ho_ca, ho_sa, first_frame, stream=None):
+    def step_host(self, hq, hk, hv, hkp, hvp, ho_ca, ho_sa, first_frame, stream=None, dev_in=None,
+                  join=True):
         """The chunk from host memory to host memory (pinned tensors, same
         shapes as step's; ho_ca, ho_sa receive o_ca and o_sa).
 
@@ -109,19 +126,28 @@ class ChunkPath:
         keys and the prompt values for the cross-attention branch, which
         also builds the query CSR that AnnSA needs), each branch hashes and
         starts as soon as its inputs have landed, and each output is copied
-        out as soon as it is final.  `stream` (default: the current stream)
-        waits for all of it, so the host buffers are complete once it has
-        synchronised."""
+        out on a third stream as soon as it is final.  The copies into this
+        path's device buffers (dev_in: (q, k, v, kp, vp) tensors to use; by
+        default buffers of its own) wait only for the previous chunk of this
+        path to have read them, so with several paths (layers) the copies of
+        one run ahead of the kernels of another.  With join (the default)
+        `stream` (default: the current stream) waits for all of it, so the
+        host buffers are complete once it has synchronised; without, call
+        join_outputs before reading them."""
         main = self._main(stream)
         dev = self.q_codes.device
-        if self._dev_in is None or self._dev_in[0].shape != hq.shape or self._dev_in[3].shape != hkp.shape:
+        if dev_in is not None:
+            self._dev_in = list(dev_in)
+        elif self._dev_in is None or self._dev_in[0].shape != hq.shape or self._dev_in[3].shape != hkp.shape:
             self._dev_in = [torch.empty(x.shape, dtype=x.dtype, device=dev) for x in (hq, hk, hv, hkp, hvp)]
         dq, dk, dv, dkp, dvp = self._dev_in
-        # the staging buffers are free once the previous work on `main` is
-        self._in_free.record(main)
+        # the device inputs and outputs are free once this path's previous
+        # chunk has finished and its outputs have been copied out (never
+        # recorded before the first chunk); every stream of this chunk waits
+        # for that through the copies it depends on
         cm, cx = self._copy_in
         for c in (cm, cx):
-            c.wait_event(self._in_free)
+            c.wait_event(self._out_done)
         with torch.cuda.stream(cm):
             dk.copy_(hk, non_blocking=True)
             self._in_k.record(cm)
@@ -133,7 +159,23 @@ class ChunkPath:
             self._in_qp.record(cx)
             dvp.copy_(hvp, non_blocking=True)
             self._in_vp.record(cx)
+        main.wait_event(self._out_done)
         self._run(dq, dk, dv, dkp, dvp, first_frame, main, host_out=(ho_ca, ho_sa))
+        co = self._copy_out
+        co.wait_event(self._ca_done)
+        with torch.cuda.stream(co):
+            ho_ca.copy_(self.o_ca, non_blocking=True)
+        co.wait_event(self._sa_done)
+        with torch.cuda.stream(co):
+            ho_sa.copy_(self.o_sa, non_blocking=True)
+        self._out_done.record(co)
+        if join:
+            self.join_outputs(main)
+
+    def join_outputs(self, stream=None):
+        """Make `stream` (default: the current stream) wait until the host
+        outputs of this path's last step_host are complete."""
+        self._main(stream).wait_event(self._out_done)
 
     # -- denoising steps -----------------------------------------------------
     def denoise_step(self, s, S, q, k, v, kp, vp, first_frame, dense_frac=DENSE_FRAC):
@@ -258,6 +300,10 @@ class ChunkPath:
         # (candidate setup, the first frame's NN search and plan need only k
         # and the cache); the merge waits for the key codes (and v) right
         # before its first apply.
+        # the second stream starts after the work already on `main` (so that
+        # layers run one after the other, as in a model)
+        self._fork.record(main)
+        side.wait_event(self._fork)
         if staged:
             main.wait_event(self._in_k)
             side.wait_event(self._in_k)
@@ -268,8 +314,6 @@ class ChunkPath:
             side.wait_event(self._in_qp)
             fastar_hash_many(cross, self.planes, self.T, self.B, status=st, stream=side)
         else:
-            self._fork.record(main)
-            side.wait_event(self._fork)
             fastar_hash_many([(k, self.k_codes, None, None)] + cross, self.planes, self.T, self.B,
                              status=st, stream=side)
             self._codes_ready.record(side)
@@ -282,8 +326,7 @@ class ChunkPath:
         fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f,
                                self.scale, self.o_ca, ws=self.ws_annca, status=st, stream=side)
         if staged:
-            with torch.cuda.stream(side):
-                host_out[0].copy_(self.o_ca, non_blocking=True)
+            self._ca_done.record(side)
         self._cross_done.record(side)
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
@@ -293,6 +336,43 @@ class ChunkPath:
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
                                stream=main)
         if staged:
-            with torch.cuda.stream(main):
-                host_out[1].copy_(self.o_sa, non_blocking=True)
+            self._sa_done.record(main)
         main.wait_event(self._cross_done)
+
+
+class ChunkStack:
+    """The per-chunk path of several independent layers of one model.
+
+    One ChunkPath per layer (own cache, codes and outputs) sharing one set
+    of workspaces and streams; `step` runs the layers one after the other on
+    the calling stream, as the attention layers of a model run (a layer's
+    second stream starts after the previous layer's work)."""
+
+    def __init__(self, layers, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last"):
+        self.paths = []
+        for _ in range(layers):
+            self.paths.append(ChunkPath(H, D, n_f, F, P, T, B, C, tau, dtype, device, rep,
+                                        share=self.paths[0] if self.paths else None))
+
+    def __len__(self):
+        return len(self.paths)
+
+    def step(self, inputs, first_frame, stream=None):
+        """inputs[l] = (q, k, v, kp, vp) of layer l, as for ChunkPath.step."""
+        if len(inputs) != len(self.paths):
+            raise ValueError("one input tuple per layer")
+        for p, x in zip(self.paths, inputs):
+            p.step(*x, first_frame, stream=stream)
+
+    def step_host(self, host_inputs, host_outputs, first_frame, stream=None, dev_in=None):
+        """Host-to-host chunk of every layer: host_inputs[l] = (q, k, v, kp,
+        vp) pinned, host_outputs[l] = (o_ca, o_sa) pinned; dev_in[l] optional
+        device buffers for layer l's inputs.  The copies of later layers run
+        ahead of the kernels of earlier ones; `stream` waits for every output."""
+        if len(host_inputs) != len(self.paths) or len(host_outputs) != len(self.paths):
+            raise ValueError("one input and one output tuple per layer")
+        for i, p in enumerate(self.paths):
+            p.step_host(*host_inputs[i], *host_outputs[i], first_frame, stream=stream,
+                        dev_in=None if dev_in is None else dev_in[i], join=False)
+        for p in self.paths:
+            p.join_outputs(stream)
