@@ -337,13 +337,15 @@ def tempcache_apply_frame(state: CacheState, k, v, codes, f: int, match, rep: st
 
 def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int,
                     first_frame: int, tau: float, match_override=None, rep: str = "last",
-                    planes=None, B: int | None = None):
+                    planes=None, B: int | None = None, search: str = "prev"):
     """Merge a chunk of F frames, frame by frame, into a copy of `state`.
 
     k_new, v_new: [H][F*n_f][D]; codes_new: [H][T][F*n_f].
     match_override: optional [H][F*n_f] matches to use instead of the
     oracle's own (to continue from another implementation's decisions).
     rep, planes, B: the representative mode (tempcache_apply_frame).
+    search: "prev" (the method: frame f-1's groups, tempcache_nn) or "lsh"
+    (every earlier group sharing a bucket, tempcache_nn_lsh).
     Returns (new_state, match [H][F*n_f], listed [H][F*n_f]).
     """
     st = state.copy()
@@ -353,7 +355,12 @@ def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int
     for fi in range(F):
         sl = slice(fi * n_f, (fi + 1) * n_f)
         f = first_frame + fi
-        mt, ls = tempcache_nn(st, np.asarray(k_new)[:, sl], f, tau)
+        if search == "lsh":
+            mt, ls = tempcache_nn_lsh(st, np.asarray(k_new)[:, sl], np.asarray(codes_new)[:, :, sl], f, tau)
+        elif search == "prev":
+            mt, ls = tempcache_nn(st, np.asarray(k_new)[:, sl], f, tau)
+        else:
+            raise ValueError(search)
         if match_override is not None:
             mt = np.asarray(match_override)[:, sl].astype(np.int64)
         match[:, sl], listed[:, sl] = mt, ls
@@ -613,6 +620,35 @@ def quant_topk(q, keys, bias, k: int, bits: int, scale: float):
     return allowed
 
 
+QUANT_MARGIN = 1e-4   # score gap, relative to the vector norms, below which a selection is listed
+
+
+def quant_topk_listed(q, keys, bias, k: int, bits: int, scale: float):
+    """quant_topk with its near-boundary keys: (allowed [n][M], listed [n][M]).
+
+    For query i the selection boundary is its k-th largest approximate score
+    thr_i.  When two or more keys score within eps_i = QUANT_MARGIN * scale *
+    |q_i| * max_s |decoded key s| of thr_i, those keys are listed: any of
+    them may be the one kept (another implementation's rounding decides), so
+    a comparison accepts either side for them.  Otherwise nothing is listed."""
+    q = np.asarray(q, dtype=np.float64)
+    keys = np.asarray(keys, dtype=np.float64)
+    n, M = q.shape[0], keys.shape[0]
+    allowed = quant_topk(q, keys, bias, k, bits, scale)
+    listed = np.zeros((n, M), dtype=bool)
+    if M == 0 or k <= 0 or k >= M:
+        return allowed, listed
+    lo, hi = sq_range(keys)
+    xt = sq_decode(sq_encode(keys, lo, hi, bits), lo, hi, bits)
+    s = scale * (q @ xt.T) + np.asarray(bias, dtype=np.float64)[None, :]
+    thr = np.partition(s, M - k, axis=1)[:, M - k]          # the k-th largest
+    eps = QUANT_MARGIN * scale * np.linalg.norm(q, axis=1) * np.linalg.norm(xt, axis=1).max()
+    near = np.abs(s - thr[:, None]) < eps[:, None]
+    several = near.sum(axis=1) >= 2
+    listed[several] = near[several]
+    return allowed, listed
+
+
 def annsa_quant_attention(q, state: CacheState, k: int, bits: int, scale: float):
     """AnnSA with the quantised matcher: per query the k live slots of largest
     approximate logit, attended exactly.  Returns (o, lse)."""
@@ -639,6 +675,41 @@ def annca_quant_attention(q, k_p, v_p, k: int, bits: int, scale: float):
         allowed = quant_topk(q[h], k_p[h], np.zeros(P), k, bits, scale)
         o[h], _ = masked_attention(q[h], k_p[h], v_p[h], allowed, np.zeros(P), scale)
     return o
+
+
+def tempcache_nn_quant_listed(state: CacheState, k: np.ndarray, f: int, tau: float, bits: int):
+    """tempcache_nn_quant with its near-boundary decisions: (match, listed).
+    A decision is listed when the two best approximate cosines are within
+    QUANT_MARGIN (either candidate may be taken), or when the exact cosine
+    of the approximate best is within QUANT_MARGIN of tau."""
+    k = np.asarray(k, dtype=np.float64)
+    H, n, D = k.shape
+    match = tempcache_nn_quant(state, k, f, tau, bits)
+    listed = np.zeros((H, n), dtype=bool)
+    for h in range(H):
+        size = int(state.size[h])
+        cand = np.nonzero(state.last_frame[h, :size] == f - 1)[0]
+        if cand.size == 0:
+            continue
+        Kc = state.K[h, cand]
+        lo, hi = sq_range(Kc)
+        Kt = sq_decode(sq_encode(Kc, lo, hi, bits), lo, hi, bits)
+        kn = np.linalg.norm(k[h], axis=1)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            approx = (k[h] @ Kt.T) / (kn[:, None] * np.linalg.norm(Kt, axis=1)[None, :])
+            exact = (k[h] @ Kc.T) / (kn[:, None] * np.linalg.norm(Kc, axis=1)[None, :])
+        approx[~np.isfinite(approx)] = -np.inf
+        best = np.argmax(approx, axis=1)
+        ex = exact[np.arange(n), best]
+        near_tau = np.isfinite(ex) & (np.abs(ex - tau) < QUANT_MARGIN)
+        if cand.size > 1:
+            top2 = np.partition(approx, cand.size - 2, axis=1)
+            with np.errstate(invalid="ignore"):
+                near_tie = np.isfinite(top2[:, -1]) & ((top2[:, -1] - top2[:, -2]) < QUANT_MARGIN)
+        else:
+            near_tie = np.zeros(n, dtype=bool)
+        listed[h] = near_tau | near_tie
+    return match, listed
 
 
 def tempcache_nn_quant(state: CacheState, k: np.ndarray, f: int, tau: float, bits: int):

@@ -892,3 +892,86 @@ def test_tempcache_nn_lsh_searches_older_frames_in_the_bucket():
     st.K[0, 0] = (2.0, 0.0)                     # previous-frame group now aligned too
     match, listed = O.tempcache_nn_lsh(st, k, np.array([[[3]]], dtype=np.uint32), 4, _TAU)
     assert match[0, 0] == 0 and listed[0, 0]
+
+
+def test_tempcache_merge_lsh_search_equals_previous_frame_search_after_one_frame():
+    """After a single merged frame every live group was refreshed in that
+    frame, so with every code equal (one bucket) the search over every
+    earlier frame has exactly the previous-frame search's candidates: the
+    next frame's merge must come out identical, bit for bit."""
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(redraw=0.3)
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    zero = np.zeros((cfg.H, cfg.T, cfg.n_f), np.uint32)
+    st, _, _ = O.tempcache_merge(st, d.past_k[0], d.past_v[0], zero, 1, cfg.n_f, 0, cfg.tau)
+    a, ma, la = O.tempcache_merge(st, d.past_k[1], d.past_v[1], zero, 1, cfg.n_f, 1, cfg.tau)
+    b, mb, lb = O.tempcache_merge(st, d.past_k[1], d.past_v[1], zero, 1, cfg.n_f, 1, cfg.tau, search="lsh")
+    np.testing.assert_array_equal(ma, mb)
+    np.testing.assert_array_equal(la, lb)
+    assert (ma >= 0).any() and (ma < 0).any()
+    for name in ("K", "V", "m", "codes", "last_frame", "size", "inserted", "evicted"):
+        np.testing.assert_array_equal(getattr(a, name), getattr(b, name), err_msg=name)
+
+
+def test_tempcache_merge_lsh_search_reaches_older_groups_and_never_evicts_a_joined_one():
+    """Hand history: frame 0 holds groups A = (1, 0) and B = (0, 1); frame 1
+    only (0, 1) again (it joins B; A is not refreshed); in frame 2 the key
+    (1, 0) finds A (refreshed in frame 0) with the search over every earlier
+    frame but not with the previous-frame search; and with the capacity
+    full, the evicted slot is an unmatched one, never the group just joined."""
+    st = O.CacheState.empty(1, 3, 2, 1, "f64")
+    z = lambda n: np.zeros((1, 1, n), np.uint32)  # noqa: E731
+    st, _, _ = O.tempcache_merge(st, np.array([[[1.0, 0.0], [0.0, 1.0]]]), np.ones((1, 2, 2)), z(2), 1, 2, 0,
+                                 0.95, search="lsh")
+    st, m1, _ = O.tempcache_merge(st, np.array([[[0.0, 2.0]]]), np.ones((1, 1, 2)), z(1), 1, 1, 1, 0.95,
+                                  search="lsh")
+    assert m1[0].tolist() == [1]
+    k2 = np.array([[[3.0, 0.0], [1.0, 1.0], [-1.0, 1.0]]])   # A, then two fresh keys
+    lsh, m2, _ = O.tempcache_merge(st, k2, np.ones((1, 3, 2)), z(3), 1, 3, 2, 0.95, search="lsh")
+    prev, m2p, _ = O.tempcache_merge(st, k2, np.ones((1, 3, 2)), z(3), 1, 3, 2, 0.95)
+    assert m2[0].tolist() == [0, -1, -1]
+    assert m2p[0].tolist() == [-1, -1, -1]
+    # lsh: slot 2 is free (one insert), slot 1 (B, last refreshed in frame 1) is
+    # evicted for the other; slot 0 (A, joined now) is kept
+    assert lsh.last_frame[0].tolist() == [2, 2, 2] and lsh.m[0].tolist() == [2, 1, 1]
+    assert lsh.evicted[0] == 2 and lsh.inserted[0] == 6
+
+
+def test_quant_topk_listing_hand_cases():
+    """Keys (0, 0), (1, 3), (3, 1) at 2 bits are decoded exactly (the hand
+    fixture).  Query (1, 1) scores 0, 4, 4: with k = 1 the two keys at the
+    boundary tie, so both are listed (either may be kept); query (1, 0)
+    scores 0, 1, 3: with k = 1 key 2 is a clear winner, nothing is listed;
+    with k = 3 (every key) nothing is listed either."""
+    keys = np.array([[0.0, 0.0], [1.0, 3.0], [3.0, 1.0]])
+    q = np.array([[1.0, 1.0], [1.0, 0.0]])
+    allowed, listed = O.quant_topk_listed(q, keys, np.zeros(3), 1, 2, 1.0)
+    assert allowed.tolist() == [[False, True, False], [False, False, True]]
+    assert listed.tolist() == [[False, True, True], [False, False, False]]
+    allowed, listed = O.quant_topk_listed(q, keys, np.zeros(3), 3, 2, 1.0)
+    assert allowed.all() and not listed.any()
+    # a bias that breaks the tie by more than the margin: nothing listed
+    allowed, listed = O.quant_topk_listed(q, keys, np.array([0.0, 0.0, 0.01]), 1, 2, 1.0)
+    assert allowed[0].tolist() == [False, False, True] and not listed[0].any()
+
+
+def test_quant_tempcache_listing_hand_cases():
+    """Candidates (1, 0) and (0, 1) (refreshed in frame 0) quantise exactly at
+    any bits >= 1 (each coordinate is its range's end).  Key (1, 1) has
+    approximate cosines 0.7071 to both: a tie, listed; its exact cosine is
+    below tau = 0.95 anyway.  Key (1, 0.01) picks (1, 0) clearly, exact
+    cosine 0.99995 >= tau: matched, not listed.  With tau = 0.99995 - 5e-5
+    the same decision sits within the margin of tau: listed."""
+    st = O.CacheState.empty(1, 4, 2, 1, "f64")
+    st.K[0, :2] = [[1.0, 0.0], [0.0, 1.0]]
+    st.last_frame[0, :2] = 0
+    st.m[0, :2] = 1
+    st.size[0] = 2
+    k = np.array([[[1.0, 1.0], [1.0, 0.01]]])
+    match, listed = O.tempcache_nn_quant_listed(st, k, 1, 0.95, 4)
+    assert match[0].tolist() == [-1, 0]
+    assert listed[0].tolist() == [True, False]
+    c = 1.0 / math.sqrt(1.0 + 1e-4)
+    match, listed = O.tempcache_nn_quant_listed(st, k, 1, c - 5e-5, 4)
+    assert match[0].tolist() == [-1, 0] and listed[0].tolist() == [True, True]
