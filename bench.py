@@ -65,6 +65,13 @@ def parse(argv=None):
                     help="skip the 200-chunk rollout measurement appended to the default line")
     ap.add_argument("--rep", default="last", choices=["last", "mean"],
                     help="TempCache representative: last key (the method) or mean key (ablation)")
+    ap.add_argument("--search", default="prev",
+                    help="TempCache search: prev (the previous frame's groups, the method), lsh (every earlier "
+                         "group sharing an LSH bucket) or quant<bits> (the previous frame's groups ranked by "
+                         "their quantised keys)")
+    ap.add_argument("--quant", type=str, default="",
+                    help="comma-separated bits (e.g. 2,4,8,16): the quantised matcher (TempCache-Quant, "
+                         "AnnCA-Quant, AnnSA-Quant) per chunk, recall and density (one JSON line)")
     ap.add_argument("--denoise", type=int, default=0,
                     help="time the S denoising steps of one chunk (dense for the first 30%%) against "
                          "all-dense and all-sparse schedules (one JSON line)")
@@ -100,7 +107,7 @@ def config_dict(cfg, args, world):
     """The workload description printed by both arms (identical keys)."""
     return {"workload": cfg.name, "layers": cfg.layers, "H": cfg.H, "D": cfg.D, "n_f": cfg.n_f, "F": cfg.F,
             "Nq": cfg.Nq, "P": cfg.P, "T": cfg.T, "B": cfg.B, "C": cfg.C, "tau": cfg.tau,
-            "past_frames": cfg.past_frames, "representative": args.rep,
+            "past_frames": cfg.past_frames, "representative": args.rep, "search": args.search,
             "l2": "flushed before every step (256 MiB write); inputs larger than L2",
             "parallelism": (f"{args.shard}-sharded x{world}, no collective on the data path" if world > 1
                             else "single GPU")}
@@ -711,7 +718,7 @@ def prepare_stack(cfg, args, layers, heads, keep_history=False):
     from merged_attention_autoregressive_gb300.path import ChunkStack
     tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
     stack = ChunkStack(len(layers), len(heads), cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, tdt,
-                       rep=args.rep)
+                       rep=args.rep, search=args.search)
     inputs, sources, hist = [], [], None
     for i, layer in enumerate(layers):
         src = LayerSource(cfg, layer, heads)
@@ -754,7 +761,8 @@ def run_stages(path, x, first, cfg, args, ev):
     fa.fastar_hash_many(jobs, path.planes, cfg.T, cfg.B, status=st)
     ev[1].record(stream)
     fa.fastar_tempcache_merge(path.cache, k, v, path.k_codes, cfg.F, cfg.n_f, first, cfg.tau,
-                              match_out=path.match, ws=path.ws_merge, status=st, rep=args.rep, planes=path.planes)
+                              match_out=path.match, ws=path.ws_merge, status=st, rep=args.rep, planes=path.planes,
+                              search=args.search)
     ev[2].record(stream)
     fa.fastar_annca_prune(path.q_codes, path.p_codes[:, :, :cfg.P], cfg.F, cfg.n_f, cfg.B, path.kept_idx,
                           path.kept_cnt, status=st)
@@ -1224,6 +1232,111 @@ def run_rollout(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def run_quant(args, cfg):
+    """The quantised matcher in place of the LSH buckets, per precision: one
+    chunk of cfg's layer (past frames merged with the same search), the
+    merge with TempCache-Quant, AnnCA-Quant and AnnSA-Quant one after the
+    other on one stream (cache restored and L2 flushed before every rep),
+    with k set to the pages' densities (AnnSA-Quant 28 %, AnnCA-Quant
+    29.5 % of the keys); the share of the dense softmax mass each query
+    keeps (same logits) and the density.  One JSON line."""
+    import torch
+
+    import merged_attention_autoregressive_gb300 as fa
+    from merged_attention_autoregressive_gb300 import build as fbuild
+    from merged_attention_autoregressive_gb300.path import ChunkPath
+
+    fbuild.build()
+    fa.lib()
+    bits_list = [int(b) for b in args.quant.split(",") if b]
+    d = layer_data(cfg, chunks=1)
+    todev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda", torch.bfloat16)  # noqa: E731
+    q, k, v = (todev(x) for x in (d.chunk_q[0], d.chunk_k[0], d.chunk_v[0]))
+    kp, vp = todev(d.prompt_k), todev(d.prompt_v)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    rows = []
+    for bits in bits_list:
+        path = ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau, torch.bfloat16,
+                         search=f"quant{bits}")
+        path.planes.copy_(todev(d.planes))
+        f = 0
+        while f < cfg.past_frames:
+            nF = min(cfg.F, cfg.past_frames - f)
+            path.merge(todev(np.concatenate(d.past_k[f:f + nF], 1)), todev(np.concatenate(d.past_v[f:f + nF], 1)),
+                       f, F=nF)
+            f += nF
+        torch.cuda.synchronize()
+        snap = path.cache.snapshot()
+        n_live = float(path.cache.size.float().mean())
+        k_sa = max(1, int(round(0.28 * n_live)))
+        k_ca = max(1, int(round(0.295 * cfg.P)))
+        ws_sa = torch.empty(fa.fastar_workspace_size(fa.OP_QUANT, cfg.H, cfg.Nq, cfg.D, bits, 0, cfg.C),
+                            dtype=torch.uint8, device="cuda")
+        ws_ca = torch.empty(fa.fastar_workspace_size(fa.OP_QUANT, cfg.H, cfg.Nq, cfg.D, bits, 0, cfg.P),
+                            dtype=torch.uint8, device="cuda")
+        sel_ca = torch.zeros(cfg.H, cfg.Nq, (cfg.P + 31) // 32, dtype=torch.int32, device="cuda")
+        st = path.status
+
+        def chunk(ev=None):
+            if ev:
+                ev[0].record(stream)
+            fa.fastar_hash(k, path.planes, cfg.T, cfg.B, path.k_codes, status=st)
+            fa.fastar_tempcache_merge(path.cache, k, v, path.k_codes, cfg.F, cfg.n_f, cfg.past_frames, cfg.tau,
+                                      match_out=path.match, ws=path.ws_merge, status=st, search=f"quant{bits}")
+            if ev:
+                ev[1].record(stream)
+            fa.fastar_annca_quant_attention(q, kp, vp, path.scale, k_ca, bits, path.o_ca, sel_mask=sel_ca,
+                                            ws=ws_ca, status=st)
+            if ev:
+                ev[2].record(stream)
+            fa.fastar_annsa_quant_attention(q, path.cache, path.scale, k_sa, bits, path.o_sa, path.lse, ws=ws_sa,
+                                            status=st)
+            if ev:
+                ev[3].record(stream)
+
+        for _ in range(3):
+            path.cache.restore(snap)
+            chunk()
+        reps = max(3, min(args.steps, 20))
+        t = []
+        for _ in range(reps):
+            path.cache.restore(snap)
+            flush.fill_(1)
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            chunk(ev)
+            torch.cuda.synchronize()
+            t.append([ev[i].elapsed_time(ev[i + 1]) for i in range(3)])
+        assert int(st.item()) == 0, fa.STATUS.get(int(st.item()))
+        t = np.median(np.array(t), axis=0)
+        # recall: share of the dense softmax mass (same logits) each query keeps
+        qf = q.float()
+        sa_ret, ca_ret = [], []
+        for h in range(cfg.H):
+            n = int(path.cache.size[h])
+            logits = path.scale * qf[h] @ path.cache.K[h, :n].float().T + torch.log(
+                path.cache.m[h, :n].float())[None, :]
+            sa_ret.append(float(torch.exp(path.lse[h] - torch.logsumexp(logits, dim=1)).mean()))
+            sp = torch.softmax(path.scale * qf[h] @ kp[h].float().T, dim=1)
+            m = sel_ca[h].long() & 0xFFFFFFFF
+            bitsm = ((m[:, :, None] >> torch.arange(32, device="cuda")[None, None, :]) & 1).reshape(cfg.Nq, -1)
+            ca_ret.append(float((sp * bitsm[:, :cfg.P].float()).sum(dim=1).mean()))
+        rows.append({"bits": bits, "ms_merge": float(t[0]), "ms_annca_quant": float(t[1]),
+                     "ms_annsa_quant": float(t[2]), "ms_chunk": float(t.sum()),
+                     "n_live_per_head": n_live, "annsa_k": k_sa, "annsa_density": k_sa / n_live,
+                     "annsa_retained": float(np.mean(sa_ret)), "annca_k": k_ca, "annca_density": k_ca / cfg.P,
+                     "annca_retained": float(np.mean(ca_ret))})
+        del path, ws_sa, ws_ca
+        torch.cuda.empty_cache()
+    line = {"metric": "per-chunk ms and retained softmax share of the quantised matcher", "unit": "ms/chunk",
+            "value": rows[0]["ms_chunk"] if rows else None, "higher_is_better": False, "data": "synthetic",
+            "config": {"workload": cfg.name, "H": cfg.H, "Nq": cfg.Nq, "P": cfg.P, "past_frames": cfg.past_frames,
+                       "l2": "flushed before every chunk (256 MiB write)",
+                       "k": "28 % of the live groups (AnnSA-Quant), 29.5 % of the prompt (AnnCA-Quant)"},
+            "sweep": rows}
+    print(json.dumps(line), flush=True)
+
+
 def run_denoise(args, cfg):
     """The S denoising steps of one chunk on cfg's shapes (cache of the past
     frames built first): per chunk and per step device time with the
@@ -1295,10 +1408,12 @@ def run_denoise(args, cfg):
 def main():
     args = parse()
     if args.config is None:
-        args.config = 1 if (args.denoise or args.recall) else 4
+        args.config = 1 if (args.denoise or args.recall or args.quant) else 4
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.quant:
+        run_quant(args, cfg)
     elif args.denoise:
         run_denoise(args, cfg)
     elif args.recall:

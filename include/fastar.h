@@ -302,6 +302,48 @@ int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new,
                                cudaEvent_t codes_ready);
 
 /*
+ * fastar_tempcache_merge_search -- fastar_tempcache_merge with a choice of
+ * where step 1 looks for the nearest earlier group.
+ *
+ * Passage: FAST-AR technical summary (gist.science) 2.A (the nearest key
+ * among the earlier frames is found with LSH or quantisation); FAST-AR
+ * analysis (paper.rainbus.top), method steps, TempCache (the default looks
+ * at the previous frame).
+ *
+ * search = FASTAR_SEARCH_PREV: exactly fastar_tempcache_merge_ev (the
+ * groups refreshed in frame f-1).  search = FASTAR_SEARCH_LSH: the
+ * candidates of k_j are every live group (refreshed in any earlier frame)
+ * that shares an LSH bucket with k_j in some table (the cache's stored
+ * codes against codes_new); largest cosine, ties to the lowest slot, joined
+ * iff the cosine >= tau; step 3 never evicts a group joined in the same
+ * frame.  The cache CSR (perm, offsets) is rebuilt before every frame's
+ * search, so the caller's CSR need not be current; with FASTAR_SEARCH_LSH
+ * codes_ready (NULL: none) is waited for before the first search.
+ * search = FASTAR_SEARCH_QUANT_BITS(b), 1 <= b <= 16 (the quantised
+ * matcher, TempCache-Quant; FAST-AR summary (paperlayer.ai) section 5 "ANN
+ * Attention" and appendix C; paper.rainbus.top, reproduction: 8-bit codes
+ * by default): the candidates are frame f-1's groups as in
+ * FASTAR_SEARCH_PREV, quantised per dimension over their own range to b-bit
+ * codes (code = floor((x - lo) / (hi - lo) (2^b - 1) + 0.5), computed in
+ * fp64); k_j takes the candidate of largest cosine to its decoded key (ties:
+ * lowest slot) and joins it iff the exact cosine reaches tau.  bf16 with
+ * D = 128 only (FASTAR_ERR_UNSUPPORTED otherwise); a frame with more than
+ * n_f candidates (left by a call with larger frames) sets
+ * FASTAR_ERR_DEVICE_ARG.  Same workspace as fastar_tempcache_merge; errors
+ * as fastar_tempcache_merge, plus FASTAR_ERR_ARG for an unknown search.
+ */
+#define FASTAR_SEARCH_PREV 0
+#define FASTAR_SEARCH_LSH 1
+#define FASTAR_SEARCH_QUANT 2
+#define FASTAR_SEARCH_QUANT_BITS(b) (FASTAR_SEARCH_QUANT | ((b) << 8))
+int fastar_tempcache_merge_search(const fastar_cache* cache, const void* k_new,
+                                  const void* v_new, const uint32_t* codes_new,
+                                  int F, int n_f, int32_t first_frame, float tau,
+                                  int search, int32_t* match_out, void* ws,
+                                  size_t ws_bytes, int32_t* dev_status,
+                                  cudaStream_t stream, cudaEvent_t codes_ready);
+
+/*
  * fastar_tempcache_merge_noalloc -- fastar_tempcache_merge without a
  * caller workspace.  The paper has no counterpart: this is a convenience of
  * this library for callers that cannot allocate device memory, such as a
@@ -431,6 +473,44 @@ int fastar_annsa_attention_part(fastar_dtype dt, const void* q,
 int fastar_annsa_combine(int H, int Nq, int D, int part_total, const void* ws,
                          size_t ws_bytes, void* out, float* lse,
                          int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * fastar_annsa_quant_attention / fastar_annca_quant_attention -- AnnSA and
+ * AnnCA with the quantised matcher instead of the LSH buckets.
+ *
+ * Passage: FAST-AR summary (paperlayer.ai) section 5 "ANN Attention" (keep
+ * the keys of largest query-key product, found by LSH or by quantised
+ * similarity search without offline preprocessing) and appendix C
+ * (quantisation precision for ANN matching, 2 to 32 bits); FAST-AR analysis
+ * (paper.rainbus.top), reproduction (FAISS, 8-bit by default).
+ *
+ * The keys of each head (AnnSA: the live cache slots; AnnCA: the P prompt
+ * tokens) are quantised per dimension over their own range [lo, hi] to
+ * `bits`-bit codes, code = floor((x - lo) / (hi - lo) (2^bits - 1) + 0.5)
+ * (0 where hi == lo; computed in fp64), decoded as lo + code (hi - lo) /
+ * (2^bits - 1).  Each query keeps the topk keys of largest approximate
+ * score scale q . decoded + bias (AnnSA: bias ln m; AnnCA: 0; ties: lower
+ * index; every key when topk >= their number) and attends them exactly:
+ *   out[h][i] = sum_{kept s} softmax_s(scale q_i.K[s] + bias_s) V[s]
+ * (lse as for fastar_annsa_attention).  sel_mask, optional [H][Nq][ceil(N /
+ * 32)] uint32 (N = C or P), receives the kept keys as bits (bit s % 32 of
+ * word s / 32).  bf16 with D = 128; 1 <= bits <= 16 (FASTAR_ERR_UNSUPPORTED
+ * otherwise).  ws: fastar_workspace_size(FASTAR_OP_QUANT, H, Nq, D, bits, 0,
+ * N) bytes (codes, scores of a batch of heads, the selection).  Approximate
+ * scores are fp32; keys whose score is within rounding of the topk-th may
+ * fall on either side.  Errors as fastar_annsa_attention.
+ */
+#define FASTAR_OP_QUANT 6
+int fastar_annsa_quant_attention(fastar_dtype dt, const void* q, int Nq,
+                                 const fastar_cache* cache, float scale, int topk,
+                                 int bits, void* out, float* lse, uint32_t* sel_mask,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status,
+                                 cudaStream_t stream);
+int fastar_annca_quant_attention(fastar_dtype dt, const void* q, const void* k_p,
+                                 const void* v_p, int H, int Nq, int P, int D,
+                                 float scale, int topk, int bits, void* out,
+                                 uint32_t* sel_mask, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

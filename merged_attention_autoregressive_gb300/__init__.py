@@ -21,6 +21,20 @@ BF16, F32 = 0, 1
 OP_HASH, OP_MERGE, OP_PRUNE, OP_ANNCA, OP_ANNSA, OP_ANNSA_PARTS = 0, 1, 2, 3, 4, 5
 REP_LAST, REP_MEAN = 0, 1
 REPS = {"last": REP_LAST, "mean": REP_MEAN}
+SEARCH_PREV, SEARCH_LSH, SEARCH_QUANT = 0, 1, 2
+OP_QUANT = 6
+
+
+def search_code(search: str) -> int:
+    """"prev", "lsh" or "quant<bits>" (e.g. "quant8") as the C ABI's search value."""
+    if search == "prev":
+        return SEARCH_PREV
+    if search == "lsh":
+        return SEARCH_LSH
+    if search.startswith("quant"):
+        bits = int(search[5:])
+        return SEARCH_QUANT | (bits << 8)
+    raise ValueError(f"unknown search {search!r}")
 STATUS = {0: "FASTAR_OK", 1: "FASTAR_ERR_ARG", 2: "FASTAR_ERR_UNSUPPORTED", 3: "FASTAR_ERR_CUDA",
           4: "FASTAR_ERR_WORKSPACE", 16: "FASTAR_ERR_CAPACITY", 17: "FASTAR_ERR_TIMEOUT",
           18: "FASTAR_ERR_DEVICE_ARG"}
@@ -29,7 +43,8 @@ EXPORTS = ["fastar_status_string", "fastar_version", "fastar_launch_count",
            "fastar_workspace_size", "fastar_hash", "fastar_hash_many", "fastar_bucket_csr",
            "fastar_tempcache_merge", "fastar_tempcache_merge_ev", "fastar_annca_prune", "fastar_annca_attention",
            "fastar_annsa_attention", "fastar_check_bounded_wait", "fastar_tempcache_merge_rep",
-           "fastar_annsa_attention_part", "fastar_annsa_combine"]
+           "fastar_annsa_attention_part", "fastar_annsa_combine", "fastar_tempcache_merge_search",
+           "fastar_annsa_quant_attention", "fastar_annca_quant_attention"]
 
 
 class FastarError(RuntimeError):
@@ -96,6 +111,12 @@ def lib() -> ctypes.CDLL:
         L.fastar_annsa_combine.argtypes = [_I, _I, _I, _I, _VP, _SZ, _VP, _VP, _VP, _VP]
         L.fastar_tempcache_merge_rep.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
                                                  ctypes.c_int32, _F, _I, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]
+        L.fastar_tempcache_merge_search.argtypes = [ctypes.POINTER(CacheStruct), _VP, _VP, _VP, _I, _I,
+                                                    ctypes.c_int32, _F, _I, _VP, _VP, _SZ, _VP, _VP, _VP]
+        L.fastar_annsa_quant_attention.argtypes = [_I, _VP, _I, ctypes.POINTER(CacheStruct), _F, _I, _I, _VP, _VP,
+                                                   _VP, _VP, _SZ, _VP, _VP]
+        L.fastar_annca_quant_attention.argtypes = [_I, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP, _VP, _VP,
+                                                   _SZ, _VP, _VP]
         for name in EXPORTS[7:]:
             getattr(L, name).restype = _I
         _lib = L
@@ -283,15 +304,26 @@ class Cache:
 
 def fastar_tempcache_merge(cache: Cache, k_new, v_new, codes_new, F, n_f, first_frame, tau,
                            match_out=None, ws=None, status=None, stream=None, codes_ready=None,
-                           rep="last", planes=None):
+                           rep="last", planes=None, search="prev"):
     """Merge the F frames of a chunk (k_new/v_new [H][F*n_f][D]) into `cache`.
 
     codes_ready: a torch.cuda.Event after which codes_new and v_new are
     final (fastar_tempcache_merge_ev); None: they are ready on `stream`.
     rep: "last" (the method's representative) or "mean" (the mean-key
-    ablation, fastar_tempcache_merge_rep; needs the hash `planes`)."""
+    ablation, fastar_tempcache_merge_rep; needs the hash `planes`).
+    search: "prev" (the previous frame's groups, the method), "lsh" (every
+    earlier group sharing a bucket) or "quant<bits>" (the previous frame's
+    groups ranked by their b-bit quantised keys), fastar_tempcache_merge_search."""
     ws, nbytes = _ws(OP_MERGE, cache.H, n_f, cache.D, cache.T, cache.B, cache.C, ws, k_new.device)
     cs = cache.struct()
+    if search != "prev":
+        if rep != "last":
+            raise ValueError("the search over every earlier frame keeps the last key")
+        _check(lib().fastar_tempcache_merge_search(
+            ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F, n_f, first_frame, tau, search_code(search),
+            _p(match_out), _p(ws), nbytes, _p(status), _stream(stream),
+            None if codes_ready is None else codes_ready.cuda_event), "fastar_tempcache_merge_search")
+        return
     if rep != "last":
         _check(lib().fastar_tempcache_merge_rep(
             ctypes.byref(cs), _p(k_new), _p(v_new), _p(codes_new), F, n_f, first_frame, tau, REPS[rep],
@@ -358,3 +390,28 @@ def fastar_annsa_attention(q, q_codes, q_perm, q_offsets, cache: Cache, scale, o
     _check(lib().fastar_annsa_attention(_dt(q), _p(q), _p(q_codes), _p(q_perm), _p(q_offsets), Nq,
                                         ctypes.byref(cs), scale, _p(out), _p(lse), _p(ws), nbytes,
                                         _p(status), _stream(stream)), "fastar_annsa_attention")
+
+
+def fastar_annsa_quant_attention(q, cache: Cache, scale, topk, bits, out, lse=None, sel_mask=None, ws=None,
+                                 status=None, stream=None):
+    """out [H][Nq][D]: each query attends its topk live slots of largest
+    approximate score under bits-bit quantised keys (sel_mask optional
+    [H][Nq][ceil(C/32)] int32 receives the kept slots as bits)."""
+    H, Nq, D = q.shape
+    ws, nbytes = _ws(OP_QUANT, cache.H, Nq, cache.D, bits, 0, cache.C, ws, q.device)
+    cs = cache.struct()
+    _check(lib().fastar_annsa_quant_attention(_dt(q), _p(q), Nq, ctypes.byref(cs), scale, topk, bits, _p(out),
+                                              _p(lse), _p(sel_mask), _p(ws), nbytes, _p(status), _stream(stream)),
+           "fastar_annsa_quant_attention")
+
+
+def fastar_annca_quant_attention(q, k_p, v_p, scale, topk, bits, out, sel_mask=None, ws=None, status=None,
+                                 stream=None):
+    """out [H][Nq][D]: each query attends its topk prompt tokens of largest
+    approximate score under bits-bit quantised prompt keys."""
+    H, Nq, D = q.shape
+    P = k_p.shape[1]
+    ws, nbytes = _ws(OP_QUANT, H, Nq, D, bits, 0, P, ws, q.device)
+    _check(lib().fastar_annca_quant_attention(_dt(q), _p(q), _p(k_p), _p(v_p), H, Nq, P, D, scale, topk, bits,
+                                              _p(out), _p(sel_mask), _p(ws), nbytes, _p(status), _stream(stream)),
+           "fastar_annca_quant_attention")

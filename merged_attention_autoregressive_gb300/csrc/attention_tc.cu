@@ -98,6 +98,11 @@ struct SaArgs {
   float* lse;
   int slot0;       // first partial slot of this call (table t writes slot0 + t)
   int parts_only;  // write partials even for one table (no output)
+  // optional per-query selection (the quantised matcher): key position p of
+  // query i is allowed only if bit p % 32 of row_mask[(h Nq + i) mask_words
+  // + p / 32] is set (with the one-bucket description, position = slot)
+  const uint32_t* row_mask;
+  int mask_words;
 };
 
 // Wait until the PV product of key tile j has landed in O (and, since one
@@ -534,6 +539,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       tc::tc_fence_after();
       const uint64_t run = range_bits(run_a - j * kN, run_b - j * kN);
       uint32_t bits[2] = {(uint32_t)run, (uint32_t)(run >> 32)};
+      if constexpr (kSA) {
+        if (sa.row_mask && my_row >= 0) {
+          const uint32_t* mw = sa.row_mask + ((size_t)h * Nq + my_row) * sa.mask_words;
+          const int w0 = (kbeg + j * kN) >> 5;  // kbeg = 0 with the one-bucket description
+#pragma unroll
+          for (int q = 0; q < 2; ++q) bits[q] &= (w0 + q < sa.mask_words) ? mw[w0 + q] : 0u;
+        }
+      }
       bool live[2];
 #pragma unroll
       for (int q = 0; q < 2; ++q) live[q] = __any_sync(0xffffffffu, bits[q] != 0u);
@@ -879,7 +892,7 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   const size_t o_bytes = ((size_t)c->T * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
   SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
-            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0};
+            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0, nullptr, 0};
   CaArgs ca{};
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
@@ -893,6 +906,23 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   return FASTAR_OK;
 }
 
+
+// AnnSA over a one-table description of the keys with a per-query selection
+// mask (the quantised matcher): the CTA writes the normalised output.
+int launch_annsa_masked(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
+                        const int32_t* q_offsets, int Nq, const fastar_cache* c, float scale, void* out, float* lse,
+                        const uint32_t* mask, int mask_words, int32_t* st, cudaStream_t s) {
+  (void)q_offsets;
+  if (dt != FASTAR_BF16 || c->D != kD || c->T != 1) return FASTAR_ERR_UNSUPPORTED;
+  if (Nq == 0 || c->H == 0) return FASTAR_OK;
+  SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
+            (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, 1,
+            1 << c->B, nullptr, nullptr, (__nv_bfloat16*)out, lse, 0, 0, mask, mask_words};
+  CaArgs ca{};
+  CUtensorMap dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  return launch_attn<true>(dummy, dummy, dummy, dim3((Nq + kM - 1) / kM, 1, c->H), c->H, Nq, scale, ca, sa, st, s);
+}
 
 size_t annsa_parts_ws_bytes(int H, int Nq, int D, int parts) {
   if (D != kD || parts < 1 || parts > kMaxT) return 0;
@@ -911,7 +941,7 @@ int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_
   const size_t o_bytes = ((size_t)parts * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
   SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
-            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1};
+            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1, nullptr, 0};
   CaArgs ca{};
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));

@@ -192,7 +192,8 @@ int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_d
 int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
                  const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                  int32_t* match_out, void* ws, int32_t* st, cudaStream_t s,
-                 cudaEvent_t codes_ready = nullptr, int rep = 0, const void* planes = nullptr);
+                 cudaEvent_t codes_ready = nullptr, int rep = 0, const void* planes = nullptr,
+                 int search = 0);
 size_t merge_ws_bytes(int H, int n_f, int C);
 int launch_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,
                  int P, int T, int B, int32_t* kept_idx, int32_t* kept_cnt, int32_t* st,
@@ -205,6 +206,14 @@ int launch_annsa(fastar_dtype dt, const void* q, const uint32_t* q_codes,
                  const fastar_cache* c, float scale, void* out, float* lse, void* ws,
                  int32_t* st, cudaStream_t s);
 size_t annsa_ws_bytes(int H, int Nq, int D, int T);
+int launch_annsa_masked(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
+                        const int32_t* q_offsets, int Nq, const fastar_cache* c, float scale, void* out, float* lse,
+                        const uint32_t* mask, int mask_words, int32_t* st, cudaStream_t s);
+size_t quant_ws_bytes(int H, int Nq, int N, int D, int bits);
+int launch_annsa_quant(const void* q, int Nq, const fastar_cache* c, float scale, int topk, int bits, void* out,
+                       float* lse, uint32_t* sel_mask, void* ws, int32_t* st, cudaStream_t s);
+int launch_annca_quant(const void* q, const void* k_p, const void* v_p, int H, int Nq, int P, float scale, int topk,
+                       int bits, void* out, uint32_t* sel_mask, void* ws, int32_t* st, cudaStream_t s);
 }  // namespace fastar
 
 namespace fastar {

@@ -115,7 +115,7 @@ const char* fastar_status_string(int status) {
   }
 }
 
-int fastar_version(void) { return 200; }
+int fastar_version(void) { return 300; }
 
 uint64_t fastar_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -150,6 +150,7 @@ size_t fastar_workspace_size(int op, int H, int N, int D, int T, int B, int C) {
     case FASTAR_OP_ANNCA: return annca_tc_ws_bytes(H, N, C, D);  // N = frames F, C = prompt tokens P
     case FASTAR_OP_ANNSA: return annsa_ws_bytes(H, N, D, T);
     case FASTAR_OP_ANNSA_PARTS: return annsa_parts_ws_bytes(H, N, D, T);  // T = part_total
+    case FASTAR_OP_QUANT: return quant_ws_bytes(H, N, C, D, T);  // N = Nq, T = bits, C = keys per head
     default: return 0;
   }
 }
@@ -239,10 +240,12 @@ static int merge_checked(const fastar_cache* cache, const void* k_new, const voi
                          const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                          int32_t* match_out, void* ws, size_t ws_bytes, int32_t* dev_status,
                          cudaStream_t stream, cudaEvent_t codes_ready, int rep = FASTAR_REP_LAST,
-                         const void* planes = nullptr) {
+                         const void* planes = nullptr, int search = FASTAR_SEARCH_PREV) {
   int rc = check_cache(cache);
   if (rc != FASTAR_OK) return rc;
   if (rep != FASTAR_REP_LAST && rep != FASTAR_REP_MEAN) return FASTAR_ERR_ARG;
+  const bool quant_ok = (search & 0xff) == FASTAR_SEARCH_QUANT && (search >> 8) >= 1 && (search >> 8) <= 16;
+  if (search != FASTAR_SEARCH_PREV && search != FASTAR_SEARCH_LSH && !quant_ok) return FASTAR_ERR_ARG;
   if (rep == FASTAR_REP_MEAN) {
     if (!planes || !aligned16(planes)) return FASTAR_ERR_ARG;
     if (cache->T * cache->B > 64) return FASTAR_ERR_UNSUPPORTED;
@@ -263,7 +266,7 @@ static int merge_checked(const fastar_cache* cache, const void* k_new, const voi
   const size_t need = merge_ws_bytes(cache->H, n_f, cache->C);
   if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
   return launch_merge(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws,
-                      dev_status, stream, codes_ready, rep, planes);
+                      dev_status, stream, codes_ready, rep, planes, search);
 }
 
 int fastar_tempcache_merge(const fastar_cache* cache, const void* k_new, const void* v_new,
@@ -291,6 +294,15 @@ int fastar_tempcache_merge_rep(const fastar_cache* cache, const void* k_new, con
   CallRange range("fastar_tempcache_merge_rep");
   return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
                        dev_status, stream, codes_ready, rep, planes);
+}
+
+int fastar_tempcache_merge_search(const fastar_cache* cache, const void* k_new, const void* v_new,
+                                  const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
+                                  int search, int32_t* match_out, void* ws, size_t ws_bytes,
+                                  int32_t* dev_status, cudaStream_t stream, cudaEvent_t codes_ready) {
+  CallRange range("fastar_tempcache_merge_search");
+  return merge_checked(cache, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, ws_bytes,
+                       dev_status, stream, codes_ready, FASTAR_REP_LAST, nullptr, search);
 }
 
 int fastar_annca_prune(const uint32_t* q_codes, const uint32_t* p_codes, int H, int F, int n_f,
@@ -380,3 +392,44 @@ int fastar_annsa_combine(int H, int Nq, int D, int part_total, const void* ws, s
 }
 
 }  // extern "C"
+
+static int quant_common(int H, int Nq, int N, int D, float scale, int topk, int bits, const void* q,
+                        const void* out, void* ws, size_t ws_bytes) {
+  if (H < 0 || Nq < 0 || N < 0 || topk < 0) return FASTAR_ERR_ARG;
+  if (!(scale > 0.f && scale < INFINITY)) return FASTAR_ERR_ARG;
+  if (bits < 1 || bits > 16) return FASTAR_ERR_UNSUPPORTED;
+  if (D != 128) return FASTAR_ERR_UNSUPPORTED;
+  if (H == 0 || Nq == 0) return -1;  // nothing to do
+  if (!q || !out || !aligned16(q) || !aligned16(out)) return FASTAR_ERR_ARG;
+  if (N == 0) return FASTAR_ERR_ARG;
+  const size_t need = quant_ws_bytes(H, Nq, N, D, bits);
+  if (!ws || ws_bytes < need || ((uintptr_t)ws & 255)) return FASTAR_ERR_WORKSPACE;
+  return FASTAR_OK;
+}
+
+int fastar_annsa_quant_attention(fastar_dtype dt, const void* q, int Nq, const fastar_cache* cache, float scale,
+                                 int topk, int bits, void* out, float* lse, uint32_t* sel_mask, void* ws,
+                                 size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annsa_quant_attention");
+  int rc = check_cache(cache);
+  if (rc != FASTAR_OK) return rc;
+  if (dt != cache->dt) return FASTAR_ERR_ARG;
+  if (dt != FASTAR_BF16) return FASTAR_ERR_UNSUPPORTED;
+  rc = quant_common(cache->H, Nq, cache->C, cache->D, scale, topk, bits, q, out, ws, ws_bytes);
+  if (rc == -1) return FASTAR_OK;
+  if (rc != FASTAR_OK) return rc;
+  return launch_annsa_quant(q, Nq, cache, scale, topk, bits, out, lse, sel_mask, ws, dev_status, stream);
+}
+
+int fastar_annca_quant_attention(fastar_dtype dt, const void* q, const void* k_p, const void* v_p, int H, int Nq,
+                                 int P, int D, float scale, int topk, int bits, void* out, uint32_t* sel_mask,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  CallRange range("fastar_annca_quant_attention");
+  if (!dtype_ok(dt)) return FASTAR_ERR_UNSUPPORTED;
+  if (dt != FASTAR_BF16) return FASTAR_ERR_UNSUPPORTED;
+  int rc = quant_common(H, Nq, P, D, scale, topk, bits, q, out, ws, ws_bytes);
+  if (rc == -1) return FASTAR_OK;
+  if (rc != FASTAR_OK) return rc;
+  if (!k_p || !v_p || !aligned16(k_p) || !aligned16(v_p)) return FASTAR_ERR_ARG;
+  return launch_annca_quant(q, k_p, v_p, H, Nq, P, scale, topk, bits, out, sel_mask, ws, dev_status, stream);
+}

@@ -53,8 +53,14 @@ struct MergeWs {
   float* cinv;
   float* invn[2];
   __nv_bfloat16* stage;
+  void* qsmall;  // the quantised search's per-dimension ranges
   int ldc, ldn;  // row strides of cinv and invn (multiples of 4 floats)
 };
+
+size_t quant_nn_ws_bytes(int H, int n_f);
+int launch_quant_nn(const void* k_frame, long long a_rows, int n_f, int H, const void* K, int C, const int32_t* cand,
+                    const int32_t* ncand, int bits, void* ws_small, void* codes, float* dec_inv, int ld_inv,
+                    unsigned long long* best, int32_t* st, cudaStream_t s);
 
 static inline int round4(int x) { return (x + 3) & ~3; }
 
@@ -68,7 +74,8 @@ size_t merge_ws_bytes(int H, int n_f, int C) {
   b += align256((size_t)H * n_f * 8);     // best
   b += align256((size_t)H * round4(C) * 4);       // cinv
   b += 2 * align256((size_t)H * round4(n_f) * 4); // invn
-  b += align256((size_t)H * n_f * 128 * 2); // stage
+  b += align256((size_t)H * n_f * 128 * 2); // stage (the quantised search's codes)
+  b += align256(quant_nn_ws_bytes(H, n_f)); // quantised search ranges
   return b;
 }
 
@@ -92,6 +99,7 @@ static MergeWs carve(void* ws, int H, int n_f, int C) {
   w.invn[0] = (float*)take((size_t)H * w.ldn * 4);
   w.invn[1] = (float*)take((size_t)H * w.ldn * 4);
   w.stage = (__nv_bfloat16*)take((size_t)H * n_f * 128 * 2);
+  w.qsmall = (void*)take(quant_nn_ws_bytes(H, n_f));
   return w;
 }
 
@@ -226,6 +234,114 @@ __global__ void __launch_bounds__(256) nn_simt_kernel(const T* __restrict__ k_fr
   pdl_trigger();
 }
 
+// ---------------------------------------------------------------- NN over every earlier frame
+// The search variant that looks for the nearest earlier group over every
+// previous frame through the LSH buckets (gist.science technical summary
+// 2.A: the nearest earlier key is found with LSH or quantisation; the
+// method's default searches the previous frame only): the candidates of new
+// key j are the live groups sharing an LSH bucket with it in some table,
+// read from the cache's bucket CSR (rebuilt before every frame); a group
+// found through table t is skipped when an earlier table already offered
+// it.  One warp per key, one candidate per lane (32 at a time): each lane
+// reads its candidate's slot, its earlier-table codes and its whole row
+// (independent loads), and the key is read from shared memory; the warp
+// keeps the top-1 cosine, ties to the lowest slot, packed as by the NN
+// kernels; the plan merges iff the cosine reaches tau.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) nn_lsh_kernel(const T* __restrict__ k_frame, int n_f, int row_stride_keys,
+                                                     const uint32_t* __restrict__ codes_frame,
+                                                     const T* __restrict__ K, const uint32_t* __restrict__ codes,
+                                                     const int32_t* __restrict__ size,
+                                                     const int32_t* __restrict__ perm,
+                                                     const int32_t* __restrict__ offsets, int C, int Tt, int nb,
+                                                     unsigned long long* __restrict__ best_out, int32_t* st) {
+  pdl_wait();
+  constexpr int PER = D / 32;
+  constexpr int VN = 16 / (int)sizeof(T);  // elements per 16-byte load
+  __shared__ float s_key[8][D];
+  if (status_bad(st)) return;
+  const int h = blockIdx.y, wib = threadIdx.x >> 5;
+  const int j = blockIdx.x * 8 + wib;
+  const int lane = threadIdx.x & 31;
+  if (j >= n_f) return;  // a whole warp; no block barrier follows
+  const T* kj = k_frame + ((size_t)h * row_stride_keys + j) * D;
+  float nk = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const float v = Elem<T>::ld(kj + lane + 32 * i);
+    s_key[wib][lane + 32 * i] = v;
+    nk = fmaf(v, v, nk);
+  }
+  nk = warp_sum(nk);
+  __syncwarp();
+  uint32_t kc[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) kc[t] = t < Tt ? codes_frame[((size_t)h * Tt + t) * row_stride_keys + j] : 0u;
+  const int n_live = min(max(size[h], 0), C);
+  float best = -INFINITY;
+  int best_slot = 0x7fffffff;
+  bool bad = false;
+  if (nk > 0.f) {
+    const float sk = sqrtf(nk);
+    for (int t = 0; t < Tt; ++t) {
+      if (kc[t] >= (uint32_t)nb) {
+        bad = true;
+        continue;
+      }
+      const int32_t* off = offsets + ((size_t)h * Tt + t) * (nb + 1);
+      const int a = min(max(off[kc[t]], 0), n_live);
+      const int b = min(max(off[kc[t] + 1], a), n_live);
+      const int32_t* pt = perm + ((size_t)h * Tt + t) * C;
+      for (int p0 = a; p0 < b; p0 += 32) {
+        const int p = p0 + lane;
+        if (p >= b) continue;
+        const int s = pt[p];
+        if (s < 0 || s >= n_live) {
+          bad = true;
+          continue;
+        }
+        bool seen = false;
+        for (int u = 0; u < t; ++u) seen |= codes[((size_t)h * Tt + u) * C + s] == kc[u];
+        if (seen) continue;
+        const T* ks = K + ((size_t)h * C + s) * D;
+        float dot = 0.f, nn = 0.f;
+#pragma unroll 4
+        for (int d = 0; d < D; d += VN) {
+          float kv[VN];
+          ld_vec<T, VN>(ks + d, kv);
+#pragma unroll
+          for (int e = 0; e < VN; ++e) {
+            dot = fmaf(s_key[wib][d + e], kv[e], dot);
+            nn = fmaf(kv[e], kv[e], nn);
+          }
+        }
+        if (nn > 0.f) {
+          const float cs = dot / (sk * sqrtf(nn));
+          if (cs > best || (cs == best && s < best_slot)) {
+            best = cs;
+            best_slot = s;
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int os = __shfl_xor_sync(0xffffffffu, best_slot, o);
+    if (ob > best || (ob == best && os < best_slot)) {
+      best = ob;
+      best_slot = os;
+    }
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    best_out[(size_t)h * n_f + j] = best_slot != 0x7fffffff ? pack_best(best, best_slot) : 0ull;
+    if (bad) status_set(st, FASTAR_ERR_DEVICE_ARG);
+  }
+  pdl_trigger();
+}
+
 // ---------------------------------------------------------------- plan
 // The frame's matches and groups live in shared memory: s_key[n_f] holds
 // each key's matched slot (later its planned slot), and an open-addressing
@@ -272,7 +388,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
                                                             const int32_t* __restrict__ m,
                                                             int32_t* size, int64_t* inserted,
                                                             int64_t* evicted, float* __restrict__ invn, int ldn,
-                                                            int32_t* st) {
+                                                            int any_frame, int32_t* st) {
   pdl_wait();
   extern __shared__ int plan_smem[];
   const int ntab = 1 << lg_tab;
@@ -321,11 +437,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
   // 1. eviction: the E smallest (last_frame, slot) among slots with
   //    last_frame < f that no key of this frame joined
   if (E > 0) {
-    // eligible: lf < f, and not a slot matched now (only lf == f-1 can be)
+    // eligible: lf < f, and not a slot matched now (only lf == f-1 can be,
+    // unless the search covers every earlier frame)
     auto eligible = [&](int s) -> bool {
       const int l = lf[s];
       if (l >= f) return false;
-      if (l == f - 1 && plan_find(tab_slot, s, lg_tab) >= 0) return false;
+      if ((any_frame || l == f - 1) && plan_find(tab_slot, s, lg_tab) >= 0) return false;
       return true;
     };
     int lo = 0x7fffffff;
@@ -642,8 +759,19 @@ template <typename T, int D>
 static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_new,
                       const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                       int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready,
-                      int rep, const void* planes) {
+                      int rep, const void* planes, int search) {
   const int H = c->H, C = c->C, Tt = c->T;
+  // search over every earlier frame (LSH candidates): the cache CSR is
+  // rebuilt before each frame and a warp per key walks its buckets
+  const bool lsh = search == FASTAR_SEARCH_LSH;
+  // quantised search (TempCache-Quant): the previous frame's groups, ranked
+  // by approximate cosine to their b-bit codes, the best merged iff its
+  // exact cosine reaches tau
+  const bool quant = (search & 0xff) == FASTAR_SEARCH_QUANT;
+  const int qbits = search >> 8;
+  if ((lsh || quant) && rep != FASTAR_REP_LAST) return FASTAR_ERR_UNSUPPORTED;
+  if (quant && (!std::is_same<T, __nv_bfloat16>::value || D != 128 || qbits < 1 || qbits > 16))
+    return FASTAR_ERR_UNSUPPORTED;
   // mean-key groups: every frame's candidates are cache rows (their stored
   // means), staged like the first frame's; the apply re-hashes merged keys
   const bool mean_key = rep == FASTAR_REP_MEAN;
@@ -660,11 +788,20 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     return FASTAR_ERR_UNSUPPORTED;
   }
   const int Nrow = F * n_f;
-  fastar::launch_pdl((cand_init_kernel), H, kPlanThreads, 0, s, c->last_frame, c->size, C, first_frame - 1,
-                                              w.cand[0], w.ncand[0], w.best, n_f, st);
-  FASTAR_LAUNCHED(s, "cand_init");
   const dim3 wgrid((n_f + 7) / 8, H), wblock(256);
-  const bool tc_nn = std::is_same<T, __nv_bfloat16>::value && D == 128;
+  const bool tc_nn = !lsh && !quant && std::is_same<T, __nv_bfloat16>::value && D == 128;
+  if (lsh) {
+    // every frame's search reads its keys' codes
+    if (codes_ready && cudaStreamWaitEvent(s, codes_ready, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return FASTAR_ERR_CUDA;
+    }
+    codes_ready = nullptr;
+  } else {
+    fastar::launch_pdl((cand_init_kernel), H, kPlanThreads, 0, s, c->last_frame, c->size, C, first_frame - 1,
+                       w.cand[0], w.ncand[0], w.best, n_f, st);
+    FASTAR_LAUNCHED(s, "cand_init");
+  }
   if (tc_nn) {
     fastar::launch_pdl((cand_norm_kernel), dim3((n_f + 8 * kNormCands - 1) / (8 * kNormCands), H), wblock, 0, s, (const __nv_bfloat16*)c->K, C, w.cand[0], w.ncand[0], w.cinv,
                                               w.ldc, w.stage, n_f, st);
@@ -677,6 +814,18 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     const T* vf = (const T*)v_new + (size_t)fi * n_f * D;
     const uint32_t* cf = codes_new + (size_t)fi * n_f;
     int rc = FASTAR_ERR_UNSUPPORTED;
+    if (lsh) {
+      rc = launch_csr(c->codes, H * Tt, C, c->size, Tt, 1 << c->B, c->perm, c->offsets, st, s);
+      if (rc != FASTAR_OK) return rc;
+      fastar::launch_pdl((nn_lsh_kernel<T, D>), wgrid, wblock, 0, s, kf, n_f, Nrow, cf, (const T*)c->K,
+                         (const uint32_t*)c->codes, c->size, c->perm, c->offsets, C, Tt, 1 << c->B, w.best, st);
+      FASTAR_LAUNCHED(s, "nn_lsh");
+    }
+    if (quant) {
+      rc = launch_quant_nn((const void*)kf, Nrow, n_f, H, c->K, C, w.cand[cur],
+                           w.ncand[cur], qbits, w.qsmall, w.stage, w.cinv, w.ldc, w.best, st, s);
+      if (rc != FASTAR_OK) return rc;
+    }
     if (tc_nn && mean_key && fi > 0) {
       // the candidates the previous plan listed, with the keys its apply wrote
       fastar::launch_pdl((cand_norm_kernel), dim3((n_f + 8 * kNormCands - 1) / (8 * kNormCands), H), wblock, 0, s,
@@ -687,7 +836,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
       rc = launch_nn_tc(FASTAR_BF16, k_new, n_f, Nrow, H, fi, c->K, C, D, w.cand[cur], w.ncand[cur], w.cinv,
                         w.ldc, w.plan_slot, w.invn[(fi + 1) & 1], w.invn[fi & 1], w.ldn, w.best, w.stage,
                         tau, st, s, mean_key ? 1 : 0);
-    if (rc == FASTAR_ERR_UNSUPPORTED) {
+    if (rc == FASTAR_ERR_UNSUPPORTED && !lsh && !quant) {
       fastar::launch_pdl((nn_simt_kernel<T, D>), wgrid, wblock, 0, s, kf, n_f, Nrow, (const T*)c->K, C, w.cand[cur],
                                                     w.ncand[cur], w.best, st);
       FASTAR_LAUNCHED(s, "nn_simt");
@@ -697,7 +846,7 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
     fastar::launch_pdl((plan_kernel), H, kPlanThreads, plan_smem, s, n_f, C, f, tau, lg_tab, w.best, match_out,
                        fi * n_f, Nrow, w.match, w.cand[nxt], w.ncand[nxt], w.plan_slot, w.plan_kind, w.plan_cnt,
                        w.evict, c->last_frame, c->m, c->size, c->inserted, c->evicted,
-                       tc_nn ? w.invn[fi & 1] : nullptr, w.ldn, st);
+                       tc_nn ? w.invn[fi & 1] : nullptr, w.ldn, lsh ? 1 : 0, st);
     FASTAR_LAUNCHED(s, "plan");
     // the first kernel that reads codes_new (or v_new): wait for them here
     if (fi == 0 && codes_ready && cudaStreamWaitEvent(s, codes_ready, 0) != cudaSuccess) {
@@ -721,15 +870,15 @@ static int merge_impl(const fastar_cache* c, const void* k_new, const void* v_ne
 int launch_merge(const fastar_cache* c, const void* k_new, const void* v_new,
                  const uint32_t* codes_new, int F, int n_f, int32_t first_frame, float tau,
                  int32_t* match_out, void* ws, int32_t* st, cudaStream_t s, cudaEvent_t codes_ready,
-                 int rep, const void* planes) {
-  if (c->dt == FASTAR_F32 && c->D == 64)
-    return merge_impl<float, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
-  if (c->dt == FASTAR_F32 && c->D == 128)
-    return merge_impl<float, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
-  if (c->dt == FASTAR_BF16 && c->D == 64)
-    return merge_impl<__nv_bfloat16, 64>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
-  if (c->dt == FASTAR_BF16 && c->D == 128)
-    return merge_impl<__nv_bfloat16, 128>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, rep, planes);
+                 int rep, const void* planes, int search) {
+#define FASTAR_MERGE(T, D)                                                                                   \
+  return merge_impl<T, D>(c, k_new, v_new, codes_new, F, n_f, first_frame, tau, match_out, ws, st, s, codes_ready, \
+                          rep, planes, search)
+  if (c->dt == FASTAR_F32 && c->D == 64) FASTAR_MERGE(float, 64);
+  if (c->dt == FASTAR_F32 && c->D == 128) FASTAR_MERGE(float, 128);
+  if (c->dt == FASTAR_BF16 && c->D == 64) FASTAR_MERGE(__nv_bfloat16, 64);
+  if (c->dt == FASTAR_BF16 && c->D == 128) FASTAR_MERGE(__nv_bfloat16, 128);
+#undef FASTAR_MERGE
   return FASTAR_ERR_UNSUPPORTED;
 }
 

@@ -24,13 +24,18 @@ class ChunkPath:
     """Buffers and calls of one layer's per-chunk path."""
 
     def __init__(self, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last",
-                 share=None):
-        """share: another ChunkPath of the same shapes whose workspaces and
+                 share=None, search="prev"):
+        """rep: TempCache representative, "last" (the method) or "mean";
+        search: where a new key's group is looked for, "prev" (the previous
+        frame's groups, the method) or "lsh" (every earlier group sharing an
+        LSH bucket);
+        share: another ChunkPath of the same shapes whose workspaces and
         streams this one reuses (layers run one after the other on the same
         streams, so their scratch never overlaps in time); caches, codes,
         outputs and events stay per layer."""
         self.H, self.D, self.n_f, self.F, self.P = H, D, n_f, F, P
         self.rep = rep  # TempCache representative: "last" (the method) or "mean" (ablation)
+        self.search = search
         self.T, self.B, self.C, self.tau, self.dtype = T, B, C, tau, dtype
         self.Nq = F * n_f
         self.scale = D ** -0.5
@@ -101,7 +106,8 @@ class ChunkPath:
         fastar_hash(k, self.planes, self.T, self.B, codes, status=self.status, stream=stream)
         fastar_tempcache_merge(self.cache, k, v, codes, F, self.n_f, first_frame, self.tau,
                                match_out=match, ws=self.ws_merge, status=self.status,
-                               stream=stream, rep=self.rep, planes=self.planes)
+                               stream=stream, rep=self.rep, planes=self.planes,
+                               search=self.search)
         return codes, match
 
     def step(self, q, k, v, kp, vp, first_frame, stream=None):
@@ -330,7 +336,8 @@ class ChunkPath:
         self._cross_done.record(side)
         fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame,
                                self.tau, match_out=self.match, ws=self.ws_merge, status=st,
-                               stream=main, codes_ready=self._codes_ready, rep=self.rep, planes=self.planes)
+                               stream=main, codes_ready=self._codes_ready, rep=self.rep, planes=self.planes,
+                               search=self.search)
         main.wait_event(self._csr_done)
         fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache,
                                self.scale, self.o_sa, self.lse, ws=self.ws_annsa, status=st,
@@ -348,11 +355,12 @@ class ChunkStack:
     the calling stream, as the attention layers of a model run (a layer's
     second stream starts after the previous layer's work)."""
 
-    def __init__(self, layers, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last"):
+    def __init__(self, layers, H, D, n_f, F, P, T, B, C, tau, dtype=torch.bfloat16, device="cuda", rep="last",
+                 search="prev"):
         self.paths = []
         for _ in range(layers):
             self.paths.append(ChunkPath(H, D, n_f, F, P, T, B, C, tau, dtype, device, rep,
-                                        share=self.paths[0] if self.paths else None))
+                                        share=self.paths[0] if self.paths else None, search=search))
 
     def __len__(self):
         return len(self.paths)

@@ -344,8 +344,9 @@ def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int
     match_override: optional [H][F*n_f] matches to use instead of the
     oracle's own (to continue from another implementation's decisions).
     rep, planes, B: the representative mode (tempcache_apply_frame).
-    search: "prev" (the method: frame f-1's groups, tempcache_nn) or "lsh"
-    (every earlier group sharing a bucket, tempcache_nn_lsh).
+    search: "prev" (the method: frame f-1's groups, tempcache_nn), "lsh"
+    (every earlier group sharing a bucket, tempcache_nn_lsh) or "quant<b>"
+    (frame f-1's groups ranked by their b-bit codes, tempcache_nn_quant).
     Returns (new_state, match [H][F*n_f], listed [H][F*n_f]).
     """
     st = state.copy()
@@ -357,6 +358,8 @@ def tempcache_merge(state: CacheState, k_new, v_new, codes_new, F: int, n_f: int
         f = first_frame + fi
         if search == "lsh":
             mt, ls = tempcache_nn_lsh(st, np.asarray(k_new)[:, sl], np.asarray(codes_new)[:, :, sl], f, tau)
+        elif search.startswith("quant"):
+            mt, ls = tempcache_nn_quant_listed(st, np.asarray(k_new)[:, sl], f, tau, int(search[5:]))
         elif search == "prev":
             mt, ls = tempcache_nn(st, np.asarray(k_new)[:, sl], f, tau)
         else:

@@ -87,9 +87,10 @@ def _ulp_bf16(x):
 
 
 def check_merge(path, st_before: O.CacheState, k, v, gpu_codes, gpu_match, F, n_f, first_frame,
-                tau, dtype, rep: Report, what=""):
+                tau, dtype, rep: Report, what="", search="prev"):
     """Compare one merge call; returns the oracle state continued from the GPU."""
-    st_o, match_o, listed = O.tempcache_merge(st_before, k, v, gpu_codes, F, n_f, first_frame, tau)
+    st_o, match_o, listed = O.tempcache_merge(st_before, k, v, gpu_codes, F, n_f, first_frame, tau,
+                                              search=search)
     gm = host(gpu_match).astype(np.int64)
     bad = (gm != match_o) & ~listed
     assert not bad.any(), f"{what}: {int(bad.sum())} NN decisions differ (first at " \
@@ -98,7 +99,7 @@ def check_merge(path, st_before: O.CacheState, k, v, gpu_codes, gpu_match, F, n_
     rep.differing_listed_nn += int(((gm != match_o) & listed).sum())
     if ((gm != match_o) & listed).any():
         st_o, _, _ = O.tempcache_merge(st_before, k, v, gpu_codes, F, n_f, first_frame, tau,
-                                       match_override=gm)
+                                       match_override=gm, search=search)
     g = cache_to_oracle(path.cache, dtype)
     for name in ("size", "inserted", "evicted"):
         np.testing.assert_array_equal(getattr(g, name), getattr(st_o, name), err_msg=f"{what} {name}")

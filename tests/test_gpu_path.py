@@ -16,10 +16,10 @@ from workloads import CONFIGS, layer_data
 pytestmark = pytest.mark.gpu
 
 
-def _path(cfg):
+def _path(cfg, search="prev"):
     from merged_attention_autoregressive_gb300.path import ChunkPath
     return ChunkPath(cfg.H, cfg.D, cfg.n_f, cfg.F, cfg.P, cfg.T, cfg.B, cfg.C, cfg.tau,
-                     dtype={"bf16": torch.bfloat16, "f32": torch.float32}[cfg.dtype])
+                     dtype={"bf16": torch.bfloat16, "f32": torch.float32}[cfg.dtype], search=search)
 
 
 def build_cache(cfg, d, path, rep, check=True):
@@ -35,7 +35,7 @@ def build_cache(cfg, d, path, rep, check=True):
         if check:
             gc = check_codes(codes, k, d.planes, cfg.T, cfg.B, rep, f"past {f} key codes")
             st = check_merge(path, st, k, v, gc, match, nF, cfg.n_f, f, cfg.tau, cfg.dtype, rep,
-                             f"past frames {f}..{f + nF - 1}")
+                             f"past frames {f}..{f + nF - 1}", search=path.search)
             check_csr(path.cache.perm, path.cache.offsets, st.codes, 1 << cfg.B, st.size,
                       f"cache CSR after frame {f + nF - 1}")
         f += nF
@@ -56,7 +56,7 @@ def run_chunk(cfg, d, path, st, rep, chunk=0, rows=None):
     pc = check_codes(path.p_codes[:, :, :cfg.P], d.prompt_k, d.planes, cfg.T, cfg.B, rep,
                      "prompt codes")
     st = check_merge(path, st, k, v, kc, path.match, cfg.F, cfg.n_f, first, cfg.tau, cfg.dtype,
-                     rep, "chunk merge")
+                     rep, "chunk merge", search=path.search)
     check_csr(path.cache.perm, path.cache.offsets, st.codes, 1 << cfg.B, st.size, "cache CSR")
     idx, cnt = O.annca_prune(qc, pc, cfg.F, cfg.n_f)
     np.testing.assert_array_equal(host(path.kept_cnt), cnt)

@@ -975,3 +975,26 @@ def test_quant_tempcache_listing_hand_cases():
     c = 1.0 / math.sqrt(1.0 + 1e-4)
     match, listed = O.tempcache_nn_quant_listed(st, k, 1, c - 5e-5, 4)
     assert match[0].tolist() == [-1, 0] and listed[0].tolist() == [True, True]
+
+
+def test_tempcache_merge_quant_search_at_many_bits_equals_the_exact_search():
+    """At 20 bits the decoded candidates are the candidates to about 1e-6,
+    so the quantised search's merge makes the exact search's decisions
+    wherever neither is listed, and then the same cache."""
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(redraw=0.3)
+    d = layer_data(cfg)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    for f in range(cfg.past_frames):
+        c, _ = O.hash_codes(d.past_k[f], d.planes, cfg.T, cfg.B)
+        st, _, _ = O.tempcache_merge(st, d.past_k[f], d.past_v[f], c, 1, cfg.n_f, f, cfg.tau)
+    c, _ = O.hash_codes(d.chunk_k[0], d.planes, cfg.T, cfg.B)
+    a, ma, la = O.tempcache_merge(st, d.chunk_k[0], d.chunk_v[0], c, 1, cfg.n_f, cfg.past_frames, cfg.tau)
+    b, mb, lb = O.tempcache_merge(st, d.chunk_k[0], d.chunk_v[0], c, 1, cfg.n_f, cfg.past_frames, cfg.tau,
+                                  search="quant20")
+    ok = ~(la | lb)
+    np.testing.assert_array_equal(ma[ok], mb[ok])
+    assert (ma >= 0).sum() > 10
+    if (ma == mb).all():
+        np.testing.assert_array_equal(a.K, b.K)
+        np.testing.assert_array_equal(a.m, b.m)
