@@ -59,6 +59,9 @@ def parse(argv=None):
                          "default to the one-layer Wan-1.3B-like chunk)")
     ap.add_argument("--shard", default="heads", choices=["heads", "layers"],
                     help="multi-GPU split of the chunk: heads of every layer (default) or whole layers")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only this many of the workload's layers (a small case for profilers; the "
+                         "printed line then describes that many layers)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-rollout", action="store_true",
@@ -1370,17 +1373,39 @@ def run_denoise(args, cfg):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
-    def chunk(frac, ev=None):
+    def chunk(frac, ev=None, reuse=False, after=None):
         for s, (q, k, v) in enumerate(steps):
-            path.denoise_step(s, S, q, k, v, kp, vp, cfg.past_frames, dense_frac=frac)
+            path.denoise_step(s, S, q, k, v, kp, vp, cfg.past_frames, dense_frac=frac, reuse=reuse)
             if ev is not None:
                 ev[s + 1].record(stream)
+            if after is not None:
+                after(s)
+
+    heads = [0, 5]
+
+    def retained(s):
+        """Per step, on heads 0 and 5: the share of the dense softmax mass
+        (same logits) that the step's selection keeps, exp(lse - dense lse);
+        before the last step the dense set is the cache's groups (+ ln m)
+        and the step's own keys, at the last step the merged cache."""
+        q, k, _ = steps[s]
+        out = []
+        for h in heads:
+            n = int(path.cache.size[h])
+            logits = path.scale * q[h].float() @ path.cache.K[h, :n].float().T + torch.log(
+                path.cache.m[h, :n].float())[None, :]
+            if s + 1 < S:
+                logits = torch.cat([logits, path.scale * q[h].float() @ k[h].float().T], dim=1)
+            out.append(float(torch.exp(path.lse[h] - torch.logsumexp(logits, dim=1)).mean()))
+        return float(np.mean(out))
 
     out = {}
-    for name, frac in (("schedule_0.3", 0.3), ("all_dense", 1.01), ("all_sparse", 0.0)):
+    for name, frac, reuse in (("schedule_0.3", 0.3, False), ("schedule_0.3_reuse_codes", 0.3, True),
+                              ("all_dense", 1.01, False), ("all_sparse", 0.0, False),
+                              ("all_sparse_reuse_codes", 0.0, True)):
         for _ in range(3):
             path.cache.restore(snap)
-            chunk(frac)
+            chunk(frac, reuse=reuse)
         reps = max(3, min(args.steps, 20))
         per_chunk, per_step = [], []
         for _ in range(reps):
@@ -1388,19 +1413,25 @@ def run_denoise(args, cfg):
             flush.fill_(1)
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(S + 1)]
             ev[0].record(stream)
-            chunk(frac, ev)
+            chunk(frac, ev, reuse=reuse)
             torch.cuda.synchronize()
             per_chunk.append(ev[0].elapsed_time(ev[S]))
             per_step.append([ev[s].elapsed_time(ev[s + 1]) for s in range(S)])
         assert int(path.status.item()) == 0, fa.STATUS.get(int(path.status.item()))
+        ret = []
+        path.cache.restore(snap)
+        chunk(frac, reuse=reuse, after=lambda s_: ret.append(retained(s_)))
         out[name] = {"ms_per_chunk": float(np.median(per_chunk)),
                      "ms_per_step": np.median(np.array(per_step), axis=0).round(4).tolist(),
-                     "dense_steps": [s < frac * S for s in range(S)]}
+                     "dense_steps": [s < frac * S for s in range(S)],
+                     "retained_share_per_step_heads_0_5": [round(x, 5) for x in ret]}
     line = {"metric": "per-chunk FAST-AR attention ms over the denoising steps of a chunk", "unit": "ms/chunk",
             "value": out["schedule_0.3"]["ms_per_chunk"], "higher_is_better": False, "data": "synthetic",
             "config": {"workload": cfg.name, "H": cfg.H, "Nq": cfg.Nq, "P": cfg.P, "T": cfg.T, "B": cfg.B,
                        "past_frames": cfg.past_frames, "denoise_steps": S,
-                       "l2": "flushed before every chunk (256 MiB write)"},
+                       "l2": "flushed before every chunk (256 MiB write)",
+                       "reuse_codes": "codes, query CSR and kept lists of the first sparse step reused by the "
+                                      "later sparse steps (the last step re-hashes its keys for the merge)"},
             "schedules": out}
     print(json.dumps(line), flush=True)
 
@@ -1410,6 +1441,8 @@ def main():
     if args.config is None:
         args.config = 1 if (args.denoise or args.recall or args.quant) else 4
     cfg = CONFIGS[args.config]
+    if args.layers:
+        cfg = cfg.replace(layers=min(args.layers, cfg.layers))
     if args.impl == "reference":
         run_reference(args, cfg)
     elif args.quant:

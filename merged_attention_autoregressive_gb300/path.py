@@ -184,7 +184,7 @@ class ChunkPath:
         self._main(stream).wait_event(self._out_done)
 
     # -- denoising steps -----------------------------------------------------
-    def denoise_step(self, s, S, q, k, v, kp, vp, first_frame, dense_frac=DENSE_FRAC):
+    def denoise_step(self, s, S, q, k, v, kp, vp, first_frame, dense_frac=DENSE_FRAC, reuse=False):
         """Step s of the S denoising steps of a chunk (FAST-AR analysis,
         paper.rainbus.top: sparse attention is off for the first 30 % of the
         steps; each chunk is denoised conditioned on the history).
@@ -196,12 +196,29 @@ class ChunkPath:
         fastar_annsa_combine; dense steps give both key sets one table of one
         bit with every code 0, and keep every prompt token.  The last step
         merges its keys into the cache and attends the merged cache, as
-        `step` does (dense per the schedule).  Outputs: o_sa, lse, o_ca."""
+        `step` does (dense per the schedule).  Outputs: o_sa, lse, o_ca.
+
+        reuse: the codes (queries, the step's keys, the prompt), the query
+        CSR and the kept prompt lists are computed at the chunk's first
+        sparse step only and reused by its later sparse steps; the last step
+        still hashes its keys, whose codes the merge stores with them."""
         dense = s < dense_frac * S
+        first_sparse = not dense and (s == 0 or (s - 1) < dense_frac * S)
+        reuse_now = reuse and not dense and not first_sparse
         dn = self._denoise_views()
         st = self.status
         if s + 1 == S and not dense:
-            self.step(q, k, v, kp, vp, first_frame)
+            if not reuse_now:
+                self.step(q, k, v, kp, vp, first_frame)
+                return
+            fastar_hash(k, self.planes, self.T, self.B, self.k_codes, status=st)
+            fastar_tempcache_merge(self.cache, k, v, self.k_codes, self.F, self.n_f, first_frame, self.tau,
+                                   match_out=self.match, ws=self.ws_merge, status=st, rep=self.rep,
+                                   planes=self.planes, search=self.search)
+            fastar_annsa_attention(q, self.q_codes, self.q_perm, self.q_offsets, self.cache, self.scale, self.o_sa,
+                                   self.lse, ws=self.ws_annsa, status=st)
+            fastar_annca_attention(q, kp, vp, self.kept_idx, self.kept_cnt, self.F, self.n_f, self.scale,
+                                   self.o_ca, ws=self.ws_annca, status=st)
             return
         if s + 1 == S:
             fastar_hash(k, self.planes, self.T, self.B, self.k_codes, status=st)
@@ -222,7 +239,8 @@ class ChunkPath:
             jobs = [(q, self.q_codes, self.q_perm, self.q_offsets), (k, self.k_codes, dn.k_perm, dn.k_off)]
             if self.P:
                 jobs.append((kp, self.p_codes, None, None))
-            fastar_hash_many(jobs, self.planes, T, self.B, status=st)
+            if not reuse_now:
+                fastar_hash_many(jobs, self.planes, T, self.B, status=st)
             chunk = self._chunk_view(k, v, dense=False)
             fastar_annsa_attention_part(q, self.q_codes, self.q_perm, self.q_offsets, self.cache, self.scale, 0,
                                         2 * T, dn.ws, status=st)
@@ -231,6 +249,8 @@ class ChunkPath:
             fastar_annsa_combine(2 * T, dn.ws, self.o_sa, self.lse, status=st)
         if dense:
             kept, cnt = dn.kept_all, dn.cnt_all
+        elif reuse_now:
+            kept, cnt = self.kept_idx, self.kept_cnt
         else:
             fastar_annca_prune(self.q_codes, self.p_codes[:, :, :self.P], self.F, self.n_f, self.B,
                                self.kept_idx, self.kept_cnt, status=st)

@@ -536,24 +536,37 @@ def denoise_step_attention(q, q_codes, state: CacheState, k, v, k_codes, dense: 
 
 
 def denoise_chunk(state: CacheState, steps, k_p, v_p, planes, T: int, B: int, F: int, n_f: int,
-                  first_frame: int, tau: float, scale: float, dense_frac: float = DENSE_FRAC):
+                  first_frame: int, tau: float, scale: float, dense_frac: float = DENSE_FRAC,
+                  reuse: bool = False):
     """The S denoising steps of one chunk.  steps: list of (q, k, v), each
     [H][F*n_f][D].  Returns (outs, final_state, match) where outs[s] =
-    (o_sa, lse_sa, o_ca) and match is the final merge's."""
+    (o_sa, lse_sa, o_ca) and match is the final merge's.
+    reuse: the codes of the queries and of the step's keys and the kept
+    prompt lists of the chunk's first sparse step serve its later sparse
+    steps too (the codes are computed once per chunk); the last step's keys
+    are still hashed for the merge, which stores their codes."""
     dense = denoise_schedule(len(steps), dense_frac)
     pc, _ = hash_codes(k_p, planes, T, B)
     H, P = np.asarray(k_p).shape[:2]
     st = state
     outs = []
     match = None
+    kept = None   # (qc, kc, idx, cnt) of the first sparse step, with reuse
     for s, (q, k, v) in enumerate(steps):
-        qc, _ = hash_codes(q, planes, T, B)
-        kc, _ = hash_codes(k, planes, T, B)
-        if dense[s]:
-            idx = np.tile(np.arange(P), (H, F, 1))
-            cnt = np.full((H, F), P)
+        if reuse and not dense[s] and kept is not None:
+            qc, kc, idx, cnt = kept
+            if s + 1 == len(steps):
+                kc, _ = hash_codes(k, planes, T, B)
         else:
-            idx, cnt = annca_prune(qc, pc, F, n_f)
+            qc, _ = hash_codes(q, planes, T, B)
+            kc, _ = hash_codes(k, planes, T, B)
+            if dense[s]:
+                idx = np.tile(np.arange(P), (H, F, 1))
+                cnt = np.full((H, F), P)
+            else:
+                idx, cnt = annca_prune(qc, pc, F, n_f)
+                if reuse:
+                    kept = (qc, kc, idx, cnt)
         o_ca = annca_attention(q, k_p, v_p, idx, cnt, F, n_f, scale)
         if s + 1 < len(steps):
             o_sa, lse = denoise_step_attention(q, qc, st, k, v, kc, dense[s], scale)

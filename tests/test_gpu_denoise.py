@@ -31,7 +31,7 @@ def _setup(cfg):
     return d, path
 
 
-def _run(cfg, S):
+def _run(cfg, S, reuse=False):
     d, path = _setup(cfg)
     rep = Report()
     kp, vp = dev(d.prompt_k, cfg.dtype), dev(d.prompt_v, cfg.dtype)
@@ -39,15 +39,23 @@ def _run(cfg, S):
     dense = O.denoise_schedule(S)
     first = cfg.past_frames
     pc, _ = O.hash_codes(d.prompt_k, d.planes, cfg.T, cfg.B)
+    kept = None  # with reuse: the GPU's codes and kept lists of the first sparse step
     for s, (q, k, v) in enumerate(steps):
         st = cache_to_oracle(path.cache, cfg.dtype)
-        path.denoise_step(s, S, dev(q, cfg.dtype), dev(k, cfg.dtype), dev(v, cfg.dtype), kp, vp, first)
+        path.denoise_step(s, S, dev(q, cfg.dtype), dev(k, cfg.dtype), dev(v, cfg.dtype), kp, vp, first,
+                          reuse=reuse)
         torch.cuda.synchronize()
         assert int(path.status.item()) == 0
         if dense[s]:
             idx = np.tile(np.arange(cfg.P), (cfg.H, cfg.F, 1))
             cnt = np.full((cfg.H, cfg.F), cfg.P)
             qc = None
+        elif kept is not None:
+            # reused: the first sparse step's codes and kept lists, untouched
+            qc, kc_first, idx, cnt = kept
+            np.testing.assert_array_equal(host(path.q_codes).astype(np.uint32), qc)
+            np.testing.assert_array_equal(host(path.kept_cnt), cnt)
+            np.testing.assert_array_equal(host(path.kept_idx), idx)
         else:
             qc = check_codes(path.q_codes, q, d.planes, cfg.T, cfg.B, rep, f"step {s} query codes")
             gpc = host(path.p_codes[:, :, :cfg.P]).astype(np.uint32)
@@ -55,13 +63,21 @@ def _run(cfg, S):
             idx, cnt = O.annca_prune(qc, gpc, cfg.F, cfg.n_f)
             np.testing.assert_array_equal(host(path.kept_cnt), cnt)
             np.testing.assert_array_equal(host(path.kept_idx), idx)
+            if reuse:
+                kept = (qc, host(path.k_codes).astype(np.uint32), idx, cnt)
         o_ca = O.annca_attention(q, d.prompt_k, d.prompt_v, idx, cnt, cfg.F, cfg.n_f, cfg.scale)
         check_att(path.o_ca, o_ca, f"step {s} cross", rep)
         if s + 1 < S:
             g = cache_to_oracle(path.cache, cfg.dtype)
             for name in ("K", "V", "m", "codes", "size"):
                 np.testing.assert_array_equal(getattr(g, name), getattr(st, name), err_msg=f"step {s} wrote {name}")
-            kc = None if dense[s] else check_codes(path.k_codes, k, d.planes, cfg.T, cfg.B, rep, f"step {s} key codes")
+            if dense[s]:
+                kc = None
+            elif reuse and s > _first_sparse(dense):
+                kc = kept[1]  # the first sparse step's key codes, still in place
+                np.testing.assert_array_equal(host(path.k_codes).astype(np.uint32), kc)
+            else:
+                kc = check_codes(path.k_codes, k, d.planes, cfg.T, cfg.B, rep, f"step {s} key codes")
             o_sa, lse = O.denoise_step_attention(q, qc, st, k, v, kc, dense[s], cfg.scale)
         else:
             kc = check_codes(path.k_codes, k, d.planes, cfg.T, cfg.B, rep, "last step key codes")
@@ -81,6 +97,10 @@ def _run(cfg, S):
     return rep
 
 
+def _first_sparse(dense):
+    return dense.index(False) if False in dense else -1
+
+
 def test_denoise_four_steps():
     """Steps 0 and 1 dense, step 2 sparse (cache + own keys), step 3 the
     merging chunk step (sparse): 2 heads, 300 tokens, 6 past frames."""
@@ -93,3 +113,12 @@ def test_denoise_single_dense_step_two_frames():
     merged cache; two frames per chunk (per-frame cross-attention)."""
     cfg = CONFIGS[1].replace(H=2, n_f=200, F=2, past_frames=4, C=2048, P=48, redraw=0.3)
     _run(cfg, 1)
+
+
+def test_denoise_reuse_codes_six_steps():
+    """Codes computed once per chunk: steps 0 and 1 dense, steps 2 to 4
+    sparse with the codes, query CSR and kept lists of step 2, step 5 the
+    merging step (its keys hashed again, its queries' codes and kept lists
+    still step 2's)."""
+    cfg = CONFIGS[1].replace(H=2, n_f=300, F=1, past_frames=6, C=2048, P=64, redraw=0.3)
+    _run(cfg, 6, reuse=True)

@@ -998,3 +998,39 @@ def test_tempcache_merge_quant_search_at_many_bits_equals_the_exact_search():
     if (ma == mb).all():
         np.testing.assert_array_equal(a.K, b.K)
         np.testing.assert_array_equal(a.m, b.m)
+
+
+def test_denoise_reuse_is_identity_when_the_steps_agree_and_reuses_otherwise():
+    """With every step given the same inputs, reusing the first sparse
+    step's codes and kept lists changes nothing (bit for bit); with the
+    usual noisy steps the first sparse step is unchanged and a later sparse
+    step attends with the first one's selection (checked against the plain
+    step function given those codes)."""
+    from workloads import CONFIGS, denoise_steps, layer_data
+    cfg = CONFIGS[0].replace(F=1, n_f=64, past_frames=2, P=16, T=2, B=3)
+    d = layer_data(cfg, chunks=1)
+    st = O.CacheState.empty(cfg.H, cfg.C, cfg.D, cfg.T, cfg.dtype)
+    for f in range(cfg.past_frames):
+        c, _ = O.hash_codes(d.past_k[f], d.planes, cfg.T, cfg.B)
+        st, _, _ = O.tempcache_merge(st, d.past_k[f], d.past_v[f], c, 1, cfg.n_f, f, cfg.tau)
+    same = [(d.chunk_q[0], d.chunk_k[0], d.chunk_v[0])] * 5
+    args = (d.prompt_k, d.prompt_v, d.planes, cfg.T, cfg.B, cfg.F, cfg.n_f, cfg.past_frames, cfg.tau, cfg.scale)
+    a, sa, _ = O.denoise_chunk(st, same, *args)
+    b, sb, _ = O.denoise_chunk(st, same, *args, reuse=True)
+    for x, y in zip(a, b):
+        for u, w in zip(x, y):
+            np.testing.assert_array_equal(u, w)
+    steps = denoise_steps(cfg, d, 5)
+    a, _, _ = O.denoise_chunk(st, steps, *args)
+    b, _, _ = O.denoise_chunk(st, steps, *args, reuse=True)
+    dense = O.denoise_schedule(5)
+    first = dense.index(False)
+    np.testing.assert_array_equal(a[first][0], b[first][0])
+    s = first + 1
+    q, k, v = steps[s]
+    q1, k1, _ = steps[first]
+    qc, _ = O.hash_codes(q1, d.planes, cfg.T, cfg.B)
+    kc, _ = O.hash_codes(k1, d.planes, cfg.T, cfg.B)
+    o, lse = O.denoise_step_attention(q, qc, st, k, v, kc, False, cfg.scale)
+    np.testing.assert_array_equal(b[s][0], o)
+    assert not np.array_equal(a[s][0], b[s][0])
