@@ -39,6 +39,7 @@
 // normalised output and the log-sum-exp; with more, each table writes an
 // unnormalised partial (o, running max, sum) and a combine kernel merges the
 // T partials of each query.
+#include <cuda_fp16.h>
 #include <limits.h>
 #include <math.h>
 
@@ -92,7 +93,7 @@ struct SaArgs {
   const int32_t* perm;
   const int32_t* offsets;
   int C, T, nb;
-  float* ws_o;   // [T][H][Nq][D] per-table unnormalised partials (T >= 2)
+  __half* ws_o;  // [T][H][Nq][D] per-table partials, normalised by their own sums (fp16)
   float2* ws_ml; // [T][H][Nq] their (max in log2 units, sum)
   __nv_bfloat16* out;
   float* lse;
@@ -698,12 +699,21 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
             *reinterpret_cast<uint2*>(sa.out + ((size_t)h * Nq + row) * kD + lane * 4) = u;
           }
         } else {
-          // this table's partial; the combine kernel merges the tables
+          // this table's partial, normalised by its own sum and stored in
+          // fp16 (a convex combination of value rows, so well inside fp16's
+          // range); the combine kernel weighs the tables by their sums
+          const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
           for (int rr = 0; rr < 32; ++rr) {
             const int row = __shfl_sync(0xffffffffu, my_row, rr);
+            const float iv = __shfl_sync(0xffffffffu, inv, rr);
             if (row < 0) continue;
             const float4 x = *reinterpret_cast<const float4*>(wbase + rr * 512 + ((lane + rr) & 31) * 16);
-            *reinterpret_cast<float4*>(sa.ws_o + (((size_t)(sa.slot0 + kT) * H + h) * Nq + row) * kD + lane * 4) = x;
+            const __half2 h0 = __floats2half2_rn(x.x * iv, x.y * iv);
+            const __half2 h1 = __floats2half2_rn(x.z * iv, x.w * iv);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t*>(&h0);
+            u.y = *reinterpret_cast<const uint32_t*>(&h1);
+            *reinterpret_cast<uint2*>(sa.ws_o + (((size_t)(sa.slot0 + kT) * H + h) * Nq + row) * kD + lane * 4) = u;
           }
           if (my_row >= 0)
             sa.ws_ml[((size_t)(sa.slot0 + kT) * H + h) * Nq + my_row] = make_float2(l_run > 0.f ? m_run : -INFINITY, l_run);
@@ -763,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 // Two queries per warp at four CTAs per SM (fewer registers, more warps in
 // flight) measured 2 us faster than four queries per warp at two.
 constexpr int kCombineQ = 2;
-__global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const float* __restrict__ ws_o,
+__global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const __half* __restrict__ ws_o,
                                                             const float2* __restrict__ ws_ml, int T, int H,
                                                             int Nq, __nv_bfloat16* __restrict__ out,
                                                             float* __restrict__ lse, int32_t* st) {
@@ -773,17 +783,17 @@ __global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const float* __re
   const int i0 = (blockIdx.x * 8 + (threadIdx.x >> 5)) * kCombineQ;
   const int lane = threadIdx.x & 31;
   float2 ml[kCombineQ][kMaxT];
-  float4 o[kCombineQ][kMaxT];
+  uint2 o[kCombineQ][kMaxT];
 #pragma unroll
   for (int k = 0; k < kCombineQ; ++k) {
 #pragma unroll
     for (int t = 0; t < kMaxT; ++t) {
       ml[k][t] = make_float2(-INFINITY, 0.f);
-      o[k][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      o[k][t] = make_uint2(0u, 0u);
       if (t < T && i0 + k < Nq) {
         const size_t r = ((size_t)t * H + h) * Nq + i0 + k;
         ml[k][t] = __ldcs(ws_ml + r);
-        o[k][t] = __ldcs(reinterpret_cast<const float4*>(ws_o + r * kD) + lane);
+        o[k][t] = __ldcs(reinterpret_cast<const uint2*>(ws_o + r * kD) + lane);
       }
     }
   }
@@ -798,12 +808,15 @@ __global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const float* __re
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int t = 0; t < kMaxT; ++t) {
-      const float w = ml[k][t].x == -INFINITY ? 0.f : exp2f(ml[k][t].x - M);
-      L = fmaf(ml[k][t].y, w, L);
-      acc.x = fmaf(o[k][t].x, w, acc.x);
-      acc.y = fmaf(o[k][t].y, w, acc.y);
-      acc.z = fmaf(o[k][t].z, w, acc.z);
-      acc.w = fmaf(o[k][t].w, w, acc.w);
+      // weight of table t's normalised partial: its sum on the common scale
+      const float w = ml[k][t].x == -INFINITY ? 0.f : exp2f(ml[k][t].x - M) * ml[k][t].y;
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&o[k][t].x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&o[k][t].y));
+      L += w;
+      acc.x = fmaf(a.x, w, acc.x);
+      acc.y = fmaf(a.y, w, acc.y);
+      acc.z = fmaf(b.x, w, acc.z);
+      acc.w = fmaf(b.y, w, acc.w);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const __nv_bfloat162 b0 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
@@ -838,7 +851,7 @@ int p64_of(int P) { return (P + kN - 1) / kN * kN; }
 size_t annsa_tc_ws_bytes(int H, int Nq, int D, int T) {
   if (D != kD || T > kMaxT) return 0;
   if (T == 1) return 0;  // a single table writes the output directly
-  const size_t o = (size_t)T * H * Nq * kD * sizeof(float);
+  const size_t o = (size_t)T * H * Nq * kD * sizeof(__half);
   const size_t ml = (size_t)T * H * Nq * sizeof(float2);
   return ((o + 255) & ~(size_t)255) + ((ml + 255) & ~(size_t)255);
 }
@@ -889,10 +902,10 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
   if (dt != FASTAR_BF16 || c->D != kD || c->T > kMaxT) return FASTAR_ERR_UNSUPPORTED;
   if (Nq == 0 || c->H == 0) return FASTAR_OK;
   if (c->T > 1 && !ws) return FASTAR_ERR_WORKSPACE;
-  const size_t o_bytes = ((size_t)c->T * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
+  const size_t o_bytes = ((size_t)c->T * c->H * Nq * kD * sizeof(__half) + 255) & ~(size_t)255;
   SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
-            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0, nullptr, 0};
+            1 << c->B, (__half*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0, nullptr, 0};
   CaArgs ca{};
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
@@ -926,7 +939,7 @@ int launch_annsa_masked(fastar_dtype dt, const void* q, const uint32_t* q_codes,
 
 size_t annsa_parts_ws_bytes(int H, int Nq, int D, int parts) {
   if (D != kD || parts < 1 || parts > kMaxT) return 0;
-  const size_t o = (size_t)parts * H * Nq * kD * sizeof(float);
+  const size_t o = (size_t)parts * H * Nq * kD * sizeof(__half);
   const size_t ml = (size_t)parts * H * Nq * sizeof(float2);
   return ((o + 255) & ~(size_t)255) + ((ml + 255) & ~(size_t)255);
 }
@@ -938,10 +951,10 @@ int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_
                        cudaStream_t s) {
   if (c->dt != FASTAR_BF16 || c->D != kD) return FASTAR_ERR_UNSUPPORTED;
   if (Nq == 0 || c->H == 0) return FASTAR_OK;
-  const size_t o_bytes = ((size_t)parts * c->H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
+  const size_t o_bytes = ((size_t)parts * c->H * Nq * kD * sizeof(__half) + 255) & ~(size_t)255;
   SaArgs sa{(const __nv_bfloat16*)q, q_codes, q_perm, (const __nv_bfloat16*)c->K,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
-            1 << c->B, (float*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1, nullptr, 0};
+            1 << c->B, (__half*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1, nullptr, 0};
   CaArgs ca{};
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
@@ -952,9 +965,9 @@ int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_
 int launch_annsa_combine(int H, int Nq, int parts, const void* ws, void* out, float* lse, int32_t* st,
                          cudaStream_t s) {
   if (Nq == 0 || H == 0) return FASTAR_OK;
-  const size_t o_bytes = ((size_t)parts * H * Nq * kD * sizeof(float) + 255) & ~(size_t)255;
+  const size_t o_bytes = ((size_t)parts * H * Nq * kD * sizeof(__half) + 255) & ~(size_t)255;
   fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), H), 256, 0, s,
-                     (const float*)ws, (const float2*)((const char*)ws + o_bytes), parts, H, Nq,
+                     (const __half*)ws, (const float2*)((const char*)ws + o_bytes), parts, H, Nq,
                      (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");
   return FASTAR_OK;

@@ -399,15 +399,19 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
         if (c < s.nc) {
           float cs[32];
           tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + b * kN + half * 32, cs);
-          // cs = dot * inverse candidate norm, in place (NaN: not a group)
+          // cs = dot * inverse candidate norm, in place (NaN: not a group),
+          // two products per instruction (each rounded as on its own)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) cs[i] *= mi[i];
+          for (int i = 0; i < 32; i += 2) tc::mul2(cs[i], cs[i + 1], mi[i], mi[i + 1]);
           // phase 1: the tile's largest cosine (NaN columns are ignored);
-          // four independent chains keep the dependency depth short
+          // three-input maxima in four independent chains
           float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int i = 0; i < 32; ++i) t4[i & 3] = fmaxf(t4[i & 3], cs[i]);
-          const float tmax = fmaxf(fmaxf(t4[0], t4[1]), fmaxf(t4[2], t4[3]));
+          for (int i = 0; i < 32; i += 8) {
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) t4[c4] = tc::max3(t4[c4], cs[i + c4], cs[i + 4 + c4]);
+          }
+          const float tmax = tc::max3(t4[0], t4[1], fmaxf(t4[2], t4[3]));
           // phase 2 (only when it can change the answer): the columns
           // attaining it as a bit mask; several equal columns take the
           // lowest slot

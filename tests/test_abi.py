@@ -157,7 +157,7 @@ def test_annsa_parts_workspace_grows_with_slots(L):
     from merged_attention_autoregressive_gb300 import OP_ANNSA, OP_ANNSA_PARTS
     w1 = L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 1, 8, 32768)
     w4 = L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 4, 8, 32768)
-    assert w1 >= 12 * 4680 * (128 * 4 + 8) and w4 >= 4 * 12 * 4680 * (128 * 4 + 8)
+    assert w1 >= 12 * 4680 * (128 * 2 + 8) and w4 >= 4 * 12 * 4680 * (128 * 2 + 8)
     # two slots hold what the two-table call keeps; a single table keeps nothing
     assert L.fastar_workspace_size(OP_ANNSA_PARTS, 12, 4680, 128, 2, 8, 32768) == \
         L.fastar_workspace_size(OP_ANNSA, 12, 4680, 128, 2, 8, 32768)
