@@ -355,8 +355,8 @@ int fastar_tempcache_merge_search(const fastar_cache* cache, const void* k_new,
  * library's device memory, held by every GPU that loads the library until
  * the process exits.  Returns FASTAR_ERR_WORKSPACE when the merge needs more
  * (fastar_workspace_size(FASTAR_OP_MERGE, ...) > FASTAR_NOALLOC_SCRATCH_BYTES;
- * e.g. 12 heads x C 32768 x n_f 1560 needs about 9.7 MiB and fits, 40 heads
- * x n_f 3600 needs about 55 MiB and is refused).  All calls
+ * e.g. 12 heads x C 32768 x n_f 1560 needs about 10 MiB and fits, 40 heads
+ * x n_f 3600 needs about 56 MiB and is refused).  All calls
  * share the array, so calls that overlap on the GPU race and must be ordered
  * by the caller; it keeps the last call's contents (the merge needs none of
  * it zeroed).  The first call on a device looks up the array's address with

@@ -35,7 +35,7 @@ def _noalloc(L):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    """40 heads x C 32768 x n_f 3600 needs about 55 MiB of scratch: refused, nothing launched."""
+    """40 heads x C 32768 x n_f 3600 needs about 56 MiB of scratch: refused, nothing launched."""
     import merged_attention_autoregressive_gb300 as fa
     from merged_attention_autoregressive_gb300 import build
     build.build()
