@@ -52,7 +52,7 @@ namespace fastar {
 
 namespace {
 
-constexpr int kM = 128, kN = 64, kD = 128, kStages = 4, kAcc = 4;
+constexpr int kM = 128, kN = 128, kD = 128, kStages = 2, kAcc = 2;
 constexpr int kThreads = 320;   // 10 warps
 constexpr int kTmemCols = kAcc * kN;
 
@@ -375,36 +375,43 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
       int best_slot = 0x7fffffff, best_c = -1;
       for (int t = 0; t < s.tiles; ++t, ++g) {
         const int b = g % kAcc;
-        const int c = (s.ct0 + t) * kN + half * 32;  // this warp's first column
-        // the candidates' inverse norms are loaded before the wait, so that
-        // their latency overlaps it (NaN past the last candidate)
+        const int c0 = (s.ct0 + t) * kN + half * (kN / 2);  // this warp's first column
+        // the first pass's candidate inverse norms are loaded before the
+        // wait, so that their latency overlaps it (NaN past the last one)
         float mi[32];
-        if (c + 32 <= s.nc) {
-          const float4* m4 = reinterpret_cast<const float4*>(mrow + c);  // 16-byte aligned: ld % 4 == 0
+        auto load_mi = [&](int c) {
+          if (c + 32 <= s.nc) {
+            const float4* m4 = reinterpret_cast<const float4*>(mrow + c);  // 16-byte aligned: ld % 4 == 0
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float4 ib = __ldg(m4 + i);
-            mi[4 * i] = ib.x;
-            mi[4 * i + 1] = ib.y;
-            mi[4 * i + 2] = ib.z;
-            mi[4 * i + 3] = ib.w;
+            for (int i = 0; i < 8; ++i) {
+              const float4 ib = __ldg(m4 + i);
+              mi[4 * i] = ib.x;
+              mi[4 * i + 1] = ib.y;
+              mi[4 * i + 2] = ib.z;
+              mi[4 * i + 3] = ib.w;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mi[i] = c + i < s.nc ? __ldg(mrow + c + i) : __int_as_float(0x7fc00000);
           }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mi[i] = c + i < s.nc ? __ldg(mrow + c + i) : __int_as_float(0x7fc00000);
-        }
+        };
+        load_mi(c0);
         if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.tfull[b], (uint32_t)(g / kAcc) & 1u));
         if (!ok) continue;
         tc::tc_fence_after();
-        if (c < s.nc) {
+#pragma unroll 1
+        for (int part = 0; part < kN / 64; ++part) {
+          const int c = c0 + part * 32;
+          if (c >= s.nc) break;
+          if (part > 0) load_mi(c);
           float cs[32];
-          tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + b * kN + half * 32, cs);
+          tc::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + b * kN + half * (kN / 2) + part * 32, cs);
           // cs = dot * inverse candidate norm, in place (NaN: not a group),
           // two products per instruction (each rounded as on its own)
 #pragma unroll
           for (int i = 0; i < 32; i += 2) tc::mul2(cs[i], cs[i + 1], mi[i], mi[i + 1]);
-          // phase 1: the tile's largest cosine (NaN columns are ignored);
-          // three-input maxima in four independent chains
+          // phase 1: the largest cosine of the 32 columns (NaN columns are
+          // ignored); three-input maxima in four independent chains
           float t4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
