@@ -4,8 +4,10 @@
 // at a time through a warp-specialised pipeline:
 //   warp 0     producer: AnnCA's queries (one TMA box pair), then the key
 //              rows and, separately, the value rows and mask metadata of
-//              every tile (cp.async gathers into the 128-byte swizzled
-//              layout, 2-stage rings), each as soon as its stage is free: a
+//              every tile (AnnCA: TMA tile loads of the compacted rows;
+//              AnnSA: TMA tile::gather4 loads, four slot rows each, into the
+//              128-byte swizzled layout; 2-stage rings), each as soon as its
+//              stage is free: a
 //              key stage once its QK product is done, a value stage once its
 //              PV product is; row sources and metadata are fetched ahead;
 //   warp 1     MMA issuer: S_j = Q K_j^T (M 128, N 64, K 128) into one of two
@@ -197,10 +199,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   if (tid == 0) {
     tc::mbar_init(&sm.bar_q, kSA ? 128 : 1);  // AnnSA: every softmax thread gathers its query row
     for (int s = 0; s < kStages; ++s) {
-      // AnnCA: one arrival with the TMA bytes; AnnSA: 32 cp.async lanes (+
-      // the metadata arrive for the values)
-      tc::mbar_init(&sm.kfull[s], kSA ? 32 : 1);
-      tc::mbar_init(&sm.vfull[s], kSA ? 32 + 1 : 1);
+      // one arrival with the TMA bytes (AnnSA: after the tile's metadata)
+      tc::mbar_init(&sm.kfull[s], 1);
+      tc::mbar_init(&sm.vfull[s], 1);
       tc::mbar_init(&sm.kempty[s], 1);     // QK commit
       tc::mbar_init(&sm.vempty[s], 1);     // PV commit (also: O holds this tile's product)
     }
@@ -265,6 +266,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     }
   }
   const int ntiles = (nkeys + kN - 1) / kN;
+  int issued_k = 0, issued_v = 0;  // producer: key / value tiles whose loads were issued
 
   if (warp == 0) {
     // ================================================= producer
@@ -316,25 +318,38 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         }
       }
     };
-    const __nv_bfloat16* kb = kSA ? sa.K : ca.k_p;
-    const __nv_bfloat16* vb = kSA ? sa.V : ca.v_p;
     const size_t rows_per_head = kSA ? (size_t)sa.C : (size_t)ca.P;
     // Key and value gathers advance independently: the key rows of tile j go
     // into key stage j % kStages once QK_{j-2} has freed it, the value rows
     // and metadata into value stage j % kStages once PV_{j-2} has.  Each side
     // keeps its own row sources, fetched one tile ahead.
-    auto gather = [&](uint32_t tile, const __nv_bfloat16* base, const int* src) {
+    // AnnSA: the 64 rows of a key or value tile gathered by TMA, four rows
+    // per tile::gather4 (one-row-high boxes of 64 columns): lane l fetches
+    // rows 4 (l % 16) .. + 3 of column half l / 16.  Rows past the key list
+    // read slot 0 (always a row of the tensor; those columns are masked).
+    auto gather = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* bar, const int* src) {
+      const int r0 = 4 * (lane & 15), hf = lane >> 4;
+      int ys[4];
 #pragma unroll
-      for (int i = 0; i < kN * 16 / 32; ++i) {
-        const int rr = 2 * i + (lane >> 4), ch = lane & 15;
-        const int sr = __shfl_sync(0xffffffffu, src[rr >> 5], rr & 31);
-        const uint32_t off = tc::sw128_offset(rr, ch, kN);
-        if (sr >= 0) tc::cp_async16(tile + off, (const char*)(base + ((size_t)h * rows_per_head + sr) * kD) + ch * 16, 16u);
-        else tc::cp_async16(tile + off, base, 0u);
+      for (int e = 0; e < 4; ++e) {
+        const int r = r0 + e;
+        const int a = __shfl_sync(0xffffffffu, src[0], r & 31);
+        const int b = __shfl_sync(0xffffffffu, src[1], r & 31);
+        const int sr = (r >> 5) ? b : a;
+        ys[e] = (int)((size_t)h * rows_per_head) + (sr >= 0 ? sr : 0);
       }
+      // every lane's metadata stores are ordered before lane 0's arrival
+      // (a complete_tx that lands before the expect_tx is allowed)
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_expect_tx(bar, kN * kD * 2);
+      tc::tma_gather4_2d(tile + hf * (kN * 128) + r0 * 128, map, bar, hf * 64, ys[0], ys[1], ys[2], ys[3]);
     };
     int ksrc[2] = {kNoRow, kNoRow}, knext[2] = {kNoRow, kNoRow}, vsrc[2] = {kNoRow, kNoRow},
         vnext[2] = {kNoRow, kNoRow};
+    if (lane == 0) {
+      tc::prefetch_tensormap(&mapK);
+      tc::prefetch_tensormap(&mapV);
+    }
     if constexpr (kSA) {
       fetch_src(0, ksrc);
       check_src(ksrc);
@@ -345,9 +360,6 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         fetch_src(1, knext);
         fetch_src(1, vnext);
       }
-    } else if (lane == 0) {
-      tc::prefetch_tensormap(&mapK);
-      tc::prefetch_tensormap(&mapV);
     }
     int jk = 0, jv = 0;
     uint32_t idle = 0;
@@ -367,8 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
               tc::tma_load_2d(sm.K[s] + kN * 128, &mapK, &sm.kfull[s], 64, row);
             }
           } else {
-            gather(tc::smem_u32(sm.K[s]), kb, ksrc);
-            tc::cp_async_arrive_noinc(&sm.kfull[s]);
+            gather(sm.K[s], &mapK, &sm.kfull[s], ksrc);
           }
           ++jk;
           if constexpr (kSA) {
@@ -404,10 +415,9 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
               tc::tma_load_2d(sm.V[s] + kN * 128, &mapV, &sm.vfull[s], 64, row);
             }
           } else {
-            gather(tc::smem_u32(sm.V[s]), vb, vsrc);
-            tc::cp_async_arrive_noinc(&sm.vfull[s]);
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&sm.vfull[s]);  // the metadata written above
+            // the metadata written above are published by the arrival that
+            // carries the gather's bytes (after the warp barrier in gather)
+            gather(sm.V[s], &mapV, &sm.vfull[s], vsrc);
           }
           ++jv;
           if constexpr (kSA) {
@@ -429,6 +439,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         __nanosleep(32);
       }
     }
+    issued_k = jk;
+    issued_v = jv;
   } else if (warp == 1) {
     // ================================================= MMA issuer
     // Issues QK_j (S_j = Q K_j^T into TMEM buffer j & 1) and PV_j (O += P_j
@@ -756,9 +768,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   if (bad_index) status_set(st, FASTAR_ERR_DEVICE_ARG);
   if (!ok) status_set(st, FASTAR_ERR_TIMEOUT);
   if (warp == 0) {
-    // the producer's copies have landed before the CTA exits
+    // the producer's copies have landed before the CTA exits (also when a
+    // wait elsewhere ran out and nobody consumed the last tiles): the last
+    // kStages key and value loads are waited for, with the bounded wait
     tc::cp_async_wait_all();
     if (!kSA && ntiles > 0 && lane == 0 && !tc::mbar_wait(&sm.bar_q, 0)) status_set(st, FASTAR_ERR_TIMEOUT);
+    if (lane == 0) {
+      for (int t = max(0, issued_k - kStages); t < issued_k; ++t)
+        if (!tc::mbar_wait(&sm.kfull[t % kStages], (uint32_t)(t / kStages) & 1u)) status_set(st, FASTAR_ERR_TIMEOUT);
+      for (int t = max(0, issued_v - kStages); t < issued_v; ++t)
+        if (!tc::mbar_wait(&sm.vfull[t % kStages], (uint32_t)(t / kStages) & 1u)) status_set(st, FASTAR_ERR_TIMEOUT);
+    }
+    __syncwarp();
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -769,14 +790,16 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 
 // Merge the T per-table partials of each query: a warp handles kCombineQ
 // queries, four dimensions per lane; every (max, sum) and partial row of its
-// queries is loaded before any is used.
-// Two queries per warp at four CTAs per SM (fewer registers, more warps in
-// flight) measured 2 us faster than four queries per warp at two.
-constexpr int kCombineQ = 2;
+// queries is loaded before any is used.  Compiled for the number of partials
+// (kT = 2, the workloads' two tables, or up to four), so that a warp holds
+// only the partials there are: four queries per warp (two with up to four
+// partials, within the register budget) at four CTAs per SM.
+template <int kT, int kCombineQ>
 __global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const __half* __restrict__ ws_o,
                                                             const float2* __restrict__ ws_ml, int T, int H,
                                                             int Nq, __nv_bfloat16* __restrict__ out,
                                                             float* __restrict__ lse, int32_t* st) {
+  constexpr int kMaxT = kT;  // partials held per query
   pdl_wait();
   if (status_bad(st)) return;
   const int h = blockIdx.y;
@@ -846,6 +869,15 @@ int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
 
 int p64_of(int P) { return (P + kN - 1) / kN * kN; }
 
+// AnnSA: tensor maps of the cache's K and V ([H * C][D] bf16) with
+// one-row-high boxes of 64 columns, for the producer's tile::gather4 loads.
+int make_sa_maps(const fastar_cache* c, CUtensorMap* mk, CUtensorMap* mv) {
+  const uint64_t rows = (uint64_t)c->H * (uint64_t)c->C;
+  if (make_tmap_bf16_2d(mk, c->K, rows, kD, 1, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(mv, c->V, rows, kD, 1, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  return FASTAR_OK;
+}
+
 }  // namespace
 
 size_t annsa_tc_ws_bytes(int H, int Nq, int D, int T) {
@@ -907,13 +939,16 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
             1 << c->B, (__half*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0, nullptr, 0};
   CaArgs ca{};
-  CUtensorMap dummy;
+  CUtensorMap dummy, mk, mv;
   memset(&dummy, 0, sizeof(dummy));
+  if (make_sa_maps(c, &mk, &mv) != FASTAR_OK) return FASTAR_ERR_CUDA;
   // every table in one launch: the tables' CTAs fill each other's waves
-  const int rc = launch_attn<true>(dummy, dummy, dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca,
+  const int rc = launch_attn<true>(dummy, mk, mv, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca,
                                    sa, st, s);
   if (rc != FASTAR_OK || c->T == 1) return rc;
-  fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
+  const int cq = c->T <= 2 ? 4 : 2;  // queries per warp of the combine kernel
+  fastar::launch_pdl(c->T <= 2 ? annsa_combine_kernel<2, 4> : annsa_combine_kernel<4, 2>,
+                     dim3((Nq + 8 * cq - 1) / (8 * cq), c->H), 256, 0, s, sa.ws_o, sa.ws_ml, c->T, c->H, Nq,
                                                                  (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");
   return FASTAR_OK;
@@ -932,9 +967,10 @@ int launch_annsa_masked(fastar_dtype dt, const void* q, const uint32_t* q_codes,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, 1,
             1 << c->B, nullptr, nullptr, (__nv_bfloat16*)out, lse, 0, 0, mask, mask_words};
   CaArgs ca{};
-  CUtensorMap dummy;
+  CUtensorMap dummy, mk, mv;
   memset(&dummy, 0, sizeof(dummy));
-  return launch_attn<true>(dummy, dummy, dummy, dim3((Nq + kM - 1) / kM, 1, c->H), c->H, Nq, scale, ca, sa, st, s);
+  if (make_sa_maps(c, &mk, &mv) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  return launch_attn<true>(dummy, mk, mv, dim3((Nq + kM - 1) / kM, 1, c->H), c->H, Nq, scale, ca, sa, st, s);
 }
 
 size_t annsa_parts_ws_bytes(int H, int Nq, int D, int parts) {
@@ -956,9 +992,10 @@ int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
             1 << c->B, (__half*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1, nullptr, 0};
   CaArgs ca{};
-  CUtensorMap dummy;
+  CUtensorMap dummy, mk, mv;
   memset(&dummy, 0, sizeof(dummy));
-  return launch_attn<true>(dummy, dummy, dummy, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa,
+  if (make_sa_maps(c, &mk, &mv) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  return launch_attn<true>(dummy, mk, mv, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa,
                            st, s);
 }
 
@@ -966,7 +1003,9 @@ int launch_annsa_combine(int H, int Nq, int parts, const void* ws, void* out, fl
                          cudaStream_t s) {
   if (Nq == 0 || H == 0) return FASTAR_OK;
   const size_t o_bytes = ((size_t)parts * H * Nq * kD * sizeof(__half) + 255) & ~(size_t)255;
-  fastar::launch_pdl((annsa_combine_kernel), dim3((Nq + 8 * kCombineQ - 1) / (8 * kCombineQ), H), 256, 0, s,
+  const int cq = parts <= 2 ? 4 : 2;  // queries per warp of the combine kernel
+  fastar::launch_pdl(parts <= 2 ? annsa_combine_kernel<2, 4> : annsa_combine_kernel<4, 2>,
+                     dim3((Nq + 8 * cq - 1) / (8 * cq), H), 256, 0, s,
                      (const __half*)ws, (const float2*)((const char*)ws + o_bytes), parts, H, Nq,
                      (__nv_bfloat16*)out, lse, st);
   FASTAR_LAUNCHED(s, "annsa_combine");
