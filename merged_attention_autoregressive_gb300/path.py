@@ -72,7 +72,7 @@ class ChunkPath:
             # the second stream (query CSR, cross-attention branch)
             self._side = torch.cuda.Stream(device=dev)
             # host-to-host chunks: the streams that copy inputs in and outputs out
-            self._copy_in = (torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev))
+            self._copy_in = torch.cuda.Stream(device=dev)
             self._copy_out = torch.cuda.Stream(device=dev)
         # the events that fork and join the second stream
         self._fork = torch.cuda.Event()
@@ -127,12 +127,13 @@ class ChunkPath:
         """The chunk from host memory to host memory (pinned tensors, same
         shapes as step's; ho_ca, ho_sa receive o_ca and o_sa).
 
-        The inputs are copied in on two copy streams in the order the
-        branches need them (k then v for the merge branch; q, the prompt
+        The inputs are copied in on one copy stream in the order the
+        branches need them (k and v for the merge branch, then q, the prompt
         keys and the prompt values for the cross-attention branch, which
-        also builds the query CSR that AnnSA needs), each branch hashes and
-        starts as soon as its inputs have landed, and each output is copied
-        out on a third stream as soon as it is final.  The copies into this
+        also builds the query CSR that AnnSA needs; one host-to-device stream
+        beside the device-to-host one moves more in total than two), each
+        branch hashes and starts as soon as its inputs have landed, and each
+        output is copied out on a second stream as soon as it is final.  The copies into this
         path's device buffers (dev_in: (q, k, v, kp, vp) tensors to use; by
         default buffers of its own) wait only for the previous chunk of this
         path to have read them, so with several paths (layers) the copies of
@@ -151,20 +152,18 @@ class ChunkPath:
         # chunk has finished and its outputs have been copied out (never
         # recorded before the first chunk); every stream of this chunk waits
         # for that through the copies it depends on
-        cm, cx = self._copy_in
-        for c in (cm, cx):
-            c.wait_event(self._out_done)
-        with torch.cuda.stream(cm):
+        ci = self._copy_in
+        ci.wait_event(self._out_done)
+        with torch.cuda.stream(ci):
             dk.copy_(hk, non_blocking=True)
-            self._in_k.record(cm)
+            self._in_k.record(ci)
             dv.copy_(hv, non_blocking=True)
-            self._in_v.record(cm)
-        with torch.cuda.stream(cx):
+            self._in_v.record(ci)
             dq.copy_(hq, non_blocking=True)
             dkp.copy_(hkp, non_blocking=True)
-            self._in_qp.record(cx)
+            self._in_qp.record(ci)
             dvp.copy_(hvp, non_blocking=True)
-            self._in_vp.record(cx)
+            self._in_vp.record(ci)
         main.wait_event(self._out_done)
         self._run(dq, dk, dv, dkp, dvp, first_frame, main, host_out=(ho_ca, ho_sa))
         co = self._copy_out
