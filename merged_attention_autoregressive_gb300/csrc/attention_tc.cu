@@ -179,10 +179,17 @@ __global__ void __launch_bounds__(256) annca_compact_kernel(const __nv_bfloat16*
 
 // AnnCA: grid (query tiles, frames, heads); AnnSA: grid (query tiles,
 // tables, heads).
-template <bool kSA>
+// kRuns (AnnSA over a description of at most two buckets in one table, i.e.
+// dense attention, dense denoising steps and the quantised matcher): tiles of
+// consecutive slots are loaded as 64-row boxes (mapK64 / mapV64).  The
+// bucketed form is compiled without that path, which would cost its gathers
+// about 4 % even where it is never taken.
+template <bool kSA, bool kRuns>
 __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_constant__ CUtensorMap mapQ,
                                                              const __grid_constant__ CUtensorMap mapK,
-                                                             const __grid_constant__ CUtensorMap mapV, int H,
+                                                             const __grid_constant__ CUtensorMap mapV,
+                                                             const __grid_constant__ CUtensorMap mapK64,
+                                                             const __grid_constant__ CUtensorMap mapV64, int H,
                                                              int Nq, float scale, CaArgs ca, SaArgs sa,
                                                              int32_t* st) {
   pdl_wait();
@@ -327,7 +334,33 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     // per tile::gather4 (one-row-high boxes of 64 columns): lane l fetches
     // rows 4 (l % 16) .. + 3 of column half l / 16.  Rows past the key list
     // read slot 0 (always a row of the tensor; those columns are masked).
-    auto gather = [&](uint8_t* tile, const CUtensorMap* map, uint64_t* bar, const int* src) {
+    // A tile whose 64 slots are one run of consecutive rows of the head (a
+    // one-bucket description of the cache) comes as two 64-row boxes
+    // instead of 32 four-row gathers.  The test is taken for every tile only
+    // in CTAs whose first tile is such a run (elsewhere runs are rare and the
+    // test costs more than it saves), when the tile's slots are checked,
+    // ahead of its gather.
+    bool runs = false;
+    auto is_run = [&](const int* src) -> bool {
+      if (!kRuns || !runs) return false;
+      const int base = __shfl_sync(0xffffffffu, src[0], 0);
+      return __all_sync(0xffffffffu, base >= 0 && base + kN <= (int)rows_per_head && src[0] == base + lane &&
+                                         src[1] == base + 32 + lane);
+    };
+    auto gather = [&](uint8_t* tile, const CUtensorMap* map, const CUtensorMap* map64, uint64_t* bar,
+                      const int* src, bool run) {
+      if constexpr (kRuns) {
+        if (run) {
+          const int y = (int)((size_t)h * rows_per_head) + __shfl_sync(0xffffffffu, src[0], 0);
+          __syncwarp();  // the metadata stores, before lane 0's arrival
+          if (lane == 0) {
+            tc::mbar_arrive_expect_tx(bar, kN * kD * 2);
+            tc::tma_load_2d(tile, map64, bar, 0, y);
+            tc::tma_load_2d(tile + kN * 128, map64, bar, 64, y);
+          }
+          return;
+        }
+      }
       const int r0 = 4 * (lane & 15), hf = lane >> 4;
       int ys[4];
 #pragma unroll
@@ -346,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     };
     int ksrc[2] = {kNoRow, kNoRow}, knext[2] = {kNoRow, kNoRow}, vsrc[2] = {kNoRow, kNoRow},
         vnext[2] = {kNoRow, kNoRow};
+    bool krun = false, vrun = false;
     if (lane == 0) {
       tc::prefetch_tensormap(&mapK);
       tc::prefetch_tensormap(&mapV);
@@ -353,6 +387,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     if constexpr (kSA) {
       fetch_src(0, ksrc);
       check_src(ksrc);
+      runs = kRuns;
+      krun = is_run(ksrc);
+      runs = krun;
+      vrun = krun;
+      if (runs && lane == 0) {
+        tc::prefetch_tensormap(&mapK64);
+        tc::prefetch_tensormap(&mapV64);
+      }
       vsrc[0] = ksrc[0];
       vsrc[1] = ksrc[1];
       fetch_meta(vsrc);
@@ -379,13 +421,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
               tc::tma_load_2d(sm.K[s] + kN * 128, &mapK, &sm.kfull[s], 64, row);
             }
           } else {
-            gather(sm.K[s], &mapK, &sm.kfull[s], ksrc);
+            gather(sm.K[s], &mapK, &mapK64, &sm.kfull[s], ksrc, krun);
           }
           ++jk;
           if constexpr (kSA) {
             ksrc[0] = knext[0];
             ksrc[1] = knext[1];
             check_src(ksrc);
+            krun = is_run(ksrc);
             knext[0] = knext[1] = kNoRow;
             if (jk + 1 < ntiles) fetch_src(jk + 1, knext);
           }
@@ -417,13 +460,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
           } else {
             // the metadata written above are published by the arrival that
             // carries the gather's bytes (after the warp barrier in gather)
-            gather(sm.V[s], &mapV, &sm.vfull[s], vsrc);
+            gather(sm.V[s], &mapV, &mapV64, &sm.vfull[s], vsrc, vrun);
           }
           ++jv;
           if constexpr (kSA) {
             vsrc[0] = vnext[0];
             vsrc[1] = vnext[1];
             check_src(vsrc);
+            vrun = is_run(vsrc);
             if (jv < ntiles) fetch_meta(vsrc);  // lands while tile jv - 1 is consumed
             vnext[0] = vnext[1] = kNoRow;
             if (jv + 1 < ntiles) fetch_src(jv + 1, vnext);
@@ -853,28 +897,45 @@ __global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const __half* __r
   pdl_trigger();
 }
 
-template <bool kSA>
-int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, dim3 grid, int H, int Nq,
-                float scale, const CaArgs& ca, const SaArgs& sa, int32_t* st, cudaStream_t s) {
+// mk64 / mv64: AnnSA's 64-row-box maps of the cache keys and values (for
+// tiles of consecutive slots); AnnCA passes its key and value maps again.
+template <bool kSA, bool kRuns = false>
+int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mk64,
+                const CUtensorMap& mv64, dim3 grid, int H, int Nq, float scale, const CaArgs& ca, const SaArgs& sa,
+                int32_t* st, cudaStream_t s) {
   const size_t smem = sizeof(AttnSmem) + 1024;
-  if (cudaFuncSetAttribute(attn_tc_kernel<kSA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+  if (cudaFuncSetAttribute(attn_tc_kernel<kSA, kRuns>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess) {
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  fastar::launch_pdl((attn_tc_kernel<kSA>), grid, kThreads, smem, s, mq, mk, mv, H, Nq, scale, ca, sa, st);
+  fastar::launch_pdl((attn_tc_kernel<kSA, kRuns>), grid, kThreads, smem, s, mq, mk, mv, mk64, mv64, H, Nq, scale, ca, sa,
+                     st);
   FASTAR_LAUNCHED(s, kSA ? "annsa_tc" : "annca_tc");
   return FASTAR_OK;
 }
 
 int p64_of(int P) { return (P + kN - 1) / kN * kN; }
 
+// AnnSA: the run-capable kernel for a description of at most two buckets in
+// one table (dense attention, dense denoising steps), the bucketed one
+// otherwise.
+int sa_launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mk64,
+              const CUtensorMap& mv64, dim3 grid, int H, int Nq, float scale, const CaArgs& ca, const SaArgs& sa,
+              int32_t* st, cudaStream_t s) {
+  if (sa.T == 1 && sa.nb <= 2) return launch_attn<true, true>(mq, mk, mv, mk64, mv64, grid, H, Nq, scale, ca, sa, st, s);
+  return launch_attn<true, false>(mq, mk, mv, mk64, mv64, grid, H, Nq, scale, ca, sa, st, s);
+}
+
 // AnnSA: tensor maps of the cache's K and V ([H * C][D] bf16) with
-// one-row-high boxes of 64 columns, for the producer's tile::gather4 loads.
-int make_sa_maps(const fastar_cache* c, CUtensorMap* mk, CUtensorMap* mv) {
+// one-row-high boxes of 64 columns, for the producer's tile::gather4 loads,
+// and with 64-row boxes, for tiles of consecutive slots.
+int make_sa_maps(const fastar_cache* c, CUtensorMap* mk, CUtensorMap* mv, CUtensorMap* mk64, CUtensorMap* mv64) {
   const uint64_t rows = (uint64_t)c->H * (uint64_t)c->C;
   if (make_tmap_bf16_2d(mk, c->K, rows, kD, 1, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   if (make_tmap_bf16_2d(mv, c->V, rows, kD, 1, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(mk64, c->K, rows, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(mv64, c->V, rows, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   return FASTAR_OK;
 }
 
@@ -908,7 +969,7 @@ int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void*
     CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P, 0,
               (__nv_bfloat16*)out};
     SaArgs sa{};
-    return launch_attn<false>(mq, mq, mq, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
+    return launch_attn<false>(mq, mq, mq, mq, mq, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
   }
   if (!ws || ws_bytes < annca_tc_ws_bytes(H, F, P, D)) return FASTAR_ERR_WORKSPACE;
   const size_t half = (((size_t)H * F * P64 * kD * sizeof(__nv_bfloat16)) + 255) & ~(size_t)255;
@@ -924,7 +985,7 @@ int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void*
   CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P, P64,
             (__nv_bfloat16*)out};
   SaArgs sa{};
-  return launch_attn<false>(mq, mk, mv, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
+  return launch_attn<false>(mq, mk, mv, mk, mv, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
 }
 
 int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
@@ -939,11 +1000,11 @@ int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, con
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
             1 << c->B, (__half*)ws, (float2*)((char*)ws + o_bytes), (__nv_bfloat16*)out, lse, 0, 0, nullptr, 0};
   CaArgs ca{};
-  CUtensorMap dummy, mk, mv;
+  CUtensorMap dummy, mk, mv, mk64, mv64;
   memset(&dummy, 0, sizeof(dummy));
-  if (make_sa_maps(c, &mk, &mv) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_sa_maps(c, &mk, &mv, &mk64, &mv64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   // every table in one launch: the tables' CTAs fill each other's waves
-  const int rc = launch_attn<true>(dummy, mk, mv, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca,
+  const int rc = sa_launch(dummy, mk, mv, mk64, mv64, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca,
                                    sa, st, s);
   if (rc != FASTAR_OK || c->T == 1) return rc;
   const int cq = c->T <= 2 ? 4 : 2;  // queries per warp of the combine kernel
@@ -967,10 +1028,11 @@ int launch_annsa_masked(fastar_dtype dt, const void* q, const uint32_t* q_codes,
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, 1,
             1 << c->B, nullptr, nullptr, (__nv_bfloat16*)out, lse, 0, 0, mask, mask_words};
   CaArgs ca{};
-  CUtensorMap dummy, mk, mv;
+  CUtensorMap dummy, mk, mv, mk64, mv64;
   memset(&dummy, 0, sizeof(dummy));
-  if (make_sa_maps(c, &mk, &mv) != FASTAR_OK) return FASTAR_ERR_CUDA;
-  return launch_attn<true>(dummy, mk, mv, dim3((Nq + kM - 1) / kM, 1, c->H), c->H, Nq, scale, ca, sa, st, s);
+  if (make_sa_maps(c, &mk, &mv, &mk64, &mv64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  return launch_attn<true, true>(dummy, mk, mv, mk64, mv64, dim3((Nq + kM - 1) / kM, 1, c->H), c->H, Nq, scale, ca,
+                                 sa, st, s);
 }
 
 size_t annsa_parts_ws_bytes(int H, int Nq, int D, int parts) {
@@ -992,10 +1054,10 @@ int launch_annsa_parts(const void* q, const uint32_t* q_codes, const int32_t* q_
             (const __nv_bfloat16*)c->V, c->m, c->codes, c->size, c->perm, c->offsets, c->C, c->T,
             1 << c->B, (__half*)ws, (float2*)((char*)ws + o_bytes), nullptr, nullptr, base, 1, nullptr, 0};
   CaArgs ca{};
-  CUtensorMap dummy, mk, mv;
+  CUtensorMap dummy, mk, mv, mk64, mv64;
   memset(&dummy, 0, sizeof(dummy));
-  if (make_sa_maps(c, &mk, &mv) != FASTAR_OK) return FASTAR_ERR_CUDA;
-  return launch_attn<true>(dummy, mk, mv, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa,
+  if (make_sa_maps(c, &mk, &mv, &mk64, &mv64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  return sa_launch(dummy, mk, mv, mk64, mv64, dim3((Nq + kM - 1) / kM, c->T, c->H), c->H, Nq, scale, ca, sa,
                            st, s);
 }
 
