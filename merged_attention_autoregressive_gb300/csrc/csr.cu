@@ -6,7 +6,8 @@
 // LSH tables: FAST-AR summary, paperlayer.ai, section 2; AnnSA restricts a
 // query to keys of its own buckets, gist.science technical summary 2.C.)
 //
-// Each of W warps (a power of two) owns a contiguous segment of the ids.
+// Each of W warps (a power of two, up to 32) owns a contiguous segment of
+// the ids.
 // Pass 1 counts codes per (warp, bucket) in shared memory; pass 2 scans those
 // counts in (bucket, warp) order, which makes the placement stable; pass 3
 // walks each segment in order, ranking equal codes inside a warp step with
@@ -15,7 +16,7 @@
 
 namespace fastar {
 
-constexpr int kCsrThreads = 256;  // 8 warps
+constexpr int kCsrThreads = 1024;  // up to 32 warps
 
 // cnt holds the (warp, bucket) counts bucket-major with a padded row of W+1
 // entries per bucket: warp w's lanes, which hit different buckets, land in
@@ -23,7 +24,7 @@ constexpr int kCsrThreads = 256;  // 8 warps
 // Codes a warp holds in registers for passes 1 and 3: up to kCsrRegs per
 // lane (segments of up to 32 * kCsrRegs ids); longer segments are read
 // again from global memory in pass 3.
-constexpr int kCsrRegs = 24;
+constexpr int kCsrRegs = 12;
 
 __global__ void __launch_bounds__(kCsrThreads) csr_kernel(const uint32_t* __restrict__ keys, int N,
                                                           const int32_t* __restrict__ n_dev, int n_div,
@@ -120,10 +121,13 @@ int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_d
                int32_t* perm, int32_t* offsets, int32_t* st, cudaStream_t s) {
   if (G == 0) return FASTAR_OK;
   if (nb > (1 << kMaxCsrBits)) return FASTAR_ERR_UNSUPPORTED;
-  // 8 warps per histogram: a (bucket, warp) scan of 8 nb entries; more warps
-  // would add scan work faster than they take counting and placing work
-  int lgW = 3;
-  while (lgW > 0 && (size_t)((1 << lgW) + 1) * nb * sizeof(int) > 128 * 1024) --lgW;
+  // Up to 32 warps per group, each placing its segment 32 ids per step in
+  // order: the (bucket, warp) scan grows with the warps but is spread over
+  // the same number of threads, while each warp's serial placement shrinks
+  // (with 1,024 buckets: 26 us per group with 8 warps).  The (warp, bucket)
+  // counts must fit in shared memory.
+  int lgW = 5;
+  while (lgW > 0 && (size_t)((1 << lgW) + 1) * nb * sizeof(int) > 200 * 1024) --lgW;
   const size_t smem = (size_t)((1 << lgW) + 1) * nb * sizeof(int);
   if (smem > 48 * 1024 &&
       cudaFuncSetAttribute(csr_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -131,8 +135,8 @@ int launch_csr(const uint32_t* keys, int G, int N, const int32_t* n_dev, int n_d
     (void)cudaGetLastError();
     return FASTAR_ERR_CUDA;
   }
-  fastar::launch_pdl((csr_kernel), G, kCsrThreads, smem, s, keys, N, n_dev, n_div > 0 ? n_div : 1, nb, lgW, perm,
-                                          offsets, st);
+  fastar::launch_pdl((csr_kernel), G, 32 << lgW, smem, s, keys, N, n_dev, n_div > 0 ? n_div : 1, nb, lgW, perm,
+                     offsets, st);
   FASTAR_LAUNCHED(s, "csr");
   return FASTAR_OK;
 }
