@@ -841,6 +841,22 @@ def run_ours(args, cfg):
     # the job's time per chunk is its slowest rank's; the ranks together ran
     # every (layer, head) of the chunk once per step
     value = job_max(ms, world, "cuda")
+    ms_median = job_max(statistics.median(step_ms), world, "cuda")
+
+    # the same steps with L2 left warm (the caches are restored, nothing is
+    # flushed), beside the flushed measurement above
+    warm_ms = []
+    for _ in range(min(args.steps, 5)):
+        for p, sn in zip(stack.paths, snaps):
+            p.cache.restore(sn)
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record(stream)
+        stack.step(inputs, first)
+        w1.record(stream)
+        torch.cuda.synchronize()
+        warm_ms.append(w0.elapsed_time(w1))
+    check()
+    l2_warm = job_max(statistics.mean(warm_ms), world, "cuda")
 
     # per-stage times: the stages of every layer one after the other
     n_ss = min(args.steps, 3)
@@ -950,7 +966,13 @@ def run_ours(args, cfg):
                         "frac_of_peak_issued": kern[k_]["work_flops"] / t_k / 1e9 / pk["bf16_tflops"],
                         "TFLOP/s_algorithmic": kern[k_]["flops"] / t_k / 1e9,
                         "GB/s_algorithmic": kern[k_]["bytes"] / t_k / 1e6,
-                        "hbm_frac_algorithmic": kern[k_]["bytes"] / t_k / 1e6 / pk["hbm_gbs"]}
+                        "hbm_frac_algorithmic": kern[k_]["bytes"] / t_k / 1e6 / pk["hbm_gbs"],
+                        # softmax exponentials: one per allowed (query, key)
+                        # pair; at most one per tile element issued (32-key
+                        # halves that no query of a warp meets are skipped)
+                        "exp_algorithmic": kern[k_]["flops"] / (4 * cfg.D),
+                        "exp_issued_at_most": kern[k_]["work_flops"] / (4 * cfg.D),
+                        "exp_per_s_issued_at_most": kern[k_]["work_flops"] / (4 * cfg.D) / t_k * 1e3}
     kernel_roofs = {}
     for k_, m_ in kern.items():
         if k_ in kernels:
@@ -966,6 +988,8 @@ def run_ours(args, cfg):
             if cfg.prompt_clusters == 0 else "synthetic (seeded; host generator)",
             "config": config_dict(cfg, args, world),
             "rank0_share": {"layers": len(layers), "heads": len(heads)},
+            "ms_median": ms_median,
+            "l2_warm_ms": l2_warm,
             "effective_tflops": eff_tflops,
             "stages_ms": stage_ms,
             "roofline": roof,

@@ -568,6 +568,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(int n_f, int C, int3
 // stored mean: one warp-reduced dot product per hyperplane, a zero
 // projection giving bit 0.
 constexpr int kApplyKeys = 4;
+// Three CTAs per SM: the register budget of four spills the rows in flight,
+// that of two halves the warps hiding the dependent loads (14B-like frame:
+// 57 us at three, 59 at four, 75 at two; eight keys per warp at two, 71).
 
 // Sign bits of 16 warp-wide dot products: p[r] is this lane's share of
 // product r.  A reduce-scatter over the warp (lanes exchange half of their
@@ -610,7 +613,7 @@ __device__ __forceinline__ float stored(float x) {
   return Elem<T>::ld(&y);
 }
 template <typename T, int D, bool kMean>
-__global__ void __launch_bounds__(256, 4) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
+__global__ void __launch_bounds__(256, 3) apply_kernel(const T* __restrict__ k_frame, const T* __restrict__ v_frame,
                                                     const uint32_t* __restrict__ codes_frame, int n_f,
                                                     int row_stride_keys, int Tt, int32_t f,
                                                     const int32_t* __restrict__ match,
