@@ -106,7 +106,9 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Every earlier cp.async of this thread has landed (cp.async.wait_all also
+// commits the copies not yet in a group; wait_group alone would skip them).
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // byte offset of 16-byte chunk c (0..15 over 128 bf16 columns) of row r in a
 // tile of `rows` rows stored as two swizzled 64-column halves
