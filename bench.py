@@ -330,6 +330,32 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def host_cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo; "unknown" elsewhere)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            k, _, v = line.partition(":")
+            if k.strip() == "Model name" and v.strip():
+                return v.strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                k, _, v = line.partition(":")
+                if k.strip().lower() in ("model name", "cpu model", "hardware") and v.strip():
+                    return v.strip()
+            fh.seek(0)
+            for line in fh:
+                k, _, v = line.partition(":")
+                if k.strip().lower() == "cpu part":
+                    return "cpu part " + v.strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def oracle_baseline(cfg, timed_steps: int, warm_steps: int):
     """Time the oracle on the host cores (see above).  Returns the JSON
     object of the measurement: per-chunk ms extrapolated from the measured
@@ -352,6 +378,7 @@ def oracle_baseline(cfg, timed_steps: int, warm_steps: int):
     return {"value": chunk_ms, "unit": "ms/chunk", "cores": workers, "kind": "oracle",
             "ms_per_step": step_s * 1e3, "steps": timed_steps, "warmup": warm_steps,
             "unit_ms_mean": statistics.mean(units) * 1e3, "setup_s": team.setup_s,
+            "cpu_model": host_cpu_model(), "host_cores": host_cores(),
             "sample": (f"{workers} (layer, head) units of the {cfg.layers}-layer x {cfg.H}-head chunk, one per "
                        f"process (one BLAS thread each, {workers} processes on {host_cores()} host cores); a step "
                        f"times every process's unit once (hash, query CSR, merge of the chunk's {cfg.F} frames, "
@@ -374,7 +401,7 @@ def run_reference(args, cfg):
             "config": config_dict(cfg, args, world),
             "extrapolated_to_chunk": {"value": ob["value"], "unit": "ms/chunk",
                                       "from": "unit throughput of the timed steps (see cpu_baseline.sample)"},
-            "cpu_baseline": {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean",
+            "cpu_baseline": {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean", "cpu_model", "host_cores",
                                                 "setup_s")},
             "wall_s": t_run,
             "e2e": {"value": ob["value"], "unit": "ms/chunk", "h2d_bytes_per_step": 0,
@@ -1046,7 +1073,7 @@ def run_ours(args, cfg):
         line["rollout"] = rollout_measure(CONFIGS[2], args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ob = oracle_baseline(cfg, 1, 0)
-        line["cpu_baseline"] = {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean",
+        line["cpu_baseline"] = {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean", "cpu_model", "host_cores",
                                                    "setup_s")}
     if rank == 0:
         print(json.dumps(line), flush=True)
