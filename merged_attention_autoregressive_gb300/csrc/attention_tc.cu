@@ -142,7 +142,8 @@ __device__ __forceinline__ uint64_t range_bits(int lo, int hi) {
 // order into Kc/Vc [(h * F + f) * P64 + k][D] (P64 = P rounded up to 64),
 // with zero rows up to the next multiple of 64, so that the attention kernel
 // loads whole key tiles with two TMA boxes.  One CTA per 64-row tile, a
-// warp per row at a time (8 bytes per lane).
+// warp per row at a time (8 bytes per lane).  A (head, frame) that keeps
+// every token is not copied: the attention kernel reads the prompt's rows.
 __global__ void __launch_bounds__(256) annca_compact_kernel(const __nv_bfloat16* __restrict__ k_p,
                                                             const __nv_bfloat16* __restrict__ v_p,
                                                             const int32_t* __restrict__ kept_idx,
@@ -154,7 +155,9 @@ __global__ void __launch_bounds__(256) annca_compact_kernel(const __nv_bfloat16*
   const int t = blockIdx.x, f = blockIdx.y, h = blockIdx.z;
   const int cnt = min(max(kept_cnt[(size_t)h * F + f], 0), P);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (t * kN < cnt) {
+  // a (head, frame) that keeps every prompt token reads the prompt's own
+  // rows (the kept list is the prompt in order): nothing to copy
+  if (cnt < P && t * kN < cnt) {
     bool bad = false;
     for (int r = warp; r < kN; r += 8) {
       const int k = t * kN + r;
@@ -383,6 +386,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     if (lane == 0) {
       tc::prefetch_tensormap(&mapK);
       tc::prefetch_tensormap(&mapV);
+      if constexpr (!kSA) {  // AnnCA: the prompt's own rows
+        tc::prefetch_tensormap(&mapK64);
+        tc::prefetch_tensormap(&mapV64);
+      }
     }
     if constexpr (kSA) {
       fetch_src(0, ksrc);
@@ -415,10 +422,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         if (__shfl_sync(0xffffffffu, ready, 0)) {
           if constexpr (!kSA) {
             if (lane == 0) {
-              const int row = (h * ca.F + g) * ca.P64 + jk * kN;
+              // every prompt token kept (the kept list is the prompt in
+              // order): the prompt's own rows (mapK64); else the compacted ones
+              const bool all = nkeys == ca.P;
+              const int row = all ? h * ca.P + jk * kN : (h * ca.F + g) * ca.P64 + jk * kN;
+              const CUtensorMap* map = all ? &mapK64 : &mapK;
               tc::mbar_arrive_expect_tx(&sm.kfull[s], kN * kD * 2);
-              tc::tma_load_2d(sm.K[s], &mapK, &sm.kfull[s], 0, row);
-              tc::tma_load_2d(sm.K[s] + kN * 128, &mapK, &sm.kfull[s], 64, row);
+              tc::tma_load_2d(sm.K[s], map, &sm.kfull[s], 0, row);
+              tc::tma_load_2d(sm.K[s] + kN * 128, map, &sm.kfull[s], 64, row);
             }
           } else {
             gather(sm.K[s], &mapK, &mapK64, &sm.kfull[s], ksrc, krun);
@@ -452,10 +463,12 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
           }
           if constexpr (!kSA) {
             if (lane == 0) {
-              const int row = (h * ca.F + g) * ca.P64 + jv * kN;
+              const bool all = nkeys == ca.P;
+              const int row = all ? h * ca.P + jv * kN : (h * ca.F + g) * ca.P64 + jv * kN;
+              const CUtensorMap* map = all ? &mapV64 : &mapV;
               tc::mbar_arrive_expect_tx(&sm.vfull[s], kN * kD * 2);
-              tc::tma_load_2d(sm.V[s], &mapV, &sm.vfull[s], 0, row);
-              tc::tma_load_2d(sm.V[s] + kN * 128, &mapV, &sm.vfull[s], 64, row);
+              tc::tma_load_2d(sm.V[s], map, &sm.vfull[s], 0, row);
+              tc::tma_load_2d(sm.V[s] + kN * 128, map, &sm.vfull[s], 64, row);
             }
           } else {
             // the metadata written above are published by the arrival that
@@ -898,7 +911,8 @@ __global__ void __launch_bounds__(256, 4) annsa_combine_kernel(const __half* __r
 }
 
 // mk64 / mv64: AnnSA's 64-row-box maps of the cache keys and values (for
-// tiles of consecutive slots); AnnCA passes its key and value maps again.
+// tiles of consecutive slots); AnnCA's maps of the prompt's keys and values
+// (for the (head, frame)s that keep every prompt token).
 template <bool kSA, bool kRuns = false>
 int launch_attn(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mk64,
                 const CUtensorMap& mv64, dim3 grid, int H, int Nq, float scale, const CaArgs& ca, const SaArgs& sa,
@@ -978,14 +992,17 @@ int launch_annca_tc(fastar_dtype dt, const void* q, const void* k_p, const void*
   fastar::launch_pdl((annca_compact_kernel), dim3(P64 / kN, F, H), 256, 0, s, (const __nv_bfloat16*)k_p,
                      (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, P, P64, kc, vc, st);
   FASTAR_LAUNCHED(s, "annca_compact");
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mkp, mvp;
   if (make_tmap_bf16_2d(&mq, q, (uint64_t)H * Nq, kD, kM, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   if (make_tmap_bf16_2d(&mk, kc, (uint64_t)H * F * P64, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   if (make_tmap_bf16_2d(&mv, vc, (uint64_t)H * F * P64, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  // the prompt itself, for the (head, frame)s that keep all of it
+  if (make_tmap_bf16_2d(&mkp, k_p, (uint64_t)H * P, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
+  if (make_tmap_bf16_2d(&mvp, v_p, (uint64_t)H * P, kD, kN, 64) != FASTAR_OK) return FASTAR_ERR_CUDA;
   CaArgs ca{(const __nv_bfloat16*)k_p, (const __nv_bfloat16*)v_p, kept_idx, kept_cnt, F, n_f, P, P64,
             (__nv_bfloat16*)out};
   SaArgs sa{};
-  return launch_attn<false>(mq, mk, mv, mk, mv, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
+  return launch_attn<false>(mq, mk, mv, mkp, mvp, dim3((n_f + kM - 1) / kM, F, H), H, Nq, scale, ca, sa, st, s);
 }
 
 int launch_annsa_tc(fastar_dtype dt, const void* q, const uint32_t* q_codes, const int32_t* q_perm,
