@@ -4,12 +4,14 @@
 // at a time through a warp-specialised pipeline:
 //   warp 0     producer: AnnCA's queries (one TMA box pair), then the key
 //              rows and, separately, the value rows and mask metadata of
-//              every tile (AnnCA: TMA tile loads of the compacted rows;
+//              every tile (AnnCA: TMA tile loads of the compacted kept rows,
+//              or of the prompt's own rows where a frame keeps all of them;
 //              AnnSA: TMA tile::gather4 loads, four slot rows each, into the
-//              128-byte swizzled layout; 2-stage rings), each as soon as its
-//              stage is free: a
-//              key stage once its QK product is done, a value stage once its
-//              PV product is; row sources and metadata are fetched ahead;
+//              128-byte swizzled layout, or two 64-row boxes for a run of
+//              consecutive slots in one-bucket descriptions; 2-stage rings),
+//              each as soon as its stage is free: a key stage once its QK
+//              product is done, a value stage once its PV product is; row
+//              sources and metadata are fetched one tile ahead;
 //   warp 1     MMA issuer: S_j = Q K_j^T (M 128, N 64, K 128) into one of two
 //              TMEM buffers and O += P_j V_j (M 128, N 128, K 64; P_j read
 //              from TMEM, V as an MN-major operand) into the TMEM
@@ -38,9 +40,9 @@
 // tables.  The slots of a query's own table-t bucket form one run of the
 // CTA's key list (from the cache CSR offsets); a warp skips every 32-key
 // chunk that no run of its queries meets.  With one table the CTA writes the
-// normalised output and the log-sum-exp; with more, each table writes an
-// unnormalised partial (o, running max, sum) and a combine kernel merges the
-// T partials of each query.
+// normalised output and the log-sum-exp; with more, each table writes its
+// partial (normalised by its own sum, in fp16, with its running max and sum)
+// and a combine kernel merges the T partials of each query.
 #include <cuda_fp16.h>
 #include <limits.h>
 #include <math.h>

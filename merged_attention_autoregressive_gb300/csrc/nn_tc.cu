@@ -6,7 +6,7 @@
 // the previous frame) by cosine, and matched to the best one (ties: lowest
 // slot) iff the cosine reaches tau.
 //
-// Work units: an item is (head, 128 new keys); a unit is one 64-candidate
+// Work units: an item is (head, 128 new keys); a unit is one 128-candidate
 // tile of an item (an item without candidates has one empty unit, so that
 // its keys' norms are still written).  The kernel is persistent: two CTAs
 // per SM, each taking a contiguous range of the units in (head, key tile,
@@ -16,20 +16,21 @@
 // result does not depend on the split.  The CTA is warp-specialised:
 //   warp 0     producer: per item, once the MMAs and the norm readers of
 //              the previous item are done with it, loads the item's keys (A,
-//              128 x 128) by TMA; fills a 4-stage ring of candidate tiles by
+//              128 x 128) by TMA; fills a 2-stage ring of candidate tiles by
 //              TMA.  After the first frame of a call the candidates are the
 //              rows of the previous frame, contiguous in k_new; for the first
 //              frame they are cache rows that an earlier kernel copied, in
 //              candidate order, into a contiguous staging buffer.  A head
 //              with more first-frame candidates than the staging buffer holds
 //              gathers its scattered cache rows with cp.async instead;
-//   warp 1     one elected thread issues 8 MMAs (M 128, N 64, K 16) per tile
-//              into one of four 64-column fp32 TMEM accumulators; the MMA
+//   warp 1     one elected thread issues 8 MMAs (M 128, N 128, K 16) per tile
+//              into one of two 128-column fp32 TMEM accumulators; the MMA
 //              commit frees the tile's stage, and after an item's last tile
 //              the item's A tile;
 //   warps 2-9  epilogue: per item the squared norms of the keys (from the A
-//              tile), then per tile two warps per TMEM lane quarter, 32
-//              columns each: a thread scales its key's dot products by the
+//              tile), then per tile two warps per TMEM lane quarter, 64
+//              columns each in two 32-column passes: a thread scales its
+//              key's dot products by the
 //              candidates' inverse norms (NaN for a candidate that is not a
 //              group or has a zero norm, which drops out of every comparison)
 //              and keeps the best (cosine, slot) among the candidates that
