@@ -451,8 +451,9 @@ int fastar_annsa_attention(fastar_dtype dt, const void* q,
  * are all 0 (every pair allowed).
  *
  * fastar_annsa_attention_part computes what fastar_annsa_attention does
- * for `cache`, but leaves each table's unnormalised partial (fp32 o, max,
- * sum) in slots part_base .. part_base + T - 1 of a workspace of part_total
+ * for `cache`, but leaves each table's partial (its output normalised by its
+ * own sum, in fp16, with its max and sum in fp32) in slots part_base ..
+ * part_base + T - 1 of a workspace of part_total
  * slots (sized by fastar_workspace_size(FASTAR_OP_ANNSA_PARTS, H, Nq, D,
  * part_total, ...)); nothing else is written.  fastar_annsa_combine then
  * merges the part_total partials of every query (the softmax over the union
