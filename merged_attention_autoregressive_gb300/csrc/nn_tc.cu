@@ -352,8 +352,11 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
       u += s.ct1 - s.ct0;
       if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.bar_a, (uint32_t)si & 1u));
       const int j = s.qt * kM + row;
+      // a warp whose 32 rows are all past the frame's keys (the last key
+      // tile of a head) only keeps the accumulator handshake
+      const bool rows_live = __any_sync(0xffffffffu, j < a.n_f);
       float na2 = 0.f;
-      if (ok) na2 = row_sq_norm(sm.A, row, kM);
+      if (ok && rows_live) na2 = row_sq_norm(sm.A, row, kM);
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&sm.a_free);  // this warp is done reading A
       const float ia = na2 > 0.f ? 1.f / sqrtf(na2) : 0.f;
@@ -396,12 +399,12 @@ __global__ void __launch_bounds__(kThreads, 2) nn_tc_kernel(const __grid_constan
             for (int i = 0; i < 32; ++i) mi[i] = c + i < s.nc ? __ldg(mrow + c + i) : __int_as_float(0x7fc00000);
           }
         };
-        load_mi(c0);
+        if (rows_live) load_mi(c0);
         if (ok) ok = __all_sync(0xffffffffu, tc::mbar_wait(&sm.tfull[b], (uint32_t)(g / kAcc) & 1u));
         if (!ok) continue;
         tc::tc_fence_after();
 #pragma unroll 1
-        for (int part = 0; part < kN / 64; ++part) {
+        for (int part = 0; part < (rows_live ? kN / 64 : 0); ++part) {
           const int c = c0 + part * 32;
           if (c >= s.nc) break;
           if (part > 0) load_mi(c);
