@@ -1247,7 +1247,11 @@ def rollout_measure(cfg, args):
            "ms_median_last50": float(np.median(last50)),
            "slope_last100_pct_of_mean_per_100_chunks": slope,
            "max_over_median_last50": float(last50.max() / np.median(last50)),
-           "flat": bool(abs(slope) < 1.0 and last50.max() <= 1.1 * np.median(last50)
+           "p95_over_median_last50": float(np.percentile(last50, 95) / np.median(last50)),
+           # flat = no growth: the trend of the last 100 chunks, the spread of
+           # the last 50 (95th percentile, so that one chunk's jitter on a
+           # sub-millisecond call does not decide it) and the memory held
+           "flat": bool(abs(slope) < 1.0 and np.percentile(last50, 95) <= 1.1 * np.median(last50)
                         and min(resident) == max(resident)),
            "ms_every_10th_chunk": ms[::10],
            "n_live_every_10th_chunk": n_live[::10], "n_live_final": n_live[-1],
