@@ -378,6 +378,9 @@ def oracle_baseline(cfg, timed_steps: int, warm_steps: int):
     return {"value": chunk_ms, "unit": "ms/chunk", "cores": workers, "kind": "oracle",
             "ms_per_step": step_s * 1e3, "steps": timed_steps, "warmup": warm_steps,
             "unit_ms_mean": statistics.mean(units) * 1e3, "setup_s": team.setup_s,
+            # the chunk on one core: every process is one thread (one BLAS
+            # thread), so a unit's time is its one-core time
+            "one_core_ms_per_chunk": statistics.mean(units) * 1e3 * units_per_chunk,
             "cpu_model": host_cpu_model(), "host_cores": host_cores(),
             "sample": (f"{workers} (layer, head) units of the {cfg.layers}-layer x {cfg.H}-head chunk, one per "
                        f"process (one BLAS thread each, {workers} processes on {host_cores()} host cores); a step "
@@ -401,8 +404,8 @@ def run_reference(args, cfg):
             "config": config_dict(cfg, args, world),
             "extrapolated_to_chunk": {"value": ob["value"], "unit": "ms/chunk",
                                       "from": "unit throughput of the timed steps (see cpu_baseline.sample)"},
-            "cpu_baseline": {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean", "cpu_model", "host_cores",
-                                                "setup_s")},
+            "cpu_baseline": {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean", "one_core_ms_per_chunk",
+                                                "cpu_model", "host_cores", "setup_s")},
             "wall_s": t_run,
             "e2e": {"value": ob["value"], "unit": "ms/chunk", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -1073,7 +1076,8 @@ def run_ours(args, cfg):
         line["rollout"] = rollout_measure(CONFIGS[2], args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ob = oracle_baseline(cfg, 1, 0)
-        line["cpu_baseline"] = {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean", "cpu_model", "host_cores",
+        line["cpu_baseline"] = {k: ob[k] for k in ("value", "unit", "cores", "kind", "sample", "unit_ms_mean",
+                                                   "one_core_ms_per_chunk", "cpu_model", "host_cores",
                                                    "setup_s")}
     if rank == 0:
         print(json.dumps(line), flush=True)
