@@ -1204,6 +1204,50 @@ def run_recall(args, cfg):
     print(json.dumps(line), flush=True)
 
 
+def _slope_pct(ms):
+    """Trend of a latency series in percent of its mean per 100 chunks (0
+    for fewer than two chunks): the Theil-Sen estimate, the median of the
+    slopes between every two chunks, so that a single slow chunk near either
+    end of the window does not tilt it as it tilts a least-squares line."""
+    y = np.asarray(ms, dtype=np.float64)
+    if len(y) < 2:
+        return 0.0
+    i, j = np.triu_indices(len(y), 1)
+    return float(np.median((y[j] - y[i]) / (j - i))) * 100.0 / float(y.mean()) * 100.0
+
+
+def flatness(ms, resident, n_live=None, capacity=None):
+    """Whether a rollout's per-chunk latency and memory stay flat.
+
+    The trend is judged over the chunks at which the cache is full (n_live
+    at capacity; at least 50 of them), else over the last 100 chunks: until
+    the cache is full its live groups grow and the attention's cost with
+    them, which is the expected fill, not growth of a full cache.  Flat =
+    that trend under 1 % of the mean per 100 chunks, the 95th percentile of
+    the last 50 chunks within 1.1 x their median (a percentile, so that one
+    chunk's jitter on a sub-millisecond call does not decide it; the maximum
+    is reported beside it) and the device bytes held identical at every
+    chunk.  The trend of the last 100 chunks is reported either way."""
+    ms = list(ms)
+    slope100 = _slope_pct(ms[-100:])
+    full = None
+    if n_live is not None and capacity is not None:
+        full = next((i for i, x in enumerate(n_live) if x >= capacity), None)
+    steady = ms[full:] if full is not None and len(ms) - full >= 50 else None
+    slope = _slope_pct(steady) if steady is not None else slope100
+    last50 = np.array(ms[-50:], dtype=np.float64)
+    med = float(np.median(last50))
+    p95 = float(np.percentile(last50, 95))
+    return {"ms_median_last50": med,
+            "slope_last100_pct_of_mean_per_100_chunks": slope100,
+            "slope_at_capacity_pct_of_mean_per_100_chunks": _slope_pct(steady) if steady is not None else None,
+            "chunks_at_capacity": len(steady) if steady is not None else 0,
+            "trend_window": "chunks at capacity" if steady is not None else "last 100 chunks",
+            "max_over_median_last50": float(last50.max()) / med,
+            "p95_over_median_last50": p95 / med,
+            "flat": bool(abs(slope) < 1.0 and p95 <= 1.1 * med and min(resident) == max(resident))}
+
+
 def rollout_measure(cfg, args):
     """A rollout of cfg.chunks chunks from an empty cache (the long-rollout
     workload, inputs drawn on the device): per chunk the latency of the
@@ -1242,22 +1286,12 @@ def rollout_measure(cfg, args):
     t_wall = time.perf_counter() - t_wall
     assert int(path.status.item()) == 0, fa.STATUS.get(int(path.status.item()))
     launches = fa.fastar_launch_count() - n0
-    tail = np.array(ms[-100:]) if len(ms) >= 100 else np.array(ms)
-    slope = float(np.polyfit(np.arange(len(tail)), tail, 1)[0]) * 100 / float(tail.mean())
-    last50 = np.array(ms[-50:])
     row = cfg.D * 2 * (2 if cfg.dtype == "bf16" else 4)  # K and V bytes per key
     out = {"workload": cfg.name, "chunks": cfg.chunks, "H": cfg.H, "C": cfg.C,
            "ms_mean": float(np.mean(ms)), "ms_first_chunk": ms[0], "ms_median": float(np.median(ms)),
-           "ms_median_last50": float(np.median(last50)),
-           "slope_last100_pct_of_mean_per_100_chunks": slope,
-           "max_over_median_last50": float(last50.max() / np.median(last50)),
-           "p95_over_median_last50": float(np.percentile(last50, 95) / np.median(last50)),
-           # flat = no growth: the trend of the last 100 chunks, the spread of
-           # the last 50 (95th percentile, so that one chunk's jitter on a
-           # sub-millisecond call does not decide it) and the memory held
-           "flat": bool(abs(slope) < 1.0 and np.percentile(last50, 95) <= 1.1 * np.median(last50)
-                        and min(resident) == max(resident)),
+           **flatness(ms, resident, n_live, cfg.C),
            "ms_every_10th_chunk": ms[::10],
+           "ms_last_100_chunks": [round(x, 5) for x in ms[-100:]],
            "n_live_every_10th_chunk": n_live[::10], "n_live_final": n_live[-1],
            "first_chunk_at_capacity": next((i for i, x in enumerate(n_live) if x >= cfg.C), None),
            "device_bytes_allocated": {"min": min(resident), "max": max(resident)},

@@ -44,3 +44,39 @@ def test_oracle_team_times_units():
     units = cfg.layers * cfg.H
     assert ob["value"] == pytest.approx(ob["ms_per_step"] * units / ob["cores"])
     assert ob["unit_ms_mean"] > 0 and ob["ms_per_step"] >= ob["unit_ms_mean"] * 0.5
+
+
+def test_rollout_flatness_rule():
+    """The rollout's flatness verdict: a flat series with one outlier chunk
+    stays flat (the spread is judged on the 95th percentile); a series whose
+    latency grows by 2 % per 100 chunks is not, nor is one with a few slow
+    chunks in the last 50, nor one whose device memory changes; the trend is
+    in percent of the mean per 100 chunks, and with the live-group counts
+    given it is judged over the chunks at capacity, after the fill."""
+    import bench
+    rng = np.random.default_rng(7)
+    base = list(0.6 + 0.005 * rng.standard_normal(200))
+    mem = [1000] * 200
+    spike = base.copy()
+    spike[190] = 0.6 * 1.3
+    r = bench.flatness(spike, mem)
+    assert r["flat"] and r["max_over_median_last50"] > 1.25 and r["p95_over_median_last50"] < 1.05
+    trend = [x * (1 + 0.0002 * i) for i, x in enumerate(base)]  # +0.02 % per chunk
+    r = bench.flatness(trend, mem)
+    assert not r["flat"] and 1.5 < r["slope_last100_pct_of_mean_per_100_chunks"] < 2.5
+    slow = base.copy()
+    for i in (160, 170, 180, 190):  # 4 of the last 50 chunks 30 % slower: above the 95th percentile
+        slow[i] *= 1.3
+    assert not bench.flatness(slow, mem)["flat"]
+    assert bench.flatness(base, mem)["flat"]
+    assert not bench.flatness(base, mem[:-1] + [1001])["flat"]
+    # a cache that fills until chunk 140 (latency rising with it), flat after
+    fill = [0.3 + 0.3 * min(i, 140) / 140 + 0.003 * rng.standard_normal() for i in range(200)]
+    live = [min(1000 * (i + 1), 140_000) for i in range(200)]
+    r = bench.flatness(fill, mem, live, 140_000)
+    assert r["slope_last100_pct_of_mean_per_100_chunks"] > 5.0
+    assert r["trend_window"] == "chunks at capacity" and r["chunks_at_capacity"] == 61
+    assert abs(r["slope_at_capacity_pct_of_mean_per_100_chunks"]) < 1.0 and r["flat"]
+    # fewer than 50 chunks at capacity: the last 100 chunks decide
+    r = bench.flatness(fill, mem, live, 170_000)
+    assert r["trend_window"] == "last 100 chunks" and not r["flat"]
