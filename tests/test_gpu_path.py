@@ -110,6 +110,34 @@ def test_ragged_bf16_chain():
     run_chunk(cfg, d, path, st, rep)
 
 
+@pytest.mark.parametrize("tau", [1.5, -1.0])
+def test_degenerate_thresholds_chain(tau):
+    """The two degenerate thresholds on ragged sizes.  tau above 1: no key
+    joins a group, so the cache is the append history of every key and
+    evicts once full.  tau = -1: every key that has a candidate joins its
+    best one, so nothing is inserted after the first frame and groups take
+    several members in one frame (the merge's many-to-one path)."""
+    cfg = CONFIGS[0].replace(dtype="bf16", n_f=197, F=2, past_frames=5, P=77, T=2, B=7, C=700,
+                             D=128, H=2, redraw=0.3, tau=tau)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    run_chunk(cfg, d, path, st, rep)
+    m = host(path.cache.m)
+    match = host(path.match)
+    if tau > 1:
+        assert (match < 0).all() and int(m.max()) == 1
+        assert int(host(path.cache.evicted).sum()) > 0
+    else:
+        assert (host(path.cache.size) == cfg.n_f).all()
+        # some frame of the chunk has a slot that several of its keys joined
+        per_frame = match.reshape(cfg.H, cfg.F, cfg.n_f)
+        assert any(np.bincount(per_frame[h, f][per_frame[h, f] >= 0]).max() > 1
+                   for h in range(cfg.H) for f in range(cfg.F))
+
+
 def test_wan_layer_chain():
     """Bench workload: 12 heads, D 128, 3 x 1560 queries, 21 merged past frames."""
     cfg = CONFIGS[1]
