@@ -138,6 +138,36 @@ def test_degenerate_thresholds_chain(tau):
                    for h in range(cfg.H) for f in range(cfg.F))
 
 
+def test_smaller_frames_after_larger_frames():
+    """Calls of 300-key frames, then a call of 197-key frames on the same
+    cache: the first frame of that call has more candidates (the ~300
+    groups the previous frame refreshed) than keys, more than the staging
+    copy holds, so the NN reads the candidates' scattered cache rows."""
+    cfg = CONFIGS[0].replace(dtype="bf16", n_f=300, F=2, past_frames=4, P=77, T=2, B=7, C=2000,
+                             D=128, H=3, redraw=0.3)
+    d = layer_data(cfg)
+    big = _path(cfg)
+    big.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, big, rep)
+    n_small = 197
+    small = _path(cfg.replace(n_f=n_small))
+    small.cache = big.cache
+    small.planes.copy_(big.planes)
+    first = cfg.past_frames
+    assert int((np.asarray(st.last_frame) == first - 1).sum(axis=1).min()) > n_small
+    cut = lambda a: np.concatenate([a[:, i * cfg.n_f:i * cfg.n_f + n_small] for i in range(cfg.F)], axis=1)  # noqa: E731
+    k, v = cut(d.chunk_k[0]), cut(d.chunk_v[0])
+    codes, match = small.merge(dev(k, cfg.dtype), dev(v, cfg.dtype), first, F=cfg.F)
+    torch.cuda.synchronize()
+    assert int(small.status.item()) == 0
+    gc = check_codes(codes, k, d.planes, cfg.T, cfg.B, rep, "197-key frame codes")
+    st = check_merge(small, st, k, v, gc, match, cfg.F, n_small, first, cfg.tau, cfg.dtype, rep,
+                     "197-key frames after 300-key frames")
+    check_csr(small.cache.perm, small.cache.offsets, st.codes, 1 << cfg.B, st.size, "cache CSR")
+    assert int((host(match) >= 0).sum()) > 0
+
+
 def test_wan_layer_chain():
     """Bench workload: 12 heads, D 128, 3 x 1560 queries, 21 merged past frames."""
     cfg = CONFIGS[1]
