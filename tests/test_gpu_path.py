@@ -168,6 +168,21 @@ def test_smaller_frames_after_larger_frames():
     assert int((host(match) >= 0).sum()) > 0
 
 
+def test_largest_frame_and_bits():
+    """The documented maxima: 6144 keys per frame (FASTAR_MAX_FRAME_KEYS),
+    B = 12 (4096 buckets per table) with T * B = 48 hyperplanes, and a
+    capacity the chunk's frame overflows, so the cache evicts."""
+    cfg = CONFIGS[0].replace(dtype="bf16", n_f=6144, F=1, past_frames=2, P=64, T=4, B=12, C=8192,
+                             D=128, H=2, redraw=0.3)
+    d = layer_data(cfg)
+    path = _path(cfg)
+    path.planes.copy_(dev(d.planes, cfg.dtype))
+    rep = Report()
+    st = build_cache(cfg, d, path, rep)
+    run_chunk(cfg, d, path, st, rep)
+    assert int(host(path.cache.evicted).min()) > 0
+
+
 def test_wan_layer_chain():
     """Bench workload: 12 heads, D 128, 3 x 1560 queries, 21 merged past frames."""
     cfg = CONFIGS[1]
