@@ -151,6 +151,15 @@ def test_host_argument_errors_need_no_gpu(L):
     # merge: null cache
     assert L.fastar_tempcache_merge(None, fake, fake, fake, 1, 4, 0, ctypes.c_float(0.9), None,
                                     None, 0, None, None) == 1
+    # merge: a frame above the frame-key limit (6144) or above the capacity;
+    # no frames: nothing to do, OK without device work
+    big = m2.CacheStruct(1, 128, 8192, 1, 4, 0, *([0x1000] * 10))
+    assert L.fastar_tempcache_merge(ctypes.byref(big), fake, fake, fake, 1, 6145, 0, ctypes.c_float(0.9),
+                                    None, None, 0, None, None) == 2
+    assert L.fastar_tempcache_merge(ctypes.byref(cs), fake, fake, fake, 1, 65, 0, ctypes.c_float(0.9),
+                                    None, None, 0, None, None) == 1
+    assert L.fastar_tempcache_merge(ctypes.byref(cs), fake, fake, fake, 0, 4, 0, ctypes.c_float(0.9),
+                                    None, None, 0, None, None) == 0
 
 
 def test_annsa_parts_workspace_grows_with_slots(L):
