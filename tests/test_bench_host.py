@@ -80,3 +80,56 @@ def test_rollout_flatness_rule():
     # fewer than 50 chunks at capacity: the last 100 chunks decide
     r = bench.flatness(fill, mem, live, 170_000)
     assert r["trend_window"] == "last 100 chunks" and not r["flat"]
+
+
+def test_layer_work_counts_follow_the_oracle():
+    """The work model behind every roofline fraction, on the CPU: for a
+    small chain merged by the oracle frame by frame, the NN flops are
+    2 D n_f per candidate, the candidates of a frame being the groups the
+    previous frame refreshed (counted here from the oracle's cache state);
+    the AnnSA flops are 4 D per pair the oracle's mask allows; the kept
+    count is the oracle's prune; and the merge bytes count every slot the
+    chunk's frames wrote."""
+    import types
+    import bench
+    from workloads import CONFIGS, layer_data
+    cfg = CONFIGS[0].replace(H=2, n_f=40, F=3, past_frames=3, P=24, T=2, B=4, C=200, redraw=0.3)
+    d = layer_data(cfg)
+    H, D, T, n_f, F, C, nb = cfg.H, cfg.D, cfg.T, cfg.n_f, cfg.F, cfg.C, 1 << cfg.B
+    st = O.CacheState.empty(H, C, D, T, cfg.dtype)
+    for f in range(cfg.past_frames):
+        st, _, _ = O.tempcache_merge(st, d.past_k[f], d.past_v[f], O.hash_codes(d.past_k[f], d.planes, T, cfg.B)[0],
+                                     1, n_f, f, cfg.tau)
+    snap = {"last_frame": torch.from_numpy(st.last_frame.copy()), "size": torch.from_numpy(st.size.copy())}
+    first = cfg.past_frames
+    k, v, q = d.chunk_k[0], d.chunk_v[0], d.chunk_q[0]
+    kc = O.hash_codes(k, d.planes, T, cfg.B)[0]
+    matches, want_nn, touched = [], 0, 0
+    for fi in range(F):
+        sl = slice(fi * n_f, (fi + 1) * n_f)
+        live = np.arange(C)[None] < st.size[:, None]
+        want_nn += 2 * D * n_f * int(((st.last_frame == first + fi - 1) & live).sum())
+        st, mt, _ = O.tempcache_merge(st, k[:, sl], v[:, sl], kc[:, :, sl], 1, n_f, first + fi, cfg.tau)
+        matches.append(np.asarray(mt))
+        touched += int((st.last_frame == first + fi).sum())
+    qc = O.hash_codes(q, d.planes, T, cfg.B)[0]
+    pc = O.hash_codes(d.prompt_k, d.planes, T, cfg.B)[0]
+    kept_idx, kept_cnt = O.annca_prune(qc, pc, F, n_f)
+    q_perm, _ = O.bucket_csr(qc, nb)
+    offs = np.stack([O.bucket_csr(st.codes[h], nb, int(st.size[h]))[1] for h in range(H)])
+    t32 = lambda a: torch.from_numpy(np.ascontiguousarray(a).astype(np.int32))  # noqa: E731
+    cache = types.SimpleNamespace(size=t32(st.size), codes=t32(st.codes), offsets=t32(offs))
+    path = types.SimpleNamespace(H=H, C=C, B=cfg.B, cache=cache, kept_cnt=t32(kept_cnt),
+                                 match=t32(np.concatenate(matches, axis=1)), q_codes=t32(qc), q_perm=t32(q_perm))
+    w = bench.layer_work(cfg, path, snap)
+    assert w["flops"]["merge"] == want_nn and w["kern"]["nn_tc"]["flops"] == want_nn
+    pairs = sum(int(O.annsa_allowed(qc[h], st.codes[h][:, :int(st.size[h])]).sum()) for h in range(H))
+    assert w["flops"]["annsa"] == 4 * D * pairs and w["stats"]["allowed_pairs"] == pairs
+    assert w["stats"]["kept"] == int(np.asarray(kept_cnt).sum())
+    assert w["stats"]["n_live"] == int(st.size.sum())
+    # apply: the frames' k and v read, each refreshed group's old value read,
+    # and K, V, m, last_frame and codes written for every slot written
+    e = 2 if cfg.dtype == "bf16" else 4
+    groups = sum(len(np.unique(mt[h][mt[h] >= 0])) for mt in matches for h in range(H))
+    assert w["kern"]["apply"]["bytes"] == (F * 2 * H * n_f * D * e + groups * D * e
+                                           + touched * (2 * D * e + 8 + T * 4))
